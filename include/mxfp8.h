@@ -1,0 +1,194 @@
+/*
+ * mxfp8.h - C ABI of the MXFP8 block-scaled quantiser, GEMM and grouped GEMM
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow two web pages that describe MXFP8 training of linear
+ * and MoE-expert layers:
+ *   [DSV3] "DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" (hyper-parallel issue #329)
+ *   [TT]   "低精度训练特性（MXFP8 / HiFloat8）" (torchtitan-npu)
+ * and one page on number formats:
+ *   [FMT]  "浮点格式、数值稳定性与混合精度" (arganzheng.life)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All pointers named *_data, *_scale, x, c and group_offsets are DEVICE
+ *   pointers, allocated and owned by the caller. The library never allocates,
+ *   frees or keeps device memory, and keeps no state between calls.
+ * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *   void*; NULL is the legacy default stream) on the current device, which must
+ *   be an sm_103 GPU. Nothing is synchronised.
+ * - Every call validates its arguments on the host first; on failure it
+ *   returns a non-OK status and launches nothing. There is no fallback to any
+ *   other kernel or precision ([DSV3] §13.4 and §15: a failure must be raised,
+ *   never replaced by a high-precision GEMM).
+ * - `dev_status` (device int*, may be NULL): checks that only the device can
+ *   make (group offsets) and bounded waits that expire write a non-zero
+ *   mx_status value there; the kernels never trap. The caller zeroes it
+ *   before the call and reads it after synchronising. The host-side return
+ *   value cannot report these.
+ *
+ * Data formats ([DSV3] §3, §3.1; [TT] 线性层低精度; [FMT] §二.2)
+ * -------------------------------------------------------------
+ * - Input: BF16, row-major.
+ * - Data: E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ *   infinities, S.1111.111 is NaN, largest finite 448), one byte per element.
+ * - Scales: E8M0 codes (2**(code-127); 0xFF is NaN), one per block of 32
+ *   consecutive elements along the contraction dimension.
+ * - Scale rule: X = floor(log2(amax)) - 8 clamped to [-127, 127], code = X+127;
+ *   element code = E4M3(x * 2**-X) rounded to nearest, ties to even, magnitudes
+ *   above 448 saturate. amax = 0 gives code 0x00; a block holding NaN/Inf gives
+ *   scale 0xFF and data 0x7F with each element's sign.
+ * - Row copy of T[R, C]: 1x32 blocks along each row; data [R, C].
+ * - Column copy of T[R, C]: 32x1 blocks down each column, stored TRANSPOSED:
+ *   data [C, R], so its blocks are 1x32 along its rows. Every GEMM operand is
+ *   therefore K-major with blocks along K.
+ *
+ * Scale-tile layout (the one the sm_103a block-scaled MMA consumes; the pages
+ * describe none): the logical scale matrix S[rows, kb] (kb = ceil(k/32)) is
+ * padded with zero bytes to [ceil(rows/128)*128, ceil(kb/4)*4] and cut into
+ * 512-byte atoms of 128 rows x 4 scale columns. Atom (ra, ka) = (r/128, k/4)
+ * starts at byte (ra * ceil(kb/4) + ka) * 512 (scale-column atoms fastest).
+ * Inside an atom the byte of S[r, k] sits at (r%32)*16 + ((r/32)%4)*4 + (k%4),
+ * i.e. 32 lines of 16 bytes, line r%32 holding rows r%32, +32, +64, +96.
+ * mx_scale_bytes()
+ * returns the padded size. Padding bytes are written as 0 by mx_quantize.
+ */
+#ifndef MXFP8_GB300_H
+#define MXFP8_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MXFP8_ABI_VERSION 1
+
+typedef enum mx_status {
+  MX_OK = 0,
+  MX_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, negative size, inconsistent operands */
+  MX_ERR_UNSUPPORTED_SHAPE = 2, /* a size the kernels do not take (e.g. K not a multiple of 32) */
+  MX_ERR_ALIGNMENT = 3,         /* a pointer or pitch is not 16-byte aligned */
+  MX_ERR_CUDA = 4,              /* a CUDA call failed; mx_last_error() has the message */
+  MX_ERR_DEVICE_CHECK = 5,      /* device-side validation failed (reported via dev_status) */
+  MX_ERR_TIMEOUT = 6,           /* a bounded device wait expired (reported via dev_status) */
+  MX_ERR_NO_DEVICE = 7          /* the current device is not an sm_103 GPU */
+} mx_status;
+
+typedef enum mx_axis {
+  MX_ROWWISE = 1, /* 1x32 blocks along rows (the "row" copy of [DSV3] §3.1) */
+  MX_COLWISE = 2, /* 32x1 blocks down columns, stored transposed (the "col" copy) */
+  MX_BOTH = 3     /* both copies from one read of the input ([DSV3] §8.1 dual-axis) */
+} mx_axis;
+
+/* GEMM modes of the direction table in [DSV3] §8 (layouts NT, NN, TN of §13.4).
+ * With column copies stored transposed, each mode computes C = A . B^T:
+ *   MX_FPROP  Y[M,N]  = X . W^T      a = X row copy [M,K],   b = W row copy [N,K]
+ *   MX_DGRAD  dX[M,K] = dY . W       a = dY row copy [M,N],  b = W col copy [K,N]
+ *   MX_WGRAD  dW[N,K] = dY^T . X     a = dY col copy [N,M],  b = X col copy [K,M]
+ * The mode only selects which operand orientations are accepted. */
+typedef enum mx_mode { MX_FPROP = 0, MX_DGRAD = 1, MX_WGRAD = 2 } mx_mode;
+
+/* One quantised operand ([DSV3] §7.4 QuantizedOperand: data, scale, orientation). */
+typedef struct mx_operand {
+  const void* data;  /* E4M3 codes: row r starts at data + r*ld bytes; k contiguous */
+  const void* scale; /* swizzled E8M0 scales of the logical [rows, ceil(k/32)] */
+  int64_t rows;      /* rows of this operand (M for a, N for b) */
+  int64_t k;         /* contraction length (for grouped wgrad: the padded capacity) */
+  int64_t ld;        /* bytes between rows, 0 means k; multiple of 16 */
+  int32_t orient;    /* MX_ROWWISE or MX_COLWISE: which copy of its source tensor */
+  int32_t reserved;  /* must be 0 */
+} mx_operand;
+
+/* Size in bytes of the swizzled scale buffer of a [rows, k] operand
+ * (ceil(rows/128)*128 * ceil(ceil(k/32)/4)*4). Host-only, pure function. */
+size_t mx_scale_bytes(int64_t rows, int64_t k);
+
+/* Total padded length of a grouped column copy: sum over groups of
+ * ceil(m_e/128)*128 for m_e = host_offsets[e+1] - host_offsets[e].
+ * Returns -1 if the offsets are not non-decreasing from 0. Host pointer. */
+int64_t mx_grouped_padded_rows(const int64_t* host_offsets, int n_groups);
+
+/*
+ * mx_quantize - dynamic MX quantisation of a BF16 matrix ([DSV3] §8.1, §13.3
+ * Quantizer.quantize(tensor, orientation, group_list); [TT] npu_dynamic_mx_quant
+ * and, with groups, npu_grouped_dynamic_mx_quant).
+ *
+ *   x        BF16 [rows, cols], row pitch ldx elements (ldx >= cols); 16-byte aligned,
+ *            ldx a multiple of 8.
+ *   axis     MX_ROWWISE, MX_COLWISE or MX_BOTH.
+ *   Row copy (ROWWISE/BOTH): row_data [rows, cols] E4M3 (pitch cols bytes),
+ *            row_scale mx_scale_bytes(rows, cols) bytes. Needs cols % 32 == 0.
+ *   Column copy (COLWISE/BOTH), dense (group_offsets == NULL):
+ *            col_data [cols, rows] E4M3 (pitch rows bytes), col_scale
+ *            mx_scale_bytes(cols, rows) bytes. Needs rows % 32 == 0.
+ *   Column copy, grouped (group_offsets != NULL): group e is rows
+ *            [off[e], off[e+1]) of x (int64 device array of n_groups+1 entries,
+ *            off[0] = 0, non-decreasing, off[n_groups] = rows). 32x1 blocks
+ *            restart at each group's first row; group e's segment is padded
+ *            with zero codes to a multiple of 128 and starts at column
+ *            poff[e] = sum_{i<e} ceil(m_i/128)*128 of col_data [cols, col_capacity]
+ *            (pitch col_capacity bytes). col_scale holds
+ *            mx_scale_bytes(cols, col_capacity) bytes. col_capacity must be a
+ *            multiple of 128 and >= the padded total; columns beyond the padded
+ *            total are not written. Bad offsets or too small a capacity are
+ *            reported as MX_ERR_DEVICE_CHECK through dev_status and nothing is
+ *            written. The row copy is unaffected by groups.
+ *   All outputs 16-byte aligned. Unused outputs may be NULL.
+ */
+mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int axis,
+                      void* row_data, void* row_scale, void* col_data, void* col_scale,
+                      const int64_t* group_offsets, int n_groups, int64_t col_capacity,
+                      int* dev_status, void* stream);
+
+/*
+ * mx_gemm - block-scaled GEMM C[M,N] = A[M,K] . B[N,K]^T with FP32 accumulation
+ * and BF16 output rounded to nearest even ([DSV3] §8 and §13.4
+ * low_precision_matmul; [TT] npu_quant_matmul; [FMT] §五.1).
+ *
+ *   mode     MX_FPROP (a, b row copies), MX_DGRAD (a row, b col copy) or
+ *            MX_WGRAD (a, b col copies); a mismatch is MX_ERR_INVALID_ARG.
+ *   a, b     operands (host pointers to the structs); M = a->rows,
+ *            N = b->rows, K = a->k = b->k, K % 32 == 0. K == 0 writes zeros.
+ *   c        BF16 [M, N], row pitch ldc elements (ldc >= N), 2-byte aligned.
+ *            With c 16-byte aligned and ldc % 8 == 0 the epilogue uses
+ *            16-byte stores; otherwise element stores.
+ * Deterministic: no split-K and no atomics, so repeated calls give identical bits.
+ */
+mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,
+                  int* dev_status, void* stream);
+
+/*
+ * mx_grouped_gemm - per-expert block-scaled GEMMs over contiguous token ranges
+ * ([DSV3] §5.2 routed experts and §13.4 low_precision_grouped_matmul with
+ * group_list; [TT] npu_grouped_matmul). group_offsets is the int64 device array
+ * described for mx_quantize. Empty and uneven groups are allowed ([DSV3] §16.3).
+ *
+ *   MX_FPROP / MX_DGRAD (rows ragged): a = [M_total, K] row copy whose rows are
+ *     grouped by expert; b = stacked per-expert copies: expert e's rows start at
+ *     b->data + e*b->rows*ld and its scales at b->scale + e*mx_scale_bytes(b->rows, K);
+ *     c = [M_total, N] (pitch ldc). Rows of group e use expert e's weights.
+ *   MX_WGRAD (contraction ragged): a = grouped column copy of dY [N, cap],
+ *     b = grouped column copy of X [Kout, cap] (both from mx_quantize with the
+ *     same offsets and cap = a->k = b->k); c = [n_groups, N, Kout] with row
+ *     pitch ldc and expert stride N*ldc. An empty group writes exact zeros.
+ */
+mx_status mx_grouped_gemm(int mode, const mx_operand* a, const mx_operand* b,
+                          const int64_t* group_offsets, int n_groups, void* c, int64_t ldc,
+                          int* dev_status, void* stream);
+
+/* Static description of a status code. */
+const char* mx_status_string(mx_status s);
+
+/* Message of the last MX_ERR_CUDA / validation failure on this host thread. */
+const char* mx_last_error(void);
+
+/* MXFP8_ABI_VERSION of the loaded library. */
+int mx_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_GB300_H */

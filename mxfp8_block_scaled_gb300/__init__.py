@@ -1,0 +1,266 @@
+"""Python binding of the MXFP8 C-ABI library (include/mxfp8.h).
+
+Argument marshalling only: every step of quantisation and GEMM runs in the
+library's sm_103a kernels. PyTorch supplies device memory and streams. If the
+shared library has not been built, importing the binding's functions raises;
+there is no fallback path.
+
+The raw entry points keep the C names (``mx_quantize``, ``mx_gemm``,
+``mx_grouped_gemm``, ``mx_scale_bytes``, ``mx_grouped_padded_rows``,
+``mx_status_string``, ``mx_last_error``, ``mx_abi_version``) and take integer
+device pointers. ``quantize`` / ``gemm`` / ``grouped_gemm`` wrap them for
+torch tensors, allocating outputs with torch.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmxfp8_gb300.so")
+
+MX_ROWWISE, MX_COLWISE, MX_BOTH = 1, 2, 3
+MX_FPROP, MX_DGRAD, MX_WGRAD = 0, 1, 2
+STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAPE", 3: "MX_ERR_ALIGNMENT",
+                4: "MX_ERR_CUDA", 5: "MX_ERR_DEVICE_CHECK", 6: "MX_ERR_TIMEOUT", 7: "MX_ERR_NO_DEVICE"}
+
+# Symbols the header declares (the CPU tests check the library exports them).
+EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_gemm", "mx_grouped_gemm",
+            "mx_status_string", "mx_last_error", "mx_abi_version")
+
+
+class MXError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+class MXOperandC(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("k", ctypes.c_int64), ("ld", ctypes.c_int64), ("orient", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m mxfp8_block_scaled_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.mx_scale_bytes.argtypes = [i64, i64]
+    L.mx_scale_bytes.restype = ctypes.c_size_t
+    L.mx_grouped_padded_rows.argtypes = [ctypes.POINTER(ctypes.c_int64), i32]
+    L.mx_grouped_padded_rows.restype = i64
+    L.mx_quantize.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, vp, i32, i64, vp, vp]
+    L.mx_quantize.restype = i32
+    L.mx_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp, vp]
+    L.mx_gemm.restype = i32
+    L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
+                                  vp, vp]
+    L.mx_grouped_gemm.restype = i32
+    L.mx_status_string.argtypes = [i32]
+    L.mx_status_string.restype = ctypes.c_char_p
+    L.mx_last_error.argtypes = []
+    L.mx_last_error.restype = ctypes.c_char_p
+    L.mx_abi_version.argtypes = []
+    L.mx_abi_version.restype = i32
+    _lib = L
+    return L
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise MXError(status, where, lib().mx_last_error().decode(errors="replace"))
+
+
+# ---------------------------------------------------------------------------
+# Raw entry points (same names as the C ABI; integer device pointers)
+# ---------------------------------------------------------------------------
+
+def mx_scale_bytes(rows: int, k: int) -> int:
+    return int(lib().mx_scale_bytes(rows, k))
+
+
+def mx_grouped_padded_rows(host_offsets) -> int:
+    offs = [int(v) for v in host_offsets]
+    arr = (ctypes.c_int64 * len(offs))(*offs)
+    return int(lib().mx_grouped_padded_rows(arr, len(offs) - 1))
+
+
+def mx_status_string(status: int) -> str:
+    return lib().mx_status_string(status).decode()
+
+
+def mx_last_error() -> str:
+    return lib().mx_last_error().decode(errors="replace")
+
+
+def mx_abi_version() -> int:
+    return int(lib().mx_abi_version())
+
+
+def mx_quantize(x, rows, cols, ldx, axis, row_data, row_scale, col_data, col_scale, group_offsets, n_groups,
+                col_capacity, dev_status, stream) -> None:
+    _check(lib().mx_quantize(x, rows, cols, ldx, axis, row_data, row_scale, col_data, col_scale, group_offsets,
+                             n_groups, col_capacity, dev_status, stream), "mx_quantize")
+
+
+def _ref(op):
+    return None if op is None else ctypes.byref(op)
+
+
+def mx_gemm(mode, a: MXOperandC, b: MXOperandC, c, ldc, dev_status, stream) -> None:
+    _check(lib().mx_gemm(mode, _ref(a), _ref(b), c, ldc, dev_status, stream), "mx_gemm")
+
+
+def mx_grouped_gemm(mode, a: MXOperandC, b: MXOperandC, group_offsets, n_groups, c, ldc, dev_status,
+                    stream) -> None:
+    _check(lib().mx_grouped_gemm(mode, _ref(a), _ref(b), group_offsets, n_groups, c, ldc,
+                                 dev_status, stream), "mx_grouped_gemm")
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor wrappers
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclass
+class MXTensor:
+    """One quantised copy ([rows, k] E4M3 codes + swizzled E8M0 scales)."""
+    data: "object"      # torch.uint8 [rows, ld]
+    scale: "object"     # torch.uint8 [mx_scale_bytes(rows, k)]
+    rows: int
+    k: int
+    orient: int         # MX_ROWWISE or MX_COLWISE
+
+    def c_operand(self) -> MXOperandC:
+        return MXOperandC(self.data.data_ptr(), self.scale.data_ptr(), self.rows, self.k,
+                          int(self.data.stride(0)), self.orient, 0)
+
+
+def new_status(device=None):
+    """A zeroed device int32 for the kernels' device-side status."""
+    torch = _torch()
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_status(status) -> int:
+    return int(status.item())
+
+
+def quantize(x, axis: int = MX_BOTH, group_offsets=None, col_capacity: Optional[int] = None, status=None,
+             stream=None):
+    """MX-quantise a 2-D BF16 CUDA tensor. Returns (row_copy, col_copy), each an
+    MXTensor or None. With ``group_offsets`` (int64 CUDA tensor [E+1]) the
+    column copy is per-group padded with width ``col_capacity``."""
+    torch = _torch()
+    assert x.dim() == 2 and x.dtype == torch.bfloat16 and x.is_cuda and x.stride(1) == 1
+    R, C = x.shape
+    dev = x.device
+    row = col = None
+    if axis & MX_ROWWISE:
+        row = MXTensor(torch.empty((R, C), dtype=torch.uint8, device=dev),
+                       torch.empty(mx_scale_bytes(R, C), dtype=torch.uint8, device=dev), R, C, MX_ROWWISE)
+    n_groups = 0
+    cap = 0
+    if axis & MX_COLWISE:
+        if group_offsets is not None:
+            n_groups = group_offsets.numel() - 1
+            cap = int(col_capacity) if col_capacity is not None else ((R + 127 * n_groups + 127) // 128) * 128
+            col = MXTensor(torch.empty((C, cap), dtype=torch.uint8, device=dev),
+                           torch.empty(mx_scale_bytes(C, cap), dtype=torch.uint8, device=dev), C, cap, MX_COLWISE)
+        else:
+            col = MXTensor(torch.empty((C, R), dtype=torch.uint8, device=dev),
+                           torch.empty(mx_scale_bytes(C, R), dtype=torch.uint8, device=dev), C, R, MX_COLWISE)
+    mx_quantize(x.data_ptr(), R, C, x.stride(0), axis,
+                _ptr(row.data) if row else None, _ptr(row.scale) if row else None,
+                _ptr(col.data) if col else None, _ptr(col.scale) if col else None,
+                _ptr(group_offsets), n_groups, cap, _ptr(status), _stream(stream))
+    return row, col
+
+
+def gemm(mode: int, a: MXTensor, b: MXTensor, out=None, status=None, stream=None):
+    """C[M, N] = A . B^T in BF16 (FP32 accumulation)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
+    mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), _ptr(status), _stream(stream))
+    return out
+
+
+@dataclass
+class MXStacked:
+    """Per-expert quantised copies stacked as [E][rows][k] with per-expert
+    scale blocks of mx_scale_bytes(rows, k) bytes."""
+    data: "object"      # torch.uint8 [E, rows, k]
+    scale: "object"     # torch.uint8 [E, mx_scale_bytes(rows, k)]
+    rows: int
+    k: int
+    orient: int
+
+    def c_operand(self) -> MXOperandC:
+        return MXOperandC(self.data.data_ptr(), self.scale.data_ptr(), self.rows, self.k,
+                          int(self.data.stride(1)), self.orient, 0)
+
+
+def quantize_stacked(w, axis: int, status=None, stream=None):
+    """Quantise stacked expert weights w[E, N, K] (BF16) expert by expert.
+    Returns (row_stack [E][N][K], col_stack [E][K][N]); entries None if not asked."""
+    torch = _torch()
+    E, N, K = w.shape
+    dev = w.device
+    row = col = None
+    if axis & MX_ROWWISE:
+        row = MXStacked(torch.empty((E, N, K), dtype=torch.uint8, device=dev),
+                        torch.empty((E, mx_scale_bytes(N, K)), dtype=torch.uint8, device=dev), N, K, MX_ROWWISE)
+    if axis & MX_COLWISE:
+        col = MXStacked(torch.empty((E, K, N), dtype=torch.uint8, device=dev),
+                        torch.empty((E, mx_scale_bytes(K, N)), dtype=torch.uint8, device=dev), K, N, MX_COLWISE)
+    s = _stream(stream)
+    for e in range(E):
+        we = w[e]
+        mx_quantize(we.data_ptr(), N, K, we.stride(0), axis,
+                    _ptr(row.data[e]) if row else None, _ptr(row.scale[e]) if row else None,
+                    _ptr(col.data[e]) if col else None, _ptr(col.scale[e]) if col else None,
+                    None, 0, 0, _ptr(status), s)
+    return row, col
+
+
+def grouped_gemm(mode: int, a, b, group_offsets, out=None, status=None, stream=None):
+    """Grouped GEMM. fprop/dgrad: a MXTensor [M_total, K] (rows grouped by
+    expert), b MXStacked [E][N][K] -> out [M_total, N]. wgrad: a, b grouped
+    column copies (MXTensor [N, cap], [Kout, cap]) -> out [E, N, Kout]."""
+    torch = _torch()
+    E = group_offsets.numel() - 1
+    if out is None:
+        if mode == MX_WGRAD:
+            out = torch.empty((E, a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
+        else:
+            out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
+    ldc = out.stride(-2)
+    mx_grouped_gemm(mode, a.c_operand(), b.c_operand(), group_offsets.data_ptr(), E, out.data_ptr(), ldc,
+                    _ptr(status), _stream(stream))
+    return out

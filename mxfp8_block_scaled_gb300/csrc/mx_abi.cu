@@ -1,0 +1,388 @@
+// mx_abi.cu - the C ABI (include/mxfp8.h): host-side validation, dispatch
+// to the kernels on the caller's stream, status strings. No device memory is
+// allocated here or anywhere else in the library.
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "mx_internal.h"
+
+namespace mx {
+
+namespace {
+thread_local char g_err[512] = "";
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The current device must be an sm_103 part (the kernels are built for sm_103a only).
+mx_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) {
+    set_error("device %d is sm_%d%d; this library runs on sm_103 only", dev, major, minor);
+    return MX_ERR_NO_DEVICE;
+  }
+  return MX_OK;
+}
+
+mx_status check_operand(const mx_operand* o, const char* name) {
+  if (!o) {
+    set_error("%s: null operand", name);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (o->rows < 0 || o->k < 0 || o->ld < 0 || o->reserved != 0) {
+    set_error("%s: negative size or reserved field set", name);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (o->orient != MX_ROWWISE && o->orient != MX_COLWISE) {
+    set_error("%s: orient must be MX_ROWWISE or MX_COLWISE", name);
+    return MX_ERR_INVALID_ARG;
+  }
+  const int64_t ld = o->ld ? o->ld : o->k;
+  if (ld < o->k) {
+    set_error("%s: ld < k", name);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (o->k % 32 != 0) {
+    set_error("%s: k = %lld is not a multiple of 32", name, static_cast<long long>(o->k));
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (o->rows > 0 && o->k > 0) {
+    if (!o->data || !o->scale) {
+      set_error("%s: null data or scale", name);
+      return MX_ERR_INVALID_ARG;
+    }
+    if (!aligned16(o->data) || !aligned16(o->scale) || ld % 16 != 0) {
+      set_error("%s: data/scale must be 16-byte aligned and ld a multiple of 16", name);
+      return MX_ERR_ALIGNMENT;
+    }
+  }
+  return MX_OK;
+}
+
+// fprop (row, row), dgrad (row of dY, col of W), wgrad (col of dY, col of X):
+// the direction table of the design page, §8.
+mx_status check_mode(int mode, const mx_operand* a, const mx_operand* b) {
+  int want_a, want_b;
+  switch (mode) {
+    case MX_FPROP: want_a = MX_ROWWISE; want_b = MX_ROWWISE; break;
+    case MX_DGRAD: want_a = MX_ROWWISE; want_b = MX_COLWISE; break;
+    case MX_WGRAD: want_a = MX_COLWISE; want_b = MX_COLWISE; break;
+    default:
+      set_error("unknown GEMM mode %d", mode);
+      return MX_ERR_INVALID_ARG;
+  }
+  if (a->orient != want_a || b->orient != want_b) {
+    set_error("mode %d needs operand orientations (%d, %d), got (%d, %d)", mode, want_a, want_b, a->orient,
+              b->orient);
+    return MX_ERR_INVALID_ARG;
+  }
+  return MX_OK;
+}
+
+mx_status check_output(void* c, int64_t ldc, int64_t N, int64_t rows) {
+  if (rows > 0 && N > 0) {
+    if (!c) {
+      set_error("null output");
+      return MX_ERR_INVALID_ARG;
+    }
+    if (ldc < N) {
+      set_error("ldc < N");
+      return MX_ERR_INVALID_ARG;
+    }
+    if ((reinterpret_cast<uintptr_t>(c) & 1u) != 0) {
+      set_error("output must be 2-byte aligned (BF16)");
+      return MX_ERR_ALIGNMENT;
+    }
+  }
+  return MX_OK;
+}
+
+mx_status zero_output(void* c, int64_t ldc, int64_t N, int64_t rows, cudaStream_t s) {
+  if (rows == 0 || N == 0) return MX_OK;
+  return cuda_status(cudaMemset2DAsync(c, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(N) * 2,
+                                       static_cast<size_t>(rows), s),
+                     "cudaMemset2DAsync");
+}
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+mx_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MX_OK;
+  set_error("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  return MX_ERR_CUDA;
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("MXFP8_WAIT_TIMEOUT_NS");
+    if (s && *s) {
+      const unsigned long long x = std::strtoull(s, nullptr, 10);
+      if (x > 0) return static_cast<uint64_t>(x);
+    }
+    return static_cast<uint64_t>(2000000000ull);
+  }();
+  return v;
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" {
+
+int mx_abi_version(void) { return MXFP8_ABI_VERSION; }
+
+const char* mx_last_error(void) { return g_err; }
+
+const char* mx_status_string(mx_status s) {
+  switch (s) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG: invalid argument";
+    case MX_ERR_UNSUPPORTED_SHAPE: return "MX_ERR_UNSUPPORTED_SHAPE: unsupported shape";
+    case MX_ERR_ALIGNMENT: return "MX_ERR_ALIGNMENT: pointer or pitch not 16-byte aligned";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA: CUDA call failed";
+    case MX_ERR_DEVICE_CHECK: return "MX_ERR_DEVICE_CHECK: device-side validation failed";
+    case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT: bounded device wait expired";
+    case MX_ERR_NO_DEVICE: return "MX_ERR_NO_DEVICE: current device is not sm_103";
+  }
+  return "unknown mx_status";
+}
+
+size_t mx_scale_bytes(int64_t rows, int64_t k) {
+  if (rows <= 0 || k <= 0) return 0;
+  const int64_t kb = (k + 31) / 32;
+  return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>((kb + 3) / 4 * 4);
+}
+
+int64_t mx_grouped_padded_rows(const int64_t* host_offsets, int n_groups) {
+  if (!host_offsets || n_groups < 0 || host_offsets[0] != 0) return -1;
+  int64_t total = 0;
+  for (int e = 0; e < n_groups; ++e) {
+    const int64_t m = host_offsets[e + 1] - host_offsets[e];
+    if (m < 0) return -1;
+    total += (m + 127) / 128 * 128;
+  }
+  return total;
+}
+
+mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int axis, void* row_data,
+                      void* row_scale, void* col_data, void* col_scale, const int64_t* group_offsets,
+                      int n_groups, int64_t col_capacity, int* dev_status, void* stream) {
+  if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) {
+    set_error("mx_quantize: axis must be MX_ROWWISE, MX_COLWISE or MX_BOTH");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (rows < 0 || cols < 0 || ldx < cols) {
+    set_error("mx_quantize: bad sizes rows=%lld cols=%lld ldx=%lld", static_cast<long long>(rows),
+              static_cast<long long>(cols), static_cast<long long>(ldx));
+    return MX_ERR_INVALID_ARG;
+  }
+  if (rows > 0x7FFFFFFFLL) {
+    set_error("mx_quantize: rows must be < 2^31");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  const bool do_row = (axis & MX_ROWWISE) != 0;
+  const bool do_col = (axis & MX_COLWISE) != 0;
+  const bool grouped = group_offsets != nullptr;
+  if (cols % 32 != 0) {
+    set_error("mx_quantize: cols = %lld is not a multiple of 32", static_cast<long long>(cols));
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (do_col && !grouped && rows % 32 != 0) {
+    set_error("mx_quantize: dense column copy needs rows %% 32 == 0 (rows = %lld)", static_cast<long long>(rows));
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (grouped) {
+    if (!do_col) {
+      set_error("mx_quantize: group offsets only apply to the column copy");
+      return MX_ERR_INVALID_ARG;
+    }
+    if (n_groups < 1) {
+      set_error("mx_quantize: n_groups must be >= 1");
+      return MX_ERR_INVALID_ARG;
+    }
+    if (col_capacity < 0 || col_capacity % 128 != 0) {
+      set_error("mx_quantize: col_capacity must be a non-negative multiple of 128");
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+  }
+  if (rows == 0 || cols == 0) return MX_OK;
+  if (!x || !aligned16(x) || ldx % 8 != 0) {
+    set_error("mx_quantize: x must be non-null, 16-byte aligned, ldx a multiple of 8");
+    return x ? MX_ERR_ALIGNMENT : MX_ERR_INVALID_ARG;
+  }
+  if (do_row && (!row_data || !row_scale)) {
+    set_error("mx_quantize: row copy requested but row_data/row_scale is null");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (do_col && (!col_data || !col_scale)) {
+    set_error("mx_quantize: column copy requested but col_data/col_scale is null");
+    return MX_ERR_INVALID_ARG;
+  }
+  if ((do_row && (!aligned16(row_data) || !aligned16(row_scale))) ||
+      (do_col && (!aligned16(col_data) || !aligned16(col_scale)))) {
+    set_error("mx_quantize: outputs must be 16-byte aligned");
+    return MX_ERR_ALIGNMENT;
+  }
+  if (grouped && col_capacity == 0) {
+    set_error("mx_quantize: col_capacity is 0 but rows > 0");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  mx_status st = check_device();
+  if (st != MX_OK) return st;
+  QuantLaunch q;
+  q.x = x;
+  q.rows = rows;
+  q.cols = cols;
+  q.ldx = ldx;
+  q.row_data = row_data;
+  q.row_scale = row_scale;
+  q.col_data = col_data;
+  q.col_scale = col_scale;
+  q.offsets = group_offsets;
+  q.n_groups = n_groups;
+  q.col_pitch = grouped ? col_capacity : rows;
+  q.dev_status = dev_status;
+  return launch_quantize(q, do_row, do_col, static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,
+                  void* stream) {
+  mx_status st = check_operand(a, "a");
+  if (st != MX_OK) return st;
+  st = check_operand(b, "b");
+  if (st != MX_OK) return st;
+  st = check_mode(mode, a, b);
+  if (st != MX_OK) return st;
+  if (a->k != b->k) {
+    set_error("mx_gemm: a.k (%lld) != b.k (%lld)", static_cast<long long>(a->k), static_cast<long long>(b->k));
+    return MX_ERR_INVALID_ARG;
+  }
+  if (a->rows > 0x7FFFFFFFLL || b->rows > 0x7FFFFFFFLL || a->k > 0x7FFFFFFFLL) {
+    set_error("mx_gemm: sizes must be < 2^31");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  st = check_output(c, ldc, b->rows, a->rows);
+  if (st != MX_OK) return st;
+  if (a->rows == 0 || b->rows == 0) return MX_OK;
+  st = check_device();
+  if (st != MX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->k == 0) return zero_output(c, ldc, b->rows, a->rows, s);
+  GemmLaunch L;
+  L.kind = GEMM_DENSE;
+  L.a_data = a->data;
+  L.a_scale = a->scale;
+  L.a_ld = a->ld ? a->ld : a->k;
+  L.b_data = b->data;
+  L.b_scale = b->scale;
+  L.b_ld = b->ld ? b->ld : b->k;
+  L.M = a->rows;
+  L.N = b->rows;
+  L.K = a->k;
+  L.b_rows_total = b->rows;
+  L.c = c;
+  L.ldc = ldc;
+  L.offsets = nullptr;
+  L.n_groups = 0;
+  L.dev_status = dev_status;
+  return launch_gemm(L, s);
+}
+
+mx_status mx_grouped_gemm(int mode, const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                          int n_groups, void* c, int64_t ldc, int* dev_status, void* stream) {
+  mx_status st = check_operand(a, "a");
+  if (st != MX_OK) return st;
+  st = check_operand(b, "b");
+  if (st != MX_OK) return st;
+  st = check_mode(mode, a, b);
+  if (st != MX_OK) return st;
+  if (!group_offsets || n_groups < 1) {
+    set_error("mx_grouped_gemm: group_offsets must be non-null and n_groups >= 1");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (a->k != b->k) {
+    set_error("mx_grouped_gemm: a.k != b.k");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (a->rows > 0x7FFFFFFFLL || b->rows > 0x7FFFFFFFLL || a->k > 0x7FFFFFFFLL) {
+    set_error("mx_grouped_gemm: sizes must be < 2^31");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemmLaunch L;
+  L.a_data = a->data;
+  L.a_scale = a->scale;
+  L.a_ld = a->ld ? a->ld : a->k;
+  L.b_data = b->data;
+  L.b_scale = b->scale;
+  L.b_ld = b->ld ? b->ld : b->k;
+  L.K = a->k;
+  L.c = c;
+  L.ldc = ldc;
+  L.offsets = group_offsets;
+  L.n_groups = n_groups;
+  L.dev_status = dev_status;
+  if (mode == MX_WGRAD) {
+    // c = [E, N, Kout]: N = a.rows (dY columns), Kout = b.rows (X columns).
+    if (a->k % 128 != 0) {
+      set_error("mx_grouped_gemm: wgrad capacity (a.k) must be a multiple of 128");
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+    st = check_output(c, ldc, b->rows, a->rows * static_cast<int64_t>(n_groups));
+    if (st != MX_OK) return st;
+    if (a->rows == 0 || b->rows == 0) return MX_OK;
+    st = check_device();
+    if (st != MX_OK) return st;
+    if (a->k == 0) return zero_output(c, ldc, b->rows, a->rows * static_cast<int64_t>(n_groups), s);
+    L.kind = GEMM_GROUPED_K;
+    L.M = a->rows;
+    L.N = b->rows;
+    L.b_rows_total = b->rows;
+  } else {
+    // a = [M_total, K] tokens grouped by expert; b = [E][N][K] stacked weights.
+    st = check_output(c, ldc, b->rows, a->rows);
+    if (st != MX_OK) return st;
+    if (a->rows == 0 || b->rows == 0) return MX_OK;
+    st = check_device();
+    if (st != MX_OK) return st;
+    if (a->k == 0) return zero_output(c, ldc, b->rows, a->rows, s);
+    L.kind = GEMM_GROUPED_M;
+    L.M = a->rows;
+    L.N = b->rows;
+    L.b_rows_total = b->rows * static_cast<int64_t>(n_groups);
+  }
+  return launch_gemm(L, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,635 @@
+// mx_gemm.cu - block-scaled MXFP8 GEMM and grouped GEMM on the sm_103a
+// tensor cores (tcgen05.mma kind::mxf8f6f4 with UE8M0 block scales).
+//
+// Computes C[M, N] = A[M, K] . B[N, K]^T with both operands K-major E4M3
+// codes and one E8M0 scale per 32 elements along K, FP32 accumulation in
+// tensor memory and a BF16 round-to-nearest-even epilogue. This is the GEMM of
+// the direction table in "DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §8
+// (fprop / dgrad / wgrad all reduce to A . B^T once column copies are stored
+// transposed) and of §5.2 / §13.4 for the routed experts (grouped GEMM over
+// group_list offsets); FP32 accumulation with BF16 output follows
+// "浮点格式、数值稳定性与混合精度" §五.1. The block scales vary along K, so
+// they are applied inside the accumulation (by the MMA itself, per 32-K step),
+// not in the epilogue (same page, §七.3).
+//
+// Kernel structure (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A and B tiles (128-byte swizzled boxes of 128 K
+//               elements) and the 512-byte scale atoms of each K block into a
+//               ring of shared-memory stages, completion on mbarriers.
+//   warp 1      allocates tensor memory; lane 0 issues, per K block, two-plus
+//               tcgen05.cp of the scale atoms into TMEM and four K=32 MMAs
+//               (scale byte selector = K step), then commits the stage back to
+//               the producer; after the last K block it commits the
+//               accumulator to the epilogue.
+//   warps 2-9   epilogue: wait for the accumulator, pull the tile out of TMEM
+//               with tcgen05.ld, release the accumulator at once (the next
+//               tile's MMAs start while this tile is still being stored),
+//               convert to BF16 and store.
+// Every mbarrier wait is bounded in wall time; on expiry the CTA records
+// MX_ERR_TIMEOUT in dev_status, drains its own copies and MMAs, frees its
+// tensor memory and returns.
+//
+// Grouped variants: rows-ragged (fprop/dgrad over contiguous token ranges per
+// expert; A tiles start at arbitrary rows, so the producer warp gathers their
+// scale atoms with plain loads) and contraction-ragged (wgrad; per-expert K
+// segments padded to 128, one output matrix per expert, experts with most K
+// scheduled first; an empty expert writes zeros).
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <algorithm>
+#include <mutex>
+
+#include "mx_internal.h"
+#include "mx_ptx.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int kBM = 128;       // tile rows (MMA M)
+constexpr int kBK = 128;       // K elements (= bytes) per stage: four K=32 MMAs
+constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kEpiThreads = 256;
+constexpr int kMaxGroups = 1024;
+constexpr uint32_t kTmemCols = 512;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kAcc = (BN == 256) ? 1 : 2;
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kSfbAtoms = BN / 128;
+  static constexpr int kSfbBytes = kSfbAtoms * 512;
+  static constexpr int kSfCols = 4 + BN / 32;           // TMEM columns of one stage's scales
+  static constexpr uint32_t kSfCol0 = kAcc * BN;        // first scale column
+  static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
+  static constexpr int kGroupBytes = 3 * (kMaxGroups + 1) * 4;
+  __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
+    return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + 512 + kSfbBytes) + kBarBytes +
+           (grouped ? kGroupBytes : 0);
+  }
+};
+
+struct GParams {
+  const uint8_t* a_scale;
+  const uint8_t* b_scale;
+  int64_t M, N, K;
+  int64_t ka;             // scale-column atoms along K: ceil(K/128)
+  int64_t a_ra;           // row atoms of A's scales
+  int64_t b_ra;           // row atoms of B's scales (per expert when grouped by rows)
+  int64_t b_rows_group;   // rows of one expert's B (grouped by rows)
+  int64_t b_scale_stride; // bytes of one expert's B scales (grouped by rows)
+  __nv_bfloat16* c;
+  int64_t ldc;
+  int64_t c_group_stride; // elements between experts' outputs (grouped by K)
+  int32_t c_vec;          // 1: every output row start is 16-byte aligned (16-byte stores)
+  const int64_t* offsets;
+  int n_groups;
+  int* dev_status;
+  uint64_t timeout_ns;
+};
+
+struct Tile {
+  int64_t m0, n0;      // output tile origin within the (per-expert) C
+  int64_t a_row;       // first row of A to load
+  int64_t b_row;       // first row of B's 2-D view to load
+  int64_t k_atom0;     // first 128-K block of the contraction
+  int32_t nkb;         // number of 128-K blocks
+  int32_t valid_m;     // rows of the tile that exist
+  int32_t group;       // expert (grouped kinds)
+  const uint8_t* sfb;  // base of B's scales for this tile's expert
+  __nv_bfloat16* cbase;  // C element (m0, n0)
+};
+
+struct GroupInfo {
+  int32_t* off;    // [E+1] row offsets
+  int32_t* tile;   // [E+1] rows-ragged: m-tile prefix; K-ragged: padded 128-block prefix
+  int32_t* order;  // [E] K-ragged: experts by decreasing K
+  int32_t total;   // rows-ragged: sum of m-tiles; K-ragged: sum of padded blocks
+};
+
+__device__ __forceinline__ int32_t last_le(const int32_t* v, int n, int32_t x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (v[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int BN, int KIND>
+__device__ __forceinline__ int64_t num_tiles(const GParams& p, const GroupInfo& g) {
+  const int64_t nt = (p.N + BN - 1) / BN;
+  const int64_t mt = (p.M + kBM - 1) / kBM;
+  if (KIND == GEMM_DENSE) return mt * nt;
+  if (KIND == GEMM_GROUPED_M) return static_cast<int64_t>(g.total) * nt;
+  return static_cast<int64_t>(p.n_groups) * mt * nt;
+}
+
+template <int BN, int KIND>
+__device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, int64_t t) {
+  Tile ti;
+  const int64_t nt = (p.N + BN - 1) / BN;
+  const int64_t mt = (p.M + kBM - 1) / kBM;
+  if (KIND == GEMM_DENSE) {
+    const int64_t mb = t % mt, nb = t / mt;
+    ti.m0 = mb * kBM;
+    ti.n0 = nb * BN;
+    ti.a_row = ti.m0;
+    ti.b_row = ti.n0;
+    ti.k_atom0 = 0;
+    ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
+    ti.valid_m = static_cast<int32_t>(min64(kBM, p.M - ti.m0));
+    ti.group = 0;
+    ti.sfb = p.b_scale;
+    ti.cbase = p.c + ti.m0 * p.ldc + ti.n0;
+  } else if (KIND == GEMM_GROUPED_M) {
+    const int64_t T = g.total;
+    const int32_t u = static_cast<int32_t>(t % T);
+    const int64_t nb = t / T;
+    const int e = last_le(g.tile, p.n_groups, u);
+    ti.m0 = static_cast<int64_t>(g.off[e]) + static_cast<int64_t>(u - g.tile[e]) * kBM;
+    ti.n0 = nb * BN;
+    ti.a_row = ti.m0;
+    ti.b_row = static_cast<int64_t>(e) * p.b_rows_group + ti.n0;
+    ti.k_atom0 = 0;
+    ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
+    ti.valid_m = static_cast<int32_t>(min64(kBM, g.off[e + 1] - ti.m0));
+    ti.group = e;
+    ti.sfb = p.b_scale + static_cast<int64_t>(e) * p.b_scale_stride;
+    ti.cbase = p.c + ti.m0 * p.ldc + ti.n0;
+  } else {
+    const int64_t per = mt * nt;
+    const int e = g.order[t / per];
+    const int64_t rem = t % per;
+    const int64_t mb = rem % mt, nb = rem / mt;
+    ti.m0 = mb * kBM;
+    ti.n0 = nb * BN;
+    ti.a_row = ti.m0;
+    ti.b_row = ti.n0;
+    ti.k_atom0 = g.tile[e];
+    ti.nkb = g.tile[e + 1] - g.tile[e];
+    ti.valid_m = static_cast<int32_t>(min64(kBM, p.M - ti.m0));
+    ti.group = e;
+    ti.sfb = p.b_scale;
+    ti.cbase = p.c + static_cast<int64_t>(e) * p.c_group_stride + ti.m0 * p.ldc + ti.n0;
+  }
+  return ti;
+}
+
+// Loads and checks the group offsets into shared memory; every thread calls.
+// Returns false (after recording MX_ERR_DEVICE_CHECK) if they are invalid.
+template <int KIND>
+__device__ bool setup_groups(const GParams& p, GroupInfo& g, int32_t* s_flag, int32_t* s_total) {
+  const int tid = threadIdx.x;
+  const int E = p.n_groups;
+  if (tid == 0) *s_flag = 0;
+  __syncthreads();
+  const int64_t rows_total = (KIND == GEMM_GROUPED_M) ? p.M : -1;
+  for (int e = tid; e <= E; e += blockDim.x) {
+    const int64_t o = p.offsets[e];
+    bool bad = (o < 0) || (o > 0x7FFFFFFFLL) || (e == 0 && o != 0);
+    if (e == E && rows_total >= 0 && o != rows_total) bad = true;
+    if (e > 0 && o < p.offsets[e - 1]) bad = true;
+    g.off[e] = static_cast<int32_t>(o);
+    if (bad) *s_flag = 1;
+  }
+  __syncthreads();
+  if (*s_flag == 0) {
+    if (tid == 0) {
+      // Serial prefix: E <= 1024 small integers, once per CTA.
+      int32_t run = 0;
+      for (int e = 0; e < E; ++e) {
+        const int32_t m = g.off[e + 1] - g.off[e];
+        g.tile[e] = run;
+        run += (m + 127) / 128;
+      }
+      g.tile[E] = run;
+      *s_total = run;
+      if (KIND == GEMM_GROUPED_K && static_cast<int64_t>(run) * 128 > p.K) *s_flag = 1;
+    }
+    __syncthreads();
+    if (KIND == GEMM_GROUPED_K && *s_flag == 0) {
+      // Experts ordered by decreasing K length (ties by index): rank sort.
+      for (int e = tid; e < E; e += blockDim.x) {
+        const int32_t me = g.tile[e + 1] - g.tile[e];
+        int32_t rank = 0;
+        for (int f = 0; f < E; ++f) {
+          const int32_t mf = g.tile[f + 1] - g.tile[f];
+          rank += (mf > me) || (mf == me && f < e);
+        }
+        g.order[rank] = e;
+      }
+    }
+  }
+  __syncthreads();
+  g.total = *s_total;
+  if (*s_flag != 0) {
+    if (tid == 0 && blockIdx.x == 0 && p.dev_status) atomicExch(p.dev_status, static_cast<int>(MX_ERR_DEVICE_CHECK));
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void record_timeout(const GParams& p, volatile int32_t* abort_flag) {
+  *abort_flag = 1;
+  if (p.dev_status) atomicExch(p.dev_status, static_cast<int>(MX_ERR_TIMEOUT));
+}
+
+// Bounded wait that also gives up once another role of the CTA has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const GParams& p,
+                                              volatile int32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > p.timeout_ns) {
+      record_timeout(p, abort_flag);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int BN, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   const GParams p) {
+  using C = Cfg<BN>;
+  constexpr int S = C::kStages;
+  constexpr int ACC = C::kAcc;
+  constexpr bool kGatherSfa = (KIND == GEMM_GROUPED_M);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * C::kABytes;
+  uint8_t* sSfa = sB + S * C::kBBytes;
+  uint8_t* sSfb = sSfa + S * 512;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sSfb + S * C::kSfbBytes);
+  uint64_t* empty_bar = full_bar + S;
+  uint64_t* acc_full = empty_bar + S;
+  uint64_t* acc_empty = acc_full + ACC;
+  uint64_t* drain_bar = acc_empty + ACC;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(s_tmem + 1);
+  int32_t* s_flag = reinterpret_cast<int32_t*>(s_tmem + 2);
+  int32_t* s_total = reinterpret_cast<int32_t*>(s_tmem + 3);
+  GroupInfo g;
+  g.off = reinterpret_cast<int32_t*>(smem + C::smem_bytes(false) - 1024);
+  g.tile = g.off + (kMaxGroups + 1);
+  g.order = g.tile + (kMaxGroups + 1);
+  g.total = 0;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (KIND != GEMM_DENSE) {
+    if (!setup_groups<KIND>(p, g, s_flag, s_total)) return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kEpiThreads);
+    }
+    mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
+  const int64_t ntiles = num_tiles<BN, KIND>(p, g);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile ti = get_tile<BN, KIND>(p, g, t);
+      const int64_t sfb_row_atom0 = ti.n0 / 128;
+      for (int kb = 0; kb < ti.nkb; ++kb) {
+        uint32_t good = 1;
+        if (lane == 0) good = wait_or_abort(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
+        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        const int64_t katom = ti.k_atom0 + kb;
+        if constexpr (kGatherSfa) {
+          // Scale bytes of A rows m0 .. m0+127 (any start row) into one atom.
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t r = ti.a_row + lane + 32 * q;
+            w[q] = 0u;
+            if (r < p.a_ra * 128)
+              w[q] = __ldg(reinterpret_cast<const uint32_t*>(p.a_scale + (((r >> 7) * p.ka + katom) << 9) +
+                                                              ((r & 31) << 4) + (((r >> 5) & 3) << 2)));
+          }
+          *reinterpret_cast<uint4*>(sSfa + stage * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          uint32_t bytes = C::kABytes + C::kBBytes + (kGatherSfa ? 0 : 512);
+#pragma unroll
+          for (int j = 0; j < C::kSfbAtoms; ++j)
+            if (sfb_row_atom0 + j < p.b_ra) bytes += 512;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          const int32_t kx = static_cast<int32_t>(katom * kBK);
+          tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full_bar[stage], kx, static_cast<int32_t>(ti.a_row));
+          tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full_bar[stage], kx, static_cast<int32_t>(ti.b_row));
+          if constexpr (!kGatherSfa)
+            bulk_load(sSfa + stage * 512, p.a_scale + (((ti.m0 >> 7) * p.ka + katom) << 9), 512, &full_bar[stage]);
+#pragma unroll
+          for (int j = 0; j < C::kSfbAtoms; ++j)
+            if (sfb_row_atom0 + j < p.b_ra)
+              bulk_load(sSfb + stage * C::kSfbBytes + j * 512, ti.sfb + (((sfb_row_atom0 + j) * p.ka + katom) << 9),
+                        512, &full_bar[stage]);
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (*s_abort && lane == 0) {
+      // Let the copies already issued land before the CTA goes away.
+      int st = stage;
+      uint32_t ph = phase;
+      for (int64_t i = 0; i < min64(issued, S); ++i) {
+        if (--st < 0) {
+          st = S - 1;
+          ph ^= 1;
+        }
+        mbar_wait(&full_bar[st], ph, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_mxf8_e4m3(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const Tile ti = get_tile<BN, KIND>(p, g, t);
+        if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1, p, s_abort)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!wait_or_abort(&full_bar[stage], phase, p, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sfa_t = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
+          const uint32_t sfb_t = sfa_t + 4;
+          tc_cp_32x128b_warpx4(sfa_t, sdesc_scale_atom(smem_u32(sSfa + stage * 512)));
+#pragma unroll
+          for (int j = 0; j < C::kSfbAtoms; ++j)
+            tc_cp_32x128b_warpx4(sfb_t + 4 * j, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes + j * 512)));
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::kABytes));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::kBBytes));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // +32 bytes along K inside the 128-byte swizzle atom = +2 in the address field.
+            tc_mma_mxf8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
+                        (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        if (++acc == ACC) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // All copies into and MMAs on tensor memory must finish before it is freed.
+      tc_commit(drain_bar);
+      mbar_wait(drain_bar, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;         // TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;     // which half of the tile's columns
+    constexpr int kCols = BN / 2;
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile ti = get_tile<BN, KIND>(p, g, t);
+      if (!wait_or_abort(&acc_full[acc], acc_phase, p, s_abort)) break;
+      tc_fence_after_sync();
+      uint32_t r[kCols];
+      if (ti.nkb > 0) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(acc * BN + half * kCols);
+#pragma unroll
+        for (int ch = 0; ch < kCols / 32; ++ch) tmem_ld_32x32b_x32(taddr + ch * 32, r + ch * 32);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < kCols; ++i) r[i] = 0u;  // empty contraction: exact zeros
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&acc_empty[acc]);
+      if (++acc == ACC) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+      if (row < ti.valid_m) {
+        const int64_t col0 = ti.n0 + half * kCols;
+        const int64_t ncols = min64(kCols, p.N - col0);
+        __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(row) * p.ldc + half * kCols;
+        if (ncols == kCols && p.c_vec) {
+#pragma unroll
+          for (int j = 0; j < kCols; j += 8) {
+            uint4 o;
+            o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
+            o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+            o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+            o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+            *reinterpret_cast<uint4*>(dst + j) = o;
+          }
+        } else if (ncols > 0) {
+#pragma unroll
+          for (int j = 0; j < kCols; ++j)
+            if (j < ncols) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2-D map over an E4M3 matrix [rows, k] (pitch ld bytes), box 128 K x box_rows,
+// 128-byte swizzle, zero fill outside.
+mx_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return MX_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d) for rows=%lld k=%lld ld=%lld", static_cast<int>(r),
+              static_cast<long long>(rows), static_cast<long long>(k), static_cast<long long>(ld));
+    return MX_ERR_CUDA;
+  }
+  return MX_OK;
+}
+
+template <int BN, int KIND>
+mx_status launch_cfg(const GemmLaunch& L, const GParams& p, int64_t tiles_upper, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  mx_status st = make_map(&ma, L.a_data, L.M, L.K, L.a_ld, kBM);
+  if (st != MX_OK) return st;
+  st = make_map(&mb, L.b_data, L.b_rows_total, L.K, L.b_ld, BN);
+  if (st != MX_OK) return st;
+  const size_t smem = Cfg<BN>::smem_bytes(KIND != GEMM_DENSE);
+  auto kern = mx_gemm_kernel<BN, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(smem)");
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_upper, sm_count()));
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(ma, mb, p);
+  return cuda_status(cudaGetLastError(), "mx_gemm launch");
+}
+
+int choose_bn(const GemmLaunch& L) {
+  static int forced = [] {
+    const char* v = std::getenv("MXFP8_GEMM_BN");
+    return v ? std::atoi(v) : 0;
+  }();
+  if (forced == 128 || forced == 256) return forced;
+  if (L.N <= 128) return 128;
+  const int64_t mt = (L.M + kBM - 1) / kBM;
+  const int64_t tiles256 = mt * ((L.N + 255) / 256);
+  if (L.kind == GEMM_DENSE && tiles256 < sm_count()) return 128;
+  return 256;
+}
+
+}  // namespace
+
+mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
+  if (L.M == 0 || L.N == 0) return MX_OK;
+  if (L.kind != GEMM_DENSE && L.n_groups > kMaxGroups) {
+    set_error("mx_grouped_gemm: at most %d groups", kMaxGroups);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (L.kind == GEMM_GROUPED_K && L.n_groups == 0) return MX_OK;
+  GParams p;
+  p.a_scale = static_cast<const uint8_t*>(L.a_scale);
+  p.b_scale = static_cast<const uint8_t*>(L.b_scale);
+  p.M = L.M;
+  p.N = L.N;
+  p.K = L.K;
+  p.ka = (L.K + 127) / 128;
+  p.a_ra = (L.M + 127) / 128;
+  p.b_rows_group = L.N;
+  p.b_ra = (L.N + 127) / 128;
+  p.b_scale_stride = static_cast<int64_t>(mx_scale_bytes(L.N, L.K));
+  p.c = static_cast<__nv_bfloat16*>(L.c);
+  p.ldc = L.ldc;
+  p.c_group_stride = L.M * L.ldc;
+  p.c_vec = ((reinterpret_cast<uintptr_t>(L.c) & 15u) == 0 && L.ldc % 8 == 0) ? 1 : 0;
+  p.offsets = L.offsets;
+  p.n_groups = L.n_groups;
+  p.dev_status = L.dev_status;
+  p.timeout_ns = wait_timeout_ns();
+
+  const int bn = choose_bn(L);
+  const int64_t mt = (L.M + kBM - 1) / kBM;
+  const int64_t nt = (L.N + bn - 1) / bn;
+  int64_t tiles_upper = mt * nt;
+  if (L.kind == GEMM_GROUPED_M) tiles_upper = (mt + L.n_groups) * nt;
+  if (L.kind == GEMM_GROUPED_K) tiles_upper = static_cast<int64_t>(L.n_groups) * mt * nt;
+
+  switch (L.kind) {
+    case GEMM_DENSE:
+      return bn == 256 ? launch_cfg<256, GEMM_DENSE>(L, p, tiles_upper, s)
+                       : launch_cfg<128, GEMM_DENSE>(L, p, tiles_upper, s);
+    case GEMM_GROUPED_M:
+      return bn == 256 ? launch_cfg<256, GEMM_GROUPED_M>(L, p, tiles_upper, s)
+                       : launch_cfg<128, GEMM_GROUPED_M>(L, p, tiles_upper, s);
+    default:
+      return bn == 256 ? launch_cfg<256, GEMM_GROUPED_K>(L, p, tiles_upper, s)
+                       : launch_cfg<128, GEMM_GROUPED_K>(L, p, tiles_upper, s);
+  }
+}
+
+}  // namespace mx

@@ -1,0 +1,63 @@
+// mx_internal.h - declarations shared by the translation units of the library
+// (host side only; no device code here).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/mxfp8.h"
+
+namespace mx {
+
+// Last error message of this host thread (returned by mx_last_error()).
+void set_error(const char* fmt, ...);
+
+// MX_OK if e == cudaSuccess, else records the message and returns MX_ERR_CUDA.
+mx_status cuda_status(cudaError_t e, const char* what);
+
+// Bounded-wait limit (nanoseconds) for device-side mbarrier waits. Read once
+// from the MXFP8_WAIT_TIMEOUT_NS environment variable (default 2 s).
+uint64_t wait_timeout_ns();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// --- quantiser -------------------------------------------------------------
+struct QuantLaunch {
+  const void* x;
+  int64_t rows, cols, ldx;
+  void* row_data;
+  void* row_scale;
+  void* col_data;
+  void* col_scale;
+  const int64_t* offsets;  // nullptr: dense column copy
+  int n_groups;
+  int64_t col_pitch;       // rows (dense) or the grouped capacity
+  int* dev_status;
+};
+mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s);
+
+// --- GEMM ------------------------------------------------------------------
+enum GemmKind { GEMM_DENSE = 0, GEMM_GROUPED_M = 1, GEMM_GROUPED_K = 2 };
+
+struct GemmLaunch {
+  GemmKind kind;
+  const void* a_data;
+  const void* a_scale;
+  int64_t a_ld;
+  const void* b_data;
+  const void* b_scale;
+  int64_t b_ld;
+  int64_t M;        // rows of C (per group for GROUPED_K)
+  int64_t N;        // columns of C
+  int64_t K;        // contraction length (capacity for GROUPED_K)
+  int64_t b_rows_total;  // rows of the 2-D view of b (E*N for GROUPED_M, else N)
+  void* c;
+  int64_t ldc;
+  const int64_t* offsets;
+  int n_groups;
+  int* dev_status;
+};
+mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
+
+}  // namespace mx

@@ -1,0 +1,369 @@
+// mx_quant.cu - fused single-pass MX quantiser (BF16 -> E4M3 data + E8M0
+// scales) for the row copy (1x32 blocks), the transposed column copy (32x1
+// blocks) and the per-group padded column copy.
+//
+// What is computed follows "DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §3 and
+// §3.1 (E4M3 data, E8M0 scale, 1x32 / 32x1 blocks, row and col copies), §8.1
+// (dynamic quantisation of activations and gradients, dual-axis weights) and
+// "低精度训练特性（MXFP8 / HiFloat8）" (block size 32; per-group quantisation
+// for the grouped wgrad). Scale rule: X = floor(log2 amax) - 8 clamped to
+// [-127, 127], element = E4M3(x * 2**-X) round-to-nearest-even, saturating.
+//
+// Design: one CTA per 128x128 tile of the input, 256 threads. Each thread
+// issues its eight 16-byte loads up front; the row copy is quantised straight
+// from registers (a 1x32 block is four neighbouring lanes: amax by two xor
+// shuffles); the tile is staged in shared memory for the column copy, where
+// each thread owns two adjacent columns of one 32-row block (bank-conflict
+// free 4-byte reads). amax is an unsigned max over the magnitude bits of the
+// BF16 patterns (NaN > Inf > finite), the exponent comes from its bits, and
+// the conversion is the hardware's round-to-nearest-even satfinite E4M3 cvt.
+// Scale bytes are written as whole 32-bit words of the swizzled layout.
+
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mx_internal.h"
+#include "mx_ptx.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int kTileRows = 128;
+constexpr int kTileCols = 128;
+constexpr int kThreads = 256;
+constexpr int kMaxGroups = 1024;
+
+struct QParams {
+  const uint16_t* __restrict__ x;
+  int64_t rows, cols, ldx;
+  uint8_t* __restrict__ row_data;
+  uint8_t* __restrict__ row_scale;
+  uint8_t* __restrict__ col_data;
+  uint8_t* __restrict__ col_scale;
+  const int64_t* __restrict__ offsets;
+  int n_groups;
+  int64_t col_pitch;
+  int64_t row_ka;  // scale-column atoms of the row copy: ceil(cols/128)
+  int64_t col_ka;  // scale-column atoms of the column copy: ceil(col_pitch/128)
+  int* dev_status;
+};
+
+// Byte offset of logical scale (r, kb) in the swizzled layout with `ka`
+// scale-column atoms per 128-row band.
+__device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t kb, int64_t ka) {
+  return (((r >> 7) * ka + (kb >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (kb & 3);
+}
+
+// E8M0 code from the largest BF16 magnitude pattern of a block.
+__device__ __forceinline__ uint32_t scale_code(uint32_t amax_bits) {
+  const int e = static_cast<int>(amax_bits >> 7);  // biased exponent, shared with FP32
+  if (e == 0xFF) return 0xFFu;                     // block holds Inf or NaN
+  const int x = e - 127 - 8;                       // floor(log2 amax) - 8 for normal amax
+  return static_cast<uint32_t>(max(x, -127) + 127);
+}
+
+// 2**-X as an FP32 number (exponent field 254 - code, always normal).
+__device__ __forceinline__ float inv_scale(uint32_t code) { return __uint_as_float((254u - code) << 23); }
+
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two values -> two E4M3 bytes (a in the low byte).
+__device__ __forceinline__ uint32_t cvt_pair(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// NaN codes keeping the sign of the two BF16 halves of w.
+__device__ __forceinline__ uint32_t nan_pair(uint32_t w) {
+  return (0x7Fu | ((w >> 8) & 0x80u)) | ((0x7Fu | ((w >> 24) & 0x80u)) << 8);
+}
+
+// Quantise the two BF16 values of one word (low half -> low byte).
+__device__ __forceinline__ uint32_t quant_word(uint32_t w, float inv, bool nan_block) {
+  return nan_block ? nan_pair(w) : cvt_pair(lo_f(w) * inv, hi_f(w) * inv);
+}
+
+__device__ __forceinline__ uint32_t half_max(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Exclusive scan of v[0, n) (n <= 4 * kThreads) in shared memory; returns the
+// total. Every thread of the block must call it.
+__device__ int32_t block_exclusive_scan(int32_t* v, int n, int32_t* warp_tot) {
+  const int tid = threadIdx.x;
+  int32_t loc[4];
+  int32_t sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = tid * 4 + j;
+    loc[j] = (i < n) ? v[i] : 0;
+    sum += loc[j];
+  }
+  int32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if ((tid & 31) >= o) incl += t;
+  }
+  if ((tid & 31) == 31) warp_tot[tid >> 5] = incl;
+  __syncthreads();
+  int32_t before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int32_t t = warp_tot[w];
+    before += (w < (tid >> 5)) ? t : 0;
+    total += t;
+  }
+  int32_t run = before + incl - sum;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = tid * 4 + j;
+    if (i < n) v[i] = run;
+    run += loc[j];
+  }
+  __syncthreads();
+  return total;
+}
+
+template <bool kRow, bool kCol, bool kGrouped>
+__global__ void __launch_bounds__(kThreads) mx_quant_kernel(QParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* tile = reinterpret_cast<uint32_t*>(smem);                          // [128][64] words
+  uint8_t* col_sc = smem + (kCol ? kTileRows * kTileCols * 2 : 0);             // [128][4]
+  int32_t* g_off = reinterpret_cast<int32_t*>(col_sc + (kCol ? 512 : 0));      // [E+1] row offsets
+  int32_t* g_tile = g_off + (kMaxGroups + 1);                                  // [E+1] padded tile starts
+  __shared__ int32_t warp_tot[kThreads / 32];
+  __shared__ int32_t s_bad;
+  __shared__ int32_t s_total_tiles;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTileCols;
+  const int valid_cols = static_cast<int>(min64(kTileCols, p.cols - c0));
+
+  int64_t row0 = static_cast<int64_t>(blockIdx.y) * kTileRows;  // first input row of the tile
+  int valid_rows = 0;
+  int64_t kpos = row0;                                           // position along the column copy
+
+  if constexpr (kGrouped) {
+    const int E = p.n_groups;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    for (int e = tid; e <= E; e += kThreads) {
+      const int64_t o = p.offsets[e];
+      g_off[e] = static_cast<int32_t>(o);
+      bool bad = (o < 0) || (o > p.rows) || (e == 0 && o != 0) || (e == E && o != p.rows);
+      if (e > 0 && o < p.offsets[e - 1]) bad = true;
+      if (bad) s_bad = 1;
+    }
+    __syncthreads();
+    if (s_bad == 0) {
+      for (int e = tid; e < E; e += kThreads) g_tile[e] = (g_off[e + 1] - g_off[e] + kTileRows - 1) / kTileRows;
+      __syncthreads();
+      const int32_t total = block_exclusive_scan(g_tile, E, warp_tot);
+      if (tid == 0) {
+        g_tile[E] = total;
+        s_total_tiles = total;
+        if (static_cast<int64_t>(total) * kTileRows > p.col_pitch) s_bad = 1;
+      }
+    }
+    __syncthreads();
+    if (s_bad) {
+      if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.dev_status)
+        atomicExch(p.dev_status, static_cast<int>(MX_ERR_DEVICE_CHECK));
+      return;
+    }
+    // Row-scale padding rows [rows, ceil(rows/128)*128) belong to no group tile.
+    if (kRow && blockIdx.y == 0) {
+      const int64_t padded = (p.rows + kTileRows - 1) / kTileRows * kTileRows;
+      for (int64_t r = p.rows + tid; r < padded; r += kThreads)
+        *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(r, c0 >> 5, p.row_ka)) = 0u;
+    }
+    const int32_t tp = static_cast<int32_t>(blockIdx.y);
+    if (tp >= s_total_tiles) return;
+    // Last group e with g_tile[e] <= tp (it is non-empty).
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (g_tile[mid] <= tp) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int lt = tp - g_tile[e];
+    row0 = static_cast<int64_t>(g_off[e]) + static_cast<int64_t>(lt) * kTileRows;
+    valid_rows = min(kTileRows, g_off[e + 1] - g_off[e] - lt * kTileRows);
+    kpos = static_cast<int64_t>(tp) * kTileRows;
+  } else {
+    valid_rows = static_cast<int>(min64(kTileRows, p.rows - row0));
+  }
+
+  // ---- load the tile: 2048 vectors of 8 BF16, eight per thread -----------
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = i * kThreads + tid;
+    const int r = idx >> 4;
+    const int vc = idx & 15;
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < valid_rows && vc * 8 < valid_cols)
+      v[i] = ldg_stream(p.x + (row0 + r) * p.ldx + c0 + vc * 8);
+  }
+
+  // ---- row copy: 1x32 blocks = four neighbouring lanes ---------------------
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = i * kThreads + tid;
+    const int r = idx >> 4;
+    const int vc = idx & 15;
+    if constexpr (kCol) reinterpret_cast<uint4*>(tile)[r * 16 + vc] = v[i];
+    if constexpr (kRow) {
+      uint32_t m = __vmaxu2(__vmaxu2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
+                            __vmaxu2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
+      m = half_max(m);
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      const uint32_t code = scale_code(m);
+      const bool nan_block = (code == 0xFFu);
+      const float inv = inv_scale(nan_block ? 0u : code);
+      uint2 q;
+      q.x = quant_word(v[i].x, inv, nan_block) | (quant_word(v[i].y, inv, nan_block) << 16);
+      q.y = quant_word(v[i].z, inv, nan_block) | (quant_word(v[i].w, inv, nan_block) << 16);
+      const int64_t grow = row0 + r;
+      if (r < valid_rows && vc * 8 < valid_cols)
+        *reinterpret_cast<uint2*>(p.row_data + grow * p.cols + c0 + vc * 8) = q;
+      // Gather the four block codes of this row (lanes 0, 4, 8, 12 of the half-warp).
+      const int base = lane & 16;
+      const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, code, base + 0);
+      const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
+      const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, code, base + 8);
+      const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, code, base + 12);
+      const bool write_scale = kGrouped ? (r < valid_rows) : true;  // dense: padding rows get zeros
+      if ((lane & 15) == 0 && write_scale)
+        *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(grow, c0 >> 5, p.row_ka)) =
+            s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
+  }
+
+  if constexpr (kCol) {
+    __syncthreads();
+    // ---- column copy: thread = (column pair cp, 32-row block rb) ----------
+    const int cp = tid & 63;
+    const int rb = tid >> 6;
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = tile[(rb * 32 + i) * 64 + cp];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+    const uint32_t code_lo = scale_code(m & 0xFFFFu);
+    const uint32_t code_hi = scale_code(m >> 16);
+    const bool nan_lo = code_lo == 0xFFu, nan_hi = code_hi == 0xFFu;
+    const float inv_lo = inv_scale(nan_lo ? 0u : code_lo);
+    const float inv_hi = inv_scale(nan_hi ? 0u : code_hi);
+    uint32_t out_lo[8], out_hi[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a = w[4 * j], b = w[4 * j + 1], c = w[4 * j + 2], d = w[4 * j + 3];
+      if (nan_lo) {
+        out_lo[j] = (nan_pair((a & 0xFFFFu) | (b << 16))) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
+      } else {
+        out_lo[j] = cvt_pair(lo_f(a) * inv_lo, lo_f(b) * inv_lo) | (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
+      }
+      if (nan_hi) {
+        out_hi[j] = (nan_pair((a >> 16) | (b & 0xFFFF0000u))) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
+      } else {
+        out_hi[j] = cvt_pair(hi_f(a) * inv_hi, hi_f(b) * inv_hi) | (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
+      }
+    }
+    const int64_t c = c0 + 2 * cp;
+    col_sc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
+    col_sc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
+    const bool block_valid = kGrouped ? true : (rb * 32 < valid_rows);
+    if (block_valid) {
+      const int64_t k = kpos + rb * 32;
+      if (c < p.cols) {
+        uint4* dst = reinterpret_cast<uint4*>(p.col_data + c * p.col_pitch + k);
+        dst[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+        dst[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
+      }
+      if (c + 1 < p.cols) {
+        uint4* dst = reinterpret_cast<uint4*>(p.col_data + (c + 1) * p.col_pitch + k);
+        dst[0] = make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+        dst[1] = make_uint4(out_hi[4], out_hi[5], out_hi[6], out_hi[7]);
+      }
+    }
+    __syncthreads();
+    if (tid < kTileCols) {
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(col_sc + tid * 4);
+      *reinterpret_cast<uint32_t*>(p.col_scale + scale_offset(c0 + tid, kpos >> 5, p.col_ka)) = word;
+    }
+  }
+}
+
+template <bool R, bool C, bool G>
+cudaError_t launch_one(const QParams& p, dim3 grid, cudaStream_t s) {
+  size_t smem = 0;
+  if (C) smem += kTileRows * kTileCols * 2 + 512;
+  if (G) smem += 2 * (kMaxGroups + 1) * sizeof(int32_t);
+  auto kern = mx_quant_kernel<R, C, G>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s) {
+  QParams p;
+  p.x = static_cast<const uint16_t*>(q.x);
+  p.rows = q.rows;
+  p.cols = q.cols;
+  p.ldx = q.ldx;
+  p.row_data = static_cast<uint8_t*>(q.row_data);
+  p.row_scale = static_cast<uint8_t*>(q.row_scale);
+  p.col_data = static_cast<uint8_t*>(q.col_data);
+  p.col_scale = static_cast<uint8_t*>(q.col_scale);
+  p.offsets = q.offsets;
+  p.n_groups = q.n_groups;
+  p.col_pitch = q.col_pitch;
+  p.row_ka = (q.cols + 127) / 128;
+  p.col_ka = (q.col_pitch + 127) / 128;
+  p.dev_status = q.dev_status;
+  const bool grouped = q.offsets != nullptr && do_col;
+  if (grouped && q.n_groups > kMaxGroups) {
+    set_error("mx_quantize: at most %d groups", kMaxGroups);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  const int64_t col_tiles = (q.cols + kTileCols - 1) / kTileCols;
+  int64_t row_tiles = (q.rows + kTileRows - 1) / kTileRows;
+  if (grouped) row_tiles += q.n_groups;  // upper bound of sum ceil(m_e / 128)
+  if (row_tiles == 0 || col_tiles == 0) return MX_OK;
+  if (row_tiles > 65535 || col_tiles > 2147483647LL) {
+    set_error("mx_quantize: too many row tiles (%lld)", static_cast<long long>(row_tiles));
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  dim3 grid(static_cast<unsigned>(col_tiles), static_cast<unsigned>(row_tiles));
+  cudaError_t e;
+  if (grouped) {
+    e = do_row ? launch_one<true, true, true>(p, grid, s) : launch_one<false, true, true>(p, grid, s);
+  } else if (do_row && do_col) {
+    e = launch_one<true, true, false>(p, grid, s);
+  } else if (do_row) {
+    e = launch_one<true, false, false>(p, grid, s);
+  } else {
+    e = launch_one<false, true, false>(p, grid, s);
+  }
+  return cuda_status(e, "mx_quantize launch");
+}
+
+}  // namespace mx

@@ -1,0 +1,143 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports
+every function include/mxfp8.h declares, its pure size helpers agree with
+the oracle's layout, and invalid arguments are rejected on the host before
+any device work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import mxfp8_block_scaled_gb300 as mx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(mx.LIB_PATH):
+        from mxfp8_block_scaled_gb300 import build
+        build.build()
+    return mx.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(mx_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_function(L):
+    names = declared_functions()
+    assert names == set(mx.EXPORTED), names ^ set(mx.EXPORTED)
+    for n in names:
+        assert hasattr(L, n), n
+    out = os.popen(f"nm -D --defined-only {mx.LIB_PATH}").read()
+    for n in names:
+        assert re.search(rf"\bT {n}\b", out), f"{n} not exported"
+
+
+def test_version_and_strings(L):
+    assert mx.mx_abi_version() == 1
+    for code, name in mx.STATUS_NAMES.items():
+        assert mx.mx_status_string(code).startswith(name)
+
+
+@pytest.mark.parametrize("rows,k", [(1, 32), (128, 128), (129, 160), (256, 512), (8192, 2048),
+                                    (10944, 8192), (576, 16384), (7, 7168)])
+def test_scale_bytes_matches_oracle_layout(L, rows, k):
+    assert mx.mx_scale_bytes(rows, k) == oracle.mx_scale_nbytes(rows, k)
+
+
+def test_scale_bytes_degenerate(L):
+    assert mx.mx_scale_bytes(0, 128) == 0 and mx.mx_scale_bytes(128, 0) == 0
+
+
+def test_grouped_padded_rows(L):
+    offs = [0, 20, 20, 170, 171, 299]
+    assert mx.mx_grouped_padded_rows(offs) == int(oracle.mx_padded_offsets(np.array(offs))[-1])
+    assert mx.mx_grouped_padded_rows([0, 5, 3]) == -1
+    assert mx.mx_grouped_padded_rows([1, 5]) == -1
+
+
+def _op(data=0x1000, scale=0x2000, rows=128, k=256, ld=0, orient=mx.MX_ROWWISE):
+    return mx.MXOperandC(data, scale, rows, k, ld, orient, 0)
+
+
+def _status_of(fn, *args):
+    try:
+        fn(*args)
+    except mx.MXError as e:
+        return e.status
+    return 0
+
+
+INVALID, SHAPE, ALIGN = 1, 2, 3
+
+
+def test_gemm_rejects_bad_arguments_on_host(L):
+    c = 0x4000
+    # orientation vs mode (direction table)
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(), _op(orient=mx.MX_COLWISE), c, 128, None, None) == INVALID
+    assert _status_of(mx.mx_gemm, mx.MX_DGRAD, _op(), _op(), c, 128, None, None) == INVALID
+    assert _status_of(mx.mx_gemm, mx.MX_WGRAD, _op(), _op(orient=mx.MX_COLWISE), c, 128, None, None) == INVALID
+    assert _status_of(mx.mx_gemm, 7, _op(), _op(), c, 128, None, None) == INVALID
+    # K not a multiple of 32, mismatched K
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(k=48), _op(k=48), c, 128, None, None) == SHAPE
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(k=64), _op(k=96), c, 128, None, None) == INVALID
+    # alignment of data, scale, ld, output
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(data=0x1008), _op(), c, 128, None, None) == ALIGN
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(scale=0x2004), _op(), c, 128, None, None) == ALIGN
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(ld=264), _op(ld=264), c, 128, None, None) == ALIGN
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(), _op(), 0x4001, 128, None, None) == ALIGN
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(), _op(), c, 100, None, None) == INVALID  # ldc < N
+    # null pointers, negative sizes, ld < k, reserved field
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(data=0), _op(), c, 128, None, None) == INVALID
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(), _op(), 0, 128, None, None) == INVALID
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(rows=-1), _op(), c, 128, None, None) == INVALID
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, _op(ld=128), _op(), c, 128, None, None) == INVALID
+    bad = _op()
+    bad.reserved = 1
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, bad, _op(), c, 128, None, None) == INVALID
+    assert _status_of(mx.mx_gemm, mx.MX_FPROP, None, _op(), c, 128, None, None) != 0
+
+
+def test_grouped_gemm_rejects_bad_arguments_on_host(L):
+    c = 0x4000
+    g = 0x8000
+    assert _status_of(mx.mx_grouped_gemm, mx.MX_FPROP, _op(), _op(), None, 4, c, 128, None, None) == INVALID
+    assert _status_of(mx.mx_grouped_gemm, mx.MX_FPROP, _op(), _op(), g, 0, c, 128, None, None) == INVALID
+    # wgrad needs a capacity that is a multiple of 128
+    a = _op(orient=mx.MX_COLWISE, k=160)
+    assert _status_of(mx.mx_grouped_gemm, mx.MX_WGRAD, a, _op(orient=mx.MX_COLWISE, k=160), g, 2, c, 128,
+                      None, None) == SHAPE
+
+
+def test_quantize_rejects_bad_arguments_on_host(L):
+    x = 0x10000
+    assert _status_of(mx.mx_quantize, x, 64, 64, 64, 0, 0x1000, 0x2000, None, None, None, 0, 0, None, None) == INVALID
+    assert _status_of(mx.mx_quantize, x, 64, 48, 48, 1, 0x1000, 0x2000, None, None, None, 0, 0, None, None) == SHAPE
+    assert _status_of(mx.mx_quantize, x, 48, 64, 64, 2, None, None, 0x1000, 0x2000, None, 0, 0, None, None) == SHAPE
+    assert _status_of(mx.mx_quantize, x + 2, 64, 64, 64, 1, 0x1000, 0x2000, None, None, None, 0, 0, None,
+                      None) == ALIGN
+    assert _status_of(mx.mx_quantize, x, 64, 64, 68, 1, 0x1000, 0x2000, None, None, None, 0, 0, None,
+                      None) == ALIGN
+    assert _status_of(mx.mx_quantize, x, 64, 64, 64, 1, None, 0x2000, None, None, None, 0, 0, None,
+                      None) == INVALID
+    assert _status_of(mx.mx_quantize, x, 64, 64, 32, 1, 0x1000, 0x2000, None, None, None, 0, 0, None,
+                      None) == INVALID
+    # grouped: only for the column copy; capacity multiple of 128; n_groups >= 1
+    assert _status_of(mx.mx_quantize, x, 64, 64, 64, 1, 0x1000, 0x2000, None, None, 0x9000, 2, 128, None,
+                      None) == INVALID
+    assert _status_of(mx.mx_quantize, x, 64, 64, 64, 2, None, None, 0x1000, 0x2000, 0x9000, 2, 100, None,
+                      None) == SHAPE
+    assert _status_of(mx.mx_quantize, x, 64, 64, 64, 2, None, None, 0x1000, 0x2000, 0x9000, 0, 128, None,
+                      None) == INVALID
+    # empty input: nothing to do, OK without touching the device
+    assert _status_of(mx.mx_quantize, 0, 0, 64, 64, 1, None, None, None, None, None, 0, 0, None, None) == 0
