@@ -1,0 +1,448 @@
+"""Benchmark of the MXFP8 hot path on GB300.
+
+One step = one pass of the path over one batch of synthetic inputs:
+MX-quantise X, W and dY (row and column copies, one fused pass each), then the
+fprop, dgrad and wgrad block-scaled GEMMs. Default workload: the dense FFN
+up-projection (tokens M=8192, K=2048, N=10944), DeepSeek-V3 16B shaped.
+Other workloads (--workload mla|moe|quant) print their own line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dense_ffn]
+    python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Timing: CUDA events on the launching stream around exactly K steps, barrier +
+synchronize on both sides, max over ranks. Per-kernel CUDA events inside the
+timed region give the dominant kernel's average launch time for the roofline.
+The inputs and MX copies of a step (~0.7 GB) exceed the 129 MB L2, so no flush
+is done between steps. Multi-GPU: independent replicas (no data-path
+collective); value = work of all ranks / max time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAK_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx_ = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx_) if mx_ else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class Timers:
+    """CUDA events around the launches of one kernel family inside the timed region."""
+
+    def __init__(self):
+        self.pairs = {}
+
+    def span(self, name, stream):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        self.pairs.setdefault(name, []).append((s, e))
+        return e
+
+    def total_ms(self, name):
+        return sum(s.elapsed_time(e) for s, e in self.pairs.get(name, []))
+
+    def count(self, name):
+        return len(self.pairs.get(name, []))
+
+
+class DenseFFN:
+    """fprop Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X with MX copies of X, W, dY."""
+    name = "dense_ffn_up_proj"
+
+    def __init__(self, M=8192, K=2048, N=10944, seed=None):
+        import mxfp8_block_scaled_gb300 as mx
+        self.mx = mx
+        self.M, self.K, self.N = M, K, N
+        d = dense_host_inputs()
+        self.host = {k: d[k].pin_memory() for k in ("X", "W", "dY")}
+        self.dev = {k: v.cuda() for k, v in self.host.items()}
+        self.alloc()
+
+    def alloc(self):
+        mx = self.mx
+        M, K, N = self.M, self.K, self.N
+        u8 = dict(dtype=torch.uint8, device="cuda")
+
+        def copies(R, C):
+            return (mx.MXTensor(torch.empty((R, C), **u8), torch.empty(mx.mx_scale_bytes(R, C), **u8), R, C,
+                                mx.MX_ROWWISE),
+                    mx.MXTensor(torch.empty((C, R), **u8), torch.empty(mx.mx_scale_bytes(C, R), **u8), C, R,
+                                mx.MX_COLWISE))
+        self.q = {"X": copies(M, K), "W": copies(N, K), "dY": copies(M, N)}
+        bf = dict(dtype=torch.bfloat16, device="cuda")
+        self.out = {"Y": torch.empty((M, N), **bf), "dX": torch.empty((M, K), **bf), "dW": torch.empty((N, K), **bf)}
+        self.host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.out.items()}
+
+    def gemm_flops(self):
+        return 2.0 * self.M * self.N * self.K          # identical for the three modes here
+
+    def step_flops(self):
+        return 3 * self.gemm_flops()
+
+    def quant_bytes(self):
+        # algorithmic bytes of one fused both-axes pass: 2 read + 1 + 1 written + 2 * (1/32) scales per element
+        return {k: (2 + 1 + 1 + 2 / 32) * r.rows * r.k for k, (r, _) in self.q.items()}
+
+    def launches_per_step(self):
+        return 6
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+    def d2h_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.out.values())
+
+    def step(self, stream, timers=None):
+        mx = self.mx
+        sp = stream.cuda_stream
+        for k in ("X", "W", "dY"):
+            x = self.dev[k]
+            r, c = self.q[k]
+            e = timers.span("quant", stream) if timers else None
+            mx.mx_quantize(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), mx.MX_BOTH, r.data.data_ptr(),
+                           r.scale.data_ptr(), c.data.data_ptr(), c.scale.data_ptr(), None, 0, 0, None, sp)
+            if e is not None:
+                e.record(stream)
+        (xr, xc), (wr, wc), (dr, dc) = self.q["X"], self.q["W"], self.q["dY"]
+        for mode, a, b, out in ((mx.MX_FPROP, xr, wr, self.out["Y"]), (mx.MX_DGRAD, dr, wc, self.out["dX"]),
+                                (mx.MX_WGRAD, dc, xc, self.out["dW"])):
+            e = timers.span("gemm", stream) if timers else None
+            mx.mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), None, sp)
+            if e is not None:
+                e.record(stream)
+
+    def step_e2e(self, stream):
+        with torch.cuda.stream(stream):
+            for k in self.dev:
+                self.dev[k].copy_(self.host[k], non_blocking=True)
+            self.step(stream)
+            for k in self.out:
+                self.host_out[k].copy_(self.out[k], non_blocking=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+
+_DENSE_HOST = {}
+
+
+def dense_host_inputs():
+    if not _DENSE_HOST:
+        import workloads
+        _DENSE_HOST.update(workloads.dense_ffn(M=8192, K=2048, N=10944))
+    return _DENSE_HOST
+
+
+def oracle_dense_sample(rows: int, cols: int, seed: int = 7):
+    """Time the oracle on a bounded sample of the dense FFN step: for each of
+    fprop/dgrad/wgrad, a [rows x cols] block of outputs, including the oracle
+    quantisation of exactly the operand rows/columns that block reads.
+    Returns (flops_of_sample, seconds)."""
+    import oracle
+    M, K, N = 8192, 2048, 10944
+    d = dense_host_inputs()
+    g = np.random.Generator(np.random.Philox(seed))
+
+    def f64(t):
+        return oracle.bf16_bits_to_float64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+    X, W, dY = d["X"], d["W"], d["dY"]
+    picks = []
+    for (Mg, Ng, Kg) in ((M, N, K), (M, K, N), (N, K, M)):
+        picks.append((np.sort(g.choice(Mg, rows, replace=False)), np.sort(g.choice(Ng, cols, replace=False)), Kg))
+    # slices of the BF16 sources (host copies, not timed)
+    (i0, j0, _), (i1, j1, _), (i2, j2, _) = picks
+    srcs = [(f64(X[torch.from_numpy(i0)]), f64(W[torch.from_numpy(j0)])),
+            (f64(dY[torch.from_numpy(i1)]), f64(W[:, torch.from_numpy(j1)])),
+            (f64(dY[:, torch.from_numpy(i2)]), f64(X[:, torch.from_numpy(j2)]))]
+    t0 = time.perf_counter()
+    a, b = srcs[0]
+    oracle.mx_gemm_ref(*oracle.mx_quantize_rowwise(a), *oracle.mx_quantize_rowwise(b))
+    a, b = srcs[1]
+    oracle.mx_gemm_ref(*oracle.mx_quantize_rowwise(a), *oracle.mx_quantize_colwise(b))
+    a, b = srcs[2]
+    oracle.mx_gemm_ref(*oracle.mx_quantize_colwise(a), *oracle.mx_quantize_colwise(b))
+    dt = time.perf_counter() - t0
+    flops = sum(2.0 * rows * cols * Kg for (_, _, Kg) in picks)
+    return flops, dt
+
+
+def cpu_threads():
+    n = os.cpu_count() or 1
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            n = int(os.environ[v])
+    return n
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def profile_traffic(kernel: str):
+    """DRAM traffic per launch from a committed ncu summary, if it was taken
+    from the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "mxfp8_block_scaled_gb300", "csrc", ent.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return ent.get("bytes_per_launch") if h == ent.get("source_sha256_16") else None
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    rows = cols = 64
+    for _ in range(args.warmup):
+        oracle_dense_sample(rows, cols)
+    t_total = 0.0
+    flops_total = 0.0
+    for s in range(args.steps):
+        fl, dt = oracle_dense_sample(rows, cols, seed=100 + s)
+        t_total += dt
+        flops_total += fl
+    v = flops_total / t_total / 1e12
+    line = {"impl": "reference", "metric": "MXFP8 GEMM TFLOPS (fprop+dgrad+wgrad step, dense FFN up-proj)",
+            "value": v, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * t_total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "dense_ffn_up_proj M=8192 K=2048 N=10944 (fprop+dgrad+wgrad)",
+                       "sample": f"{rows}x{cols} output block per GEMM per step"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"{rows}x{cols} output block of each GEMM per step, with the oracle "
+                                       f"quantisation of the operand rows it reads"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dense_ffn", choices=["dense_ffn"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import mxfp8_block_scaled_gb300 as mx
+    mx.lib()
+    peaks, peak_src = load_peaks()
+    wl = DenseFFN()
+    stream = torch.cuda.Stream()
+
+    for _ in range(args.warmup):
+        wl.step(stream)
+    torch.cuda.synchronize()
+
+    # --- timed region: exactly K steps ---
+    timers = Timers()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        wl.step(stream, timers)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    ms_max = max_over_ranks(ms, world)
+    value = world * args.steps * wl.step_flops() / (ms_max / 1e3) / 1e12
+
+    gemm_ms = timers.total_ms("gemm") / timers.count("gemm")
+    quant_ms = timers.total_ms("quant") / timers.count("quant")
+    achieved = wl.gemm_flops() / (gemm_ms / 1e3) / 1e12
+    peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    qbytes = sum(wl.quant_bytes().values()) / 3
+    q_gbs = qbytes / (quant_ms / 1e3) / 1e9
+
+    # --- end to end: pinned host inputs -> device -> step -> host outputs ---
+    for _ in range(3):
+        wl.step_e2e(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        wl.step_e2e(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = world * args.e2e_steps * wl.step_flops() / (e2e_ms / 1e3) / 1e12
+
+    line = {
+        "metric": "MXFP8 GEMM TFLOPS (fprop+dgrad+wgrad step incl. MX quantisation, dense FFN up-proj)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": "dense_ffn_up_proj M=8192 K=2048 N=10944: quantise X,W,dY (row+col) + "
+                               "fprop + dgrad + wgrad", "M": wl.M, "K": wl.K, "N": wl.N,
+                   "parallelism": f"replicas{world}",
+                   "l2": "no flush: a step reads/writes ~0.7 GB (> 129 MB L2)"},
+        "roofline": {"bound": "tensor", "kernel": "mx_gemm_kernel", "achieved": achieved,
+                     "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
+                     "traffic": profile_traffic("mx_gemm_kernel"),
+                     "peak_source": f"{peak_src} bf16 sustained {peaks['bf16_tflops_sustained']} x nominal fp8/bf16 "
+                                    f"ratio {FP8_OVER_BF16}",
+                     "flops_per_launch": wl.gemm_flops(), "avg_launch_ms": gemm_ms},
+        "quant_roofline": {"bound": "hbm", "kernel": "mx_quant_kernel", "achieved": q_gbs,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": q_gbs / peaks["hbm_gbs"],
+                           "traffic": profile_traffic("mx_quant_kernel"), "bytes_per_launch": qbytes,
+                           "avg_launch_ms": quant_ms, "peak_source": f"{peak_src} hbm_gbs"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": wl.h2d_bytes(),
+                "d2h_bytes_per_step": wl.d2h_bytes(), "steps": args.e2e_steps},
+        "gpu_launches": wl.launches_per_step() * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        fl, dt = oracle_dense_sample(256, 256)
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+                                "kind": "oracle", "seconds": dt,
+                                "sample": "256x256 output block of each of fprop/dgrad/wgrad (dense FFN "
+                                          "up-proj), with the oracle quantisation of the operand rows it reads"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
