@@ -39,9 +39,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
-#include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "mx_internal.h"
@@ -54,8 +55,10 @@ constexpr int kBM = 128;       // tile rows (MMA M)
 constexpr int kBK = 128;       // K elements (= bytes) per stage: four K=32 MMAs
 constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
 constexpr int kEpiThreads = 256;
-constexpr int kMaxGroups = 1024;
+constexpr int kMaxGroups = 512;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kEpiWarpBytes = 32 * 64;  // one 32-row x 32-column BF16 box per epilogue warp
+constexpr int kEpiBytes = 8 * kEpiWarpBytes;
 
 template <int BN>
 struct Cfg {
@@ -71,7 +74,7 @@ struct Cfg {
   static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
   static constexpr int kGroupBytes = 3 * (kMaxGroups + 1) * 4;
   __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
-    return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + 512 + kSfbBytes) + kBarBytes +
+    return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + 512 + kSfbBytes) + kEpiBytes + kBarBytes +
            (grouped ? kGroupBytes : 0);
   }
 };
@@ -89,6 +92,7 @@ struct GParams {
   int64_t ldc;
   int64_t c_group_stride; // elements between experts' outputs (grouped by K)
   int32_t c_vec;          // 1: every output row start is 16-byte aligned (16-byte stores)
+  int32_t c_tma;          // 1: output tiles leave through TMA stores (needs c_vec)
   const int64_t* offsets;
   int n_groups;
   int* dev_status;
@@ -267,7 +271,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <int BN, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   const GParams p) {
+                   const __grid_constant__ CUtensorMap tmap_c, const GParams p) {
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
   constexpr int ACC = C::kAcc;
@@ -279,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = sA + S * C::kABytes;
   uint8_t* sSfa = sB + S * C::kBBytes;
   uint8_t* sSfb = sSfa + S * 512;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sSfb + S * C::kSfbBytes);
+  uint8_t* sEpi = sSfb + S * C::kSfbBytes;  // 1024-aligned: the stage areas are multiples of 1024 bytes
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + kEpiBytes);
   uint64_t* empty_bar = full_bar + S;
   uint64_t* acc_full = empty_bar + S;
   uint64_t* acc_empty = acc_full + ACC;
@@ -478,7 +483,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc = 0;
         acc_phase ^= 1;
       }
-      if (row < ti.valid_m) {
+      const bool tma_tile = p.c_tma && (KIND != GEMM_GROUPED_M || ti.valid_m == kBM);
+      if (tma_tile) {
+        // Stage 32-row x 32-column BF16 boxes in this warp's 64-byte-swizzled
+        // buffer and let TMA write them (rows/columns outside C are clipped).
+        uint8_t* stg = sEpi + (warp - 2) * kEpiWarpBytes;
+        const int32_t y = static_cast<int32_t>(ti.m0 + quarter * 32);
+        const int32_t z = (KIND == GEMM_GROUPED_K) ? ti.group : 0;
+#pragma unroll
+        for (int ch = 0; ch < kCols / 32; ++ch) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int j = ch * 32 + q * 8;
+            uint4 o;
+            o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
+            o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+            o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+            o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+            st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), o);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmap_c, stg, static_cast<int32_t>(ti.n0 + half * kCols + ch * 32), y, z);
+            bulk_commit_group();
+          }
+        }
+      } else if (row < ti.valid_m) {
         const int64_t col0 = ti.n0 + half * kCols;
         const int64_t ncols = min64(kCols, p.N - col0);
         __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(row) * p.ldc + half * kCols;
@@ -499,6 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // Bulk stores must have completed before the CTA's shared memory goes away.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -554,19 +590,49 @@ mx_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, 
   return MX_OK;
 }
 
+// 3-D map over the BF16 output viewed as [groups, rows, N] (row pitch ldc
+// elements, group pitch rows*ldc), box 32 x 32 x 1, 64-byte swizzle: the
+// epilogue's TMA stores clip at N and at each group's last row.
+mx_status make_out_map(CUtensorMap* map, void* c, int64_t groups, int64_t rows, int64_t N, int64_t ldc) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return MX_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(groups)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldc * 2), static_cast<cuuint64_t>(rows * ldc * 2)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (output) failed (%d)", static_cast<int>(r));
+    return MX_ERR_CUDA;
+  }
+  return MX_OK;
+}
+
 template <int BN, int KIND>
-mx_status launch_cfg(const GemmLaunch& L, const GParams& p, int64_t tiles_upper, cudaStream_t s) {
-  CUtensorMap ma, mb;
+mx_status launch_cfg(const GemmLaunch& L, const GParams& p_in, int64_t tiles_upper, cudaStream_t s) {
+  GParams p = p_in;
+  CUtensorMap ma, mb, mc;
   mx_status st = make_map(&ma, L.a_data, L.M, L.K, L.a_ld, kBM);
   if (st != MX_OK) return st;
   st = make_map(&mb, L.b_data, L.b_rows_total, L.K, L.b_ld, BN);
   if (st != MX_OK) return st;
+  std::memset(&mc, 0, sizeof(mc));
+  p.c_tma = 0;
+  if (p.c_vec) {
+    const int64_t groups = (KIND == GEMM_GROUPED_K) ? L.n_groups : 1;
+    if (make_out_map(&mc, L.c, groups, L.M, L.N, L.ldc) == MX_OK) p.c_tma = 1;
+  }
   const size_t smem = Cfg<BN>::smem_bytes(KIND != GEMM_DENSE);
   auto kern = mx_gemm_kernel<BN, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(smem)");
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_upper, sm_count()));
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(ma, mb, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(ma, mb, mc, p);
   return cuda_status(cudaGetLastError(), "mx_gemm launch");
 }
 
@@ -607,6 +673,7 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.ldc = L.ldc;
   p.c_group_stride = L.M * L.ldc;
   p.c_vec = ((reinterpret_cast<uintptr_t>(L.c) & 15u) == 0 && L.ldc % 8 == 0) ? 1 : 0;
+  p.c_tma = 0;
   p.offsets = L.offsets;
   p.n_groups = L.n_groups;
   p.dev_status = L.dev_status;
