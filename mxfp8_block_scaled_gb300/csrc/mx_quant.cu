@@ -9,20 +9,25 @@
 // for the grouped wgrad). Scale rule: X = floor(log2 amax) - 8 clamped to
 // [-127, 127], element = E4M3(x * 2**-X) round-to-nearest-even, saturating.
 //
-// Design: one CTA per 128x128 tile of the input, 256 threads. Each thread
-// issues its eight 16-byte loads up front; the row copy is quantised straight
-// from registers (a 1x32 block is four neighbouring lanes: amax by two xor
-// shuffles); the tile is staged in shared memory for the column copy, where
-// each thread owns two adjacent columns of one 32-row block (bank-conflict
-// free 4-byte reads). amax is an unsigned max over the magnitude bits of the
-// BF16 patterns (NaN > Inf > finite), the exponent comes from its bits, and
+// Design: persistent CTAs (a few per SM) walk 128x128 tiles of the input.
+// Each CTA keeps two 32 KB shared-memory buffers filled by TMA, so the load of
+// its next tile is in flight while the current one is quantised and stored;
+// the input is read from HBM exactly once. Row copy: a 1x32 block is four
+// neighbouring lanes holding 8 values each (amax by two xor shuffles). Column
+// copy: each thread owns two adjacent columns of one 32-row block (4-byte,
+// bank-conflict-free shared loads). amax is an unsigned max over the BF16
+// magnitude bits (NaN > Inf > finite), the exponent comes from its bits, and
 // the conversion is the hardware's round-to-nearest-even satfinite E4M3 cvt.
 // Scale bytes are written as whole 32-bit words of the swizzled layout.
 
+#include <cuda.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
 #include "mx_internal.h"
 #include "mx_ptx.cuh"
@@ -34,10 +39,10 @@ constexpr int kTileRows = 128;
 constexpr int kTileCols = 128;
 constexpr int kThreads = 256;
 constexpr int kMaxGroups = 1024;
+constexpr int kTileBytes = kTileRows * kTileCols * 2;
 
 struct QParams {
-  const uint16_t* __restrict__ x;
-  int64_t rows, cols, ldx;
+  int64_t rows, cols;
   uint8_t* __restrict__ row_data;
   uint8_t* __restrict__ row_scale;
   uint8_t* __restrict__ col_data;
@@ -48,6 +53,7 @@ struct QParams {
   int64_t row_ka;  // scale-column atoms of the row copy: ceil(cols/128)
   int64_t col_ka;  // scale-column atoms of the column copy: ceil(col_pitch/128)
   int* dev_status;
+  uint64_t timeout_ns;
 };
 
 // Byte offset of logical scale (r, kb) in the swizzled layout with `ka`
@@ -87,14 +93,6 @@ __device__ __forceinline__ uint32_t quant_word(uint32_t w, float inv, bool nan_b
 
 __device__ __forceinline__ uint32_t half_max(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Exclusive scan of v[0, n) (n <= 4 * kThreads) in shared memory; returns the
 // total. Every thread of the block must call it.
 __device__ int32_t block_exclusive_scan(int32_t* v, int n, int32_t* warp_tot) {
@@ -133,25 +131,59 @@ __device__ int32_t block_exclusive_scan(int32_t* v, int n, int32_t* warp_tot) {
   return total;
 }
 
+struct TileGeo {
+  int64_t row0;    // first input row
+  int64_t c0;      // first input column
+  int64_t kpos;    // first position along the column copy's contraction
+  int valid_rows;  // input rows of this tile that belong to it
+  int valid_cols;
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ TileGeo tile_geo(const QParams& p, int64_t t, int64_t col_tiles, const int32_t* g_off,
+                                            const int32_t* g_tile) {
+  TileGeo g;
+  const int64_t rt = t / col_tiles;
+  const int64_t ct = t - rt * col_tiles;
+  g.c0 = ct * kTileCols;
+  g.valid_cols = static_cast<int>(min64(kTileCols, p.cols - g.c0));
+  if constexpr (kGrouped) {
+    const int32_t tp = static_cast<int32_t>(rt);
+    int lo = 0, hi = p.n_groups - 1;  // last group e with g_tile[e] <= tp (it is non-empty)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (g_tile[mid] <= tp) lo = mid; else hi = mid - 1;
+    }
+    const int lt = tp - g_tile[lo];
+    g.row0 = static_cast<int64_t>(g_off[lo]) + static_cast<int64_t>(lt) * kTileRows;
+    g.valid_rows = min(kTileRows, g_off[lo + 1] - g_off[lo] - lt * kTileRows);
+    g.kpos = rt * kTileRows;
+  } else {
+    g.row0 = rt * kTileRows;
+    g.valid_rows = static_cast<int>(min64(kTileRows, p.rows - g.row0));
+    g.kpos = g.row0;
+  }
+  return g;
+}
+
 template <bool kRow, bool kCol, bool kGrouped>
-__global__ void __launch_bounds__(kThreads) mx_quant_kernel(QParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint32_t* tile = reinterpret_cast<uint32_t*>(smem);                          // [128][64] words
-  uint8_t* col_sc = smem + (kCol ? kTileRows * kTileCols * 2 : 0);             // [128][4]
-  int32_t* g_off = reinterpret_cast<int32_t*>(col_sc + (kCol ? 512 : 0));      // [E+1] row offsets
-  int32_t* g_tile = g_off + (kMaxGroups + 1);                                  // [E+1] padded tile starts
+__global__ void __launch_bounds__(kThreads) mx_quant_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* buf0 = smem;                                              // two [128][128] BF16 tiles
+  uint8_t* col_sc = smem + 2 * kTileBytes;                           // [128][4] column-copy scales
+  uint64_t* full = reinterpret_cast<uint64_t*>(col_sc + 512);        // [2] tile-loaded barriers
+  int32_t* g_off = reinterpret_cast<int32_t*>(full + 2);             // [E+1] row offsets
+  int32_t* g_tile = g_off + (kMaxGroups + 1);                        // [E+1] padded tile starts
   __shared__ int32_t warp_tot[kThreads / 32];
   __shared__ int32_t s_bad;
   __shared__ int32_t s_total_tiles;
+  __shared__ int32_t s_abort;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTileCols;
-  const int valid_cols = static_cast<int>(min64(kTileCols, p.cols - c0));
-
-  int64_t row0 = static_cast<int64_t>(blockIdx.y) * kTileRows;  // first input row of the tile
-  int valid_rows = 0;
-  int64_t kpos = row0;                                           // position along the column copy
+  const int64_t col_tiles = (p.cols + kTileCols - 1) / kTileCols;
+  int64_t row_tiles = (p.rows + kTileRows - 1) / kTileRows;
 
   if constexpr (kGrouped) {
     const int E = p.n_groups;
@@ -177,158 +209,203 @@ __global__ void __launch_bounds__(kThreads) mx_quant_kernel(QParams p) {
     }
     __syncthreads();
     if (s_bad) {
-      if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.dev_status)
-        atomicExch(p.dev_status, static_cast<int>(MX_ERR_DEVICE_CHECK));
+      if (tid == 0 && blockIdx.x == 0 && p.dev_status) atomicExch(p.dev_status, static_cast<int>(MX_ERR_DEVICE_CHECK));
       return;
     }
+    row_tiles = s_total_tiles;
     // Row-scale padding rows [rows, ceil(rows/128)*128) belong to no group tile.
-    if (kRow && blockIdx.y == 0) {
+    if (kRow) {
       const int64_t padded = (p.rows + kTileRows - 1) / kTileRows * kTileRows;
-      for (int64_t r = p.rows + tid; r < padded; r += kThreads)
-        *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(r, c0 >> 5, p.row_ka)) = 0u;
+      for (int64_t ct = blockIdx.x; ct < col_tiles; ct += gridDim.x)
+        for (int64_t r = p.rows + tid; r < padded; r += kThreads)
+          *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(r, ct * (kTileCols / 32), p.row_ka)) = 0u;
     }
-    const int32_t tp = static_cast<int32_t>(blockIdx.y);
-    if (tp >= s_total_tiles) return;
-    // Last group e with g_tile[e] <= tp (it is non-empty).
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (g_tile[mid] <= tp) lo = mid; else hi = mid - 1;
-    }
-    const int e = lo;
-    const int lt = tp - g_tile[e];
-    row0 = static_cast<int64_t>(g_off[e]) + static_cast<int64_t>(lt) * kTileRows;
-    valid_rows = min(kTileRows, g_off[e + 1] - g_off[e] - lt * kTileRows);
-    kpos = static_cast<int64_t>(tp) * kTileRows;
-  } else {
-    valid_rows = static_cast<int>(min64(kTileRows, p.rows - row0));
   }
 
-  // ---- load the tile: 2048 vectors of 8 BF16, eight per thread -----------
-  uint4 v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int idx = i * kThreads + tid;
-    const int r = idx >> 4;
-    const int vc = idx & 15;
-    v[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (r < valid_rows && vc * 8 < valid_cols)
-      v[i] = ldg_stream(p.x + (row0 + r) * p.ldx + c0 + vc * 8);
+  const int64_t ntiles = row_tiles * col_tiles;
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  int issued0 = 0, issued1 = 0;  // loads issued per buffer (thread 0 only)
+  auto issue = [&](int64_t t, int b) {
+    const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, g_off, g_tile);
+    if (b) ++issued1; else ++issued0;
+    mbar_arrive_expect_tx(&full[b], kTileBytes);
+    tma_load_2d(buf0 + b * kTileBytes, &tmap_x, &full[b], static_cast<int32_t>(g.c0), static_cast<int32_t>(g.row0));
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&tmap_x);
+    for (int b = 0; b < 2; ++b) {
+      const int64_t t = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
+      if (t < ntiles) issue(t, b);
+    }
   }
 
-  // ---- row copy: 1x32 blocks = four neighbouring lanes ---------------------
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int idx = i * kThreads + tid;
-    const int r = idx >> 4;
-    const int vc = idx & 15;
-    if constexpr (kCol) reinterpret_cast<uint4*>(tile)[r * 16 + vc] = v[i];
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    const int b = it & 1;
+    const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, g_off, g_tile);
+    const uint32_t* tile = reinterpret_cast<const uint32_t*>(buf0 + b * kTileBytes);
+    if (!mbar_wait(&full[b], static_cast<uint32_t>((it >> 1) & 1), p.timeout_ns)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) {
+      if (tid == 0 && p.dev_status) atomicExch(p.dev_status, static_cast<int>(MX_ERR_TIMEOUT));
+      break;
+    }
+
     if constexpr (kRow) {
-      uint32_t m = __vmaxu2(__vmaxu2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
-                            __vmaxu2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
-      m = half_max(m);
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      const uint32_t code = scale_code(m);
-      const bool nan_block = (code == 0xFFu);
-      const float inv = inv_scale(nan_block ? 0u : code);
-      uint2 q;
-      q.x = quant_word(v[i].x, inv, nan_block) | (quant_word(v[i].y, inv, nan_block) << 16);
-      q.y = quant_word(v[i].z, inv, nan_block) | (quant_word(v[i].w, inv, nan_block) << 16);
-      const int64_t grow = row0 + r;
-      if (r < valid_rows && vc * 8 < valid_cols)
-        *reinterpret_cast<uint2*>(p.row_data + grow * p.cols + c0 + vc * 8) = q;
-      // Gather the four block codes of this row (lanes 0, 4, 8, 12 of the half-warp).
-      const int base = lane & 16;
-      const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, code, base + 0);
-      const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
-      const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, code, base + 8);
-      const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, code, base + 12);
-      const bool write_scale = kGrouped ? (r < valid_rows) : true;  // dense: padding rows get zeros
-      if ((lane & 15) == 0 && write_scale)
-        *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(grow, c0 >> 5, p.row_ka)) =
-            s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      // ---- row copy: a 1x32 block is four neighbouring lanes of 8 values --
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int idx = i * kThreads + tid;
+        const int r = idx >> 4;
+        const int vc = idx & 15;
+        const uint4 v = reinterpret_cast<const uint4*>(tile)[r * 16 + vc];
+        uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                              __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+        m = half_max(m);
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        const uint32_t code = scale_code(m);
+        const bool nan_block = (code == 0xFFu);
+        const float inv = inv_scale(nan_block ? 0u : code);
+        uint2 q;
+        q.x = quant_word(v.x, inv, nan_block) | (quant_word(v.y, inv, nan_block) << 16);
+        q.y = quant_word(v.z, inv, nan_block) | (quant_word(v.w, inv, nan_block) << 16);
+        const int64_t grow = g.row0 + r;
+        if (r < g.valid_rows && vc * 8 < g.valid_cols)
+          *reinterpret_cast<uint2*>(p.row_data + grow * p.cols + g.c0 + vc * 8) = q;
+        // Gather the four block codes of this row (lanes 0, 4, 8, 12 of the half-warp).
+        const int base = lane & 16;
+        const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, code, base + 0);
+        const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
+        const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, code, base + 8);
+        const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, code, base + 12);
+        const bool write_scale = kGrouped ? (r < g.valid_rows) : true;  // dense: padding rows get zeros
+        if ((lane & 15) == 0 && write_scale)
+          *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(grow, g.c0 >> 5, p.row_ka)) =
+              s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      }
+    }
+
+    if constexpr (kCol) {
+      // ---- column copy: thread = (column pair cp, 32-row block rb) --------
+      const int cp = tid & 63;
+      const int rb = tid >> 6;
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = tile[(rb * 32 + i) * 64 + cp];
+      if (kGrouped) {
+        // rows past the group's end hold the next group's data: they count as zero padding
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (rb * 32 + i >= g.valid_rows) w[i] = 0u;
+      }
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+      const uint32_t code_lo = scale_code(m & 0xFFFFu);
+      const uint32_t code_hi = scale_code(m >> 16);
+      const bool nan_lo = code_lo == 0xFFu, nan_hi = code_hi == 0xFFu;
+      const float inv_lo = inv_scale(nan_lo ? 0u : code_lo);
+      const float inv_hi = inv_scale(nan_hi ? 0u : code_hi);
+      uint32_t out_lo[8], out_hi[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t a = w[4 * j], bb = w[4 * j + 1], c = w[4 * j + 2], d = w[4 * j + 3];
+        if (nan_lo) {
+          out_lo[j] = nan_pair((a & 0xFFFFu) | (bb << 16)) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
+        } else {
+          out_lo[j] = cvt_pair(lo_f(a) * inv_lo, lo_f(bb) * inv_lo) |
+                      (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
+        }
+        if (nan_hi) {
+          out_hi[j] = nan_pair((a >> 16) | (bb & 0xFFFF0000u)) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
+        } else {
+          out_hi[j] = cvt_pair(hi_f(a) * inv_hi, hi_f(bb) * inv_hi) |
+                      (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
+        }
+      }
+      const int64_t c = g.c0 + 2 * cp;
+      col_sc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
+      col_sc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
+      const bool block_valid = kGrouped ? true : (rb * 32 < g.valid_rows);
+      if (block_valid) {
+        const int64_t k = g.kpos + rb * 32;
+        if (c < p.cols) {
+          uint4* dst = reinterpret_cast<uint4*>(p.col_data + c * p.col_pitch + k);
+          dst[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+          dst[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
+        }
+        if (c + 1 < p.cols) {
+          uint4* dst = reinterpret_cast<uint4*>(p.col_data + (c + 1) * p.col_pitch + k);
+          dst[0] = make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+          dst[1] = make_uint4(out_hi[4], out_hi[5], out_hi[6], out_hi[7]);
+        }
+      }
+      __syncthreads();
+      if (tid < kTileCols) {
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(col_sc + tid * 4);
+        *reinterpret_cast<uint32_t*>(p.col_scale + scale_offset(g.c0 + tid, g.kpos >> 5, p.col_ka)) = word;
+      }
+    }
+    __syncthreads();  // buffer b and col_sc are free again
+    if (tid == 0) {
+      const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
+      if (tn < ntiles) issue(tn, b);
     }
   }
-
-  if constexpr (kCol) {
-    __syncthreads();
-    // ---- column copy: thread = (column pair cp, 32-row block rb) ----------
-    const int cp = tid & 63;
-    const int rb = tid >> 6;
-    uint32_t w[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = tile[(rb * 32 + i) * 64 + cp];
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
-    const uint32_t code_lo = scale_code(m & 0xFFFFu);
-    const uint32_t code_hi = scale_code(m >> 16);
-    const bool nan_lo = code_lo == 0xFFu, nan_hi = code_hi == 0xFFu;
-    const float inv_lo = inv_scale(nan_lo ? 0u : code_lo);
-    const float inv_hi = inv_scale(nan_hi ? 0u : code_hi);
-    uint32_t out_lo[8], out_hi[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t a = w[4 * j], b = w[4 * j + 1], c = w[4 * j + 2], d = w[4 * j + 3];
-      if (nan_lo) {
-        out_lo[j] = (nan_pair((a & 0xFFFFu) | (b << 16))) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
-      } else {
-        out_lo[j] = cvt_pair(lo_f(a) * inv_lo, lo_f(b) * inv_lo) | (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
-      }
-      if (nan_hi) {
-        out_hi[j] = (nan_pair((a >> 16) | (b & 0xFFFF0000u))) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
-      } else {
-        out_hi[j] = cvt_pair(hi_f(a) * inv_hi, hi_f(b) * inv_hi) | (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
-      }
-    }
-    const int64_t c = c0 + 2 * cp;
-    col_sc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
-    col_sc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
-    const bool block_valid = kGrouped ? true : (rb * 32 < valid_rows);
-    if (block_valid) {
-      const int64_t k = kpos + rb * 32;
-      if (c < p.cols) {
-        uint4* dst = reinterpret_cast<uint4*>(p.col_data + c * p.col_pitch + k);
-        dst[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
-        dst[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
-      }
-      if (c + 1 < p.cols) {
-        uint4* dst = reinterpret_cast<uint4*>(p.col_data + (c + 1) * p.col_pitch + k);
-        dst[0] = make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
-        dst[1] = make_uint4(out_hi[4], out_hi[5], out_hi[6], out_hi[7]);
-      }
-    }
-    __syncthreads();
-    if (tid < kTileCols) {
-      const uint32_t word = *reinterpret_cast<const uint32_t*>(col_sc + tid * 4);
-      *reinterpret_cast<uint32_t*>(p.col_scale + scale_offset(c0 + tid, kpos >> 5, p.col_ka)) = word;
-    }
+  // A timed-out CTA leaves only after the copies it issued have landed: the
+  // j-th load into a buffer completes that buffer's phase j.
+  if (s_abort && tid == 0) {
+    if (issued0 > 0) mbar_wait(&full[0], static_cast<uint32_t>((issued0 - 1) & 1), p.timeout_ns);
+    if (issued1 > 0) mbar_wait(&full[1], static_cast<uint32_t>((issued1 - 1) & 1), p.timeout_ns);
   }
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
 template <bool R, bool C, bool G>
-cudaError_t launch_one(const QParams& p, dim3 grid, cudaStream_t s) {
-  size_t smem = 0;
-  if (C) smem += kTileRows * kTileCols * 2 + 512;
-  if (G) smem += 2 * (kMaxGroups + 1) * sizeof(int32_t);
+mx_status launch_one(const CUtensorMap& map, const QParams& p, int64_t tiles_upper, cudaStream_t s) {
+  const size_t smem = 128 + 2 * kTileBytes + 512 + 16 + (G ? 2 * (kMaxGroups + 1) * sizeof(int32_t) : 0);
   auto kern = mx_quant_kernel<R, C, G>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  kern<<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(quant smem)");
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_upper, static_cast<int64_t>(per_sm) * sm_count()));
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(map, p);
+  return cuda_status(cudaGetLastError(), "mx_quantize launch");
 }
 
 }  // namespace
 
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s) {
   QParams p;
-  p.x = static_cast<const uint16_t*>(q.x);
   p.rows = q.rows;
   p.cols = q.cols;
-  p.ldx = q.ldx;
   p.row_data = static_cast<uint8_t*>(q.row_data);
   p.row_scale = static_cast<uint8_t*>(q.row_scale);
   p.col_data = static_cast<uint8_t*>(q.col_data);
@@ -339,6 +416,7 @@ mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaSt
   p.row_ka = (q.cols + 127) / 128;
   p.col_ka = (q.col_pitch + 127) / 128;
   p.dev_status = q.dev_status;
+  p.timeout_ns = wait_timeout_ns();
   const bool grouped = q.offsets != nullptr && do_col;
   if (grouped && q.n_groups > kMaxGroups) {
     set_error("mx_quantize: at most %d groups", kMaxGroups);
@@ -348,22 +426,32 @@ mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaSt
   int64_t row_tiles = (q.rows + kTileRows - 1) / kTileRows;
   if (grouped) row_tiles += q.n_groups;  // upper bound of sum ceil(m_e / 128)
   if (row_tiles == 0 || col_tiles == 0) return MX_OK;
-  if (row_tiles > 65535 || col_tiles > 2147483647LL) {
-    set_error("mx_quantize: too many row tiles (%lld)", static_cast<long long>(row_tiles));
-    return MX_ERR_UNSUPPORTED_SHAPE;
+
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return MX_ERR_CUDA;
   }
-  dim3 grid(static_cast<unsigned>(col_tiles), static_cast<unsigned>(row_tiles));
-  cudaError_t e;
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(q.cols), static_cast<cuuint64_t>(q.rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.ldx * 2)};
+  cuuint32_t box[2] = {kTileCols, kTileRows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q.x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (quantiser input) failed (%d)", static_cast<int>(r));
+    return MX_ERR_CUDA;
+  }
+  const int64_t tiles = row_tiles * col_tiles;
   if (grouped) {
-    e = do_row ? launch_one<true, true, true>(p, grid, s) : launch_one<false, true, true>(p, grid, s);
-  } else if (do_row && do_col) {
-    e = launch_one<true, true, false>(p, grid, s);
-  } else if (do_row) {
-    e = launch_one<true, false, false>(p, grid, s);
-  } else {
-    e = launch_one<false, true, false>(p, grid, s);
+    return do_row ? launch_one<true, true, true>(map, p, tiles, s) : launch_one<false, true, true>(map, p, tiles, s);
   }
-  return cuda_status(e, "mx_quantize launch");
+  if (do_row && do_col) return launch_one<true, true, false>(map, p, tiles, s);
+  if (do_row) return launch_one<true, false, false>(map, p, tiles, s);
+  return launch_one<false, true, false>(map, p, tiles, s);
 }
 
 }  // namespace mx
