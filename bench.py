@@ -338,13 +338,73 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+def run_quant_sweep(args, rank, world, peaks, peak_src):
+    """Quantiser bandwidth sweep: BF16 [M x 7168], M in {4096 .. 32768}, both
+    copies in one fused pass per launch. One step = one launch per M."""
+    import workloads
+    import mxfp8_block_scaled_gb300 as mx
+    C = 7168
+    xs = {M: workloads.quant_sweep(M).cuda() for M in workloads.QUANT_SWEEP_M}
+    outs = {M: mx.quantize(x, mx.MX_BOTH) for M, x in xs.items()}
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+
+    def step(timers=None):
+        for M, x in xs.items():
+            r, c = outs[M]
+            e = timers.span(M, stream) if timers else None
+            mx.mx_quantize(x.data_ptr(), M, C, C, mx.MX_BOTH, r.data.data_ptr(), r.scale.data_ptr(), c.data.data_ptr(),
+                           c.scale.data_ptr(), None, 0, 0, None, sp)
+            if e is not None:
+                e.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    timers = Timers()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(timers)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    per_elem = 2 + 1 + 1 + 2 / 32
+    step_bytes = sum(per_elem * M * C for M in xs)
+    value = world * args.steps * step_bytes / (ms / 1e3) / 1e9
+    per_m = {str(M): per_elem * M * C / (timers.total_ms(M) / timers.count(M) / 1e3) / 1e9 for M in xs}
+    big = max(xs)
+    achieved = per_m[str(big)]
+    line = {"metric": "MX quantiser GB/s (row + column copies, one fused pass)", "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
+            "data": "synthetic",
+            "config": {"workload": "quant_sweep BF16 [M x 7168], M in 4096/8192/16384/32768, axis both",
+                       "parallelism": f"replicas{world}", "l2": "no flush: each step moves ~1.8 GB (> 129 MB L2)"},
+            "per_M_gbs": per_m,
+            "roofline": {"bound": "hbm", "kernel": "mx_quant_kernel", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": profile_traffic("mx_quant_kernel"), "bytes_per_launch": per_elem * big * C,
+                         "peak_source": f"{peak_src} hbm_gbs", "launch": f"M={big}"},
+            "gpu_launches": len(xs) * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dense_ffn", choices=["dense_ffn"])
+    ap.add_argument("--workload", default="dense_ffn", choices=["dense_ffn", "quant"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
@@ -358,6 +418,9 @@ def main():
     import mxfp8_block_scaled_gb300 as mx
     mx.lib()
     peaks, peak_src = load_peaks()
+    if args.workload == "quant":
+        run_quant_sweep(args, rank, world, peaks, peak_src)
+        return
     wl = DenseFFN()
     stream = torch.cuda.Stream()
 

@@ -93,6 +93,7 @@ struct GParams {
   int64_t c_group_stride; // elements between experts' outputs (grouped by K)
   int32_t c_vec;          // 1: every output row start is 16-byte aligned (16-byte stores)
   int32_t c_tma;          // 1: output tiles leave through TMA stores (needs c_vec)
+  int32_t n_fast;         // 1: consecutive tiles walk N first (the CTAs sharing an A tile run together)
   const int64_t* offsets;
   int n_groups;
   int* dev_status;
@@ -142,7 +143,8 @@ __device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, i
   const int64_t nt = (p.N + BN - 1) / BN;
   const int64_t mt = (p.M + kBM - 1) / kBM;
   if (KIND == GEMM_DENSE) {
-    const int64_t mb = t % mt, nb = t / mt;
+    const int64_t mb = p.n_fast ? t / nt : t % mt;
+    const int64_t nb = p.n_fast ? t % nt : t / mt;
     ti.m0 = mb * kBM;
     ti.n0 = nb * BN;
     ti.a_row = ti.m0;
@@ -155,8 +157,8 @@ __device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, i
     ti.cbase = p.c + ti.m0 * p.ldc + ti.n0;
   } else if (KIND == GEMM_GROUPED_M) {
     const int64_t T = g.total;
-    const int32_t u = static_cast<int32_t>(t % T);
-    const int64_t nb = t / T;
+    const int32_t u = static_cast<int32_t>(p.n_fast ? t / nt : t % T);
+    const int64_t nb = p.n_fast ? t % nt : t / T;
     const int e = last_le(g.tile, p.n_groups, u);
     ti.m0 = static_cast<int64_t>(g.off[e]) + static_cast<int64_t>(u - g.tile[e]) * kBM;
     ti.n0 = nb * BN;
@@ -674,6 +676,10 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.c_group_stride = L.M * L.ldc;
   p.c_vec = ((reinterpret_cast<uintptr_t>(L.c) & 15u) == 0 && L.ldc % 8 == 0) ? 1 : 0;
   p.c_tma = 0;
+  // Walk N first when A is the larger operand (and always for the rows-ragged
+  // grouped GEMM): the CTAs that share an A tile then run at the same time and
+  // A leaves HBM once, while the smaller B stays resident in L2.
+  p.n_fast = (L.kind == GEMM_GROUPED_M || (L.kind == GEMM_DENSE && L.M >= L.N)) ? 1 : 0;
   p.offsets = L.offsets;
   p.n_groups = L.n_groups;
   p.dev_status = L.dev_status;

@@ -9,16 +9,17 @@
 // for the grouped wgrad). Scale rule: X = floor(log2 amax) - 8 clamped to
 // [-127, 127], element = E4M3(x * 2**-X) round-to-nearest-even, saturating.
 //
-// Design: persistent CTAs (a few per SM) walk 128x128 tiles of the input.
-// Each CTA keeps two 32 KB shared-memory buffers filled by TMA, so the load of
-// its next tile is in flight while the current one is quantised and stored;
-// the input is read from HBM exactly once. Row copy: a 1x32 block is four
-// neighbouring lanes holding 8 values each (amax by two xor shuffles). Column
-// copy: each thread owns two adjacent columns of one 32-row block (4-byte,
-// bank-conflict-free shared loads). amax is an unsigned max over the BF16
-// magnitude bits (NaN > Inf > finite), the exponent comes from its bits, and
-// the conversion is the hardware's round-to-nearest-even satfinite E4M3 cvt.
-// Scale bytes are written as whole 32-bit words of the swizzled layout.
+// Design: persistent CTAs (several per SM) walk 128x128 tiles of the input.
+// In each CTA a producer warp refills a 32 KB shared-memory tile buffer by
+// TMA as soon as eight consumer warps have read it, so the next load overlaps
+// their conversion and stores; the input is read from HBM exactly once. Row copy: a 1x32
+// block is four neighbouring lanes holding 8 values each (amax by two xor
+// shuffles). Column copy: each thread owns two adjacent columns of one 32-row
+// block (4-byte, bank-conflict-free shared loads). amax is an unsigned max
+// over the BF16 magnitude bits (NaN > Inf > finite), the exponent comes from
+// its bits, and the conversion is the hardware's round-to-nearest-even
+// satfinite E4M3 cvt. Scale bytes are written as whole 32-bit words of the
+// swizzled layout.
 
 #include <cuda.h>
 #include <cuda_fp8.h>
@@ -37,7 +38,16 @@ namespace {
 
 constexpr int kTileRows = 128;
 constexpr int kTileCols = 128;
-constexpr int kThreads = 256;
+constexpr int kConsumers = 256;               // eight math warps
+constexpr int kThreads = kConsumers + 32;     // plus one producer warp
+// Tile buffers per CTA. Measured on GB300 (M x 7168, both copies): more
+// resident CTAs beat deeper per-CTA rings; one buffer per CTA (the producer
+// refills it as soon as the consumers have read it, while they still convert
+// and store) with three register-limited CTAs per SM was best.
+#ifndef MX_QUANT_STAGES
+#define MX_QUANT_STAGES 1
+#endif
+constexpr int kStages = MX_QUANT_STAGES;
 constexpr int kMaxGroups = 1024;
 constexpr int kTileBytes = kTileRows * kTileCols * 2;
 
@@ -93,10 +103,14 @@ __device__ __forceinline__ uint32_t quant_word(uint32_t w, float inv, bool nan_b
 
 __device__ __forceinline__ uint32_t half_max(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
 
-// Exclusive scan of v[0, n) (n <= 4 * kThreads) in shared memory; returns the
-// total. Every thread of the block must call it.
+// Barrier among the eight consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// Exclusive scan of v[0, n) (n <= 4 * blockDim.x) in shared memory; returns
+// the total. Every thread of the block must call it.
 __device__ int32_t block_exclusive_scan(int32_t* v, int n, int32_t* warp_tot) {
   const int tid = threadIdx.x;
+  const int nwarps = blockDim.x >> 5;
   int32_t loc[4];
   int32_t sum = 0;
 #pragma unroll
@@ -114,8 +128,7 @@ __device__ int32_t block_exclusive_scan(int32_t* v, int n, int32_t* warp_tot) {
   if ((tid & 31) == 31) warp_tot[tid >> 5] = incl;
   __syncthreads();
   int32_t before = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) {
+  for (int w = 0; w < nwarps; ++w) {
     const int32_t t = warp_tot[w];
     before += (w < (tid >> 5)) ? t : 0;
     total += t;
@@ -166,21 +179,47 @@ __device__ __forceinline__ TileGeo tile_geo(const QParams& p, int64_t t, int64_t
   return g;
 }
 
+// Bounded wait that also gives up once another thread of the CTA has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const QParams& p,
+                                              volatile int32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > p.timeout_ns) {
+      *abort_flag = 1;
+      if (p.dev_status) atomicExch(p.dev_status, static_cast<int>(MX_ERR_TIMEOUT));
+      return false;
+    }
+  }
+}
+
+// Three resident CTAs per SM (caps registers at 75 per thread, no spills).
+#ifndef MX_QUANT_MIN_BLOCKS
+#define MX_QUANT_MIN_BLOCKS 3
+#endif
+
 template <bool kRow, bool kCol, bool kGrouped>
-__global__ void __launch_bounds__(kThreads) mx_quant_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams p) {
+__global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
+    mx_quant_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  uint8_t* buf0 = smem;                                              // two [128][128] BF16 tiles
-  uint8_t* col_sc = smem + 2 * kTileBytes;                           // [128][4] column-copy scales
-  uint64_t* full = reinterpret_cast<uint64_t*>(col_sc + 512);        // [2] tile-loaded barriers
-  int32_t* g_off = reinterpret_cast<int32_t*>(full + 2);             // [E+1] row offsets
+  uint8_t* tiles = smem;                                             // kStages x [128][128] BF16
+  uint8_t* col_sc = smem + kStages * kTileBytes;                     // 2 x [128][4] column-copy scales
+  uint64_t* full = reinterpret_cast<uint64_t*>(col_sc + 1024);       // [kStages] tile landed
+  uint64_t* empty = full + kStages;                                  // [kStages] tile consumed
+  int32_t* g_off = reinterpret_cast<int32_t*>(empty + kStages);      // [E+1] row offsets
   int32_t* g_tile = g_off + (kMaxGroups + 1);                        // [E+1] padded tile starts
   __shared__ int32_t warp_tot[kThreads / 32];
   __shared__ int32_t s_bad;
   __shared__ int32_t s_total_tiles;
-  __shared__ int32_t s_abort;
+  __shared__ volatile int32_t s_abort;
 
   const int tid = threadIdx.x;
+  const int warp = tid >> 5;
   const int lane = tid & 31;
   const int64_t col_tiles = (p.cols + kTileCols - 1) / kTileCols;
   int64_t row_tiles = (p.rows + kTileRows - 1) / kTileRows;
@@ -224,147 +263,159 @@ __global__ void __launch_bounds__(kThreads) mx_quant_kernel(const __grid_constan
 
   const int64_t ntiles = row_tiles * col_tiles;
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
     s_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  int issued0 = 0, issued1 = 0;  // loads issued per buffer (thread 0 only)
-  auto issue = [&](int64_t t, int b) {
-    const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, g_off, g_tile);
-    if (b) ++issued1; else ++issued0;
-    mbar_arrive_expect_tx(&full[b], kTileBytes);
-    tma_load_2d(buf0 + b * kTileBytes, &tmap_x, &full[b], static_cast<int32_t>(g.c0), static_cast<int32_t>(g.row0));
-  };
-  if (tid == 0) {
-    tma_prefetch_desc(&tmap_x);
-    for (int b = 0; b < 2; ++b) {
-      const int64_t t = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
-      if (t < ntiles) issue(t, b);
+  if (warp == kConsumers / 32) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_x);
+      int j = 0;
+      int last_phase_issued[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_phase_issued[s] = -1;
+      for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
+        if (!wait_or_abort(&empty[s], ph ^ 1u, p, &s_abort)) break;
+        const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, g_off, g_tile);
+        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        tma_load_2d(tiles + s * kTileBytes, &tmap_x, &full[s], static_cast<int32_t>(g.c0),
+                    static_cast<int32_t>(g.row0));
+#pragma unroll
+        for (int q = 0; q < kStages; ++q)
+          if (q == s) last_phase_issued[q] = static_cast<int>(ph);
+      }
+      if (s_abort) {
+        // Let the loads this CTA issued land before it leaves.
+#pragma unroll
+        for (int q = 0; q < kStages; ++q)
+          if (last_phase_issued[q] >= 0) mbar_wait(&full[q], static_cast<uint32_t>(last_phase_issued[q]), p.timeout_ns);
+      }
     }
-  }
+  } else {
+    // ----------------------------------------------------------- consumers
+    int j = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
+      const int s = j % kStages;
+      const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
+      const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, g_off, g_tile);
+      const uint32_t* tile = reinterpret_cast<const uint32_t*>(tiles + s * kTileBytes);
+      uint8_t* csc = col_sc + (j & 1) * 512;
+      // Every consumer runs every iteration (and every consumers_sync) even
+      // after an abort, so the named barrier can never strand a warp.
+      const bool ok = !s_abort && wait_or_abort(&full[s], ph, p, &s_abort);
 
-  int it = 0;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-    const int b = it & 1;
-    const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, g_off, g_tile);
-    const uint32_t* tile = reinterpret_cast<const uint32_t*>(buf0 + b * kTileBytes);
-    if (!mbar_wait(&full[b], static_cast<uint32_t>((it >> 1) & 1), p.timeout_ns)) s_abort = 1;
-    __syncthreads();
-    if (s_abort) {
-      if (tid == 0 && p.dev_status) atomicExch(p.dev_status, static_cast<int>(MX_ERR_TIMEOUT));
-      break;
-    }
+      if (kRow && ok) {
+        // ---- row copy: a 1x32 block is four neighbouring lanes of 8 values
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int idx = i * kConsumers + tid;
+          const int r = idx >> 4;
+          const int vc = idx & 15;
+          const uint4 v = reinterpret_cast<const uint4*>(tile)[r * 16 + vc];
+          uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+          m = half_max(m);
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+          const uint32_t code = scale_code(m);
+          const bool nan_block = (code == 0xFFu);
+          const float inv = inv_scale(nan_block ? 0u : code);
+          uint2 q;
+          q.x = quant_word(v.x, inv, nan_block) | (quant_word(v.y, inv, nan_block) << 16);
+          q.y = quant_word(v.z, inv, nan_block) | (quant_word(v.w, inv, nan_block) << 16);
+          const int64_t grow = g.row0 + r;
+          if (r < g.valid_rows && vc * 8 < g.valid_cols)
+            *reinterpret_cast<uint2*>(p.row_data + grow * p.cols + g.c0 + vc * 8) = q;
+          // Gather the four block codes of this row (lanes 0, 4, 8, 12 of the half-warp).
+          const int base = lane & 16;
+          const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, code, base + 0);
+          const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
+          const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, code, base + 8);
+          const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, code, base + 12);
+          const bool write_scale = kGrouped ? (r < g.valid_rows) : true;  // dense: padding rows get zeros
+          if ((lane & 15) == 0 && write_scale)
+            *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(grow, g.c0 >> 5, p.row_ka)) =
+                s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        }
+      }
 
-    if constexpr (kRow) {
-      // ---- row copy: a 1x32 block is four neighbouring lanes of 8 values --
+      if constexpr (kCol) {
+        if (ok) {
+          // ---- column copy: thread = (column pair cp, 32-row block rb) ----
+          const int cp = tid & 63;
+          const int rb = tid >> 6;
+          uint32_t w[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = i * kThreads + tid;
-        const int r = idx >> 4;
-        const int vc = idx & 15;
-        const uint4 v = reinterpret_cast<const uint4*>(tile)[r * 16 + vc];
-        uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                              __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-        m = half_max(m);
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        const uint32_t code = scale_code(m);
-        const bool nan_block = (code == 0xFFu);
-        const float inv = inv_scale(nan_block ? 0u : code);
-        uint2 q;
-        q.x = quant_word(v.x, inv, nan_block) | (quant_word(v.y, inv, nan_block) << 16);
-        q.y = quant_word(v.z, inv, nan_block) | (quant_word(v.w, inv, nan_block) << 16);
-        const int64_t grow = g.row0 + r;
-        if (r < g.valid_rows && vc * 8 < g.valid_cols)
-          *reinterpret_cast<uint2*>(p.row_data + grow * p.cols + g.c0 + vc * 8) = q;
-        // Gather the four block codes of this row (lanes 0, 4, 8, 12 of the half-warp).
-        const int base = lane & 16;
-        const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, code, base + 0);
-        const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
-        const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, code, base + 8);
-        const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, code, base + 12);
-        const bool write_scale = kGrouped ? (r < g.valid_rows) : true;  // dense: padding rows get zeros
-        if ((lane & 15) == 0 && write_scale)
-          *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(grow, g.c0 >> 5, p.row_ka)) =
-              s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+          for (int i = 0; i < 32; ++i) w[i] = tile[(rb * 32 + i) * 64 + cp];
+          mbar_arrive(&empty[s]);  // this thread is done with the tile
+          if (kGrouped) {
+            // rows past the group's end hold the next group's data: they count as zero padding
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (rb * 32 + i >= g.valid_rows) w[i] = 0u;
+          }
+          uint32_t m = 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+          const uint32_t code_lo = scale_code(m & 0xFFFFu);
+          const uint32_t code_hi = scale_code(m >> 16);
+          const bool nan_lo = code_lo == 0xFFu, nan_hi = code_hi == 0xFFu;
+          const float inv_lo = inv_scale(nan_lo ? 0u : code_lo);
+          const float inv_hi = inv_scale(nan_hi ? 0u : code_hi);
+          uint32_t out_lo[8], out_hi[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
+            if (nan_lo) {
+              out_lo[q] = nan_pair((a & 0xFFFFu) | (bb << 16)) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
+            } else {
+              out_lo[q] = cvt_pair(lo_f(a) * inv_lo, lo_f(bb) * inv_lo) |
+                          (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
+            }
+            if (nan_hi) {
+              out_hi[q] = nan_pair((a >> 16) | (bb & 0xFFFF0000u)) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
+            } else {
+              out_hi[q] = cvt_pair(hi_f(a) * inv_hi, hi_f(bb) * inv_hi) |
+                          (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
+            }
+          }
+          const int64_t c = g.c0 + 2 * cp;
+          csc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
+          csc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
+          const bool block_valid = kGrouped ? true : (rb * 32 < g.valid_rows);
+          if (block_valid) {
+            const int64_t k = g.kpos + rb * 32;
+            if (c < p.cols) {
+              uint4* dst = reinterpret_cast<uint4*>(p.col_data + c * p.col_pitch + k);
+              dst[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+              dst[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
+            }
+            if (c + 1 < p.cols) {
+              uint4* dst = reinterpret_cast<uint4*>(p.col_data + (c + 1) * p.col_pitch + k);
+              dst[0] = make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+              dst[1] = make_uint4(out_hi[4], out_hi[5], out_hi[6], out_hi[7]);
+            }
+          }
+        }
+        // The four 32-row blocks of a column sit in four warps: gather their
+        // scale bytes (double-buffered by iteration, so one barrier suffices).
+        consumers_sync();
+        if (ok && tid < kTileCols) {
+          const uint32_t word = *reinterpret_cast<const uint32_t*>(csc + tid * 4);
+          *reinterpret_cast<uint32_t*>(p.col_scale + scale_offset(g.c0 + tid, g.kpos >> 5, p.col_ka)) = word;
+        }
+      } else {
+        if (ok) mbar_arrive(&empty[s]);
       }
     }
-
-    if constexpr (kCol) {
-      // ---- column copy: thread = (column pair cp, 32-row block rb) --------
-      const int cp = tid & 63;
-      const int rb = tid >> 6;
-      uint32_t w[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = tile[(rb * 32 + i) * 64 + cp];
-      if (kGrouped) {
-        // rows past the group's end hold the next group's data: they count as zero padding
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (rb * 32 + i >= g.valid_rows) w[i] = 0u;
-      }
-      uint32_t m = 0;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
-      const uint32_t code_lo = scale_code(m & 0xFFFFu);
-      const uint32_t code_hi = scale_code(m >> 16);
-      const bool nan_lo = code_lo == 0xFFu, nan_hi = code_hi == 0xFFu;
-      const float inv_lo = inv_scale(nan_lo ? 0u : code_lo);
-      const float inv_hi = inv_scale(nan_hi ? 0u : code_hi);
-      uint32_t out_lo[8], out_hi[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t a = w[4 * j], bb = w[4 * j + 1], c = w[4 * j + 2], d = w[4 * j + 3];
-        if (nan_lo) {
-          out_lo[j] = nan_pair((a & 0xFFFFu) | (bb << 16)) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
-        } else {
-          out_lo[j] = cvt_pair(lo_f(a) * inv_lo, lo_f(bb) * inv_lo) |
-                      (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
-        }
-        if (nan_hi) {
-          out_hi[j] = nan_pair((a >> 16) | (bb & 0xFFFF0000u)) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
-        } else {
-          out_hi[j] = cvt_pair(hi_f(a) * inv_hi, hi_f(bb) * inv_hi) |
-                      (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
-        }
-      }
-      const int64_t c = g.c0 + 2 * cp;
-      col_sc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
-      col_sc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
-      const bool block_valid = kGrouped ? true : (rb * 32 < g.valid_rows);
-      if (block_valid) {
-        const int64_t k = g.kpos + rb * 32;
-        if (c < p.cols) {
-          uint4* dst = reinterpret_cast<uint4*>(p.col_data + c * p.col_pitch + k);
-          dst[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
-          dst[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
-        }
-        if (c + 1 < p.cols) {
-          uint4* dst = reinterpret_cast<uint4*>(p.col_data + (c + 1) * p.col_pitch + k);
-          dst[0] = make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
-          dst[1] = make_uint4(out_hi[4], out_hi[5], out_hi[6], out_hi[7]);
-        }
-      }
-      __syncthreads();
-      if (tid < kTileCols) {
-        const uint32_t word = *reinterpret_cast<const uint32_t*>(col_sc + tid * 4);
-        *reinterpret_cast<uint32_t*>(p.col_scale + scale_offset(g.c0 + tid, g.kpos >> 5, p.col_ka)) = word;
-      }
-    }
-    __syncthreads();  // buffer b and col_sc are free again
-    if (tid == 0) {
-      const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
-      if (tn < ntiles) issue(tn, b);
-    }
-  }
-  // A timed-out CTA leaves only after the copies it issued have landed: the
-  // j-th load into a buffer completes that buffer's phase j.
-  if (s_abort && tid == 0) {
-    if (issued0 > 0) mbar_wait(&full[0], static_cast<uint32_t>((issued0 - 1) & 1), p.timeout_ns);
-    if (issued1 > 0) mbar_wait(&full[1], static_cast<uint32_t>((issued1 - 1) & 1), p.timeout_ns);
   }
 }
 
@@ -388,14 +439,16 @@ EncodeTiledFn encode_fn() {
 
 template <bool R, bool C, bool G>
 mx_status launch_one(const CUtensorMap& map, const QParams& p, int64_t tiles_upper, cudaStream_t s) {
-  const size_t smem = 128 + 2 * kTileBytes + 512 + 16 + (G ? 2 * (kMaxGroups + 1) * sizeof(int32_t) : 0);
+  const size_t smem = 128 + static_cast<size_t>(kStages) * kTileBytes + 1024 + 2 * kStages * 8 +
+                      (G ? 2 * (kMaxGroups + 1) * sizeof(int32_t) : 0);
   auto kern = mx_quant_kernel<R, C, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(quant smem)");
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
   if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_upper, static_cast<int64_t>(per_sm) * sm_count()));
+  const int64_t grid =
+      std::max<int64_t>(1, std::min<int64_t>(tiles_upper, static_cast<int64_t>(std::max(per_sm, 1)) * sm_count()));
   kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(map, p);
   return cuda_status(cudaGetLastError(), "mx_quantize launch");
 }
