@@ -338,6 +338,126 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+class MoEExperts:
+    """Routed-expert step (64 experts, 49152 rows, gate_up N=2816/K=2048 and
+    down N=2048/K=1408): quantise the activation and the output gradient of each
+    projection (row copy + per-group padded column copy in one pass) and the
+    stacked weights (row + column copies per expert), then the grouped fprop,
+    dgrad and wgrad GEMMs of both projections."""
+    name = "moe_routed_experts"
+
+    def __init__(self):
+        import workloads
+        import mxfp8_block_scaled_gb300 as mx
+        self.mx = mx
+        d = workloads.moe_experts()
+        self.offsets = torch.from_numpy(d["offsets"]).cuda()
+        self.counts = d["counts"]
+        self.M = int(d["offsets"][-1])
+        self.cap = mx.mx_grouped_padded_rows(d["offsets"])
+        self.proj = []
+        for a_key, w_key, dy_key in (("X", "W_gate_up", "dY_gate_up"), ("A_down", "W_down", "dY_down")):
+            A = d[a_key].cuda()
+            W = d[w_key].cuda()
+            dY = d[dy_key].cuda()
+            E, N, K = W.shape
+            ar, ac = mx.quantize(A, mx.MX_BOTH, group_offsets=self.offsets, col_capacity=self.cap)
+            dr, dc = mx.quantize(dY, mx.MX_BOTH, group_offsets=self.offsets, col_capacity=self.cap)
+            wr, wc = mx.quantize_stacked(W, mx.MX_BOTH)
+            bf = dict(dtype=torch.bfloat16, device="cuda")
+            outs = {"Y": torch.empty((self.M, N), **bf), "dX": torch.empty((self.M, K), **bf),
+                    "dW": torch.empty((E, N, K), **bf)}
+            self.proj.append(dict(A=A, W=W, dY=dY, ar=ar, ac=ac, dr=dr, dc=dc, wr=wr, wc=wc, out=outs, E=E, N=N, K=K))
+        del d
+
+    def gemm_flops(self):
+        return [2.0 * self.M * pr["N"] * pr["K"] for pr in self.proj for _ in range(3)]
+
+    def step_flops(self):
+        return sum(self.gemm_flops())
+
+    def step(self, stream, timers=None):
+        mx = self.mx
+        sp = stream.cuda_stream
+        o = self.offsets.data_ptr()
+        E = self.offsets.numel() - 1
+        for pr in self.proj:
+            for src, r, c in ((pr["A"], pr["ar"], pr["ac"]), (pr["dY"], pr["dr"], pr["dc"])):
+                e = timers.span("quant", stream) if timers else None
+                mx.mx_quantize(src.data_ptr(), src.shape[0], src.shape[1], src.stride(0), mx.MX_BOTH,
+                               r.data.data_ptr(), r.scale.data_ptr(), c.data.data_ptr(), c.scale.data_ptr(), o, E,
+                               self.cap, None, sp)
+                if e is not None:
+                    e.record(stream)
+            W, wr, wc = pr["W"], pr["wr"], pr["wc"]
+            e = timers.span("wquant", stream) if timers else None
+            mx.mx_quantize_batched(W.data_ptr(), pr["E"], pr["N"], pr["K"], pr["K"], pr["N"] * pr["K"], mx.MX_BOTH,
+                                   wr.data.data_ptr(), wr.scale.data_ptr(), wc.data.data_ptr(), wc.scale.data_ptr(),
+                                   None, sp)
+            if e is not None:
+                e.record(stream)
+            for mode, a, b, out in ((mx.MX_FPROP, pr["ar"], wr, pr["out"]["Y"]),
+                                    (mx.MX_DGRAD, pr["dr"], wc, pr["out"]["dX"]),
+                                    (mx.MX_WGRAD, pr["dc"], pr["ac"], pr["out"]["dW"])):
+                e = timers.span("gemm", stream) if timers else None
+                mx.mx_grouped_gemm(mode, a.c_operand(), b.c_operand(), o, E, out.data_ptr(), out.stride(-2), None, sp)
+                if e is not None:
+                    e.record(stream)
+
+    def launches_per_step(self):
+        return sum(2 + 1 + 3 for pr in self.proj)
+
+
+def run_moe(args, rank, world, peaks, peak_src):
+    wl = MoEExperts()
+    stream = torch.cuda.Stream()
+    for _ in range(args.warmup):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    timers = Timers()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        wl.step(stream, timers)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    value = world * args.steps * wl.step_flops() / (ms / 1e3) / 1e12
+    pairs = timers.pairs["gemm"]
+    fl = wl.gemm_flops()
+    per_gemm = []
+    for i, name in enumerate(["gate_up fprop", "gate_up dgrad", "gate_up wgrad", "down fprop", "down dgrad",
+                              "down wgrad"]):
+        t = sum(pairs[j][0].elapsed_time(pairs[j][1]) for j in range(i, len(pairs), 6)) / args.steps
+        per_gemm.append({"gemm": name, "ms": t, "tflops": fl[i] / (t / 1e3) / 1e12})
+    gemm_ms = timers.total_ms("gemm") / timers.count("gemm")
+    achieved = (sum(fl) / 6) / (gemm_ms / 1e3) / 1e12
+    peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    line = {"metric": "MXFP8 grouped-GEMM TFLOPS (fprop+dgrad+wgrad of gate_up and down, incl. MX quantisation)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": "moe_routed_experts: 64 experts, 49152 rows (Zipf 1.1, 4 empty), gate_up "
+                                   "2048->2816, down 1408->2048", "parallelism": f"replicas{world}",
+                       "l2": "no flush: a step moves several GB (> 129 MB L2)"},
+            "per_gemm": per_gemm,
+            "roofline": {"bound": "tensor", "kernel": "mx_gemm_kernel (grouped)", "achieved": achieved,
+                         "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}"},
+            "quant_ms_per_launch": timers.total_ms("quant") / timers.count("quant"),
+            "weight_quant_ms_per_projection": timers.total_ms("wquant") / timers.count("wquant"),
+            "gpu_launches": wl.launches_per_step() * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def run_quant_sweep(args, rank, world, peaks, peak_src):
     """Quantiser bandwidth sweep: BF16 [M x 7168], M in {4096 .. 32768}, both
     copies in one fused pass per launch. One step = one launch per M."""
@@ -404,7 +524,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dense_ffn", choices=["dense_ffn", "quant"])
+    ap.add_argument("--workload", default="dense_ffn", choices=["dense_ffn", "quant", "moe"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
@@ -420,6 +540,9 @@ def main():
     peaks, peak_src = load_peaks()
     if args.workload == "quant":
         run_quant_sweep(args, rank, world, peaks, peak_src)
+        return
+    if args.workload == "moe":
+        run_moe(args, rank, world, peaks, peak_src)
         return
     wl = DenseFFN()
     stream = torch.cuda.Stream()

@@ -143,6 +143,25 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, in
                       int* dev_status, void* stream);
 
 /*
+ * mx_quantize_batched - the dense mx_quantize applied in one launch to `batch`
+ * matrices stacked in memory, e.g. the per-expert weights [E, N, K] of the
+ * routed experts ([DSV3] §5.2: stacked 3-D expert parameters; §8.1: weights
+ * are quantised into row and col copies once after each optimizer step).
+ *
+ *   x          BF16; matrix b is [rows, cols] at x + b*x_batch_stride elements,
+ *              row pitch ldx. x_batch_stride >= rows*ldx and a multiple of 8.
+ *   row_data   [batch][rows][cols] E4M3 (matrix stride rows*cols bytes);
+ *   row_scale  matrix stride mx_scale_bytes(rows, cols) bytes.
+ *   col_data   [batch][cols][rows] E4M3 (matrix stride cols*rows bytes);
+ *   col_scale  matrix stride mx_scale_bytes(cols, rows) bytes.
+ *   Per-matrix layouts, requirements and results are exactly those of the
+ *   dense mx_quantize (no groups). batch == 0 is a no-op.
+ */
+mx_status mx_quantize_batched(const void* x, int64_t batch, int64_t rows, int64_t cols, int64_t ldx,
+                              int64_t x_batch_stride, int axis, void* row_data, void* row_scale, void* col_data,
+                              void* col_scale, int* dev_status, void* stream);
+
+/*
  * mx_gemm - block-scaled GEMM C[M,N] = A[M,K] . B[N,K]^T with FP32 accumulation
  * and BF16 output rounded to nearest even ([DSV3] §8 and §13.4
  * low_precision_matmul; [TT] npu_quant_matmul; [FMT] §五.1).

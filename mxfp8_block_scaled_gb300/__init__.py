@@ -28,8 +28,8 @@ STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAP
                 4: "MX_ERR_CUDA", 5: "MX_ERR_DEVICE_CHECK", 6: "MX_ERR_TIMEOUT", 7: "MX_ERR_NO_DEVICE"}
 
 # Symbols the header declares (the CPU tests check the library exports them).
-EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_gemm", "mx_grouped_gemm",
-            "mx_status_string", "mx_last_error", "mx_abi_version")
+EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quantize_batched", "mx_gemm",
+            "mx_grouped_gemm", "mx_status_string", "mx_last_error", "mx_abi_version")
 
 
 class MXError(RuntimeError):
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.mx_grouped_padded_rows.restype = i64
     L.mx_quantize.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, vp, i32, i64, vp, vp]
     L.mx_quantize.restype = i32
+    L.mx_quantize_batched.argtypes = [vp, i64, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp]
+    L.mx_quantize_batched.restype = i32
     L.mx_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp, vp]
     L.mx_gemm.restype = i32
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
@@ -112,6 +114,12 @@ def mx_quantize(x, rows, cols, ldx, axis, row_data, row_scale, col_data, col_sca
                 col_capacity, dev_status, stream) -> None:
     _check(lib().mx_quantize(x, rows, cols, ldx, axis, row_data, row_scale, col_data, col_scale, group_offsets,
                              n_groups, col_capacity, dev_status, stream), "mx_quantize")
+
+
+def mx_quantize_batched(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, row_scale, col_data, col_scale,
+                        dev_status, stream) -> None:
+    _check(lib().mx_quantize_batched(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, row_scale, col_data,
+                                     col_scale, dev_status, stream), "mx_quantize_batched")
 
 
 def _ref(op):
@@ -227,7 +235,7 @@ class MXStacked:
 
 
 def quantize_stacked(w, axis: int, status=None, stream=None):
-    """Quantise stacked expert weights w[E, N, K] (BF16) expert by expert.
+    """Quantise stacked expert weights w[E, N, K] (BF16) in one batched launch.
     Returns (row_stack [E][N][K], col_stack [E][K][N]); entries None if not asked."""
     torch = _torch()
     E, N, K = w.shape
@@ -239,13 +247,11 @@ def quantize_stacked(w, axis: int, status=None, stream=None):
     if axis & MX_COLWISE:
         col = MXStacked(torch.empty((E, K, N), dtype=torch.uint8, device=dev),
                         torch.empty((E, mx_scale_bytes(K, N)), dtype=torch.uint8, device=dev), K, N, MX_COLWISE)
-    s = _stream(stream)
-    for e in range(E):
-        we = w[e]
-        mx_quantize(we.data_ptr(), N, K, we.stride(0), axis,
-                    _ptr(row.data[e]) if row else None, _ptr(row.scale[e]) if row else None,
-                    _ptr(col.data[e]) if col else None, _ptr(col.scale[e]) if col else None,
-                    None, 0, 0, _ptr(status), s)
+    assert w.stride(2) == 1
+    mx_quantize_batched(w.data_ptr(), E, N, K, w.stride(1), w.stride(0), axis,
+                        _ptr(row.data) if row else None, _ptr(row.scale) if row else None,
+                        _ptr(col.data) if col else None, _ptr(col.scale) if col else None,
+                        _ptr(status), _stream(stream))
     return row, col
 
 

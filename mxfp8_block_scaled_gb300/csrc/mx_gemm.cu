@@ -62,15 +62,20 @@ constexpr int kEpiBytes = 8 * kEpiWarpBytes;
 
 template <int BN>
 struct Cfg {
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  // BN = 256 leaves no tensor memory for a second accumulator next to the
+  // per-stage scale columns; narrower tiles double-buffer the accumulator so
+  // the epilogue of one tile overlaps the MMAs of the next.
+  static constexpr int kStages = (BN == 128) ? 6 : 4;
   static constexpr int kAcc = (BN == 256) ? 1 : 2;
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
-  static constexpr int kSfbAtoms = BN / 128;
+  static constexpr int kSfbAtoms = (BN + 127) / 128;
   static constexpr int kSfbBytes = kSfbAtoms * 512;
-  static constexpr int kSfCols = 4 + BN / 32;           // TMEM columns of one stage's scales
+  static constexpr int kSfCols = 4 + 4 * kSfbAtoms;     // TMEM columns of one stage's scales
   static constexpr uint32_t kSfCol0 = kAcc * BN;        // first scale column
   static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  // B tiles must start on a 128-row scale atom, so the atoms load as they are.
+  static_assert(BN % 128 == 0, "tile width must be a multiple of 128");
   static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
   static constexpr int kGroupBytes = 3 * (kMaxGroups + 1) * 4;
   __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
@@ -310,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full_bar[s], 1);
+      // Gathered scale atoms add one cp.async arrival per producer lane.
+      mbar_init(&full_bar[s], kGatherSfa ? 33 : 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < ACC; ++a) {
@@ -345,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile ti = get_tile<BN, KIND>(p, g, t);
       const int64_t sfb_row_atom0 = ti.n0 / 128;
       for (int kb = 0; kb < ti.nkb; ++kb) {
+        const int64_t katom = ti.k_atom0 + kb;
         uint32_t good = 1;
         if (lane == 0) good = wait_or_abort(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
         good = __shfl_sync(0xFFFFFFFFu, good, 0);
@@ -352,21 +359,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int64_t katom = ti.k_atom0 + kb;
         if constexpr (kGatherSfa) {
-          // Scale bytes of A rows m0 .. m0+127 (any start row) into one atom.
-          uint32_t w[4];
+          // Scale bytes of A rows m0 .. m0+127 (any start row) gathered into one
+          // atom with asynchronous 4-byte copies; each lane's arrival on the
+          // stage's full barrier fires when its copies have landed, so the
+          // producer never waits on them.
+          uint8_t* dst = sSfa + stage * 512 + lane * 16;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int64_t r = ti.a_row + lane + 32 * q;
-            w[q] = 0u;
-            if (r < p.a_ra * 128)
-              w[q] = __ldg(reinterpret_cast<const uint32_t*>(p.a_scale + (((r >> 7) * p.ka + katom) << 9) +
-                                                              ((r & 31) << 4) + (((r >> 5) & 3) << 2)));
+            const bool in = r < p.a_ra * 128;  // rows past the scale buffer read as zero
+            cp_async_4(dst + 4 * q,
+                       in ? p.a_scale + (((r >> 7) * p.ka + katom) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2)
+                          : p.a_scale,
+                       in ? 4u : 0u);
           }
-          *reinterpret_cast<uint4*>(sSfa + stage * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-          fence_proxy_async_smem();
-          __syncwarp();
+          cp_async_arrive_noinc(&full_bar[stage]);
         }
         if (lane == 0) {
           uint32_t bytes = C::kABytes + C::kBBytes + (kGatherSfa ? 0 : 512);
@@ -423,6 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // The gathered scale atom was written through the generic proxy; the
+          // tensor-core copy below reads it through the async proxy.
+          if constexpr (kGatherSfa) fence_proxy_async_smem();
           tc_fence_after_sync();
           const uint32_t sfa_t = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
           const uint32_t sfb_t = sfa_t + 4;
@@ -459,8 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;         // TMEM lanes this warp may read
-    const int half = (warp - 2) >> 2;     // which half of the tile's columns
-    constexpr int kCols = BN / 2;
+    const int half = (warp - 2) >> 2;     // which part of the tile's columns
+    constexpr int kChunks = BN / 32;      // 32-column chunks of the tile
+    constexpr int kHalf0 = (kChunks + 1) / 2;
+    constexpr int kCols = kHalf0 * 32;    // register columns per thread
+    const int my_chunks = half == 0 ? kHalf0 : kChunks - kHalf0;
+    const int col_off = half * kHalf0 * 32;
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -471,9 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t r[kCols];
       if (ti.nkb > 0) {
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               static_cast<uint32_t>(acc * BN + half * kCols);
+                               static_cast<uint32_t>(acc * BN + col_off);
 #pragma unroll
-        for (int ch = 0; ch < kCols / 32; ++ch) tmem_ld_32x32b_x32(taddr + ch * 32, r + ch * 32);
+        for (int ch = 0; ch < kHalf0; ++ch)
+          if (ch < my_chunks) tmem_ld_32x32b_x32(taddr + ch * 32, r + ch * 32);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -493,7 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t y = static_cast<int32_t>(ti.m0 + quarter * 32);
         const int32_t z = (KIND == GEMM_GROUPED_K) ? ti.group : 0;
 #pragma unroll
-        for (int ch = 0; ch < kCols / 32; ++ch) {
+        for (int ch = 0; ch < kHalf0; ++ch) {
+          if (ch >= my_chunks) break;
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
 #pragma unroll
@@ -509,17 +526,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&tmap_c, stg, static_cast<int32_t>(ti.n0 + half * kCols + ch * 32), y, z);
+            tma_store_3d(&tmap_c, stg, static_cast<int32_t>(ti.n0 + col_off + ch * 32), y, z);
             bulk_commit_group();
           }
         }
       } else if (row < ti.valid_m) {
-        const int64_t col0 = ti.n0 + half * kCols;
-        const int64_t ncols = min64(kCols, p.N - col0);
-        __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(row) * p.ldc + half * kCols;
-        if (ncols == kCols && p.c_vec) {
+        const int64_t col0 = ti.n0 + col_off;
+        const int64_t ncols = min64(my_chunks * 32, p.N - col0);
+        __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(row) * p.ldc + col_off;
+        if (ncols == my_chunks * 32 && p.c_vec) {
 #pragma unroll
           for (int j = 0; j < kCols; j += 8) {
+            if (j >= ncols) break;
             uint4 o;
             o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
             o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
@@ -651,6 +669,11 @@ int choose_bn(const GemmLaunch& L) {
   return 256;
 }
 
+template <int KIND>
+mx_status launch_bn(int bn, const GemmLaunch& L, const GParams& p, int64_t tiles_upper, cudaStream_t s) {
+  return bn == 256 ? launch_cfg<256, KIND>(L, p, tiles_upper, s) : launch_cfg<128, KIND>(L, p, tiles_upper, s);
+}
+
 }  // namespace
 
 mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
@@ -694,14 +717,11 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
 
   switch (L.kind) {
     case GEMM_DENSE:
-      return bn == 256 ? launch_cfg<256, GEMM_DENSE>(L, p, tiles_upper, s)
-                       : launch_cfg<128, GEMM_DENSE>(L, p, tiles_upper, s);
+      return launch_bn<GEMM_DENSE>(bn, L, p, tiles_upper, s);
     case GEMM_GROUPED_M:
-      return bn == 256 ? launch_cfg<256, GEMM_GROUPED_M>(L, p, tiles_upper, s)
-                       : launch_cfg<128, GEMM_GROUPED_M>(L, p, tiles_upper, s);
+      return launch_bn<GEMM_GROUPED_M>(bn, L, p, tiles_upper, s);
     default:
-      return bn == 256 ? launch_cfg<256, GEMM_GROUPED_K>(L, p, tiles_upper, s)
-                       : launch_cfg<128, GEMM_GROUPED_K>(L, p, tiles_upper, s);
+      return launch_bn<GEMM_GROUPED_K>(bn, L, p, tiles_upper, s);
   }
 }
 

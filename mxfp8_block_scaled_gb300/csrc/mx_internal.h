@@ -33,6 +33,8 @@ struct QuantLaunch {
   const int64_t* offsets;  // nullptr: dense column copy
   int n_groups;
   int64_t col_pitch;       // rows (dense) or the grouped capacity
+  int64_t batch;           // stacked matrices (1 unless batched)
+  int64_t x_batch_stride;  // elements between stacked inputs
   int* dev_status;
 };
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s);

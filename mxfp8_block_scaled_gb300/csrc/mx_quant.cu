@@ -62,6 +62,8 @@ struct QParams {
   int64_t col_pitch;
   int64_t row_ka;  // scale-column atoms of the row copy: ceil(cols/128)
   int64_t col_ka;  // scale-column atoms of the column copy: ceil(col_pitch/128)
+  int64_t batch;   // stacked matrices (1 unless batched)
+  int64_t row_data_bs, row_scale_bs, col_data_bs, col_scale_bs;  // per-matrix output strides, bytes
   int* dev_status;
   uint64_t timeout_ns;
 };
@@ -148,14 +150,17 @@ struct TileGeo {
   int64_t row0;    // first input row
   int64_t c0;      // first input column
   int64_t kpos;    // first position along the column copy's contraction
+  int64_t b;       // stacked matrix
   int valid_rows;  // input rows of this tile that belong to it
   int valid_cols;
 };
 
 template <bool kGrouped>
-__device__ __forceinline__ TileGeo tile_geo(const QParams& p, int64_t t, int64_t col_tiles, const int32_t* g_off,
-                                            const int32_t* g_tile) {
+__device__ __forceinline__ TileGeo tile_geo(const QParams& p, int64_t t, int64_t col_tiles, int64_t row_tiles,
+                                            const int32_t* g_off, const int32_t* g_tile) {
   TileGeo g;
+  g.b = t / (row_tiles * col_tiles);
+  t -= g.b * row_tiles * col_tiles;
   const int64_t rt = t / col_tiles;
   const int64_t ct = t - rt * col_tiles;
   g.c0 = ct * kTileCols;
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     }
   }
 
-  const int64_t ntiles = row_tiles * col_tiles;
+  const int64_t ntiles = row_tiles * col_tiles * p.batch;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -284,10 +289,10 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
         const int s = j % kStages;
         const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
         if (!wait_or_abort(&empty[s], ph ^ 1u, p, &s_abort)) break;
-        const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, g_off, g_tile);
+        const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile);
         mbar_arrive_expect_tx(&full[s], kTileBytes);
-        tma_load_2d(tiles + s * kTileBytes, &tmap_x, &full[s], static_cast<int32_t>(g.c0),
-                    static_cast<int32_t>(g.row0));
+        tma_load_3d(tiles + s * kTileBytes, &tmap_x, &full[s], static_cast<int32_t>(g.c0),
+                    static_cast<int32_t>(g.row0), static_cast<int32_t>(g.b));
 #pragma unroll
         for (int q = 0; q < kStages; ++q)
           if (q == s) last_phase_issued[q] = static_cast<int>(ph);
@@ -305,7 +310,11 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
       const int s = j % kStages;
       const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
-      const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, g_off, g_tile);
+      const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile);
+      uint8_t* const row_data = p.row_data + g.b * p.row_data_bs;
+      uint8_t* const row_scale = p.row_scale + g.b * p.row_scale_bs;
+      uint8_t* const col_data = p.col_data + g.b * p.col_data_bs;
+      uint8_t* const col_scale = p.col_scale + g.b * p.col_scale_bs;
       const uint32_t* tile = reinterpret_cast<const uint32_t*>(tiles + s * kTileBytes);
       uint8_t* csc = col_sc + (j & 1) * 512;
       // Every consumer runs every iteration (and every consumers_sync) even
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
           q.y = quant_word(v.z, inv, nan_block) | (quant_word(v.w, inv, nan_block) << 16);
           const int64_t grow = g.row0 + r;
           if (r < g.valid_rows && vc * 8 < g.valid_cols)
-            *reinterpret_cast<uint2*>(p.row_data + grow * p.cols + g.c0 + vc * 8) = q;
+            *reinterpret_cast<uint2*>(row_data + grow * p.cols + g.c0 + vc * 8) = q;
           // Gather the four block codes of this row (lanes 0, 4, 8, 12 of the half-warp).
           const int base = lane & 16;
           const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, code, base + 0);
@@ -342,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
           const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, code, base + 12);
           const bool write_scale = kGrouped ? (r < g.valid_rows) : true;  // dense: padding rows get zeros
           if ((lane & 15) == 0 && write_scale)
-            *reinterpret_cast<uint32_t*>(p.row_scale + scale_offset(grow, g.c0 >> 5, p.row_ka)) =
+            *reinterpret_cast<uint32_t*>(row_scale + scale_offset(grow, g.c0 >> 5, p.row_ka)) =
                 s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
         }
       }
@@ -394,12 +403,12 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
           if (block_valid) {
             const int64_t k = g.kpos + rb * 32;
             if (c < p.cols) {
-              uint4* dst = reinterpret_cast<uint4*>(p.col_data + c * p.col_pitch + k);
+              uint4* dst = reinterpret_cast<uint4*>(col_data + c * p.col_pitch + k);
               dst[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
               dst[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
             }
             if (c + 1 < p.cols) {
-              uint4* dst = reinterpret_cast<uint4*>(p.col_data + (c + 1) * p.col_pitch + k);
+              uint4* dst = reinterpret_cast<uint4*>(col_data + (c + 1) * p.col_pitch + k);
               dst[0] = make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
               dst[1] = make_uint4(out_hi[4], out_hi[5], out_hi[6], out_hi[7]);
             }
@@ -410,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
         consumers_sync();
         if (ok && tid < kTileCols) {
           const uint32_t word = *reinterpret_cast<const uint32_t*>(csc + tid * 4);
-          *reinterpret_cast<uint32_t*>(p.col_scale + scale_offset(g.c0 + tid, g.kpos >> 5, p.col_ka)) = word;
+          *reinterpret_cast<uint32_t*>(col_scale + scale_offset(g.c0 + tid, g.kpos >> 5, p.col_ka)) = word;
         }
       } else {
         if (ok) mbar_arrive(&empty[s]);
@@ -469,6 +478,11 @@ mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaSt
   p.row_ka = (q.cols + 127) / 128;
   p.col_ka = (q.col_pitch + 127) / 128;
   p.dev_status = q.dev_status;
+  p.batch = q.batch;
+  p.row_data_bs = q.rows * q.cols;
+  p.row_scale_bs = static_cast<int64_t>(mx_scale_bytes(q.rows, q.cols));
+  p.col_data_bs = q.cols * q.col_pitch;
+  p.col_scale_bs = static_cast<int64_t>(mx_scale_bytes(q.cols, q.col_pitch));
   p.timeout_ns = wait_timeout_ns();
   const bool grouped = q.offsets != nullptr && do_col;
   if (grouped && q.n_groups > kMaxGroups) {
@@ -487,18 +501,21 @@ mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaSt
   }
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(q.cols), static_cast<cuuint64_t>(q.rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.ldx * 2)};
-  cuuint32_t box[2] = {kTileCols, kTileRows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q.x), dims, strides, box, estr,
+  // [batch, rows, cols] view; a single matrix is a batch of one.
+  const int64_t bstride = q.batch > 1 ? q.x_batch_stride : q.rows * q.ldx;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.cols), static_cast<cuuint64_t>(q.rows),
+                        static_cast<cuuint64_t>(q.batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.ldx * 2), static_cast<cuuint64_t>(bstride * 2)};
+  cuuint32_t box[3] = {kTileCols, kTileRows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q.x), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled (quantiser input) failed (%d)", static_cast<int>(r));
     return MX_ERR_CUDA;
   }
-  const int64_t tiles = row_tiles * col_tiles;
+  const int64_t tiles = row_tiles * col_tiles * q.batch;
   if (grouped) {
     return do_row ? launch_one<true, true, true>(map, p, tiles, s) : launch_one<false, true, true>(map, p, tiles, s);
   }

@@ -141,3 +141,15 @@ def test_quantize_rejects_bad_arguments_on_host(L):
                       None) == INVALID
     # empty input: nothing to do, OK without touching the device
     assert _status_of(mx.mx_quantize, 0, 0, 64, 64, 1, None, None, None, None, None, 0, 0, None, None) == 0
+
+
+def test_quantize_batched_rejects_bad_arguments_on_host(L):
+    x = 0x10000
+    q = mx.mx_quantize_batched
+    assert _status_of(q, x, -1, 64, 64, 64, 4096, 3, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == INVALID
+    assert _status_of(q, x, 2, 64, 64, 64, 100, 3, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == INVALID
+    assert _status_of(q, x, 2, 64, 64, 64, 4100, 3, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == ALIGN
+    assert _status_of(q, x, 2, 48, 64, 64, 4096, 3, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == SHAPE
+    assert _status_of(q, x, 2, 64, 64, 64, 4096, 0, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == INVALID
+    assert _status_of(q, x, 2, 64, 64, 64, 4096, 3, None, 0x2000, 0x3000, 0x4000, None, None) == INVALID
+    assert _status_of(q, x, 0, 64, 64, 64, 4096, 3, None, None, None, None, None, None) == 0
