@@ -12,28 +12,38 @@
 // they are applied inside the accumulation (by the MMA itself, per 32-K step),
 // not in the epilogue (same page, §七.3).
 //
-// Kernel structure (one CTA per SM, persistent over output tiles):
+// Two kernels share the tile bookkeeping and the epilogue:
+//
+// mx_gemm_kernel (one CTA per SM, persistent over 128 x BN output tiles):
 //   warp 0      TMA producer: A and B tiles (128-byte swizzled boxes of 128 K
 //               elements) and the 512-byte scale atoms of each K block into a
 //               ring of shared-memory stages, completion on mbarriers.
-//   warp 1      allocates tensor memory; lane 0 issues, per K block, two-plus
-//               tcgen05.cp of the scale atoms into TMEM and four K=32 MMAs
-//               (scale byte selector = K step), then commits the stage back to
-//               the producer; after the last K block it commits the
-//               accumulator to the epilogue.
-//   warps 2-9   epilogue: wait for the accumulator, pull the tile out of TMEM
-//               with tcgen05.ld, release the accumulator at once (the next
-//               tile's MMAs start while this tile is still being stored),
-//               convert to BF16 and store.
+//   warp 1      allocates tensor memory; lane 0 issues, per K block, one
+//               tcgen05.cp per scale atom into TMEM and four K=32 MMAs (scale
+//               byte selector = K step), then commits the stage back to the
+//               producer; after the last K block it commits the accumulator.
+//   warps 2-9   epilogue: pull the tile out of TMEM with tcgen05.ld, release
+//               the accumulator at once, convert to BF16 and write 32 x 32
+//               boxes through swizzled shared memory with TMA stores.
+//
+// mx_gemm_pair_kernel (dense, CTA pairs = clusters of two, cta_group::2):
+//   a 256 x 256 tile per pair. Each CTA loads its 128 rows of A and its half
+//   of B (so a stage is 32 KB instead of 48 KB and six stages fit), the even
+//   CTA issues the pair-wide MMAs (M = 256) and every completion is multicast
+//   to both CTAs. The operand pipeline of the single-CTA kernel is latency
+//   bound (a stage's round trip through L2 is ~1.6 us at 4 stages in flight);
+//   halving the per-CTA bytes of B raises the stages in flight.
+//
 // Every mbarrier wait is bounded in wall time; on expiry the CTA records
 // MX_ERR_TIMEOUT in dev_status, drains its own copies and MMAs, frees its
 // tensor memory and returns.
 //
-// Grouped variants: rows-ragged (fprop/dgrad over contiguous token ranges per
-// expert; A tiles start at arbitrary rows, so the producer warp gathers their
-// scale atoms with plain loads) and contraction-ragged (wgrad; per-expert K
-// segments padded to 128, one output matrix per expert, experts with most K
-// scheduled first; an empty expert writes zeros).
+// Grouped variants (single-CTA kernel): rows-ragged (fprop/dgrad over
+// contiguous token ranges per expert; A tiles start at arbitrary rows, so the
+// producer warp gathers their scale atoms with cp.async) and
+// contraction-ragged (wgrad; per-expert K segments padded to 128, one output
+// matrix per expert, experts with most K scheduled first; an empty expert
+// writes zeros).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -51,7 +61,7 @@
 namespace mx {
 namespace {
 
-constexpr int kBM = 128;       // tile rows (MMA M)
+constexpr int kBM = 128;       // tile rows per CTA (MMA M of one CTA)
 constexpr int kBK = 128;       // K elements (= bytes) per stage: four K=32 MMAs
 constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
 constexpr int kEpiThreads = 256;
@@ -63,8 +73,8 @@ constexpr int kEpiBytes = 8 * kEpiWarpBytes;
 template <int BN>
 struct Cfg {
   // BN = 256 leaves no tensor memory for a second accumulator next to the
-  // per-stage scale columns; narrower tiles double-buffer the accumulator so
-  // the epilogue of one tile overlaps the MMAs of the next.
+  // per-stage scale columns; BN = 128 double-buffers the accumulator so the
+  // epilogue of one tile overlaps the MMAs of the next.
   static constexpr int kStages = (BN == 128) ? 6 : 4;
   static constexpr int kAcc = (BN == 256) ? 1 : 2;
   static constexpr int kABytes = kBM * kBK;
@@ -81,6 +91,24 @@ struct Cfg {
   __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
     return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + 512 + kSfbBytes) + kEpiBytes + kBarBytes +
            (grouped ? kGroupBytes : 0);
+  }
+};
+
+// CTA-pair configuration: 256 x 256 tiles, each CTA holds 128 rows of A and
+// 128 rows of B per stage plus its A scale atom and both B scale atoms.
+struct PairCfg {
+  static constexpr int BN = 256;
+  static constexpr int kStages = 6;
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = (BN / 2) * kBK;
+  static constexpr int kSfbBytes = 2 * 512;
+  static constexpr int kStageTx = kABytes + kBBytes + 512 + kSfbBytes;  // bytes one CTA loads per stage
+  static constexpr int kSfCols = 4 + 8;
+  static constexpr uint32_t kSfCol0 = BN;
+  static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
+  static constexpr size_t smem_bytes() {
+    return 1024 + static_cast<size_t>(kStages) * kStageTx + kEpiBytes + kBarBytes;
   }
 };
 
@@ -106,12 +134,12 @@ struct GParams {
 };
 
 struct Tile {
-  int64_t m0, n0;      // output tile origin within the (per-expert) C
+  int64_t m0, n0;      // output tile origin (this CTA's rows) within the (per-expert) C
   int64_t a_row;       // first row of A to load
   int64_t b_row;       // first row of B's 2-D view to load
   int64_t k_atom0;     // first 128-K block of the contraction
   int32_t nkb;         // number of 128-K blocks
-  int32_t valid_m;     // rows of the tile that exist
+  int32_t valid_m;     // rows of the tile that exist (may be <= 0 for a pair's spare tile)
   int32_t group;       // expert (grouped kinds)
   const uint8_t* sfb;  // base of B's scales for this tile's expert
   __nv_bfloat16* cbase;  // C element (m0, n0)
@@ -194,6 +222,28 @@ __device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, i
   return ti;
 }
 
+// Pair tiles: t enumerates (pair of M tiles, N tile); the CTA's rank in its
+// cluster picks the M tile, both CTAs share the 256-wide N tile.
+__device__ __forceinline__ Tile get_pair_tile(const GParams& p, int64_t t, uint32_t crank) {
+  constexpr int BN = PairCfg::BN;
+  const int64_t nt = (p.N + BN - 1) / BN;
+  const int64_t mu = ((p.M + kBM - 1) / kBM + 1) / 2;
+  const int64_t mp = p.n_fast ? t / nt : t % mu;
+  const int64_t nb = p.n_fast ? t % nt : t / mu;
+  Tile ti;
+  ti.m0 = (2 * mp + crank) * kBM;
+  ti.n0 = nb * BN;
+  ti.a_row = ti.m0;
+  ti.b_row = ti.n0 + crank * (BN / 2);
+  ti.k_atom0 = 0;
+  ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
+  ti.valid_m = static_cast<int32_t>(min64(kBM, p.M - ti.m0));
+  ti.group = 0;
+  ti.sfb = p.b_scale;
+  ti.cbase = p.c + ti.m0 * p.ldc + ti.n0;
+  return ti;
+}
+
 // Loads and checks the group offsets into shared memory; every thread calls.
 // Returns false (after recording MX_ERR_DEVICE_CHECK) if they are invalid.
 template <int KIND>
@@ -214,7 +264,7 @@ __device__ bool setup_groups(const GParams& p, GroupInfo& g, int32_t* s_flag, in
   __syncthreads();
   if (*s_flag == 0) {
     if (tid == 0) {
-      // Serial prefix: E <= 1024 small integers, once per CTA.
+      // Serial prefix: E <= 512 small integers, once per CTA.
       int32_t run = 0;
       for (int e = 0; e < E; ++e) {
         const int32_t m = g.off[e + 1] - g.off[e];
@@ -254,14 +304,17 @@ __device__ __forceinline__ void record_timeout(const GParams& p, volatile int32_
 }
 
 // Bounded wait that also gives up once another role of the CTA has aborted.
+// kCluster: acquire at cluster scope (barriers that the peer CTA signals).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const GParams& p,
                                               volatile int32_t* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto test = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (test()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (test()) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > p.timeout_ns) {
       record_timeout(p, abort_flag);
@@ -274,6 +327,68 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
+
+// Epilogue of one warp: its 32 rows (TMEM lane quarter) x my_chunks 32-column
+// chunks starting at col_off, already in registers r[] (FP32 bit patterns).
+template <int KIND, int kCols>
+__device__ __forceinline__ void store_tile(const GParams& p, const Tile& ti, const uint32_t* r, int quarter,
+                                           int lane, int my_chunks, int col_off, uint8_t* stg,
+                                           const CUtensorMap* tmap_c) {
+  const int row = quarter * 32 + lane;
+  const bool tma_tile = p.c_tma && (KIND != GEMM_GROUPED_M || ti.valid_m == kBM);
+  if (tma_tile) {
+    // Stage 32-row x 32-column BF16 boxes in this warp's 64-byte-swizzled
+    // buffer and let TMA write them (rows/columns outside C are clipped).
+    const int32_t y = static_cast<int32_t>(ti.m0 + quarter * 32);
+    const int32_t z = (KIND == GEMM_GROUPED_K) ? ti.group : 0;
+#pragma unroll
+    for (int ch = 0; ch < kCols / 32; ++ch) {
+      if (ch >= my_chunks) break;
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = ch * 32 + q * 8;
+        uint4 o;
+        o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
+        o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+        o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+        st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), o);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmap_c, stg, static_cast<int32_t>(ti.n0 + col_off + ch * 32), y, z);
+        bulk_commit_group();
+      }
+    }
+  } else if (row < ti.valid_m) {
+    const int64_t col0 = ti.n0 + col_off;
+    const int64_t ncols = min64(my_chunks * 32, p.N - col0);
+    __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(row) * p.ldc + col_off;
+    if (ncols == my_chunks * 32 && p.c_vec) {
+#pragma unroll
+      for (int j = 0; j < kCols; j += 8) {
+        if (j >= ncols) break;
+        uint4 o;
+        o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
+        o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+        o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+        *reinterpret_cast<uint4*>(dst + j) = o;
+      }
+    } else if (ncols > 0) {
+#pragma unroll
+      for (int j = 0; j < kCols; ++j)
+        if (j < ncols) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+    }
+  }
+}
+
+// ===========================================================================
+// Single-CTA kernel (dense and grouped)
+// ===========================================================================
 
 template <int BN, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -476,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kCols = kHalf0 * 32;    // register columns per thread
     const int my_chunks = half == 0 ? kHalf0 : kChunks - kHalf0;
     const int col_off = half * kHalf0 * 32;
-    const int row = quarter * 32 + lane;
+    uint8_t* stg = sEpi + (warp - 2) * kEpiWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -501,56 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc = 0;
         acc_phase ^= 1;
       }
-      const bool tma_tile = p.c_tma && (KIND != GEMM_GROUPED_M || ti.valid_m == kBM);
-      if (tma_tile) {
-        // Stage 32-row x 32-column BF16 boxes in this warp's 64-byte-swizzled
-        // buffer and let TMA write them (rows/columns outside C are clipped).
-        uint8_t* stg = sEpi + (warp - 2) * kEpiWarpBytes;
-        const int32_t y = static_cast<int32_t>(ti.m0 + quarter * 32);
-        const int32_t z = (KIND == GEMM_GROUPED_K) ? ti.group : 0;
-#pragma unroll
-        for (int ch = 0; ch < kHalf0; ++ch) {
-          if (ch >= my_chunks) break;
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int j = ch * 32 + q * 8;
-            uint4 o;
-            o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
-            o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-            o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-            o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-            st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), o);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tmap_c, stg, static_cast<int32_t>(ti.n0 + col_off + ch * 32), y, z);
-            bulk_commit_group();
-          }
-        }
-      } else if (row < ti.valid_m) {
-        const int64_t col0 = ti.n0 + col_off;
-        const int64_t ncols = min64(my_chunks * 32, p.N - col0);
-        __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(row) * p.ldc + col_off;
-        if (ncols == my_chunks * 32 && p.c_vec) {
-#pragma unroll
-          for (int j = 0; j < kCols; j += 8) {
-            if (j >= ncols) break;
-            uint4 o;
-            o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
-            o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-            o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-            o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-            *reinterpret_cast<uint4*>(dst + j) = o;
-          }
-        } else if (ncols > 0) {
-#pragma unroll
-          for (int j = 0; j < kCols; ++j)
-            if (j < ncols) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-        }
-      }
+      store_tile<KIND, kCols>(p, ti, r, quarter, lane, my_chunks, col_off, stg, &tmap_c);
     }
     // Bulk stores must have completed before the CTA's shared memory goes away.
     if (lane == 0) bulk_wait_all();
@@ -562,6 +628,202 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ===========================================================================
+// CTA-pair kernel (dense): clusters of two, tcgen05 cta_group::2, M = 256
+// ===========================================================================
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
+                        const __grid_constant__ CUtensorMap tmap_c, const GParams p) {
+  using C = PairCfg;
+  constexpr int S = C::kStages;
+  constexpr int BN = C::BN;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * C::kABytes;
+  uint8_t* sSfa = sB + S * C::kBBytes;
+  uint8_t* sSfb = sSfa + S * 512;
+  uint8_t* sEpi = sSfb + S * C::kSfbBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + kEpiBytes);  // used in the even CTA
+  uint64_t* empty_bar = full_bar + S;
+  uint64_t* acc_full = empty_bar + S;
+  uint64_t* acc_empty = acc_full + 1;  // used in the even CTA
+  uint64_t* drain_bar = acc_empty + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);   // the leader's expect_tx; both CTAs' loads complete the bytes
+      mbar_init(&empty_bar[s], 1);  // the leader's MMA commit, multicast to both CTAs
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 16);       // one arrival per epilogue warp of both CTAs
+    mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    tma_prefetch_desc(&tmap_sfa);
+    tma_prefetch_desc(&tmap_sfb);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(s_tmem, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs exist before either signals the other
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
+  const int64_t nt = (p.N + BN - 1) / BN;
+  const int64_t ntiles = (((p.M + kBM - 1) / kBM + 1) / 2) * nt;
+  const int64_t t_first = blockIdx.x >> 1;
+  const int64_t t_step = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+        const Tile ti = get_pair_tile(p, t, crank);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t lfull = mapa_shared(smem_u32(&full_bar[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kStageTx);
+          const int32_t kx = kb * kBK;
+          tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, lfull, kx, static_cast<int32_t>(ti.a_row));
+          tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, lfull, kx, static_cast<int32_t>(ti.b_row));
+          // Scale atoms through [atoms][128 words] views (rows past the end read as zero).
+          tma_load_2d_pair(sSfa + stage * 512, &tmap_sfa, lfull, 0,
+                           static_cast<int32_t>((ti.m0 >> 7) * p.ka + kb));
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load_2d_pair(sSfb + stage * C::kSfbBytes + j * 512, &tmap_sfb, lfull, 0,
+                             static_cast<int32_t>(((ti.n0 >> 7) + j) * p.ka + kb));
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (*s_abort && leader) {
+        // The leader's full barriers count both CTAs' copies: let them land.
+        int st = stage;
+        uint32_t ph = phase;
+        for (int64_t i = 0; i < min64(issued, S); ++i) {
+          if (--st < 0) {
+            st = S - 1;
+            ph ^= 1;
+          }
+          mbar_wait(&full_bar[st], ph, p.timeout_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_mxf8_e4m3(2 * kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+        const Tile ti = get_pair_tile(p, t, crank);
+        if (!wait_or_abort<true>(acc_empty, acc_phase ^ 1, p, s_abort)) break;
+        tc_fence_after_sync();
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sfa_t = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
+          const uint32_t sfb_t = sfa_t + 4;
+          tc_cp_32x128b_warpx4_pair(sfa_t, sdesc_scale_atom(smem_u32(sSfa + stage * 512)));
+          tc_cp_32x128b_warpx4_pair(sfb_t, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes)));
+          tc_cp_32x128b_warpx4_pair(sfb_t + 4, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes + 512)));
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::kABytes));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::kBBytes));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc_mma_mxf8_pair(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
+                             (kb | k) != 0 ? 1u : 0u);
+          tc_commit_pair_multicast(&empty_bar[stage], static_cast<uint16_t>(0x3));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(acc_full, static_cast<uint16_t>(0x3));
+        acc_phase ^= 1;
+      }
+      // All copies into and MMAs on tensor memory must finish before it is freed.
+      tc_commit_pair_multicast(drain_bar, static_cast<uint16_t>(0x1));
+      mbar_wait(drain_bar, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    constexpr int kCols = BN / 2;
+    const int col_off = half * kCols;
+    uint8_t* stg = sEpi + (warp - 2) * kEpiWarpBytes;
+    const uint32_t lacc_empty = mapa_shared(smem_u32(acc_empty), 0);
+    uint32_t acc_phase = 0;
+    for (int64_t t = t_first; t < ntiles; t += t_step) {
+      const Tile ti = get_pair_tile(p, t, crank);
+      if (!wait_or_abort<true>(acc_full, acc_phase, p, s_abort)) break;
+      tc_fence_after_sync();
+      uint32_t r[kCols];
+      if (ti.nkb > 0) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(col_off);
+#pragma unroll
+        for (int ch = 0; ch < kCols / 32; ++ch) tmem_ld_32x32b_x32(taddr + ch * 32, r + ch * 32);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < kCols; ++i) r[i] = 0u;
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lacc_empty);  // the even CTA's MMAs may overwrite the accumulator
+      acc_phase ^= 1;
+      store_tile<GEMM_DENSE, kCols>(p, ti, r, quarter, lane, kCols / 32, col_off, stg, &tmap_c);
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still signal it
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -587,50 +849,63 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map over an E4M3 matrix [rows, k] (pitch ld bytes), box 128 K x box_rows,
-// 128-byte swizzle, zero fill outside.
-mx_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows) {
+mx_status encode(CUtensorMap* map, CUtensorMapDataType dt, cuuint32_t rank, const void* base, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz,
+                 CUtensorMapL2promotion l2, const char* what) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
     return MX_ERR_CUDA;
   }
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
-    set_error("cuTensorMapEncodeTiled failed (%d) for rows=%lld k=%lld ld=%lld", static_cast<int>(r),
-              static_cast<long long>(rows), static_cast<long long>(k), static_cast<long long>(ld));
+    set_error("cuTensorMapEncodeTiled (%s) failed (%d)", what, static_cast<int>(r));
     return MX_ERR_CUDA;
   }
   return MX_OK;
+}
+
+// 2-D map over an E4M3 matrix [rows, k] (pitch ld bytes), box 128 K x box_rows,
+// 128-byte swizzle, zero fill outside.
+mx_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "operand");
+}
+
+// 2-D map over a swizzled scale buffer viewed as [atoms][128 x 32-bit words];
+// one box is one 512-byte atom.
+mx_status make_scale_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k) {
+  const int64_t atoms = (rows + 127) / 128 * ((k + 127) / 128);
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(atoms)};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "scales");
 }
 
 // 3-D map over the BF16 output viewed as [groups, rows, N] (row pitch ldc
 // elements, group pitch rows*ldc), box 32 x 32 x 1, 64-byte swizzle: the
 // epilogue's TMA stores clip at N and at each group's last row.
 mx_status make_out_map(CUtensorMap* map, void* c, int64_t groups, int64_t rows, int64_t N, int64_t ldc) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) {
-    set_error("cuTensorMapEncodeTiled is not available from the driver");
-    return MX_ERR_CUDA;
-  }
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(groups)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldc * 2), static_cast<cuuint64_t>(rows * ldc * 2)};
   cuuint32_t box[3] = {32, 32, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    set_error("cuTensorMapEncodeTiled (output) failed (%d)", static_cast<int>(r));
-    return MX_ERR_CUDA;
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE, "output");
+}
+
+void output_map(const GemmLaunch& L, GParams& p, CUtensorMap* mc, int kind) {
+  std::memset(mc, 0, sizeof(*mc));
+  p.c_tma = 0;
+  if (p.c_vec) {
+    const int64_t groups = (kind == GEMM_GROUPED_K) ? L.n_groups : 1;
+    if (make_out_map(mc, L.c, groups, L.M, L.N, L.ldc) == MX_OK) p.c_tma = 1;
   }
-  return MX_OK;
 }
 
 template <int BN, int KIND>
@@ -641,12 +916,7 @@ mx_status launch_cfg(const GemmLaunch& L, const GParams& p_in, int64_t tiles_upp
   if (st != MX_OK) return st;
   st = make_map(&mb, L.b_data, L.b_rows_total, L.K, L.b_ld, BN);
   if (st != MX_OK) return st;
-  std::memset(&mc, 0, sizeof(mc));
-  p.c_tma = 0;
-  if (p.c_vec) {
-    const int64_t groups = (KIND == GEMM_GROUPED_K) ? L.n_groups : 1;
-    if (make_out_map(&mc, L.c, groups, L.M, L.N, L.ldc) == MX_OK) p.c_tma = 1;
-  }
+  output_map(L, p, &mc, KIND);
   const size_t smem = Cfg<BN>::smem_bytes(KIND != GEMM_DENSE);
   auto kern = mx_gemm_kernel<BN, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -656,11 +926,49 @@ mx_status launch_cfg(const GemmLaunch& L, const GParams& p_in, int64_t tiles_upp
   return cuda_status(cudaGetLastError(), "mx_gemm launch");
 }
 
+mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) {
+  GParams p = p_in;
+  CUtensorMap ma, mb, msa, msb, mc;
+  mx_status st = make_map(&ma, L.a_data, L.M, L.K, L.a_ld, kBM);
+  if (st != MX_OK) return st;
+  st = make_map(&mb, L.b_data, L.N, L.K, L.b_ld, PairCfg::BN / 2);
+  if (st != MX_OK) return st;
+  st = make_scale_map(&msa, L.a_scale, L.M, L.K);
+  if (st != MX_OK) return st;
+  st = make_scale_map(&msb, L.b_scale, L.N, L.K);
+  if (st != MX_OK) return st;
+  output_map(L, p, &mc, GEMM_DENSE);
+  const size_t smem = PairCfg::smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(mx_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
+  const int64_t mt = (L.M + kBM - 1) / kBM;
+  const int64_t pairs = (mt + 1) / 2 * ((L.N + PairCfg::BN - 1) / PairCfg::BN);
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pairs, sm_count() / 2));
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel, ma, mb, msa, msb, mc, p),
+                     "mx_gemm launch (CTA pairs)");
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return (v && *v) ? std::atoi(v) : dflt;
+}
+
 int choose_bn(const GemmLaunch& L) {
-  static int forced = [] {
-    const char* v = std::getenv("MXFP8_GEMM_BN");
-    return v ? std::atoi(v) : 0;
-  }();
+  static const int forced = env_int("MXFP8_GEMM_BN", 0);
   if (forced == 128 || forced == 256) return forced;
   if (L.N <= 128) return 128;
   const int64_t mt = (L.M + kBM - 1) / kBM;
@@ -669,9 +977,16 @@ int choose_bn(const GemmLaunch& L) {
   return 256;
 }
 
-template <int KIND>
-mx_status launch_bn(int bn, const GemmLaunch& L, const GParams& p, int64_t tiles_upper, cudaStream_t s) {
-  return bn == 256 ? launch_cfg<256, KIND>(L, p, tiles_upper, s) : launch_cfg<128, KIND>(L, p, tiles_upper, s);
+// CTA pairs for dense GEMMs with enough 256 x 256 tiles to fill the pairs and a
+// long contraction (measured on GB300: pairs win for K >= 8192 and lose for
+// K <= 2048, where the per-tile epilogue dominates).
+bool use_pairs(const GemmLaunch& L) {
+  static const int mode = env_int("MXFP8_GEMM_PAIR", 1);
+  if (mode == 0 || L.kind != GEMM_DENSE || L.N <= 128) return false;
+  if (mode == 2) return true;
+  const int64_t mt = (L.M + kBM - 1) / kBM;
+  const int64_t pairs = (mt + 1) / 2 * ((L.N + 255) / 256);
+  return pairs >= sm_count() / 2 && L.K >= 4096;
 }
 
 }  // namespace
@@ -708,6 +1023,8 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.dev_status = L.dev_status;
   p.timeout_ns = wait_timeout_ns();
 
+  if (use_pairs(L)) return launch_pair(L, p, s);
+
   const int bn = choose_bn(L);
   const int64_t mt = (L.M + kBM - 1) / kBM;
   const int64_t nt = (L.N + bn - 1) / bn;
@@ -717,11 +1034,14 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
 
   switch (L.kind) {
     case GEMM_DENSE:
-      return launch_bn<GEMM_DENSE>(bn, L, p, tiles_upper, s);
+      return bn == 256 ? launch_cfg<256, GEMM_DENSE>(L, p, tiles_upper, s)
+                       : launch_cfg<128, GEMM_DENSE>(L, p, tiles_upper, s);
     case GEMM_GROUPED_M:
-      return launch_bn<GEMM_GROUPED_M>(bn, L, p, tiles_upper, s);
+      return bn == 256 ? launch_cfg<256, GEMM_GROUPED_M>(L, p, tiles_upper, s)
+                       : launch_cfg<128, GEMM_GROUPED_M>(L, p, tiles_upper, s);
     default:
-      return launch_bn<GEMM_GROUPED_K>(bn, L, p, tiles_upper, s);
+      return bn == 256 ? launch_cfg<256, GEMM_GROUPED_K>(L, p, tiles_upper, s)
+                       : launch_cfg<128, GEMM_GROUPED_K>(L, p, tiles_upper, s);
   }
 }
 
