@@ -18,19 +18,24 @@
 //   warp 0      TMA producer: A and B tiles (128-byte swizzled boxes of 128 K
 //               elements) and the 512-byte scale atoms of each K block into a
 //               ring of shared-memory stages, completion on mbarriers.
-//   warp 1      allocates tensor memory; lane 0 issues, per K block, one
-//               tcgen05.cp per scale atom into TMEM and four K=32 MMAs (scale
-//               byte selector = K step), then commits the stage back to the
-//               producer; after the last K block it commits the accumulator.
+//   warp 1      allocates tensor memory; lane 0 issues, per K block, four
+//               K=32 MMAs (scale byte selector = K step), then commits the
+//               stage back to the producer; after the last K block it commits
+//               the accumulator.
 //   warps 2-9   epilogue: pull the tile out of TMEM with tcgen05.ld, release
 //               the accumulator at once, convert to BF16 and write 32 x 32
-//               boxes through swizzled shared memory with TMA stores.
+//               boxes through swizzled shared memory to global memory.
+//   warp 10     scale copier: per K block, one tcgen05.cp per scale atom into
+//               the stage's TMEM slot, committed to a barrier the MMA issuer
+//               waits on. Issued from the MMA thread itself these copies sit
+//               in its instruction stream between the MMAs and cost ~10% of
+//               the tensor-pipe time; from a warp of their own they overlap.
 //
 // mx_gemm_pair_kernel (dense, CTA pairs = clusters of two, cta_group::2):
 //   a 256 x 256 tile per pair. Each CTA loads its 128 rows of A and its half
 //   of B (so a stage is 32 KB instead of 48 KB and six stages fit), the even
-//   CTA issues the pair-wide MMAs (M = 256) and every completion is multicast
-//   to both CTAs. The operand pipeline of the single-CTA kernel is latency
+//   CTA issues the pair-wide MMAs (M = 256) and scale copies, and every
+//   completion is multicast to both CTAs. The operand pipeline of the single-CTA kernel is latency
 //   bound (a stage's round trip through L2 is ~1.6 us at 4 stages in flight);
 //   halving the per-CTA bytes of B raises the stages in flight.
 //
@@ -63,12 +68,19 @@ namespace {
 
 constexpr int kBM = 128;       // tile rows per CTA (MMA M of one CTA)
 constexpr int kBK = 128;       // K elements (= bytes) per stage: four K=32 MMAs
-constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kThreads = 352;  // producer, MMA, 8 epilogue warps, scale copier
+constexpr int kCopierWarp = 10;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiWarpBytes = 32 * 64;  // one 32-row x 32-column BF16 box per epilogue warp
 constexpr int kEpiBytes = 8 * kEpiWarpBytes;
+
+// Epilogue write-out: 1 = shared-memory staging + coalesced 16-byte stores,
+// 0 = TMA tensor stores from the staging box.
+#ifndef MX_EPI_MODE
+#define MX_EPI_MODE 1
+#endif
 
 template <int BN>
 struct Cfg {
@@ -86,7 +98,7 @@ struct Cfg {
   static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
   // B tiles must start on a 128-row scale atom, so the atoms load as they are.
   static_assert(BN % 128 == 0, "tile width must be a multiple of 128");
-  static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
+  static constexpr int kBarBytes = (3 * kStages + 2 * kAcc + 2) * 8 + 16;
   static constexpr int kGroupBytes = 3 * (kMaxGroups + 1) * 4;
   __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
     return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + 512 + kSfbBytes) + kEpiBytes + kBarBytes +
@@ -96,9 +108,16 @@ struct Cfg {
 
 // CTA-pair configuration: 256 x 256 tiles, each CTA holds 128 rows of A and
 // 128 rows of B per stage plus its A scale atom and both B scale atoms.
+#ifndef MX_PAIR_STAGES
+#define MX_PAIR_STAGES 6
+#endif
+#ifndef MX_PAIR_EPI_BUFS
+#define MX_PAIR_EPI_BUFS 1
+#endif
 struct PairCfg {
   static constexpr int BN = 256;
-  static constexpr int kStages = 6;
+  static constexpr int kStages = MX_PAIR_STAGES;
+  static constexpr int kEpiBufs = MX_PAIR_EPI_BUFS;  // staging boxes per epilogue warp
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = (BN / 2) * kBK;
   static constexpr int kSfbBytes = 2 * 512;
@@ -106,9 +125,9 @@ struct PairCfg {
   static constexpr int kSfCols = 4 + 8;
   static constexpr uint32_t kSfCol0 = BN;
   static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
-  static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
+  static constexpr int kBarBytes = (3 * kStages + 4) * 8 + 16;
   static constexpr size_t smem_bytes() {
-    return 1024 + static_cast<size_t>(kStages) * kStageTx + kEpiBytes + kBarBytes;
+    return 1024 + static_cast<size_t>(kStages) * kStageTx + kEpiBufs * kEpiBytes + kBarBytes;
   }
 };
 
@@ -330,22 +349,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 // Epilogue of one warp: its 32 rows (TMEM lane quarter) x my_chunks 32-column
 // chunks starting at col_off, already in registers r[] (FP32 bit patterns).
-template <int KIND, int kCols>
+template <int KIND, int kCols, int kBufs = 1>
 __device__ __forceinline__ void store_tile(const GParams& p, const Tile& ti, const uint32_t* r, int quarter,
                                            int lane, int my_chunks, int col_off, uint8_t* stg,
                                            const CUtensorMap* tmap_c) {
   const int row = quarter * 32 + lane;
-  const bool tma_tile = p.c_tma && (KIND != GEMM_GROUPED_M || ti.valid_m == kBM);
-  if (tma_tile) {
-    // Stage 32-row x 32-column BF16 boxes in this warp's 64-byte-swizzled
-    // buffer and let TMA write them (rows/columns outside C are clipped).
-    const int32_t y = static_cast<int32_t>(ti.m0 + quarter * 32);
-    const int32_t z = (KIND == GEMM_GROUPED_K) ? ti.group : 0;
+  if (MX_EPI_MODE == 1 && p.c_vec) {
+    // Stage each 32-row x 32-column BF16 box in shared memory (64-byte
+    // swizzle: conflict-free both ways) and write it back row-major, so one
+    // warp store covers 8 rows x 64 contiguous bytes. Plain stores keep the
+    // output off the TMA unit that streams the operands.
 #pragma unroll
     for (int ch = 0; ch < kCols / 32; ++ch) {
       if (ch >= my_chunks) break;
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int j = ch * 32 + q * 8;
@@ -356,10 +372,61 @@ __device__ __forceinline__ void store_tile(const GParams& p, const Tile& ti, con
         o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
         st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), o);
       }
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int rr = q * 8 + (lane >> 2);  // row within the box
+        const int cc = lane & 3;             // 16-byte chunk within the row
+        const uint4 v = ld_shared_v4(stg + rr * 64 + ((cc ^ ((rr >> 1) & 3)) << 4));
+        const int trow = quarter * 32 + rr;
+        const int64_t tcol = col_off + ch * 32 + cc * 8;
+        const int64_t ncol = p.N - (ti.n0 + tcol);
+        if (trow < ti.valid_m && ncol > 0) {
+          __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(trow) * p.ldc + tcol;
+          if (ncol >= 8) {
+            *reinterpret_cast<uint4*>(dst) = v;
+          } else {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (e < ncol) reinterpret_cast<uint16_t*>(dst)[e] = static_cast<uint16_t>(w[e >> 1] >> ((e & 1) * 16));
+          }
+        }
+      }
+      __syncwarp();
+    }
+    return;
+  }
+  const bool tma_tile = p.c_tma && (KIND != GEMM_GROUPED_M || ti.valid_m == kBM);
+  if (tma_tile) {
+    // Stage 32-row x 32-column BF16 boxes in this warp's 64-byte-swizzled
+    // buffer and let TMA write them (rows/columns outside C are clipped).
+    const int32_t y = static_cast<int32_t>(ti.m0 + quarter * 32);
+    const int32_t z = (KIND == GEMM_GROUPED_K) ? ti.group : 0;
+#pragma unroll
+    for (int ch = 0; ch < kCols / 32; ++ch) {
+      if (ch >= my_chunks) break;
+      // A staging box is free once its previous store has been read out;
+      // with two boxes the most recent store may still be in flight.
+      if (lane == 0) {
+        if (kBufs == 2) bulk_wait_read_one_pending(); else bulk_wait_read_all();
+      }
+      __syncwarp();
+      uint8_t* box = stg + (kBufs == 2 ? (ch & 1) * kEpiWarpBytes : 0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = ch * 32 + q * 8;
+        uint4 o;
+        o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
+        o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+        o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+        st_shared_v4(box + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), o);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(tmap_c, stg, static_cast<int32_t>(ti.n0 + col_off + ch * 32), y, z);
+        tma_store_3d(tmap_c, box, static_cast<int32_t>(ti.n0 + col_off + ch * 32), y, z);
         bulk_commit_group();
       }
     }
@@ -411,7 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty_bar + S;
   uint64_t* acc_empty = acc_full + ACC;
   uint64_t* drain_bar = acc_empty + ACC;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* sf_full = drain_bar + 1;
+  uint64_t* sf_drain = sf_full + S;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(s_tmem + 1);
   int32_t* s_flag = reinterpret_cast<int32_t*>(s_tmem + 2);
   int32_t* s_total = reinterpret_cast<int32_t*>(s_tmem + 3);
@@ -439,6 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[a], kEpiThreads);
     }
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < S; ++s) mbar_init(&sf_full[s], 1);
+    mbar_init(sf_drain, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -542,20 +613,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < ti.nkb; ++kb) {
-          if (!wait_or_abort(&full_bar[stage], phase, p, s_abort)) {
+          if (!wait_or_abort(&full_bar[stage], phase, p, s_abort) ||
+              !wait_or_abort(&sf_full[stage], phase, p, s_abort)) {
             ok = false;
             break;
           }
-          // The gathered scale atom was written through the generic proxy; the
-          // tensor-core copy below reads it through the async proxy.
-          if constexpr (kGatherSfa) fence_proxy_async_smem();
           tc_fence_after_sync();
           const uint32_t sfa_t = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
           const uint32_t sfb_t = sfa_t + 4;
-          tc_cp_32x128b_warpx4(sfa_t, sdesc_scale_atom(smem_u32(sSfa + stage * 512)));
-#pragma unroll
-          for (int j = 0; j < C::kSfbAtoms; ++j)
-            tc_cp_32x128b_warpx4(sfb_t + 4 * j, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes + j * 512)));
           const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::kABytes));
           const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::kBBytes));
 #pragma unroll
@@ -580,6 +645,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       // All copies into and MMAs on tensor memory must finish before it is freed.
       tc_commit(drain_bar);
       mbar_wait(drain_bar, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == kCopierWarp) {
+    // -------------------------------------------------- scale-atom copier
+    // A stage's scale slot in tensor memory is free again once the stage's
+    // full barrier completes: the producer refilled the stage only after the
+    // MMAs that read the slot's previous contents had committed.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const Tile ti = get_tile<BN, KIND>(p, g, t);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!wait_or_abort(&full_bar[stage], phase, p, s_abort)) {
+            ok = false;
+            break;
+          }
+          // The gathered scale atom was written through the generic proxy; the
+          // tensor-core copy reads it through the async proxy.
+          if constexpr (kGatherSfa) fence_proxy_async_smem();
+          tc_fence_after_sync();
+          const uint32_t sfa = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
+          tc_cp_32x128b_warpx4(sfa, sdesc_scale_atom(smem_u32(sSfa + stage * 512)));
+#pragma unroll
+          for (int j = 0; j < C::kSfbAtoms; ++j)
+            tc_cp_32x128b_warpx4(sfa + 4 + 4 * j, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes + j * 512)));
+          tc_commit(&sf_full[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      tc_commit(sf_drain);
+      mbar_wait(sf_drain, 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
@@ -650,12 +751,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sSfa = sB + S * C::kBBytes;
   uint8_t* sSfb = sSfa + S * 512;
   uint8_t* sEpi = sSfb + S * C::kSfbBytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + kEpiBytes);  // used in the even CTA
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + C::kEpiBufs * kEpiBytes);  // used in the even CTA
   uint64_t* empty_bar = full_bar + S;
   uint64_t* acc_full = empty_bar + S;
   uint64_t* acc_empty = acc_full + 1;  // used in the even CTA
   uint64_t* drain_bar = acc_empty + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* sf_full = drain_bar + 1;  // used in the even CTA
+  uint64_t* sf_drain = sf_full + S;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -671,6 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 16);       // one arrival per epilogue warp of both CTAs
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < S; ++s) mbar_init(&sf_full[s], 1);
+    mbar_init(sf_drain, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -754,16 +859,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_or_abort<true>(acc_empty, acc_phase ^ 1, p, s_abort)) break;
         tc_fence_after_sync();
         for (int kb = 0; kb < ti.nkb; ++kb) {
-          if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort)) {
+          if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort) ||
+              !wait_or_abort<true>(&sf_full[stage], phase, p, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint32_t sfa_t = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
           const uint32_t sfb_t = sfa_t + 4;
-          tc_cp_32x128b_warpx4_pair(sfa_t, sdesc_scale_atom(smem_u32(sSfa + stage * 512)));
-          tc_cp_32x128b_warpx4_pair(sfb_t, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes)));
-          tc_cp_32x128b_warpx4_pair(sfb_t + 4, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes + 512)));
           const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::kABytes));
           const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::kBBytes));
 #pragma unroll
@@ -785,13 +888,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain_bar, 0, p.timeout_ns);
     }
     __syncwarp();
+  } else if (warp == kCopierWarp) {
+    // ------------------------------------- scale-atom copier (even CTA)
+    // A stage's slot in tensor memory is free again once its full barrier
+    // completes: the producer refilled the stage only after the MMAs that
+    // read the previous contents had committed.
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+        const Tile ti = get_pair_tile(p, t, crank);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sfa = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
+          tc_cp_32x128b_warpx4_pair(sfa, sdesc_scale_atom(smem_u32(sSfa + stage * 512)));
+          tc_cp_32x128b_warpx4_pair(sfa + 4, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes)));
+          tc_cp_32x128b_warpx4_pair(sfa + 8, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes + 512)));
+          tc_commit_pair_multicast(&sf_full[stage], static_cast<uint16_t>(0x1));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      tc_commit_pair_multicast(sf_drain, static_cast<uint16_t>(0x1));
+      mbar_wait(sf_drain, 0, p.timeout_ns);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------- epilogue (both CTAs)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     constexpr int kCols = BN / 2;
     const int col_off = half * kCols;
-    uint8_t* stg = sEpi + (warp - 2) * kEpiWarpBytes;
+    uint8_t* stg = sEpi + (warp - 2) * C::kEpiBufs * kEpiWarpBytes;
     const uint32_t lacc_empty = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t acc_phase = 0;
     for (int64_t t = t_first; t < ntiles; t += t_step) {
@@ -812,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lacc_empty);  // the even CTA's MMAs may overwrite the accumulator
       acc_phase ^= 1;
-      store_tile<GEMM_DENSE, kCols>(p, ti, r, quarter, lane, kCols / 32, col_off, stg, &tmap_c);
+      store_tile<GEMM_DENSE, kCols, C::kEpiBufs>(p, ti, r, quarter, lane, kCols / 32, col_off, stg, &tmap_c);
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
@@ -984,9 +1119,10 @@ bool use_pairs(const GemmLaunch& L) {
   static const int mode = env_int("MXFP8_GEMM_PAIR", 1);
   if (mode == 0 || L.kind != GEMM_DENSE || L.N <= 128) return false;
   if (mode == 2) return true;
+  // Pairs win whenever their 256 x 256 tiles still give every SM work.
   const int64_t mt = (L.M + kBM - 1) / kBM;
   const int64_t pairs = (mt + 1) / 2 * ((L.N + 255) / 256);
-  return pairs >= sm_count() / 2 && L.K >= 4096;
+  return pairs >= sm_count() / 2;
 }
 
 }  // namespace
