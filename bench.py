@@ -604,9 +604,9 @@ def main():
                                "fprop + dgrad + wgrad", "M": wl.M, "K": wl.K, "N": wl.N,
                    "parallelism": f"replicas{world}",
                    "l2": "no flush: a step reads/writes ~0.7 GB (> 129 MB L2)"},
-        "roofline": {"bound": "tensor", "kernel": "mx_gemm_kernel", "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": "mx_gemm_pair_kernel", "achieved": achieved,
                      "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
-                     "traffic": profile_traffic("mx_gemm_kernel"),
+                     "traffic": profile_traffic("mx_gemm_pair_kernel"),
                      "peak_source": f"{peak_src} bf16 sustained {peaks['bf16_tflops_sustained']} x nominal fp8/bf16 "
                                     f"ratio {FP8_OVER_BF16}",
                      "flops_per_launch": wl.gemm_flops(), "avg_launch_ms": gemm_ms},

@@ -12,14 +12,16 @@
 // Design: persistent CTAs (several per SM) walk 128x128 tiles of the input.
 // In each CTA a producer warp refills a 32 KB shared-memory tile buffer by
 // TMA as soon as eight consumer warps have read it, so the next load overlaps
-// their conversion and stores; the input is read from HBM exactly once. Row copy: a 1x32
-// block is four neighbouring lanes holding 8 values each (amax by two xor
-// shuffles). Column copy: each thread owns two adjacent columns of one 32-row
-// block (4-byte, bank-conflict-free shared loads). amax is an unsigned max
-// over the BF16 magnitude bits (NaN > Inf > finite), the exponent comes from
-// its bits, and the conversion is the hardware's round-to-nearest-even
-// satfinite E4M3 cvt. Scale bytes are written as whole 32-bit words of the
-// swizzled layout.
+// their conversion and stores; the input is read from HBM exactly once. The
+// tile lands as two 64-column halves in the 128-byte swizzled layout (16-byte
+// chunk c of row r at c ^ (r % 8)), which makes both passes' shared loads
+// bank-conflict free. Row copy: one thread per 1x32 block (a warp covers 8
+// rows x 4 blocks), four 16-byte loads, no shuffles, two 16-byte stores.
+// Column copy: each thread owns two adjacent columns of one 32-row block.
+// amax is an unsigned max over the BF16 magnitude bits (NaN > Inf > finite),
+// the exponent comes from its bits, and the conversion is the hardware's
+// round-to-nearest-even satfinite E4M3 cvt; blocks holding Inf or NaN take a
+// separate path only when some lane of the warp has one.
 
 #include <cuda.h>
 #include <cuda_fp8.h>
@@ -50,6 +52,7 @@ constexpr int kThreads = kConsumers + 32;     // plus one producer warp
 constexpr int kStages = MX_QUANT_STAGES;
 constexpr int kMaxGroups = 1024;
 constexpr int kTileBytes = kTileRows * kTileCols * 2;
+constexpr int kHalfCols = 64;  // columns of one swizzled TMA box (128 bytes per row)
 
 struct QParams {
   int64_t rows, cols;
@@ -99,8 +102,11 @@ __device__ __forceinline__ uint32_t nan_pair(uint32_t w) {
 }
 
 // Quantise the two BF16 values of one word (low half -> low byte).
-__device__ __forceinline__ uint32_t quant_word(uint32_t w, float inv, bool nan_block) {
-  return nan_block ? nan_pair(w) : cvt_pair(lo_f(w) * inv, hi_f(w) * inv);
+__device__ __forceinline__ uint32_t quant_word(uint32_t w, float inv) { return cvt_pair(lo_f(w) * inv, hi_f(w) * inv); }
+
+// Four BF16 values (two words) -> four E4M3 bytes.
+__device__ __forceinline__ uint32_t quant_quad(uint32_t a, uint32_t b, float inv) {
+  return quant_word(a, inv) | (quant_word(b, inv) << 16);
 }
 
 __device__ __forceinline__ uint32_t half_max(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
@@ -211,8 +217,9 @@ template <bool kRow, bool kCol, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     mx_quant_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  uint8_t* tiles = smem;                                             // kStages x [128][128] BF16
+  // 1024-byte alignment: the unit of the 128-byte swizzle pattern.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;  // kStages x 2 halves x [128 rows][128 bytes], swizzled
   uint8_t* col_sc = smem + kStages * kTileBytes;                     // 2 x [128][4] column-copy scales
   uint64_t* full = reinterpret_cast<uint64_t*>(col_sc + 1024);       // [kStages] tile landed
   uint64_t* empty = full + kStages;                                  // [kStages] tile consumed
@@ -291,8 +298,11 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
         if (!wait_or_abort(&empty[s], ph ^ 1u, p, &s_abort)) break;
         const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile);
         mbar_arrive_expect_tx(&full[s], kTileBytes);
-        tma_load_3d(tiles + s * kTileBytes, &tmap_x, &full[s], static_cast<int32_t>(g.c0),
-                    static_cast<int32_t>(g.row0), static_cast<int32_t>(g.b));
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(tiles + s * kTileBytes + h * (kTileBytes / 2), &tmap_x, &full[s],
+                      static_cast<int32_t>(g.c0 + h * kHalfCols), static_cast<int32_t>(g.row0),
+                      static_cast<int32_t>(g.b));
 #pragma unroll
         for (int q = 0; q < kStages; ++q)
           if (q == s) last_phase_issued[q] = static_cast<int>(ph);
@@ -316,43 +326,59 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
       uint8_t* const col_data = p.col_data + g.b * p.col_data_bs;
       uint8_t* const col_scale = p.col_scale + g.b * p.col_scale_bs;
       const uint32_t* tile = reinterpret_cast<const uint32_t*>(tiles + s * kTileBytes);
+      const uint4* tile16 = reinterpret_cast<const uint4*>(tiles + s * kTileBytes);
       uint8_t* csc = col_sc + (j & 1) * 512;
       // Every consumer runs every iteration (and every consumers_sync) even
       // after an abort, so the named barrier can never strand a warp.
       const bool ok = !s_abort && wait_or_abort(&full[s], ph, p, &s_abort);
 
       if (kRow && ok) {
-        // ---- row copy: a 1x32 block is four neighbouring lanes of 8 values
+        // ---- row copy: one thread per 1x32 block; lanes 8b..8b+7 take block b
+        // of eight consecutive rows, so each 8-lane load phase reads eight
+        // distinct swizzled chunk positions.
+        const int blk = lane >> 3;
+        const int rsub = lane & 7;
+        const uint4* src = tile16 + (blk >> 1) * (kTileRows * 8) + rsub * 8;
+        const int cbase = (blk & 1) * 4;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int idx = i * kConsumers + tid;
-          const int r = idx >> 4;
-          const int vc = idx & 15;
-          const uint4 v = reinterpret_cast<const uint4*>(tile)[r * 16 + vc];
-          uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-          m = half_max(m);
-          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-          const uint32_t code = scale_code(m);
+        for (int i = 0; i < 2; ++i) {
+          const int r0 = i * 64 + warp * 8;
+          const int r = r0 + rsub;
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = src[r0 * 8 + ((cbase + j) ^ rsub)];
+          uint32_t m = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            m = __vmaxu2(__vmaxu2(m, __vmaxu2(v[j].x & 0x7FFF7FFFu, v[j].y & 0x7FFF7FFFu)),
+                         __vmaxu2(v[j].z & 0x7FFF7FFFu, v[j].w & 0x7FFF7FFFu));
+          const uint32_t code = scale_code(half_max(m));
           const bool nan_block = (code == 0xFFu);
           const float inv = inv_scale(nan_block ? 0u : code);
-          uint2 q;
-          q.x = quant_word(v.x, inv, nan_block) | (quant_word(v.y, inv, nan_block) << 16);
-          q.y = quant_word(v.z, inv, nan_block) | (quant_word(v.w, inv, nan_block) << 16);
+          uint32_t q[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            q[2 * j] = quant_quad(v[j].x, v[j].y, inv);
+            q[2 * j + 1] = quant_quad(v[j].z, v[j].w, inv);
+          }
+          if (__any_sync(0xFFFFFFFFu, nan_block) && nan_block) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              q[2 * j] = nan_pair(v[j].x) | (nan_pair(v[j].y) << 16);
+              q[2 * j + 1] = nan_pair(v[j].z) | (nan_pair(v[j].w) << 16);
+            }
+          }
           const int64_t grow = g.row0 + r;
-          if (r < g.valid_rows && vc * 8 < g.valid_cols)
-            *reinterpret_cast<uint2*>(row_data + grow * p.cols + g.c0 + vc * 8) = q;
-          // Gather the four block codes of this row (lanes 0, 4, 8, 12 of the half-warp).
-          const int base = lane & 16;
-          const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, code, base + 0);
-          const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
-          const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, code, base + 8);
-          const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, code, base + 12);
-          const bool write_scale = kGrouped ? (r < g.valid_rows) : true;  // dense: padding rows get zeros
-          if ((lane & 15) == 0 && write_scale)
-            *reinterpret_cast<uint32_t*>(row_scale + scale_offset(grow, g.c0 >> 5, p.row_ka)) =
-                s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+          if (r < g.valid_rows && blk * 32 < g.valid_cols) {
+            uint4* dst = reinterpret_cast<uint4*>(row_data + grow * p.cols + g.c0 + blk * 32);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+          }
+          // Dense: rows past the end (zero-filled by the TMA) write the zero
+          // codes of the scale padding. Grouped: those rows belong to the next
+          // group's tile.
+          const bool write_scale = kGrouped ? (r < g.valid_rows) : true;
+          if (write_scale) row_scale[scale_offset(grow, (g.c0 >> 5) + blk, p.row_ka)] = static_cast<uint8_t>(code);
         }
       }
 
@@ -361,9 +387,12 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
           // ---- column copy: thread = (column pair cp, 32-row block rb) ----
           const int cp = tid & 63;
           const int rb = tid >> 6;
+          // Word cp of a 256-byte row: half cp / 32, chunk (cp / 4) % 8, word cp % 4.
+          const uint32_t* src = tile + (cp >> 5) * (kTileRows * 32) + rb * 32 * 32 + (cp & 3);
+          const int cc = (cp >> 2) & 7;
           uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = tile[(rb * 32 + i) * 64 + cp];
+          for (int i = 0; i < 32; ++i) w[i] = src[i * 32 + ((cc ^ (i & 7)) << 2)];
           mbar_arrive(&empty[s]);  // this thread is done with the tile
           if (kGrouped) {
             // rows past the group's end hold the next group's data: they count as zero padding
@@ -383,17 +412,19 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
-            if (nan_lo) {
-              out_lo[q] = nan_pair((a & 0xFFFFu) | (bb << 16)) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
-            } else {
-              out_lo[q] = cvt_pair(lo_f(a) * inv_lo, lo_f(bb) * inv_lo) |
-                          (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
-            }
-            if (nan_hi) {
-              out_hi[q] = nan_pair((a >> 16) | (bb & 0xFFFF0000u)) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
-            } else {
-              out_hi[q] = cvt_pair(hi_f(a) * inv_hi, hi_f(bb) * inv_hi) |
-                          (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
+            out_lo[q] = cvt_pair(lo_f(a) * inv_lo, lo_f(bb) * inv_lo) |
+                        (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
+            out_hi[q] = cvt_pair(hi_f(a) * inv_hi, hi_f(bb) * inv_hi) |
+                        (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
+          }
+          if (__any_sync(0xFFFFFFFFu, nan_lo || nan_hi)) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
+              if (nan_lo)
+                out_lo[q] = nan_pair((a & 0xFFFFu) | (bb << 16)) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
+              if (nan_hi)
+                out_hi[q] = nan_pair((a >> 16) | (bb & 0xFFFF0000u)) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
             }
           }
           const int64_t c = g.c0 + 2 * cp;
@@ -448,7 +479,7 @@ EncodeTiledFn encode_fn() {
 
 template <bool R, bool C, bool G>
 mx_status launch_one(const CUtensorMap& map, const QParams& p, int64_t tiles_upper, cudaStream_t s) {
-  const size_t smem = 128 + static_cast<size_t>(kStages) * kTileBytes + 1024 + 2 * kStages * 8 +
+  const size_t smem = 1024 + static_cast<size_t>(kStages) * kTileBytes + 1024 + 2 * kStages * 8 +
                       (G ? 2 * (kMaxGroups + 1) * sizeof(int32_t) : 0);
   auto kern = mx_quant_kernel<R, C, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -506,10 +537,10 @@ mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaSt
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.cols), static_cast<cuuint64_t>(q.rows),
                         static_cast<cuuint64_t>(q.batch)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.ldx * 2), static_cast<cuuint64_t>(bstride * 2)};
-  cuuint32_t box[3] = {kTileCols, kTileRows, 1};
+  cuuint32_t box[3] = {kHalfCols, kTileRows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q.x), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled (quantiser input) failed (%d)", static_cast<int>(r));
