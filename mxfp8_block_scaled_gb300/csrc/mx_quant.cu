@@ -42,17 +42,25 @@ constexpr int kTileRows = 128;
 constexpr int kTileCols = 128;
 constexpr int kConsumers = 256;               // eight math warps
 constexpr int kThreads = kConsumers + 32;     // plus one producer warp
-// Tile buffers per CTA. Measured on GB300 (M x 7168, both copies): more
-// resident CTAs beat deeper per-CTA rings; one buffer per CTA (the producer
-// refills it as soon as the consumers have read it, while they still convert
-// and store) with three register-limited CTAs per SM was best.
+// Tile buffers per CTA. Measured on GB300 (both copies, M x 7168 and
+// 8192 x 10944): two buffers per CTA with two CTAs per SM keep the most bytes
+// in flight that the shared memory allows next to the column staging buffers
+// (+5% over one buffer with three CTAs per SM; fewer CTAs with more rounds
+// each, or deeper rings with one CTA per SM, are slower).
 #ifndef MX_QUANT_STAGES
-#define MX_QUANT_STAGES 1
+#define MX_QUANT_STAGES 2
 #endif
 constexpr int kStages = MX_QUANT_STAGES;
 constexpr int kMaxGroups = 1024;
 constexpr int kTileBytes = kTileRows * kTileCols * 2;
 constexpr int kHalfCols = 64;  // columns of one swizzled TMA box (128 bytes per row)
+// 1: the column copy of a tile goes through a shared-memory staging buffer
+// and leaves as whole 128-byte output rows; 0: each thread stores its own
+// 32-byte pieces straight to global memory.
+#ifndef MX_QUANT_COL_STAGE
+#define MX_QUANT_COL_STAGE 1
+#endif
+constexpr int kColStageBytes = MX_QUANT_COL_STAGE ? kTileCols * kTileRows : 0;  // one E4M3 tile
 
 struct QParams {
   int64_t rows, cols;
@@ -208,9 +216,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   }
 }
 
-// Three resident CTAs per SM (caps registers at 75 per thread, no spills).
+// Two resident CTAs per SM.
 #ifndef MX_QUANT_MIN_BLOCKS
-#define MX_QUANT_MIN_BLOCKS 3
+#define MX_QUANT_MIN_BLOCKS 2
 #endif
 
 template <bool kRow, bool kCol, bool kGrouped>
@@ -220,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   // 1024-byte alignment: the unit of the 128-byte swizzle pattern.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;  // kStages x 2 halves x [128 rows][128 bytes], swizzled
-  uint8_t* col_sc = smem + kStages * kTileBytes;                     // 2 x [128][4] column-copy scales
+  uint8_t* col_stage = smem + kStages * kTileBytes;                  // 2 x [128 out rows][128 bytes], swizzled
+  uint8_t* col_sc = col_stage + 2 * kColStageBytes;                  // 2 x [128][4] column-copy scales
   uint64_t* full = reinterpret_cast<uint64_t*>(col_sc + 1024);       // [kStages] tile landed
   uint64_t* empty = full + kStages;                                  // [kStages] tile consumed
   int32_t* g_off = reinterpret_cast<int32_t*>(empty + kStages);      // [E+1] row offsets
@@ -427,9 +436,23 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
                 out_hi[q] = nan_pair((a >> 16) | (bb & 0xFFFF0000u)) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
             }
           }
-          const int64_t c = g.c0 + 2 * cp;
           csc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
           csc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
+#if MX_QUANT_COL_STAGE
+          // Output rows 2cp and 2cp+1, 16-byte chunks 2rb and 2rb+1 of the
+          // tile's 128 bytes along K; chunk q of row o sits at q ^ (o % 8).
+          uint8_t* stg = col_stage + (j & 1) * kColStageBytes;
+          const int o0 = 2 * cp, o1 = 2 * cp + 1;
+          *reinterpret_cast<uint4*>(stg + o0 * 128 + (((2 * rb) ^ (o0 & 7)) << 4)) =
+              make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+          *reinterpret_cast<uint4*>(stg + o0 * 128 + (((2 * rb + 1) ^ (o0 & 7)) << 4)) =
+              make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
+          *reinterpret_cast<uint4*>(stg + o1 * 128 + (((2 * rb) ^ (o1 & 7)) << 4)) =
+              make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+          *reinterpret_cast<uint4*>(stg + o1 * 128 + (((2 * rb + 1) ^ (o1 & 7)) << 4)) =
+              make_uint4(out_hi[4], out_hi[5], out_hi[6], out_hi[7]);
+#else
+          const int64_t c = g.c0 + 2 * cp;
           const bool block_valid = kGrouped ? true : (rb * 32 < g.valid_rows);
           if (block_valid) {
             const int64_t k = g.kpos + rb * 32;
@@ -444,10 +467,30 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
               dst[1] = make_uint4(out_hi[4], out_hi[5], out_hi[6], out_hi[7]);
             }
           }
+#endif
         }
         // The four 32-row blocks of a column sit in four warps: gather their
         // scale bytes (double-buffered by iteration, so one barrier suffices).
         consumers_sync();
+#if MX_QUANT_COL_STAGE
+        if (ok) {
+          // Whole output rows: eight lanes per 128-byte row, 16 bytes each.
+          const uint8_t* stg = col_stage + (j & 1) * kColStageBytes;
+#pragma unroll
+          for (int it = 0; it < (kTileCols * 8) / kConsumers; ++it) {
+            const int idx = it * kConsumers + tid;
+            const int o = idx >> 3;
+            const int q = idx & 7;
+            const int64_t c = g.c0 + o;
+            // Dense: rows past the end of the input form no block. Grouped:
+            // a segment's padding rows are zeros that must be written.
+            const bool chunk_valid = kGrouped ? true : (q * 16 < g.valid_rows);
+            if (c < p.cols && chunk_valid)
+              *reinterpret_cast<uint4*>(col_data + c * p.col_pitch + g.kpos + q * 16) =
+                  *reinterpret_cast<const uint4*>(stg + o * 128 + ((q ^ (o & 7)) << 4));
+          }
+        }
+#endif
         if (ok && tid < kTileCols) {
           const uint32_t word = *reinterpret_cast<const uint32_t*>(csc + tid * 4);
           *reinterpret_cast<uint32_t*>(col_scale + scale_offset(g.c0 + tid, g.kpos >> 5, p.col_ka)) = word;
@@ -479,7 +522,7 @@ EncodeTiledFn encode_fn() {
 
 template <bool R, bool C, bool G>
 mx_status launch_one(const CUtensorMap& map, const QParams& p, int64_t tiles_upper, cudaStream_t s) {
-  const size_t smem = 1024 + static_cast<size_t>(kStages) * kTileBytes + 1024 + 2 * kStages * 8 +
+  const size_t smem = 1024 + static_cast<size_t>(kStages) * kTileBytes + 2 * kColStageBytes + 1024 + 2 * kStages * 8 +
                       (G ? 2 * (kMaxGroups + 1) * sizeof(int32_t) : 0);
   auto kern = mx_quant_kernel<R, C, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
