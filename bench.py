@@ -169,7 +169,10 @@ class DenseFFN:
         self.M, self.K, self.N = M, K, N
         d = dense_host_inputs()
         self.host = {k: d[k].pin_memory() for k in ("X", "W", "dY")}
-        self.dev = {k: v.cuda() for k, v in self.host.items()}
+        # Two slots of device inputs and outputs, so the end-to-end run can copy
+        # one step's data while another step computes.
+        self.dev_slots = [{k: v.cuda() for k, v in self.host.items()} for _ in range(2)]
+        self.dev = self.dev_slots[0]
         self.alloc()
 
     def alloc(self):
@@ -184,8 +187,11 @@ class DenseFFN:
                                 mx.MX_COLWISE))
         self.q = {"X": copies(M, K), "W": copies(N, K), "dY": copies(M, N)}
         bf = dict(dtype=torch.bfloat16, device="cuda")
-        self.out = {"Y": torch.empty((M, N), **bf), "dX": torch.empty((M, K), **bf), "dW": torch.empty((N, K), **bf)}
-        self.host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.out.items()}
+        self.out_slots = [{"Y": torch.empty((M, N), **bf), "dX": torch.empty((M, K), **bf),
+                           "dW": torch.empty((N, K), **bf)} for _ in range(2)]
+        self.out = self.out_slots[0]
+        self.host_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.out.items()}
+                         for _ in range(2)]
 
     def gemm_flops(self):
         return 2.0 * self.M * self.N * self.K          # identical for the three modes here
@@ -206,11 +212,12 @@ class DenseFFN:
     def d2h_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.out.values())
 
-    def step(self, stream, timers=None):
+    def step(self, stream, timers=None, slot=0):
         mx = self.mx
         sp = stream.cuda_stream
+        dev, out_t = self.dev_slots[slot], self.out_slots[slot]
         for k in ("X", "W", "dY"):
-            x = self.dev[k]
+            x = dev[k]
             r, c = self.q[k]
             e = timers.span("quant", stream) if timers else None
             mx.mx_quantize(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), mx.MX_BOTH, r.data.data_ptr(),
@@ -218,20 +225,57 @@ class DenseFFN:
             if e is not None:
                 e.record(stream)
         (xr, xc), (wr, wc), (dr, dc) = self.q["X"], self.q["W"], self.q["dY"]
-        for mode, a, b, out in ((mx.MX_FPROP, xr, wr, self.out["Y"]), (mx.MX_DGRAD, dr, wc, self.out["dX"]),
-                                (mx.MX_WGRAD, dc, xc, self.out["dW"])):
+        for mode, a, b, out in ((mx.MX_FPROP, xr, wr, out_t["Y"]), (mx.MX_DGRAD, dr, wc, out_t["dX"]),
+                                (mx.MX_WGRAD, dc, xc, out_t["dW"])):
             e = timers.span("gemm", stream) if timers else None
             mx.mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), None, sp)
             if e is not None:
                 e.record(stream)
 
-    def step_e2e(self, stream):
-        with torch.cuda.stream(stream):
-            for k in self.dev:
-                self.dev[k].copy_(self.host[k], non_blocking=True)
-            self.step(stream)
-            for k in self.out:
-                self.host_out[k].copy_(self.out[k], non_blocking=True)
+    def run_e2e(self, stream, steps):
+        """`steps` end-to-end steps: each copies its inputs from pinned host memory,
+        runs the step and copies its three outputs back. Step i's inputs go in on
+        one copy stream and step i-1's outputs come out on another while step i-1
+        and step i compute, through two slots of device buffers; every copy of
+        every step stays inside the caller's timed region."""
+        h2d, d2h = self._copy_streams()
+        ev = lambda: torch.cuda.Event()
+        inputs_free = [None, None]   # slot's inputs consumed by its last step
+        outputs_free = [None, None]  # slot's outputs copied out
+        start = ev()
+        start.record(stream)
+        h2d.wait_event(start)
+        d2h.wait_event(start)
+        for i in range(steps):
+            slot = i & 1
+            if inputs_free[slot] is not None:
+                h2d.wait_event(inputs_free[slot])
+            with torch.cuda.stream(h2d):
+                for k in self.host:
+                    self.dev_slots[slot][k].copy_(self.host[k], non_blocking=True)
+            landed = ev()
+            landed.record(h2d)
+            stream.wait_event(landed)
+            if outputs_free[slot] is not None:
+                stream.wait_event(outputs_free[slot])
+            self.step(stream, slot=slot)
+            done = ev()
+            done.record(stream)
+            inputs_free[slot] = done
+            d2h.wait_event(done)
+            with torch.cuda.stream(d2h):
+                for k, t in self.out_slots[slot].items():
+                    self.host_out[slot][k].copy_(t, non_blocking=True)
+            out_done = ev()
+            out_done.record(d2h)
+            outputs_free[slot] = out_done
+        stream.wait_stream(h2d)
+        stream.wait_stream(d2h)
+
+    def _copy_streams(self):
+        if not hasattr(self, "_h2d"):
+            self._h2d, self._d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        return self._h2d, self._d2h
 
 
 # ---------------------------------------------------------------------------
@@ -580,15 +624,13 @@ def main():
     # --- end to end: pinned host inputs -> device -> step -> host outputs ---
     e2e_value = None
     if args.e2e_steps > 0:
-        for _ in range(3):
-            wl.step_e2e(stream)
+        wl.run_e2e(stream, 3)
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.e2e_steps):
-            wl.step_e2e(stream)
+        wl.run_e2e(stream, args.e2e_steps)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -615,7 +657,9 @@ def main():
                            "traffic": profile_traffic("mx_quant_kernel"), "bytes_per_launch": qbytes,
                            "avg_launch_ms": quant_ms, "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": wl.h2d_bytes(),
-                "d2h_bytes_per_step": wl.d2h_bytes(), "steps": args.e2e_steps},
+                "d2h_bytes_per_step": wl.d2h_bytes(), "steps": args.e2e_steps,
+                "overlap": "step i+1's inputs copy in and step i-1's outputs copy out while step i computes "
+                           "(two copy streams, two device buffer slots)"},
         "gpu_launches": wl.launches_per_step() * args.steps,
         "clocks": clk,
     }
