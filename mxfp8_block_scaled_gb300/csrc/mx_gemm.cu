@@ -126,8 +126,10 @@ struct PairCfg {
   static constexpr uint32_t kSfCol0 = BN;
   static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
   static constexpr int kBarBytes = (3 * kStages + 4) * 8 + 16;
-  static constexpr size_t smem_bytes() {
-    return 1024 + static_cast<size_t>(kStages) * kStageTx + kEpiBufs * kEpiBytes + kBarBytes;
+  static constexpr int kGroupBytes = 3 * (kMaxGroups + 1) * 4;
+  __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
+    return 1024 + static_cast<size_t>(kStages) * kStageTx + kEpiBufs * kEpiBytes + kBarBytes +
+           (grouped ? kGroupBytes : 0);
   }
 };
 
@@ -242,24 +244,38 @@ __device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, i
 }
 
 // Pair tiles: t enumerates (pair of M tiles, N tile); the CTA's rank in its
-// cluster picks the M tile, both CTAs share the 256-wide N tile.
-__device__ __forceinline__ Tile get_pair_tile(const GParams& p, int64_t t, uint32_t crank) {
+// cluster picks the M tile, both CTAs share the 256-wide N tile. K-ragged
+// grouped: experts in decreasing-K order, each expert's pair tiles M-fastest.
+template <int KIND>
+__device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo& g, int64_t t, uint32_t crank) {
   constexpr int BN = PairCfg::BN;
   const int64_t nt = (p.N + BN - 1) / BN;
   const int64_t mu = ((p.M + kBM - 1) / kBM + 1) / 2;
-  const int64_t mp = p.n_fast ? t / nt : t % mu;
-  const int64_t nb = p.n_fast ? t % nt : t / mu;
   Tile ti;
+  int64_t mp, nb;
+  if (KIND == GEMM_DENSE) {
+    mp = p.n_fast ? t / nt : t % mu;
+    nb = p.n_fast ? t % nt : t / mu;
+    ti.k_atom0 = 0;
+    ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
+    ti.group = 0;
+  } else {
+    const int64_t per = mu * nt;
+    const int e = g.order[t / per];
+    const int64_t rem = t % per;
+    mp = rem % mu;
+    nb = rem / mu;
+    ti.k_atom0 = g.tile[e];
+    ti.nkb = g.tile[e + 1] - g.tile[e];
+    ti.group = e;
+  }
   ti.m0 = (2 * mp + crank) * kBM;
   ti.n0 = nb * BN;
   ti.a_row = ti.m0;
   ti.b_row = ti.n0 + crank * (BN / 2);
-  ti.k_atom0 = 0;
-  ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
   ti.valid_m = static_cast<int32_t>(min64(kBM, p.M - ti.m0));
-  ti.group = 0;
   ti.sfb = p.b_scale;
-  ti.cbase = p.c + ti.m0 * p.ldc + ti.n0;
+  ti.cbase = p.c + static_cast<int64_t>(ti.group) * p.c_group_stride + ti.m0 * p.ldc + ti.n0;
   return ti;
 }
 
@@ -733,13 +749,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ===========================================================================
-// CTA-pair kernel (dense): clusters of two, tcgen05 cta_group::2, M = 256
+// CTA-pair kernel (dense and K-ragged grouped): clusters of two, tcgen05
+// cta_group::2, M = 256
 // ===========================================================================
 
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                         const __grid_constant__ CUtensorMap tmap_c, const GParams p) {
+  static_assert(KIND == GEMM_DENSE || KIND == GEMM_GROUPED_K, "pair kernel kinds");
   using C = PairCfg;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
@@ -760,11 +779,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sf_drain = sf_full + S;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(s_tmem + 1);
+  int32_t* s_flag = reinterpret_cast<int32_t*>(s_tmem + 2);
+  int32_t* s_total = reinterpret_cast<int32_t*>(s_tmem + 3);
+  GroupInfo g;
+  g.off = reinterpret_cast<int32_t*>(smem + C::smem_bytes(false) - 1024);
+  g.tile = g.off + (kMaxGroups + 1);
+  g.order = g.tile + (kMaxGroups + 1);
+  g.total = 0;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
   const bool leader = crank == 0;
+
+  // Both CTAs of a pair read the same offsets and reach the same verdict.
+  if (KIND != GEMM_DENSE) {
+    if (!setup_groups<KIND>(p, g, s_flag, s_total)) return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -795,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *s_tmem;
   const int64_t nt = (p.N + BN - 1) / BN;
-  const int64_t ntiles = (((p.M + kBM - 1) / kBM + 1) / 2) * nt;
+  const int64_t ntiles = (((p.M + kBM - 1) / kBM + 1) / 2) * nt * (KIND == GEMM_GROUPED_K ? p.n_groups : 1);
   const int64_t t_first = blockIdx.x >> 1;
   const int64_t t_step = gridDim.x >> 1;
 
@@ -807,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t issued = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile(p, t, crank);
+        const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort)) {
             ok = false;
@@ -815,16 +846,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t lfull = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kStageTx);
-          const int32_t kx = kb * kBK;
+          const int64_t katom = ti.k_atom0 + kb;
+          const int32_t kx = static_cast<int32_t>(katom * kBK);
           tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, lfull, kx, static_cast<int32_t>(ti.a_row));
           tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, lfull, kx, static_cast<int32_t>(ti.b_row));
           // Scale atoms through [atoms][128 words] views (rows past the end read as zero).
           tma_load_2d_pair(sSfa + stage * 512, &tmap_sfa, lfull, 0,
-                           static_cast<int32_t>((ti.m0 >> 7) * p.ka + kb));
+                           static_cast<int32_t>((ti.m0 >> 7) * p.ka + katom));
 #pragma unroll
           for (int j = 0; j < 2; ++j)
             tma_load_2d_pair(sSfb + stage * C::kSfbBytes + j * 512, &tmap_sfb, lfull, 0,
-                             static_cast<int32_t>(((ti.n0 >> 7) + j) * p.ka + kb));
+                             static_cast<int32_t>(((ti.n0 >> 7) + j) * p.ka + katom));
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -855,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile(p, t, crank);
+        const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
         if (!wait_or_abort<true>(acc_empty, acc_phase ^ 1, p, s_abort)) break;
         tc_fence_after_sync();
         for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -898,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile(p, t, crank);
+        const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort)) {
             ok = false;
@@ -930,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lacc_empty = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t acc_phase = 0;
     for (int64_t t = t_first; t < ntiles; t += t_step) {
-      const Tile ti = get_pair_tile(p, t, crank);
+      const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
       if (!wait_or_abort<true>(acc_full, acc_phase, p, s_abort)) break;
       tc_fence_after_sync();
       uint32_t r[kCols];
@@ -947,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lacc_empty);  // the even CTA's MMAs may overwrite the accumulator
       acc_phase ^= 1;
-      store_tile<GEMM_DENSE, kCols, C::kEpiBufs>(p, ti, r, quarter, lane, kCols / 32, col_off, stg, &tmap_c);
+      store_tile<KIND, kCols, C::kEpiBufs>(p, ti, r, quarter, lane, kCols / 32, col_off, stg, &tmap_c);
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
@@ -1061,6 +1093,7 @@ mx_status launch_cfg(const GemmLaunch& L, const GParams& p_in, int64_t tiles_upp
   return cuda_status(cudaGetLastError(), "mx_gemm launch");
 }
 
+template <int KIND>
 mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) {
   GParams p = p_in;
   CUtensorMap ma, mb, msa, msb, mc;
@@ -1072,13 +1105,14 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   if (st != MX_OK) return st;
   st = make_scale_map(&msb, L.b_scale, L.N, L.K);
   if (st != MX_OK) return st;
-  output_map(L, p, &mc, GEMM_DENSE);
-  const size_t smem = PairCfg::smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(mx_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  output_map(L, p, &mc, KIND);
+  const size_t smem = PairCfg::smem_bytes(KIND != GEMM_DENSE);
+  auto kern = mx_gemm_pair_kernel<KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
   const int64_t mt = (L.M + kBM - 1) / kBM;
-  const int64_t pairs = (mt + 1) / 2 * ((L.N + PairCfg::BN - 1) / PairCfg::BN);
+  const int64_t pairs = (mt + 1) / 2 * ((L.N + PairCfg::BN - 1) / PairCfg::BN) *
+                        (KIND == GEMM_GROUPED_K ? L.n_groups : 1);
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pairs, sm_count() / 2));
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -1093,8 +1127,7 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel, ma, mb, msa, msb, mc, p),
-                     "mx_gemm launch (CTA pairs)");
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, mc, p), "mx_gemm launch (CTA pairs)");
 }
 
 int env_int(const char* name, int dflt) {
@@ -1117,11 +1150,11 @@ int choose_bn(const GemmLaunch& L) {
 // K <= 2048, where the per-tile epilogue dominates).
 bool use_pairs(const GemmLaunch& L) {
   static const int mode = env_int("MXFP8_GEMM_PAIR", 1);
-  if (mode == 0 || L.kind != GEMM_DENSE || L.N <= 128) return false;
+  if (mode == 0 || L.kind == GEMM_GROUPED_M || L.N <= 128) return false;
   if (mode == 2) return true;
   // Pairs win whenever their 256 x 256 tiles still give every SM work.
   const int64_t mt = (L.M + kBM - 1) / kBM;
-  const int64_t pairs = (mt + 1) / 2 * ((L.N + 255) / 256);
+  const int64_t pairs = (mt + 1) / 2 * ((L.N + 255) / 256) * (L.kind == GEMM_GROUPED_K ? L.n_groups : 1);
   return pairs >= sm_count() / 2;
 }
 
@@ -1159,7 +1192,8 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.dev_status = L.dev_status;
   p.timeout_ns = wait_timeout_ns();
 
-  if (use_pairs(L)) return launch_pair(L, p, s);
+  if (use_pairs(L))
+    return L.kind == GEMM_GROUPED_K ? launch_pair<GEMM_GROUPED_K>(L, p, s) : launch_pair<GEMM_DENSE>(L, p, s);
 
   const int bn = choose_bn(L);
   const int64_t mt = (L.M + kBM - 1) / kBM;
