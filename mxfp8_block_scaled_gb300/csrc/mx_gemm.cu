@@ -125,7 +125,7 @@ struct PairCfg {
   static constexpr int kSfCols = 4 + 8;
   static constexpr uint32_t kSfCol0 = BN;
   static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
-  static constexpr int kBarBytes = (3 * kStages + 4) * 8 + 16;
+  static constexpr int kBarBytes = (4 * kStages + 4) * 8 + 16;
   static constexpr int kGroupBytes = 3 * (kMaxGroups + 1) * 4;
   __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
     return 1024 + static_cast<size_t>(kStages) * kStageTx + kEpiBufs * kEpiBytes + kBarBytes +
@@ -253,6 +253,24 @@ __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo&
   const int64_t mu = ((p.M + kBM - 1) / kBM + 1) / 2;
   Tile ti;
   int64_t mp, nb;
+  if (KIND == GEMM_GROUPED_M) {
+    // Pair row tiles of 256 inside one expert, N-fastest; the odd CTA's half
+    // of an expert's last tile may hold no rows of it (valid_m <= 0).
+    const int32_t u = static_cast<int32_t>(t / nt);
+    nb = t % nt;
+    const int e = last_le(g.tile, p.n_groups, u);
+    ti.m0 = static_cast<int64_t>(g.off[e]) + static_cast<int64_t>(u - g.tile[e]) * (2 * kBM) + crank * kBM;
+    ti.n0 = nb * BN;
+    ti.a_row = ti.m0;
+    ti.b_row = static_cast<int64_t>(e) * p.b_rows_group + ti.n0 + crank * (BN / 2);
+    ti.k_atom0 = 0;
+    ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
+    ti.valid_m = static_cast<int32_t>(min64(kBM, g.off[e + 1] - ti.m0));  // >= -127
+    ti.group = e;
+    ti.sfb = p.b_scale;
+    ti.cbase = p.c + ti.m0 * p.ldc + ti.n0;
+    return ti;
+  }
   if (KIND == GEMM_DENSE) {
     mp = p.n_fast ? t / nt : t % mu;
     nb = p.n_fast ? t % nt : t / mu;
@@ -281,8 +299,10 @@ __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo&
 
 // Loads and checks the group offsets into shared memory; every thread calls.
 // Returns false (after recording MX_ERR_DEVICE_CHECK) if they are invalid.
+// tile_rows: rows of one M tile (rows-ragged prefix of tiles per expert).
 template <int KIND>
-__device__ bool setup_groups(const GParams& p, GroupInfo& g, int32_t* s_flag, int32_t* s_total) {
+__device__ bool setup_groups(const GParams& p, GroupInfo& g, int32_t* s_flag, int32_t* s_total,
+                             int32_t tile_rows = 128) {
   const int tid = threadIdx.x;
   const int E = p.n_groups;
   if (tid == 0) *s_flag = 0;
@@ -304,7 +324,7 @@ __device__ bool setup_groups(const GParams& p, GroupInfo& g, int32_t* s_flag, in
       for (int e = 0; e < E; ++e) {
         const int32_t m = g.off[e + 1] - g.off[e];
         g.tile[e] = run;
-        run += (m + 127) / 128;
+        run += (KIND == GEMM_GROUPED_M) ? (m + tile_rows - 1) / tile_rows : (m + 127) / 128;
       }
       g.tile[E] = run;
       *s_total = run;
@@ -749,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ===========================================================================
-// CTA-pair kernel (dense and K-ragged grouped): clusters of two, tcgen05
+// CTA-pair kernel (dense and both grouped kinds): clusters of two, tcgen05
 // cta_group::2, M = 256
 // ===========================================================================
 
@@ -758,8 +778,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                         const __grid_constant__ CUtensorMap tmap_c, const GParams p) {
-  static_assert(KIND == GEMM_DENSE || KIND == GEMM_GROUPED_K, "pair kernel kinds");
   using C = PairCfg;
+  // Rows-ragged tiles start at any row: each CTA gathers its A scale atom.
+  constexpr bool kGatherSfa = (KIND == GEMM_GROUPED_M);
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
 
@@ -777,7 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain_bar = acc_empty + 1;
   uint64_t* sf_full = drain_bar + 1;  // used in the even CTA
   uint64_t* sf_drain = sf_full + S;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  uint64_t* gfull = sf_drain + 1;  // odd CTA: its own gathered scale atom landed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(gfull + S);
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(s_tmem + 1);
   int32_t* s_flag = reinterpret_cast<int32_t*>(s_tmem + 2);
   int32_t* s_total = reinterpret_cast<int32_t*>(s_tmem + 3);
@@ -794,13 +816,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Both CTAs of a pair read the same offsets and reach the same verdict.
   if (KIND != GEMM_DENSE) {
-    if (!setup_groups<KIND>(p, g, s_flag, s_total)) return;
+    if (!setup_groups<KIND>(p, g, s_flag, s_total, 2 * kBM)) return;
   }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full_bar[s], 1);   // the leader's expect_tx; both CTAs' loads complete the bytes
+      // The leader's expect_tx (both CTAs' loads complete the bytes); with a
+      // scale gather also the leader's 32 cp.async lanes and the odd CTA's relay.
+      mbar_init(&full_bar[s], kGatherSfa ? 34 : 1);
       mbar_init(&empty_bar[s], 1);  // the leader's MMA commit, multicast to both CTAs
+      mbar_init(&gfull[s], 32);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 16);       // one arrival per epilogue warp of both CTAs
@@ -826,55 +851,80 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *s_tmem;
   const int64_t nt = (p.N + BN - 1) / BN;
-  const int64_t ntiles = (((p.M + kBM - 1) / kBM + 1) / 2) * nt * (KIND == GEMM_GROUPED_K ? p.n_groups : 1);
+  const int64_t ntiles = (KIND == GEMM_GROUPED_M)
+                             ? static_cast<int64_t>(g.total) * nt
+                             : (((p.M + kBM - 1) / kBM + 1) / 2) * nt * (KIND == GEMM_GROUPED_K ? p.n_groups : 1);
   const int64_t t_first = blockIdx.x >> 1;
   const int64_t t_step = gridDim.x >> 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int64_t issued = 0;
-      bool ok = true;
-      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
-        for (int kb = 0; kb < ti.nkb; ++kb) {
-          if (!wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort)) {
-            ok = false;
-            break;
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+      const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
+      // Rows-ragged: B's scale atoms are those of the tile's expert.
+      const int64_t sfb_atom_row = (KIND == GEMM_GROUPED_M ? ti.group * p.b_ra : 0) + (ti.n0 >> 7);
+      for (int kb = 0; kb < ti.nkb; ++kb) {
+        uint32_t good = 1;
+        if (lane == 0) good = wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
+        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        const int64_t katom = ti.k_atom0 + kb;
+        if constexpr (kGatherSfa) {
+          // Scale words of A rows m0 .. m0+127 gathered into one atom with
+          // 4-byte asynchronous copies; the odd CTA counts them on a local
+          // barrier that its relay warp forwards to the leader.
+          uint8_t* dst = sSfa + stage * 512 + lane * 16;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t r = ti.a_row + lane + 32 * q;
+            const bool in = r < p.a_ra * 128;  // rows past the scale buffer read as zero
+            cp_async_4(dst + 4 * q,
+                       in ? p.a_scale + (((r >> 7) * p.ka + katom) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2)
+                          : p.a_scale,
+                       in ? 4u : 0u);
           }
+          cp_async_arrive_noinc(leader ? &full_bar[stage] : &gfull[stage]);
+        }
+        if (lane == 0) {
           const uint32_t lfull = mapa_shared(smem_u32(&full_bar[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kStageTx);
-          const int64_t katom = ti.k_atom0 + kb;
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * (C::kStageTx - (kGatherSfa ? 512 : 0)));
           const int32_t kx = static_cast<int32_t>(katom * kBK);
           tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, lfull, kx, static_cast<int32_t>(ti.a_row));
           tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, lfull, kx, static_cast<int32_t>(ti.b_row));
           // Scale atoms through [atoms][128 words] views (rows past the end read as zero).
-          tma_load_2d_pair(sSfa + stage * 512, &tmap_sfa, lfull, 0,
-                           static_cast<int32_t>((ti.m0 >> 7) * p.ka + katom));
+          if constexpr (!kGatherSfa)
+            tma_load_2d_pair(sSfa + stage * 512, &tmap_sfa, lfull, 0,
+                             static_cast<int32_t>((ti.m0 >> 7) * p.ka + katom));
 #pragma unroll
           for (int j = 0; j < 2; ++j)
             tma_load_2d_pair(sSfb + stage * C::kSfbBytes + j * 512, &tmap_sfb, lfull, 0,
-                             static_cast<int32_t>(((ti.n0 >> 7) + j) * p.ka + katom));
-          ++issued;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
-          }
+                             static_cast<int32_t>((sfb_atom_row + j) * p.ka + katom));
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-      if (*s_abort && leader) {
-        // The leader's full barriers count both CTAs' copies: let them land.
-        int st = stage;
-        uint32_t ph = phase;
-        for (int64_t i = 0; i < min64(issued, S); ++i) {
-          if (--st < 0) {
-            st = S - 1;
-            ph ^= 1;
-          }
-          mbar_wait(&full_bar[st], ph, p.timeout_ns);
+    }
+    if constexpr (kGatherSfa) cp_async_wait_all();  // no copy into this CTA's memory outlives it
+    if (*s_abort && leader && lane == 0) {
+      // The leader's full barriers count both CTAs' copies: let them land.
+      int st = stage;
+      uint32_t ph = phase;
+      for (int64_t i = 0; i < min64(issued, S); ++i) {
+        if (--st < 0) {
+          st = S - 1;
+          ph ^= 1;
         }
+        mbar_wait(&full_bar[st], ph, p.timeout_ns);
       }
     }
     __syncwarp();
@@ -925,6 +975,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A stage's slot in tensor memory is free again once its full barrier
     // completes: the producer refilled the stage only after the MMAs that
     // read the previous contents had committed.
+    if (lane == 0 && !leader && kGatherSfa) {
+      // Odd CTA: forward each stage's landed scale gather to the leader's full
+      // barrier, after making it visible to the tensor-core copies. The words
+      // sit in this CTA's own shared memory and are read by this SM's share of
+      // the pair-wide copy, which the leader can only issue after seeing this
+      // arrival; a CTA-scope arrive therefore suffices (a cluster-scope release
+      // here cost a third of the kernel's throughput).
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+        const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!wait_or_abort(&gfull[stage], phase, p, s_abort)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_smem();
+          mbar_arrive_cluster(mapa_shared(smem_u32(&full_bar[stage]), 0));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
@@ -936,6 +1012,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // The leader's gathered atom was written through the generic proxy.
+          if constexpr (kGatherSfa) fence_proxy_async_smem();
           tc_fence_after_sync();
           const uint32_t sfa = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
           tc_cp_32x128b_warpx4_pair(sfa, sdesc_scale_atom(smem_u32(sSfa + stage * 512)));
@@ -1093,26 +1171,36 @@ mx_status launch_cfg(const GemmLaunch& L, const GParams& p_in, int64_t tiles_upp
   return cuda_status(cudaGetLastError(), "mx_gemm launch");
 }
 
+// Upper bound of the 256 x 256 pair tiles (rows-ragged: one partial tile per
+// expert at most).
+int64_t pair_tiles_upper(const GemmLaunch& L) {
+  const int64_t nt = (L.N + PairCfg::BN - 1) / PairCfg::BN;
+  const int64_t mu = ((L.M + kBM - 1) / kBM + 1) / 2;
+  if (L.kind == GEMM_GROUPED_M) return (mu + L.n_groups) * nt;
+  if (L.kind == GEMM_GROUPED_K) return mu * nt * L.n_groups;
+  return mu * nt;
+}
+
 template <int KIND>
 mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) {
   GParams p = p_in;
   CUtensorMap ma, mb, msa, msb, mc;
   mx_status st = make_map(&ma, L.a_data, L.M, L.K, L.a_ld, kBM);
   if (st != MX_OK) return st;
-  st = make_map(&mb, L.b_data, L.N, L.K, L.b_ld, PairCfg::BN / 2);
+  st = make_map(&mb, L.b_data, L.b_rows_total, L.K, L.b_ld, PairCfg::BN / 2);
   if (st != MX_OK) return st;
   st = make_scale_map(&msa, L.a_scale, L.M, L.K);
   if (st != MX_OK) return st;
-  st = make_scale_map(&msb, L.b_scale, L.N, L.K);
+  // Stacked experts: one [E x row atoms x K atoms] view of all experts' scales.
+  const int64_t sfb_rows = (KIND == GEMM_GROUPED_M) ? L.n_groups * ((L.N + 127) / 128 * 128) : L.N;
+  st = make_scale_map(&msb, L.b_scale, sfb_rows, L.K);
   if (st != MX_OK) return st;
   output_map(L, p, &mc, KIND);
   const size_t smem = PairCfg::smem_bytes(KIND != GEMM_DENSE);
   auto kern = mx_gemm_pair_kernel<KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
-  const int64_t mt = (L.M + kBM - 1) / kBM;
-  const int64_t pairs = (mt + 1) / 2 * ((L.N + PairCfg::BN - 1) / PairCfg::BN) *
-                        (KIND == GEMM_GROUPED_K ? L.n_groups : 1);
+  const int64_t pairs = pair_tiles_upper(L);
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pairs, sm_count() / 2));
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -1150,12 +1238,10 @@ int choose_bn(const GemmLaunch& L) {
 // K <= 2048, where the per-tile epilogue dominates).
 bool use_pairs(const GemmLaunch& L) {
   static const int mode = env_int("MXFP8_GEMM_PAIR", 1);
-  if (mode == 0 || L.kind == GEMM_GROUPED_M || L.N <= 128) return false;
+  if (mode == 0 || L.N <= 128) return false;
   if (mode == 2) return true;
   // Pairs win whenever their 256 x 256 tiles still give every SM work.
-  const int64_t mt = (L.M + kBM - 1) / kBM;
-  const int64_t pairs = (mt + 1) / 2 * ((L.N + 255) / 256) * (L.kind == GEMM_GROUPED_K ? L.n_groups : 1);
-  return pairs >= sm_count() / 2;
+  return pair_tiles_upper(L) >= sm_count() / 2;
 }
 
 }  // namespace
@@ -1192,8 +1278,11 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.dev_status = L.dev_status;
   p.timeout_ns = wait_timeout_ns();
 
-  if (use_pairs(L))
-    return L.kind == GEMM_GROUPED_K ? launch_pair<GEMM_GROUPED_K>(L, p, s) : launch_pair<GEMM_DENSE>(L, p, s);
+  if (use_pairs(L)) {
+    if (L.kind == GEMM_GROUPED_K) return launch_pair<GEMM_GROUPED_K>(L, p, s);
+    if (L.kind == GEMM_GROUPED_M) return launch_pair<GEMM_GROUPED_M>(L, p, s);
+    return launch_pair<GEMM_DENSE>(L, p, s);
+  }
 
   const int bn = choose_bn(L);
   const int64_t mt = (L.M + kBM - 1) / kBM;

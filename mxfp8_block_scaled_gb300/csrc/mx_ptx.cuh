@@ -249,6 +249,9 @@ __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc, uin
 
 // Arrive on `bar` once every cp.async this thread issued so far has landed;
 // the barrier's expected count must include this arrival.
+// Wait until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
