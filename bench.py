@@ -562,13 +562,171 @@ def run_quant_sweep(args, rank, world, peaks, peak_src):
         print(json.dumps(line))
 
 
+def _linear_set(projs, mx):
+    """Device tensors and MX buffers for a list of (name, X, W, dY) Linear layers."""
+    layers = []
+    for name, X, W, dY in projs:
+        X, W, dY = X.cuda(), W.cuda(), dY.cuda()
+        xr, xc = mx.quantize(X, mx.MX_BOTH)
+        wr, wc = mx.quantize(W, mx.MX_BOTH)
+        dr, dc = mx.quantize(dY, mx.MX_BOTH)
+        M, K = X.shape
+        N = W.shape[0]
+        bf = dict(dtype=torch.bfloat16, device="cuda")
+        layers.append(dict(name=name, M=M, N=N, K=K, src=(X, W, dY), q=((xr, xc), (wr, wc), (dr, dc)),
+                           out=(torch.empty((M, N), **bf), torch.empty((M, K), **bf), torch.empty((N, K), **bf))))
+    return layers
+
+
+def _linear_step(layers, mx, stream, timers=None):
+    """Per layer: quantise X, W, dY (both copies each), then fprop, dgrad, wgrad."""
+    sp = stream.cuda_stream
+    for ly in layers:
+        for i, (x, (r, c)) in enumerate(zip(ly["src"], ly["q"])):
+            e = timers.span("quant", stream) if timers else None
+            mx.mx_quantize(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), mx.MX_BOTH, r.data.data_ptr(),
+                           r.scale.data_ptr(), c.data.data_ptr(), c.scale.data_ptr(), None, 0, 0, None, sp)
+            if e is not None:
+                e.record(stream)
+        (xr, xc), (wr, wc), (dr, dc) = ly["q"]
+        for j, (mode, a, b) in enumerate(((mx.MX_FPROP, xr, wr), (mx.MX_DGRAD, dr, wc), (mx.MX_WGRAD, dc, xc))):
+            out = ly["out"][j]
+            e = timers.span((ly["name"], j), stream) if timers else None
+            mx.mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), None, sp)
+            if e is not None:
+                e.record(stream)
+
+
+def _gemm_shapes(ly):
+    """(label, M, N, K) of the three GEMMs of one Linear layer."""
+    M, N, K = ly["M"], ly["N"], ly["K"]
+    return (("fprop", M, N, K), ("dgrad", M, K, N), ("wgrad", N, K, M))
+
+
+def _timed(step, args, world):
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+    timers = Timers()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    return timers, clocks
+
+
+def run_mla(args, rank, world, peaks, peak_src):
+    """MLA projection set at M = 16384 tokens (q_down 2048->1536, kv_down
+    2048->576, kv_up 512->4096, o_proj 2048->2048): per projection the three
+    quantisations and the fprop, dgrad and wgrad GEMMs. Each GEMM's roofline
+    time is max(FLOPs / FP8 peak, algorithmic bytes / HBM bandwidth)."""
+    import workloads
+    import mxfp8_block_scaled_gb300 as mx
+    projs = []
+    for name, _, _ in workloads.MLA_PROJECTIONS:
+        d = workloads.mla_projection(name)
+        projs.append((name, d["X"], d["W"], d["dY"]))
+    layers = _linear_set(projs, mx)
+    stream = torch.cuda.Stream()
+    timers, clocks = _timed(lambda t: _linear_step(layers, mx, stream, t), args, world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        _linear_step(layers, mx, stream, timers)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    per_gemm, flops_total, gemm_ms_total = [], 0.0, 0.0
+    for ly in layers:
+        for j, (label, M, N, K) in enumerate(_gemm_shapes(ly)):
+            fl = 2.0 * M * N * K
+            byts = (M * K + N * K) * (1 + 1 / 32) + 2 * M * N
+            g_ms = timers.total_ms((ly["name"], j)) / timers.count((ly["name"], j))
+            roof_ms = max(fl / (peak_fp8 * 1e12), byts / (peaks["hbm_gbs"] * 1e9)) * 1e3
+            per_gemm.append({"gemm": f"{ly['name']} {label}", "shape": [M, N, K], "ms": g_ms,
+                             "tflops": fl / (g_ms / 1e3) / 1e12, "roofline_ms": roof_ms,
+                             "bound": "tensor" if fl / (peak_fp8 * 1e12) >= byts / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                             "frac": roof_ms / g_ms})
+            flops_total += fl
+            gemm_ms_total += g_ms
+    value = world * args.steps * flops_total / (ms / 1e3) / 1e12
+    achieved = flops_total / (gemm_ms_total / 1e3) / 1e12
+    line = {"metric": "MXFP8 GEMM TFLOPS (MLA projections, fprop+dgrad+wgrad incl. MX quantisation)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": "mla_projections M=16384: q_down 2048->1536, kv_down 2048->576, "
+                                   "kv_up 512->4096, o_proj 2048->2048", "parallelism": f"replicas{world}",
+                       "l2": "no flush: a step moves ~1.5 GB (> 129 MB L2)"},
+            "per_gemm": per_gemm,
+            "roofline": {"bound": "tensor", "kernel": "mx_gemm_pair_kernel / mx_gemm_kernel", "achieved": achieved,
+                         "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}",
+                         "roofline_time_frac": sum(g["roofline_ms"] for g in per_gemm) / gemm_ms_total},
+            "gpu_launches": 6 * len(layers) * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def run_single(args, rank, world, peaks, peak_src):
+    """Single MXFP8 Linear (X[256, 512], W[256, 512]): quantise X and W (both
+    copies), then fprop. Launch-latency bound, so the line reports time."""
+    import workloads
+    import mxfp8_block_scaled_gb300 as mx
+    d = workloads.single_linear()
+    X, W = d["X"].cuda(), d["W"].cuda()
+    (xr, xc), (wr, wc) = mx.quantize(X, mx.MX_BOTH), mx.quantize(W, mx.MX_BOTH)
+    out = torch.empty((X.shape[0], W.shape[0]), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+
+    def step(timers):
+        for x, r, c in ((X, xr, xc), (W, wr, wc)):
+            e = timers.span("quant", stream) if timers else None
+            mx.mx_quantize(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), mx.MX_BOTH, r.data.data_ptr(),
+                           r.scale.data_ptr(), c.data.data_ptr(), c.scale.data_ptr(), None, 0, 0, None, sp)
+            if e is not None:
+                e.record(stream)
+        e = timers.span("gemm", stream) if timers else None
+        mx.mx_gemm(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), out.data_ptr(), out.stride(0), None, sp)
+        if e is not None:
+            e.record(stream)
+
+    timers, clocks = _timed(step, args, world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(timers)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    us = ms / args.steps * 1e3
+    line = {"metric": "single MXFP8 Linear fprop latency (quantise X and W, GEMM)", "value": us, "unit": "us",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": "single_linear M=256 N=256 K=512", "parallelism": f"replicas{world}",
+                       "l2": "inputs stay in L2 (launch-latency bound; no roofline fraction)"},
+            "per_kernel_us": {"quant": timers.total_ms("quant") / timers.count("quant") * 1e3,
+                              "gemm": timers.total_ms("gemm") / timers.count("gemm") * 1e3},
+            "gpu_launches": 3 * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dense_ffn", choices=["dense_ffn", "quant", "moe"])
+    ap.add_argument("--workload", default="dense_ffn", choices=["dense_ffn", "quant", "moe", "mla", "single"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
@@ -587,6 +745,12 @@ def main():
         return
     if args.workload == "moe":
         run_moe(args, rank, world, peaks, peak_src)
+        return
+    if args.workload == "mla":
+        run_mla(args, rank, world, peaks, peak_src)
+        return
+    if args.workload == "single":
+        run_single(args, rank, world, peaks, peak_src)
         return
     wl = DenseFFN()
     stream = torch.cuda.Stream()
