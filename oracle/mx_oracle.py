@@ -203,7 +203,7 @@ def mx_quantize_blocks(blocks) -> tuple[np.ndarray, np.ndarray]:
 
     amax = max |x| over the block; X = floor(log2 amax) - 8 (clamped);
     element code = RNE-saturating E4M3 of x * 2**-X. Power-of-two scaling is
-    exact in float64 for every BF16 input, so only the E4M3 rounding rounds.
+    exact in float64 for every BF16 or FP32 input, so only the E4M3 rounding rounds.
     """
     b = np.asarray(blocks, dtype=np.float64)
     assert b.shape[-1] == MX_BLOCK

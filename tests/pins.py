@@ -209,6 +209,35 @@ def pin_scale_hand_blocks(O):
     assert s[0] == 0xFF and c[0, 0] == 0x7F
 
 
+def pin_fp32_master_blocks(O):
+    """Hand-worked blocks of FP32 values that BF16 cannot hold ("DeepSeek-V3 16B
+    FSDP2 MXFP8/HiF8 训练设计" §8.1 and §10: weights are quantised from the
+    FP32 master). Each case below would come out differently if the input were
+    first rounded to BF16."""
+    q = lambda vals: O.mx_quantize_blocks(_block(vals)[None, :])
+    # amax 256 = 1.0 * 2**8 -> X = 0 -> code 127; 256 -> e = 15, m = 0 -> 0x78.
+    # 1.0625 is the midpoint of E4M3 1.0 (0x38) and 1.125 (0x39): ties to the even
+    # code 0x38. 1.0625 + 2**-20 (an FP32 value; BF16 would round it to 1.0625)
+    # lies above the midpoint -> 0x39, and its negative -> 0xB9.
+    s, c = q([256.0, 1.0625 + 2.0 ** -20, 1.0625, -(1.0625 + 2.0 ** -20)])
+    assert s[0] == 127 and c[0, :4].tolist() == [0x78, 0x39, 0x38, 0xB9]
+    # amax 512 - 2**-15 (FP32; BF16 rounds it up to 512 = 2**9): floor(log2) = 8 ->
+    # X = 0 -> code 127, and the element saturates to 0x7E; 3 = 1.5 * 2**1 -> 0x44.
+    s, c = q([512.0 - 2.0 ** -15, 3.0])
+    assert s[0] == 127 and c[0, 0] == 0x7E and c[0, 1] == 0x44
+    # amax 448 -> X = 0. 2**-10 is the midpoint of 0 and the smallest subnormal
+    # 2**-9: ties to even -> 0x00; 2**-10 + 2**-30 (FP32 only) lies above it -> 0x01.
+    s, c = q([448.0, 2.0 ** -10, 2.0 ** -10 + 2.0 ** -30, -(2.0 ** -10 + 2.0 ** -30)])
+    assert s[0] == 127 and c[0, :4].tolist() == [0x7E, 0x00, 0x01, 0x81]
+    # FP32 subnormal amax 3 * 2**-148: floor(log2) = -147 -> X clamps to -127 -> code 0;
+    # 3 * 2**-148 * 2**127 = 3 * 2**-21 < 2**-10 -> 0x00, its negative -> 0x80.
+    s, c = q([3 * 2.0 ** -148, -3 * 2.0 ** -148])
+    assert s[0] == 0 and c[0, 0] == 0x00 and c[0, 1] == 0x80
+    # The oracle takes the FP32 values as they are: float32 -> float64 is exact.
+    x = np.array([1.0625 + 2.0 ** -20], dtype=np.float32)
+    assert float(np.asarray(x, dtype=np.float64)[0]) == 1.0625 + 2.0 ** -20
+
+
 def pin_quant_error_bound(O):
     """Invariants of MX rounding for random blocks: each dequantised element is
     within half an E4M3 spacing of the input (<= 2**-4 relative in the normal
@@ -460,6 +489,6 @@ def pin_tolerance(O):
 ALL_PINS = [
     pin_printed_values, pin_e4m3_closed_forms, pin_e4m3_census, pin_e4m3_roundtrip_and_ties,
     pin_e4m3_vs_torch, pin_e4m3_saturation, pin_bf16_vs_torch, pin_scale_hand_blocks,
-    pin_quant_error_bound, pin_row_col_blocking, pin_scale_layout, pin_grouped_quant,
+    pin_fp32_master_blocks, pin_quant_error_bound, pin_row_col_blocking, pin_scale_layout, pin_grouped_quant,
     pin_gemm_bruteforce, pin_gemm_single_block, pin_gemm_modes, pin_grouped_gemm, pin_tolerance,
 ]

@@ -173,6 +173,11 @@ def m_bf16_truncate(O):
     O.bf16_round = r
 
 
+def m_input_bf16_prerounding(O):
+    orig = O.mx_quantize_blocks
+    O.mx_quantize_blocks = lambda blocks: orig(O.bf16_round(np.asarray(blocks, dtype=np.float64)))
+
+
 def m_tolerance_loose(O):
     O.within_tolerance = lambda out, ref, S: np.abs(np.asarray(out) - ref) <= 2.0 ** -5 * np.abs(ref) + 1e-6 * S
 
@@ -181,7 +186,7 @@ MUTANTS = [m_scale_off_by_one, m_scale_ceil, m_zero_block_scale_one, m_ties_away
            m_no_saturation, m_drop_sign, m_decode_bias8, m_decode_subnormal_hidden_one,
            m_colwise_not_transposed, m_gemm_transposed, m_gemm_drop_b_scale, m_dequant_scale_sign,
            m_swizzle_swapped, m_group_blocks_not_restarting, m_group_pad_64, m_bf16_truncate,
-           m_tolerance_loose]
+           m_tolerance_loose, m_input_bf16_prerounding]
 
 
 def _caught(O):
