@@ -162,6 +162,27 @@ mx_status mx_quantize_batched(const void* x, int64_t batch, int64_t rows, int64_
                               void* col_scale, int* dev_status, void* stream);
 
 /*
+ * mx_quantize_f32 - the weight refresh: row and column copies generated from
+ * FP32 master weights after an optimizer step ("DeepSeek-V3 16B FSDP2
+ * MXFP8/HiF8 训练设计" §8.1: weights are quantised once from the FP32 master
+ * into row/col data and scales; §10: the step data flow refreshes the MXFP8
+ * dual-axis data and E8M0 scales from the new master). The blocks are formed
+ * from the FP32 values themselves: no rounding to BF16 happens first, so a
+ * value that BF16 cannot hold quantises as itself.
+ *
+ *   x          FP32; matrix b is [rows, cols] at x + b*x_batch_stride elements,
+ *              row pitch ldx elements (ldx >= cols, a multiple of 4);
+ *              16-byte aligned; x_batch_stride >= rows*ldx and a multiple of 4
+ *              when batch > 1. A single matrix is batch = 1.
+ *   Outputs, their layouts and strides, requirements (cols % 32 == 0; rows %
+ *   32 == 0 for the column copy), alignment and error reporting are exactly
+ *   those of mx_quantize_batched. batch == 0 is a no-op.
+ */
+mx_status mx_quantize_f32(const float* x, int64_t batch, int64_t rows, int64_t cols, int64_t ldx,
+                          int64_t x_batch_stride, int axis, void* row_data, void* row_scale, void* col_data,
+                          void* col_scale, int* dev_status, void* stream);
+
+/*
  * mx_gemm - block-scaled GEMM C[M,N] = A[M,K] . B[N,K]^T with FP32 accumulation
  * and BF16 output rounded to nearest even ([DSV3] §8 and §13.4
  * low_precision_matmul; [TT] npu_quant_matmul; [FMT] §五.1).

@@ -28,8 +28,8 @@ STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAP
                 4: "MX_ERR_CUDA", 5: "MX_ERR_DEVICE_CHECK", 6: "MX_ERR_TIMEOUT", 7: "MX_ERR_NO_DEVICE"}
 
 # Symbols the header declares (the CPU tests check the library exports them).
-EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quantize_batched", "mx_gemm",
-            "mx_grouped_gemm", "mx_status_string", "mx_last_error", "mx_abi_version")
+EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quantize_batched", "mx_quantize_f32",
+            "mx_gemm", "mx_grouped_gemm", "mx_status_string", "mx_last_error", "mx_abi_version")
 
 
 class MXError(RuntimeError):
@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
     L.mx_quantize.restype = i32
     L.mx_quantize_batched.argtypes = [vp, i64, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp]
     L.mx_quantize_batched.restype = i32
+    L.mx_quantize_f32.argtypes = [vp, i64, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp]
+    L.mx_quantize_f32.restype = i32
     L.mx_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp, vp]
     L.mx_gemm.restype = i32
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
@@ -120,6 +122,12 @@ def mx_quantize_batched(x, batch, rows, cols, ldx, x_batch_stride, axis, row_dat
                         dev_status, stream) -> None:
     _check(lib().mx_quantize_batched(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, row_scale, col_data,
                                      col_scale, dev_status, stream), "mx_quantize_batched")
+
+
+def mx_quantize_f32(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, row_scale, col_data, col_scale,
+                    dev_status, stream) -> None:
+    _check(lib().mx_quantize_f32(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, row_scale, col_data,
+                                 col_scale, dev_status, stream), "mx_quantize_f32")
 
 
 def _ref(op):
@@ -181,11 +189,13 @@ def read_status(status) -> int:
 
 def quantize(x, axis: int = MX_BOTH, group_offsets=None, col_capacity: Optional[int] = None, status=None,
              stream=None):
-    """MX-quantise a 2-D BF16 CUDA tensor. Returns (row_copy, col_copy), each an
-    MXTensor or None. With ``group_offsets`` (int64 CUDA tensor [E+1]) the
-    column copy is per-group padded with width ``col_capacity``."""
+    """MX-quantise a 2-D BF16 (or FP32, no groups) CUDA tensor. Returns
+    (row_copy, col_copy), each an MXTensor or None. With ``group_offsets``
+    (int64 CUDA tensor [E+1]) the column copy is per-group padded with width
+    ``col_capacity``."""
     torch = _torch()
-    assert x.dim() == 2 and x.dtype == torch.bfloat16 and x.is_cuda and x.stride(1) == 1
+    assert x.dim() == 2 and x.dtype in (torch.bfloat16, torch.float32) and x.is_cuda and x.stride(1) == 1
+    assert x.dtype == torch.bfloat16 or group_offsets is None
     R, C = x.shape
     dev = x.device
     row = col = None
@@ -203,6 +213,12 @@ def quantize(x, axis: int = MX_BOTH, group_offsets=None, col_capacity: Optional[
         else:
             col = MXTensor(torch.empty((C, R), dtype=torch.uint8, device=dev),
                            torch.empty(mx_scale_bytes(C, R), dtype=torch.uint8, device=dev), C, R, MX_COLWISE)
+    if x.dtype == torch.float32:
+        mx_quantize_f32(x.data_ptr(), 1, R, C, x.stride(0), 0, axis,
+                        _ptr(row.data) if row else None, _ptr(row.scale) if row else None,
+                        _ptr(col.data) if col else None, _ptr(col.scale) if col else None,
+                        _ptr(status), _stream(stream))
+        return row, col
     mx_quantize(x.data_ptr(), R, C, x.stride(0), axis,
                 _ptr(row.data) if row else None, _ptr(row.scale) if row else None,
                 _ptr(col.data) if col else None, _ptr(col.scale) if col else None,
@@ -235,8 +251,9 @@ class MXStacked:
 
 
 def quantize_stacked(w, axis: int, status=None, stream=None):
-    """Quantise stacked expert weights w[E, N, K] (BF16) in one batched launch.
-    Returns (row_stack [E][N][K], col_stack [E][K][N]); entries None if not asked."""
+    """Quantise stacked expert weights w[E, N, K] (BF16, or the FP32 master) in
+    one batched launch. Returns (row_stack [E][N][K], col_stack [E][K][N]);
+    entries None if not asked."""
     torch = _torch()
     E, N, K = w.shape
     dev = w.device
@@ -247,11 +264,12 @@ def quantize_stacked(w, axis: int, status=None, stream=None):
     if axis & MX_COLWISE:
         col = MXStacked(torch.empty((E, K, N), dtype=torch.uint8, device=dev),
                         torch.empty((E, mx_scale_bytes(K, N)), dtype=torch.uint8, device=dev), K, N, MX_COLWISE)
-    assert w.stride(2) == 1
-    mx_quantize_batched(w.data_ptr(), E, N, K, w.stride(1), w.stride(0), axis,
-                        _ptr(row.data) if row else None, _ptr(row.scale) if row else None,
-                        _ptr(col.data) if col else None, _ptr(col.scale) if col else None,
-                        _ptr(status), _stream(stream))
+    assert w.stride(2) == 1 and w.dtype in (torch.bfloat16, torch.float32)
+    fn = mx_quantize_f32 if w.dtype == torch.float32 else mx_quantize_batched
+    fn(w.data_ptr(), E, N, K, w.stride(1), w.stride(0), axis,
+       _ptr(row.data) if row else None, _ptr(row.scale) if row else None,
+       _ptr(col.data) if col else None, _ptr(col.scale) if col else None,
+       _ptr(status), _stream(stream))
     return row, col
 
 

@@ -158,6 +158,84 @@ int sm_count() {
 
 using namespace mx;
 
+// Stacked dense quantisation with BF16 (elem 2) or FP32 (elem 4) input.
+static mx_status quantize_stacked(const char* fn, int elem, const void* x, int64_t batch, int64_t rows, int64_t cols,
+                                  int64_t ldx, int64_t x_batch_stride, int axis, void* row_data, void* row_scale,
+                                  void* col_data, void* col_scale, int* dev_status, void* stream) {
+  const int64_t align_elems = 16 / elem;  // elements per 16 bytes
+  if (batch < 0 || x_batch_stride < 0) {
+    set_error("%s: negative batch or stride", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (batch > 1 && x_batch_stride < rows * ldx) {
+    set_error("%s: x_batch_stride < rows * ldx", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (batch > 1 && x_batch_stride % align_elems != 0) {
+    set_error("%s: x_batch_stride must be a multiple of 16 bytes", fn);
+    return MX_ERR_ALIGNMENT;
+  }
+  if (batch > 0x7FFFFFFFLL) {
+    set_error("%s: batch must be < 2^31", fn);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  // Per-matrix validation is the dense mx_quantize's; a zero-size problem is a no-op.
+  if (batch == 0) {
+    return (axis == MX_ROWWISE || axis == MX_COLWISE || axis == MX_BOTH) ? MX_OK : MX_ERR_INVALID_ARG;
+  }
+  if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) {
+    set_error("%s: axis must be MX_ROWWISE, MX_COLWISE or MX_BOTH", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (rows < 0 || cols < 0 || ldx < cols) {
+    set_error("%s: bad sizes", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (rows > 0x7FFFFFFFLL) {
+    set_error("%s: rows must be < 2^31", fn);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  const bool do_row = (axis & MX_ROWWISE) != 0;
+  const bool do_col = (axis & MX_COLWISE) != 0;
+  if (cols % 32 != 0 || (do_col && rows % 32 != 0)) {
+    set_error("%s: cols (and rows for the column copy) must be multiples of 32", fn);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (rows == 0 || cols == 0) return MX_OK;
+  if (!x || !aligned16(x) || ldx % align_elems != 0) {
+    set_error("%s: x must be non-null and 16-byte aligned, rows 16-byte aligned (ldx)", fn);
+    return x ? MX_ERR_ALIGNMENT : MX_ERR_INVALID_ARG;
+  }
+  if ((do_row && (!row_data || !row_scale)) || (do_col && (!col_data || !col_scale))) {
+    set_error("%s: a requested output is null", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if ((do_row && (!aligned16(row_data) || !aligned16(row_scale))) ||
+      (do_col && (!aligned16(col_data) || !aligned16(col_scale)))) {
+    set_error("%s: outputs must be 16-byte aligned", fn);
+    return MX_ERR_ALIGNMENT;
+  }
+  mx_status st = check_device();
+  if (st != MX_OK) return st;
+  QuantLaunch q;
+  q.x = x;
+  q.rows = rows;
+  q.cols = cols;
+  q.ldx = ldx;
+  q.row_data = row_data;
+  q.row_scale = row_scale;
+  q.col_data = col_data;
+  q.col_scale = col_scale;
+  q.offsets = nullptr;
+  q.n_groups = 0;
+  q.col_pitch = rows;
+  q.batch = batch;
+  q.x_batch_stride = x_batch_stride;
+  q.x_f32 = (elem == 4);
+  q.dev_status = dev_status;
+  return launch_quantize(q, do_row, do_col, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" {
 
 int mx_abi_version(void) { return MXFP8_ABI_VERSION; }
@@ -281,76 +359,15 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, in
 mx_status mx_quantize_batched(const void* x, int64_t batch, int64_t rows, int64_t cols, int64_t ldx,
                               int64_t x_batch_stride, int axis, void* row_data, void* row_scale, void* col_data,
                               void* col_scale, int* dev_status, void* stream) {
-  if (batch < 0 || x_batch_stride < 0) {
-    set_error("mx_quantize_batched: negative batch or stride");
-    return MX_ERR_INVALID_ARG;
-  }
-  if (batch > 1 && x_batch_stride < rows * ldx) {
-    set_error("mx_quantize_batched: x_batch_stride < rows * ldx");
-    return MX_ERR_INVALID_ARG;
-  }
-  if (batch > 1 && x_batch_stride % 8 != 0) {
-    set_error("mx_quantize_batched: x_batch_stride must be a multiple of 8");
-    return MX_ERR_ALIGNMENT;
-  }
-  if (batch > 0x7FFFFFFFLL) {
-    set_error("mx_quantize_batched: batch must be < 2^31");
-    return MX_ERR_UNSUPPORTED_SHAPE;
-  }
-  // Per-matrix validation is the dense mx_quantize's; a zero-size problem is a no-op.
-  if (batch == 0) {
-    return (axis == MX_ROWWISE || axis == MX_COLWISE || axis == MX_BOTH) ? MX_OK : MX_ERR_INVALID_ARG;
-  }
-  if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) {
-    set_error("mx_quantize_batched: axis must be MX_ROWWISE, MX_COLWISE or MX_BOTH");
-    return MX_ERR_INVALID_ARG;
-  }
-  if (rows < 0 || cols < 0 || ldx < cols) {
-    set_error("mx_quantize_batched: bad sizes");
-    return MX_ERR_INVALID_ARG;
-  }
-  if (rows > 0x7FFFFFFFLL) {
-    set_error("mx_quantize_batched: rows must be < 2^31");
-    return MX_ERR_UNSUPPORTED_SHAPE;
-  }
-  const bool do_row = (axis & MX_ROWWISE) != 0;
-  const bool do_col = (axis & MX_COLWISE) != 0;
-  if (cols % 32 != 0 || (do_col && rows % 32 != 0)) {
-    set_error("mx_quantize_batched: cols (and rows for the column copy) must be multiples of 32");
-    return MX_ERR_UNSUPPORTED_SHAPE;
-  }
-  if (rows == 0 || cols == 0) return MX_OK;
-  if (!x || !aligned16(x) || ldx % 8 != 0) {
-    set_error("mx_quantize_batched: x must be non-null, 16-byte aligned, ldx a multiple of 8");
-    return x ? MX_ERR_ALIGNMENT : MX_ERR_INVALID_ARG;
-  }
-  if ((do_row && (!row_data || !row_scale)) || (do_col && (!col_data || !col_scale))) {
-    set_error("mx_quantize_batched: a requested output is null");
-    return MX_ERR_INVALID_ARG;
-  }
-  if ((do_row && (!aligned16(row_data) || !aligned16(row_scale))) ||
-      (do_col && (!aligned16(col_data) || !aligned16(col_scale)))) {
-    set_error("mx_quantize_batched: outputs must be 16-byte aligned");
-    return MX_ERR_ALIGNMENT;
-  }
-  mx_status st = check_device();
-  if (st != MX_OK) return st;
-  QuantLaunch q;
-  q.x = x;
-  q.rows = rows;
-  q.cols = cols;
-  q.ldx = ldx;
-  q.row_data = row_data;
-  q.row_scale = row_scale;
-  q.col_data = col_data;
-  q.col_scale = col_scale;
-  q.offsets = nullptr;
-  q.n_groups = 0;
-  q.col_pitch = rows;
-  q.batch = batch;
-  q.x_batch_stride = x_batch_stride;
-  q.dev_status = dev_status;
-  return launch_quantize(q, do_row, do_col, static_cast<cudaStream_t>(stream));
+  return quantize_stacked("mx_quantize_batched", 2, x, batch, rows, cols, ldx, x_batch_stride, axis, row_data,
+                          row_scale, col_data, col_scale, dev_status, stream);
+}
+
+mx_status mx_quantize_f32(const float* x, int64_t batch, int64_t rows, int64_t cols, int64_t ldx,
+                          int64_t x_batch_stride, int axis, void* row_data, void* row_scale, void* col_data,
+                          void* col_scale, int* dev_status, void* stream) {
+  return quantize_stacked("mx_quantize_f32", 4, x, batch, rows, cols, ldx, x_batch_stride, axis, row_data,
+                          row_scale, col_data, col_scale, dev_status, stream);
 }
 
 mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,

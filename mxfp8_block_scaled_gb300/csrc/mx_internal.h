@@ -35,6 +35,7 @@ struct QuantLaunch {
   int64_t col_pitch;       // rows (dense) or the grouped capacity
   int64_t batch;           // stacked matrices (1 unless batched)
   int64_t x_batch_stride;  // elements between stacked inputs
+  bool x_f32 = false;      // FP32 input (else BF16)
   int* dev_status;
 };
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s);

@@ -502,6 +502,220 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   }
 }
 
+// ===========================================================================
+// FP32 input (weight refresh from the FP32 master)
+// ===========================================================================
+//
+// "DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §8.1 and §10: after each
+// optimizer step the row and column copies of the weights are produced from the
+// FP32 master, so the blocks are formed from the FP32 values themselves (no BF16
+// rounding on the way). Same rule and layouts as the BF16 kernel; the tile is
+// 128 rows x 64 columns (32 KB), landing as two 32-column boxes in the 128-byte
+// swizzled layout (16-byte chunk c of row r at c ^ (r % 8)).
+
+constexpr int kF32Cols = 64;
+constexpr int kF32BoxCols = 32;
+constexpr int kF32TileBytes = kTileRows * kF32Cols * 4;
+constexpr int kF32StageBytes = kF32Cols * kTileRows;  // one E4M3 column-copy tile
+
+// E8M0 code from the largest FP32 magnitude pattern of a block.
+__device__ __forceinline__ uint32_t scale_code_f32(uint32_t amax_bits) {
+  const int e = static_cast<int>(amax_bits >> 23);  // biased exponent
+  if (e == 0xFF) return 0xFFu;                       // block holds Inf or NaN
+  return static_cast<uint32_t>(max(e - 127 - 8, -127) + 127);
+}
+
+// NaN codes keeping the signs of two FP32 values (a in the low byte).
+__device__ __forceinline__ uint32_t nan_pair_f32(uint32_t a, uint32_t b) {
+  return (0x7Fu | ((a >> 24) & 0x80u)) | ((0x7Fu | ((b >> 24) & 0x80u)) << 8);
+}
+
+// Four FP32 values -> four E4M3 bytes (first value in the low byte).
+__device__ __forceinline__ uint32_t quant4_f32(float a, float b, float c, float d, float inv) {
+  return cvt_pair(a * inv, b * inv) | (cvt_pair(c * inv, d * inv) << 16);
+}
+
+template <bool kRow, bool kCol>
+__global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
+    mx_quant_f32_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;                                        // kStages x 2 boxes x [128 rows][128 bytes]
+  uint8_t* col_stage = tiles + kStages * kF32TileBytes;         // 2 x [64 out rows][128 bytes], swizzled
+  uint8_t* col_sc = col_stage + 2 * kF32StageBytes;             // 2 x [64][4] column-copy scales
+  uint64_t* full = reinterpret_cast<uint64_t*>(col_sc + 512);
+  uint64_t* empty = full + kStages;
+  __shared__ volatile int32_t s_abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t col_tiles = (p.cols + kF32Cols - 1) / kF32Cols;
+  const int64_t row_tiles = (p.rows + kTileRows - 1) / kTileRows;
+  const int64_t ntiles = row_tiles * col_tiles * p.batch;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumers / 32) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_x);
+      int j = 0;
+      int last_phase_issued[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_phase_issued[s] = -1;
+      for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
+        if (!wait_or_abort(&empty[s], ph ^ 1u, p, &s_abort)) break;
+        const int64_t b = t / (row_tiles * col_tiles);
+        const int64_t rem = t - b * row_tiles * col_tiles;
+        const int64_t rt = rem / col_tiles, ct = rem - rt * col_tiles;
+        mbar_arrive_expect_tx(&full[s], kF32TileBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(tiles + s * kF32TileBytes + h * (kF32TileBytes / 2), &tmap_x, &full[s],
+                      static_cast<int32_t>(ct * kF32Cols + h * kF32BoxCols), static_cast<int32_t>(rt * kTileRows),
+                      static_cast<int32_t>(b));
+#pragma unroll
+        for (int q = 0; q < kStages; ++q)
+          if (q == s) last_phase_issued[q] = static_cast<int>(ph);
+      }
+      if (s_abort) {
+#pragma unroll
+        for (int q = 0; q < kStages; ++q)
+          if (last_phase_issued[q] >= 0) mbar_wait(&full[q], static_cast<uint32_t>(last_phase_issued[q]), p.timeout_ns);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- consumers
+    int j = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
+      const int s = j % kStages;
+      const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
+      const int64_t b = t / (row_tiles * col_tiles);
+      const int64_t rem = t - b * row_tiles * col_tiles;
+      const int64_t rt = rem / col_tiles, ct = rem - rt * col_tiles;
+      const int64_t row0 = rt * kTileRows, c0 = ct * kF32Cols;
+      const int valid_rows = static_cast<int>(min64(kTileRows, p.rows - row0));
+      const int valid_cols = static_cast<int>(min64(kF32Cols, p.cols - c0));
+      uint8_t* const row_data = p.row_data + b * p.row_data_bs;
+      uint8_t* const row_scale = p.row_scale + b * p.row_scale_bs;
+      uint8_t* const col_data = p.col_data + b * p.col_data_bs;
+      uint8_t* const col_scale = p.col_scale + b * p.col_scale_bs;
+      const uint8_t* tile = tiles + s * kF32TileBytes;
+      uint8_t* csc = col_sc + (j & 1) * 256;
+      uint8_t* stg = col_stage + (j & 1) * kF32StageBytes;
+      const bool ok = !s_abort && wait_or_abort(&full[s], ph, p, &s_abort);
+
+      if (kRow && ok) {
+        // ---- row copy: thread = (row r, 32-column block = box blk); the eight
+        // lanes of a load phase hold eight consecutive rows -> distinct chunks.
+        const int r = (warp & 3) * 32 + lane;
+        const int blk = warp >> 2;
+        const uint4* src = reinterpret_cast<const uint4*>(tile + blk * (kF32TileBytes / 2)) + r * 8;
+        uint4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = src[q ^ (r & 7)];
+        uint32_t m = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          m = max(max(max(m, v[q].x & 0x7FFFFFFFu), v[q].y & 0x7FFFFFFFu),
+                  max(v[q].z & 0x7FFFFFFFu, v[q].w & 0x7FFFFFFFu));
+        const uint32_t code = scale_code_f32(m);
+        const bool nan_block = (code == 0xFFu);
+        const float inv = inv_scale(nan_block ? 0u : code);
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o[q] = quant4_f32(__uint_as_float(v[q].x), __uint_as_float(v[q].y), __uint_as_float(v[q].z),
+                            __uint_as_float(v[q].w), inv);
+        if (__any_sync(0xFFFFFFFFu, nan_block) && nan_block) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o[q] = nan_pair_f32(v[q].x, v[q].y) | (nan_pair_f32(v[q].z, v[q].w) << 16);
+        }
+        const int64_t grow = row0 + r;
+        if (r < valid_rows && blk * 32 < valid_cols) {
+          uint4* dst = reinterpret_cast<uint4*>(row_data + grow * p.cols + c0 + blk * 32);
+          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        // Rows past the end were zero-filled by the TMA: they write the zero
+        // codes of the scale padding.
+        row_scale[scale_offset(grow, (c0 >> 5) + blk, p.row_ka)] = static_cast<uint8_t>(code);
+        // A last tile that starts a 4-block scale group alone also writes the
+        // zero codes of the group's two remaining (padding) blocks.
+        if ((c0 & 127) == 0 && c0 + kF32Cols >= p.cols)
+          row_scale[scale_offset(grow, (c0 >> 5) + 2 + blk, p.row_ka)] = 0;
+      }
+
+      if constexpr (kCol) {
+        if (ok) {
+          // ---- column copy: thread = (column c, 32-row block rb)
+          const int c = tid & 63;
+          const int rb = tid >> 6;
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(tile + (c >> 5) * (kF32TileBytes / 2)) +
+                                rb * 32 * 32 + (c & 3);
+          const int cc = (c & 31) >> 2;
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = src[i * 32 + ((cc ^ (i & 7)) << 2)];
+          mbar_arrive(&empty[s]);  // this thread is done with the tile
+          uint32_t m = 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) m = max(m, w[i] & 0x7FFFFFFFu);
+          const uint32_t code = scale_code_f32(m);
+          const bool nan_block = (code == 0xFFu);
+          const float inv = inv_scale(nan_block ? 0u : code);
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            o[q] = quant4_f32(__uint_as_float(w[4 * q]), __uint_as_float(w[4 * q + 1]),
+                              __uint_as_float(w[4 * q + 2]), __uint_as_float(w[4 * q + 3]), inv);
+          if (__any_sync(0xFFFFFFFFu, nan_block) && nan_block) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              o[q] = nan_pair_f32(w[4 * q], w[4 * q + 1]) | (nan_pair_f32(w[4 * q + 2], w[4 * q + 3]) << 16);
+          }
+          csc[c * 4 + rb] = static_cast<uint8_t>(code);
+          // Output row c, 16-byte chunks 2rb and 2rb+1, chunk q at q ^ (c % 8).
+          *reinterpret_cast<uint4*>(stg + c * 128 + (((2 * rb) ^ (c & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(stg + c * 128 + (((2 * rb + 1) ^ (c & 7)) << 4)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        consumers_sync();
+        if (ok) {
+#pragma unroll
+          for (int it = 0; it < (kF32Cols * 8) / kConsumers; ++it) {
+            const int idx = it * kConsumers + tid;
+            const int o = idx >> 3;
+            const int q = idx & 7;
+            if (o < valid_cols && q * 16 < valid_rows)
+              *reinterpret_cast<uint4*>(col_data + (c0 + o) * p.col_pitch + row0 + q * 16) =
+                  *reinterpret_cast<const uint4*>(stg + o * 128 + ((q ^ (o & 7)) << 4));
+          }
+          if (tid < kF32Cols)
+            *reinterpret_cast<uint32_t*>(col_scale + scale_offset(c0 + tid, row0 >> 5, p.col_ka)) =
+                *reinterpret_cast<const uint32_t*>(csc + tid * 4);
+          // Likewise the padding rows of a 128-row scale group that the last
+          // column tile starts alone.
+          else if (tid < 2 * kF32Cols && (c0 & 127) == 0 && c0 + kF32Cols >= p.cols)
+            *reinterpret_cast<uint32_t*>(col_scale + scale_offset(c0 + tid, row0 >> 5, p.col_ka)) = 0u;
+        }
+      } else {
+        if (ok) mbar_arrive(&empty[s]);
+      }
+    }
+  }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -536,6 +750,50 @@ mx_status launch_one(const CUtensorMap& map, const QParams& p, int64_t tiles_upp
   return cuda_status(cudaGetLastError(), "mx_quantize launch");
 }
 
+template <bool R, bool C>
+mx_status launch_f32_one(const CUtensorMap& map, const QParams& p, int64_t tiles, cudaStream_t s) {
+  const size_t smem = 1024 + static_cast<size_t>(kStages) * kF32TileBytes + 2 * kF32StageBytes + 512 + 2 * kStages * 8;
+  auto kern = mx_quant_f32_kernel<R, C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(quant f32 smem)");
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  const int64_t grid =
+      std::max<int64_t>(1, std::min<int64_t>(tiles, static_cast<int64_t>(std::max(per_sm, 1)) * sm_count()));
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(map, p);
+  return cuda_status(cudaGetLastError(), "mx_quantize_f32 launch");
+}
+
+// FP32 input: [batch, rows, cols] through 32-column boxes in the 128-byte swizzle.
+mx_status launch_f32(const QuantLaunch& q, const QParams& p, bool do_row, bool do_col, cudaStream_t s) {
+  const int64_t tiles = (q.rows + kTileRows - 1) / kTileRows * ((q.cols + kF32Cols - 1) / kF32Cols) * q.batch;
+  if (tiles == 0) return MX_OK;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return MX_ERR_CUDA;
+  }
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  const int64_t bstride = q.batch > 1 ? q.x_batch_stride : q.rows * q.ldx;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.cols), static_cast<cuuint64_t>(q.rows),
+                        static_cast<cuuint64_t>(q.batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.ldx * 4), static_cast<cuuint64_t>(bstride * 4)};
+  cuuint32_t box[3] = {kF32BoxCols, kTileRows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(q.x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (FP32 quantiser input) failed (%d)", static_cast<int>(r));
+    return MX_ERR_CUDA;
+  }
+  if (do_row && do_col) return launch_f32_one<true, true>(map, p, tiles, s);
+  if (do_row) return launch_f32_one<true, false>(map, p, tiles, s);
+  return launch_f32_one<false, true>(map, p, tiles, s);
+}
+
 }  // namespace
 
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s) {
@@ -563,6 +821,7 @@ mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaSt
     set_error("mx_quantize: at most %d groups", kMaxGroups);
     return MX_ERR_UNSUPPORTED_SHAPE;
   }
+  if (q.x_f32) return launch_f32(q, p, do_row, do_col, s);
   const int64_t col_tiles = (q.cols + kTileCols - 1) / kTileCols;
   int64_t row_tiles = (q.rows + kTileRows - 1) / kTileRows;
   if (grouped) row_tiles += q.n_groups;  // upper bound of sum ceil(m_e / 128)

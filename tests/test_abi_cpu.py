@@ -153,3 +153,19 @@ def test_quantize_batched_rejects_bad_arguments_on_host(L):
     assert _status_of(q, x, 2, 64, 64, 64, 4096, 0, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == INVALID
     assert _status_of(q, x, 2, 64, 64, 64, 4096, 3, None, 0x2000, 0x3000, 0x4000, None, None) == INVALID
     assert _status_of(q, x, 0, 64, 64, 64, 4096, 3, None, None, None, None, None, None) == 0
+
+
+def test_quantize_f32_rejects_bad_arguments_on_host(L):
+    x = 0x10000
+    q = mx.mx_quantize_f32
+    assert _status_of(q, x, 1, 64, 64, 66, 0, 3, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == ALIGN  # ldx % 4
+    assert _status_of(q, x + 8, 1, 64, 64, 64, 0, 3, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == ALIGN
+    assert _status_of(q, x, 2, 64, 64, 64, 4098, 3, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == ALIGN
+    assert _status_of(q, x, 2, 64, 64, 64, 100, 3, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == INVALID
+    assert _status_of(q, x, 1, 64, 48, 48, 0, 1, 0x1000, 0x2000, None, None, None, None) == SHAPE
+    assert _status_of(q, x, 1, 48, 64, 64, 0, 2, None, None, 0x3000, 0x4000, None, None) == SHAPE
+    assert _status_of(q, x, 1, 64, 64, 64, 0, 3, None, 0x2000, 0x3000, 0x4000, None, None) == INVALID
+    assert _status_of(q, x, 1, 64, 64, 64, 0, 9, 0x1000, 0x2000, 0x3000, 0x4000, None, None) == INVALID
+    assert _status_of(q, x, 0, 64, 64, 64, 0, 3, None, None, None, None, None, None) == 0
+    # a BF16-legal pitch of 66 elements is not a 16-byte FP32 pitch; 68 is
+    assert _status_of(q, 0, 1, 64, 64, 68, 0, 1, 0x1000, 0x2000, None, None, None, None) == INVALID

@@ -226,3 +226,19 @@ def quant_sweep(M: int, C: int = 7168, seed: int = SEED_BASE + 5, frac: float = 
     pos = g.choice(M * C, size=n, replace=False)
     x.reshape(-1)[pos] *= np.float32(scale)
     return to_bf16(x)
+
+
+# ---------------------------------------------------------------------------
+# Weight refresh: FP32 master weights (stacked experts or one matrix)
+# ---------------------------------------------------------------------------
+
+def fp32_master(shape, seed: int = SEED_BASE + 6, std: float = 0.02, spread: int = 6) -> torch.Tensor:
+    """FP32 master weights: N(0, std) with a per-row power-of-two factor in
+    [2**-spread, 2**spread] (seeded), kept in FP32 (24-bit mantissas, so most
+    values are not BF16 numbers)."""
+    g = philox(seed)
+    x = g.standard_normal(shape, dtype=np.float32) * np.float32(std)
+    rows = int(np.prod(shape[:-1]))
+    f = np.exp2(g.integers(-spread, spread + 1, size=rows)).astype(np.float32)
+    x = (x.reshape(rows, shape[-1]) * f[:, None]).reshape(shape)
+    return torch.from_numpy(np.ascontiguousarray(x))
