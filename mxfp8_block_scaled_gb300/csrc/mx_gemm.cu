@@ -863,14 +863,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+    // Only the scale gather needs the whole warp; otherwise lane 0 alone runs
+    // the loop (a per-stage warp shuffle cost ~5% of GEMM throughput).
+    for (int64_t t = t_first; t < ntiles && ok && (kGatherSfa || lane == 0); t += t_step) {
       const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
       // Rows-ragged: B's scale atoms are those of the tile's expert.
       const int64_t sfb_atom_row = (KIND == GEMM_GROUPED_M ? ti.group * p.b_ra : 0) + (ti.n0 >> 7);
       for (int kb = 0; kb < ti.nkb; ++kb) {
         uint32_t good = 1;
         if (lane == 0) good = wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
-        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        if constexpr (kGatherSfa) good = __shfl_sync(0xFFFFFFFFu, good, 0);
         if (!good) {
           ok = false;
           break;
@@ -1223,24 +1225,67 @@ int env_int(const char* name, int dflt) {
   return (v && *v) ? std::atoi(v) : dflt;
 }
 
+// Dense tile configurations and their estimated time: rounds of tiles over
+// the SMs (or pairs of SMs) times the tile's FLOPs at that configuration's
+// per-SM rate, plus a fixed per-round cost (accumulator drain, epilogue).
+// Rates measured on GB300 with long contractions: CTA pairs 19, single-CTA
+// 128 x 256 tiles 16, 128 x 128 tiles 11.2 TFLOP/s per SM.
+enum DenseCfg { CFG_PAIR = 0, CFG_BN256 = 1, CFG_BN128 = 2 };
+
+double dense_cfg_time_us(const GemmLaunch& L, int cfg) {
+  const int sms = sm_count();
+  const int64_t kpad = (L.K + kBK - 1) / kBK * kBK;
+  const int64_t mt = (L.M + kBM - 1) / kBM;
+  int64_t tiles, slots;
+  double tile_flops, rate;
+  if (cfg == CFG_PAIR) {
+    tiles = (mt + 1) / 2 * ((L.N + 255) / 256);
+    slots = sms / 2;
+    tile_flops = 2.0 * 256 * 256 * kpad;
+    rate = 2 * 19.0e12;
+  } else {
+    const int bn = cfg == CFG_BN256 ? 256 : 128;
+    tiles = mt * ((L.N + bn - 1) / bn);
+    slots = sms;
+    tile_flops = 2.0 * kBM * bn * kpad;
+    rate = cfg == CFG_BN256 ? 16.0e12 : 11.2e12;
+  }
+  const int64_t rounds = (tiles + slots - 1) / std::max<int64_t>(slots, 1);
+  return static_cast<double>(rounds) * (tile_flops / rate * 1e6 + 1.0);
+}
+
+int choose_dense_cfg(const GemmLaunch& L) {
+  static const int pair_mode = env_int("MXFP8_GEMM_PAIR", 1);
+  static const int forced_bn = env_int("MXFP8_GEMM_BN", 0);
+  if (pair_mode == 2 && L.N > 128) return CFG_PAIR;
+  if (forced_bn == 256) return CFG_BN256;
+  if (forced_bn == 128) return CFG_BN128;
+  int best = CFG_BN128;
+  double best_t = dense_cfg_time_us(L, CFG_BN128);
+  for (int cfg : {CFG_BN256, CFG_PAIR}) {
+    if (cfg == CFG_PAIR && (pair_mode == 0 || L.N <= 128)) continue;
+    if (cfg == CFG_BN256 && L.N <= 128) continue;
+    const double t = dense_cfg_time_us(L, cfg);
+    if (t < best_t) {
+      best_t = t;
+      best = cfg;
+    }
+  }
+  return best;
+}
+
+// Grouped kinds: 256-wide tiles unless N fits one 128-wide tile.
 int choose_bn(const GemmLaunch& L) {
   static const int forced = env_int("MXFP8_GEMM_BN", 0);
   if (forced == 128 || forced == 256) return forced;
-  if (L.N <= 128) return 128;
-  const int64_t mt = (L.M + kBM - 1) / kBM;
-  const int64_t tiles256 = mt * ((L.N + 255) / 256);
-  if (L.kind == GEMM_DENSE && tiles256 < sm_count()) return 128;
-  return 256;
+  return L.N <= 128 ? 128 : 256;
 }
 
-// CTA pairs for dense GEMMs with enough 256 x 256 tiles to fill the pairs and a
-// long contraction (measured on GB300: pairs win for K >= 8192 and lose for
-// K <= 2048, where the per-tile epilogue dominates).
+// Grouped kinds on CTA pairs when their 256 x 256 tiles still give every SM work.
 bool use_pairs(const GemmLaunch& L) {
   static const int mode = env_int("MXFP8_GEMM_PAIR", 1);
   if (mode == 0 || L.N <= 128) return false;
   if (mode == 2) return true;
-  // Pairs win whenever their 256 x 256 tiles still give every SM work.
   return pair_tiles_upper(L) >= sm_count() / 2;
 }
 
@@ -1278,13 +1323,16 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.dev_status = L.dev_status;
   p.timeout_ns = wait_timeout_ns();
 
-  if (use_pairs(L)) {
-    if (L.kind == GEMM_GROUPED_K) return launch_pair<GEMM_GROUPED_K>(L, p, s);
-    if (L.kind == GEMM_GROUPED_M) return launch_pair<GEMM_GROUPED_M>(L, p, s);
-    return launch_pair<GEMM_DENSE>(L, p, s);
+  int bn;
+  if (L.kind == GEMM_DENSE) {
+    const int cfg = choose_dense_cfg(L);
+    if (cfg == CFG_PAIR) return launch_pair<GEMM_DENSE>(L, p, s);
+    bn = cfg == CFG_BN256 ? 256 : 128;
+  } else {
+    if (use_pairs(L))
+      return L.kind == GEMM_GROUPED_K ? launch_pair<GEMM_GROUPED_K>(L, p, s) : launch_pair<GEMM_GROUPED_M>(L, p, s);
+    bn = choose_bn(L);
   }
-
-  const int bn = choose_bn(L);
   const int64_t mt = (L.M + kBM - 1) / kBM;
   const int64_t nt = (L.N + bn - 1) / bn;
   int64_t tiles_upper = mt * nt;
