@@ -41,6 +41,9 @@ Readings taken where the pages are silent (each is also pinned by a test):
   each group's segment is zero-padded to a multiple of 128 rows.
 * GEMM reference: the FP64 dot of the dequantised operands, kept unrounded,
   together with S = sum |a*b|; see ``within_tolerance`` for why.
+* SwiGLU after the grouped gate_up GEMM: gate = the first F output columns,
+  up = the last F ([DSV3] §5 lays gate_up_proj out as [E, 2F, H]), computed in
+  float64 on the unrounded dots; see ``swiglu_within_tolerance``.
 """
 
 from __future__ import annotations
@@ -414,6 +417,57 @@ def mx_grouped_gemm_ref_kragged(a_codes, a_scale, b_codes, b_scale, offsets):
 
 TOL_REL = 2.0 ** -8
 TOL_ABS_S = 1e-6
+
+
+# ----------------------------------------------------------------------------
+# Grouped SwiGLU between gate_up and down (kept in high precision)
+# ----------------------------------------------------------------------------
+
+SILU_MAX_SLOPE = 1.1     # max |d/dx x*sigmoid(x)| = 1.0998... (at x ~ 2.40)
+
+
+def silu(x) -> np.ndarray:
+    """x * sigmoid(x) = x / (1 + exp(-x)) in float64 (for x -> -inf the value
+    tends to -0, for x -> +inf to x)."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        e = np.exp(-x)
+    return np.where(np.isinf(e), -0.0 * np.abs(x), x / (1.0 + e))
+
+
+def swiglu(y) -> np.ndarray:
+    """SwiGLU of a gate_up output y[..., 2F]: gate = y[..., :F], up = y[..., F:]
+    ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §5: gate_up_proj [E, 2F, H],
+    gate rows first; the grouped SwiGLU sits between gate_up and down and is not
+    a low-precision operator, §1)."""
+    y = np.asarray(y, dtype=np.float64)
+    F = y.shape[-1] // 2
+    assert y.shape[-1] == 2 * F
+    return silu(y[..., :F]) * y[..., F:]
+
+
+def mx_grouped_swiglu_ref(a_codes, a_scale, b_codes, b_scale, offsets):
+    """Grouped gate_up fprop followed by SwiGLU, all in float64.
+
+    Returns (out [M, F], gate [M, F], up [M, F], S_gate, S_up): the unrounded
+    SwiGLU output, the unrounded gate and up dots and their sum|a*b| terms."""
+    ref, S = mx_grouped_gemm_ref_mragged(a_codes, a_scale, b_codes, b_scale, offsets)
+    F = ref.shape[1] // 2
+    gate, up = ref[:, :F], ref[:, F:]
+    return swiglu(ref), gate, up, S[:, :F], S[:, F:]
+
+
+def swiglu_within_tolerance(out, ref, gate, up, S_gate, S_up) -> np.ndarray:
+    """Acceptance for a SwiGLU computed in FP32 from FP32 accumulations and
+    rounded once to BF16: each accumulation is within 1e-6 * S of its dot (the
+    GEMM bound), so silu(g) * u moves by at most
+    SILU_MAX_SLOPE * dg * (|u| + du) + |silu(g)| * du; FP32 evaluation adds
+    <= 1e-5 * |out| and the BF16 rounding <= 2**-8 * |out|."""
+    out = np.asarray(out, dtype=np.float64)
+    dg = TOL_ABS_S * S_gate
+    du = TOL_ABS_S * S_up
+    bound = (TOL_REL + 1e-5) * np.abs(ref) + SILU_MAX_SLOPE * dg * (np.abs(up) + du) + np.abs(silu(gate)) * du
+    return np.abs(out - ref) <= bound
 
 
 def within_tolerance(out, ref, S) -> np.ndarray:

@@ -474,6 +474,58 @@ def pin_grouped_gemm(O):
         assert np.array_equal(dw2[i], dw[p])
 
 
+def pin_swiglu(O):
+    """SiLU by its closed forms, SwiGLU's gate/up halves by explicit loops, and
+    the grouped SwiGLU reference on one-hot operands whose dots are single
+    E4M3 values ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §5: gate_up_proj
+    [E, 2F, H], gate rows first)."""
+    ln3 = math.log(3.0)
+    # sigmoid(ln 3) = 1 / (1 + 1/3) = 3/4, sigmoid(-ln 3) = 1/4
+    v = O.silu(np.array([0.0, ln3, -ln3, 40.0, -40.0]))
+    assert v[0] == 0.0
+    assert abs(v[1] - 0.75 * ln3) <= 1e-15 and abs(v[2] + 0.25 * ln3) <= 1e-15
+    assert abs(v[3] - 40.0 / (1.0 + math.exp(-40.0))) <= 1e-13
+    assert abs(v[4] + 40.0 * math.exp(-40.0) / (1.0 + math.exp(-40.0))) <= 1e-30
+    x = np.random.Generator(np.random.Philox(11)).standard_normal(1000) * 8
+    assert np.allclose(O.silu(x) - O.silu(-x), x, rtol=0, atol=1e-12)       # x*s(x) + x*s(-x) = x
+    # the slope bound used by the tolerance: max |silu'| = 1.0998 at x ~ 2.40
+    t = np.linspace(-20, 20, 400001)
+    d = np.abs(np.gradient(O.silu(t), t))
+    assert 1.09 < d.max() <= O.SILU_MAX_SLOPE
+    # halves: out[:, f] = silu(y[:, f]) * y[:, F + f]
+    y = np.random.Generator(np.random.Philox(12)).standard_normal((5, 6))
+    out = O.swiglu(y)
+    for i in range(5):
+        for f in range(3):
+            g, u = y[i, f], y[i, 3 + f]
+            assert abs(out[i, f] - g / (1.0 + math.exp(-g)) * u) <= 1e-15 * (1 + abs(u))
+    # one-hot grouped case: E = 2, F = 2 (N = 4), K = 32; row i of A is 1.0 at
+    # column k_i (code 0x38, scale 2**0), so dot(i, n) = B_e[n, k_i]
+    offs = np.array([0, 2, 3])
+    ks = [3, 17, 30]
+    a = np.zeros((3, 32), dtype=np.uint8)
+    for i, k in enumerate(ks):
+        a[i, k] = 0x38
+    a_s = np.full((3, 1), 127, dtype=np.uint8)
+    g = np.random.Generator(np.random.Philox(13))
+    b = g.integers(0, 0x7E, size=(2, 4, 32)).astype(np.uint8) | (g.integers(0, 2, size=(2, 4, 32)) << 7).astype(np.uint8)
+    b_s = np.full((2, 4, 1), 127, dtype=np.uint8)
+    res, gate, up, _, _ = O.mx_grouped_swiglu_ref(a, a_s, b, b_s, offs)
+    for i, k in enumerate(ks):
+        e = 0 if i < 2 else 1
+        for f in range(2):
+            gv = float(O.e4m3_decode(np.array([b[e, f, k]]))[0])
+            uv = float(O.e4m3_decode(np.array([b[e, 2 + f, k]]))[0])
+            assert gate[i, f] == gv and up[i, f] == uv
+            assert abs(res[i, f] - gv / (1.0 + math.exp(-gv)) * uv) <= 1e-12 * (1 + abs(uv * gv))
+    # the acceptance bound: exact passes, BF16-sized rounding passes, 2**-6 fails
+    r = np.array([1.0, -3.0, 100.0])
+    z = np.zeros(3)
+    assert np.all(O.swiglu_within_tolerance(r, r, r, r, z, z))
+    assert np.all(O.swiglu_within_tolerance(r * (1 + 2.0 ** -9), r, r, r, z, z))
+    assert not np.any(O.swiglu_within_tolerance(r * (1 + 2.0 ** -6), r, r, r, z, z))
+
+
 def pin_tolerance(O):
     """Acceptance bound: BF16 rounding of the exact value passes; an error of
     2**-6 relative fails; a 1e-6*S-sized absolute error passes."""
@@ -490,5 +542,5 @@ ALL_PINS = [
     pin_printed_values, pin_e4m3_closed_forms, pin_e4m3_census, pin_e4m3_roundtrip_and_ties,
     pin_e4m3_vs_torch, pin_e4m3_saturation, pin_bf16_vs_torch, pin_scale_hand_blocks,
     pin_fp32_master_blocks, pin_quant_error_bound, pin_row_col_blocking, pin_scale_layout, pin_grouped_quant,
-    pin_gemm_bruteforce, pin_gemm_single_block, pin_gemm_modes, pin_grouped_gemm, pin_tolerance,
+    pin_gemm_bruteforce, pin_gemm_single_block, pin_gemm_modes, pin_grouped_gemm, pin_swiglu, pin_tolerance,
 ]

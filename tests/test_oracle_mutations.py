@@ -178,6 +178,18 @@ def m_input_bf16_prerounding(O):
     O.mx_quantize_blocks = lambda blocks: orig(O.bf16_round(np.asarray(blocks, dtype=np.float64)))
 
 
+def m_swiglu_halves_swapped(O):
+    def sw(y):
+        y = np.asarray(y, dtype=np.float64)
+        F = y.shape[-1] // 2
+        return O.silu(y[..., F:]) * y[..., :F]
+    O.swiglu = sw
+
+
+def m_silu_sign(O):
+    O.silu = lambda x: np.asarray(x, dtype=np.float64) / (1.0 + np.exp(np.asarray(x, dtype=np.float64)))
+
+
 def m_tolerance_loose(O):
     O.within_tolerance = lambda out, ref, S: np.abs(np.asarray(out) - ref) <= 2.0 ** -5 * np.abs(ref) + 1e-6 * S
 
@@ -186,7 +198,7 @@ MUTANTS = [m_scale_off_by_one, m_scale_ceil, m_zero_block_scale_one, m_ties_away
            m_no_saturation, m_drop_sign, m_decode_bias8, m_decode_subnormal_hidden_one,
            m_colwise_not_transposed, m_gemm_transposed, m_gemm_drop_b_scale, m_dequant_scale_sign,
            m_swizzle_swapped, m_group_blocks_not_restarting, m_group_pad_64, m_bf16_truncate,
-           m_tolerance_loose, m_input_bf16_prerounding]
+           m_tolerance_loose, m_input_bf16_prerounding, m_swiglu_halves_swapped, m_silu_sign]
 
 
 def _caught(O):
