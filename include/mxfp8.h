@@ -218,6 +218,26 @@ mx_status mx_grouped_gemm(int mode, const mx_operand* a, const mx_operand* b,
                           const int64_t* group_offsets, int n_groups, void* c, int64_t ldc,
                           int* dev_status, void* stream);
 
+/*
+ * mx_grouped_gemm_swiglu - the routed experts' gate_up fprop with the grouped
+ * SwiGLU fused into its epilogue ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计"
+ * §5: gate_up_proj [E, 2F, H] and the grouped SwiGLU between gate_up and
+ * down; §1: SwiGLU is not a low-precision operator, so it is evaluated in FP32
+ * on the FP32 accumulators and rounded once to BF16).
+ *
+ *   a       row copy of the tokens [M_total, K], rows grouped by expert as in
+ *           mx_grouped_gemm (MX_FPROP contract).
+ *   b       stacked row copies of gate_up [E][2F][K]: rows [0, F) of each
+ *           expert are its gate projection, rows [F, 2F) its up projection;
+ *           2F must be a multiple of 256.
+ *   c       BF16 [M_total, F], row pitch ldc: c[i, f] = silu(g) * u with
+ *           g = (A . B_e^T)[i, f], u = (A . B_e^T)[i, F + f], e the expert of row
+ *           i, silu(x) = x / (1 + exp(-x)).
+ *   Groups, validation, empty experts and errors as mx_grouped_gemm.
+ */
+mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                                 int n_groups, void* c, int64_t ldc, int* dev_status, void* stream);
+
 /* Static description of a status code. */
 const char* mx_status_string(mx_status s);
 

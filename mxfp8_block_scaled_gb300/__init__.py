@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAP
 
 # Symbols the header declares (the CPU tests check the library exports them).
 EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quantize_batched", "mx_quantize_f32",
-            "mx_gemm", "mx_grouped_gemm", "mx_status_string", "mx_last_error", "mx_abi_version")
+            "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_status_string", "mx_last_error",
+            "mx_abi_version")
 
 
 class MXError(RuntimeError):
@@ -71,6 +72,9 @@ def lib() -> ctypes.CDLL:
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
                                   vp, vp]
     L.mx_grouped_gemm.restype = i32
+    L.mx_grouped_gemm_swiglu.argtypes = [ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
+                                         vp, vp]
+    L.mx_grouped_gemm_swiglu.restype = i32
     L.mx_status_string.argtypes = [i32]
     L.mx_status_string.restype = ctypes.c_char_p
     L.mx_last_error.argtypes = []
@@ -142,6 +146,12 @@ def mx_grouped_gemm(mode, a: MXOperandC, b: MXOperandC, group_offsets, n_groups,
                     stream) -> None:
     _check(lib().mx_grouped_gemm(mode, _ref(a), _ref(b), group_offsets, n_groups, c, ldc,
                                  dev_status, stream), "mx_grouped_gemm")
+
+
+def mx_grouped_gemm_swiglu(a: MXOperandC, b: MXOperandC, group_offsets, n_groups, c, ldc, dev_status,
+                           stream) -> None:
+    _check(lib().mx_grouped_gemm_swiglu(_ref(a), _ref(b), group_offsets, n_groups, c, ldc, dev_status, stream),
+           "mx_grouped_gemm_swiglu")
 
 
 # ---------------------------------------------------------------------------
@@ -287,4 +297,17 @@ def grouped_gemm(mode: int, a, b, group_offsets, out=None, status=None, stream=N
     ldc = out.stride(-2)
     mx_grouped_gemm(mode, a.c_operand(), b.c_operand(), group_offsets.data_ptr(), E, out.data_ptr(), ldc,
                     _ptr(status), _stream(stream))
+    return out
+
+
+def grouped_gemm_swiglu(a, b, group_offsets, out=None, status=None, stream=None):
+    """Grouped gate_up fprop with SwiGLU in the epilogue: a MXTensor [M_total, K]
+    (rows grouped by expert), b MXStacked [E][2F][K] (gate rows first) ->
+    out [M_total, F] = silu(gate) * up in BF16."""
+    torch = _torch()
+    E = group_offsets.numel() - 1
+    if out is None:
+        out = torch.empty((a.rows, b.rows // 2), dtype=torch.bfloat16, device=a.data.device)
+    mx_grouped_gemm_swiglu(a.c_operand(), b.c_operand(), group_offsets.data_ptr(), E, out.data_ptr(), out.stride(0),
+                           _ptr(status), _stream(stream))
     return out

@@ -413,6 +413,59 @@ mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, i
   return launch_gemm(L, s);
 }
 
+mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                                 int n_groups, void* c, int64_t ldc, int* dev_status, void* stream) {
+  mx_status st = check_operand(a, "a");
+  if (st != MX_OK) return st;
+  st = check_operand(b, "b");
+  if (st != MX_OK) return st;
+  st = check_mode(MX_FPROP, a, b);
+  if (st != MX_OK) return st;
+  if (!group_offsets || n_groups < 1) {
+    set_error("mx_grouped_gemm_swiglu: group_offsets must be non-null and n_groups >= 1");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (a->k != b->k) {
+    set_error("mx_grouped_gemm_swiglu: a.k != b.k");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (a->rows > 0x7FFFFFFFLL || b->rows > 0x7FFFFFFFLL || a->k > 0x7FFFFFFFLL) {
+    set_error("mx_grouped_gemm_swiglu: sizes must be < 2^31");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (b->rows % 256 != 0) {
+    set_error("mx_grouped_gemm_swiglu: gate_up rows (2F) must be a multiple of 256");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  const int64_t F = b->rows / 2;
+  st = check_output(c, ldc, F, a->rows);
+  if (st != MX_OK) return st;
+  if (a->rows == 0 || F == 0) return MX_OK;
+  st = check_device();
+  if (st != MX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->k == 0) return zero_output(c, ldc, F, a->rows, s);  // silu(0) * 0
+  GemmLaunch L;
+  L.kind = GEMM_GROUPED_M;
+  L.a_data = a->data;
+  L.a_scale = a->scale;
+  L.a_ld = a->ld ? a->ld : a->k;
+  L.b_data = b->data;
+  L.b_scale = b->scale;
+  L.b_ld = b->ld ? b->ld : b->k;
+  L.M = a->rows;
+  L.N = b->rows;
+  L.K = a->k;
+  L.b_rows_total = b->rows * static_cast<int64_t>(n_groups);
+  L.c = c;
+  L.ldc = ldc;
+  L.offsets = group_offsets;
+  L.n_groups = n_groups;
+  L.dev_status = dev_status;
+  L.swiglu = true;
+  return launch_gemm(L, s);
+}
+
 mx_status mx_grouped_gemm(int mode, const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
                           int n_groups, void* c, int64_t ldc, int* dev_status, void* stream) {
   mx_status st = check_operand(a, "a");

@@ -137,6 +137,7 @@ struct GParams {
   const uint8_t* a_scale;
   const uint8_t* b_scale;
   int64_t M, N, K;
+  int64_t n_out;          // columns of C (N, or N/2 behind the SwiGLU epilogue)
   int64_t ka;             // scale-column atoms along K: ceil(K/128)
   int64_t a_ra;           // row atoms of A's scales
   int64_t b_ra;           // row atoms of B's scales (per expert when grouped by rows)
@@ -246,7 +247,7 @@ __device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, i
 // Pair tiles: t enumerates (pair of M tiles, N tile); the CTA's rank in its
 // cluster picks the M tile, both CTAs share the 256-wide N tile. K-ragged
 // grouped: experts in decreasing-K order, each expert's pair tiles M-fastest.
-template <int KIND>
+template <int KIND, bool kSwiGLU = false>
 __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo& g, int64_t t, uint32_t crank) {
   constexpr int BN = PairCfg::BN;
   const int64_t nt = (p.N + BN - 1) / BN;
@@ -260,9 +261,16 @@ __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo&
     nb = t % nt;
     const int e = last_le(g.tile, p.n_groups, u);
     ti.m0 = static_cast<int64_t>(g.off[e]) + static_cast<int64_t>(u - g.tile[e]) * (2 * kBM) + crank * kBM;
-    ti.n0 = nb * BN;
     ti.a_row = ti.m0;
-    ti.b_row = static_cast<int64_t>(e) * p.b_rows_group + ti.n0 + crank * (BN / 2);
+    if (kSwiGLU) {
+      // Output features [128 nb, 128 nb + 128): the even CTA loads their gate
+      // rows, the odd CTA their up rows (gate_up = [gate; up], N/2 rows each).
+      ti.n0 = nb * (BN / 2);
+      ti.b_row = static_cast<int64_t>(e) * p.b_rows_group + crank * (p.N >> 1) + ti.n0;
+    } else {
+      ti.n0 = nb * BN;
+      ti.b_row = static_cast<int64_t>(e) * p.b_rows_group + ti.n0 + crank * (BN / 2);
+    }
     ti.k_atom0 = 0;
     ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
     ti.valid_m = static_cast<int32_t>(min64(kBM, g.off[e + 1] - ti.m0));  // >= -127
@@ -416,7 +424,7 @@ __device__ __forceinline__ void store_tile(const GParams& p, const Tile& ti, con
         const uint4 v = ld_shared_v4(stg + rr * 64 + ((cc ^ ((rr >> 1) & 3)) << 4));
         const int trow = quarter * 32 + rr;
         const int64_t tcol = col_off + ch * 32 + cc * 8;
-        const int64_t ncol = p.N - (ti.n0 + tcol);
+        const int64_t ncol = p.n_out - (ti.n0 + tcol);
         if (trow < ti.valid_m && ncol > 0) {
           __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(trow) * p.ldc + tcol;
           if (ncol >= 8) {
@@ -468,7 +476,7 @@ __device__ __forceinline__ void store_tile(const GParams& p, const Tile& ti, con
     }
   } else if (row < ti.valid_m) {
     const int64_t col0 = ti.n0 + col_off;
-    const int64_t ncols = min64(my_chunks * 32, p.N - col0);
+    const int64_t ncols = min64(my_chunks * 32, p.n_out - col0);
     __nv_bfloat16* dst = ti.cbase + static_cast<int64_t>(row) * p.ldc + col_off;
     if (ncols == my_chunks * 32 && p.c_vec) {
 #pragma unroll
@@ -773,12 +781,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // cta_group::2, M = 256
 // ===========================================================================
 
-template <int KIND>
+template <int KIND, bool kSwiGLU = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                         const __grid_constant__ CUtensorMap tmap_c, const GParams p) {
   using C = PairCfg;
+  static_assert(!kSwiGLU || KIND == GEMM_GROUPED_M, "the SwiGLU epilogue follows the grouped gate_up fprop");
   // Rows-ragged tiles start at any row: each CTA gathers its A scale atom.
   constexpr bool kGatherSfa = (KIND == GEMM_GROUPED_M);
   constexpr int S = C::kStages;
@@ -866,9 +875,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Only the scale gather needs the whole warp; otherwise lane 0 alone runs
     // the loop (a per-stage warp shuffle cost ~5% of GEMM throughput).
     for (int64_t t = t_first; t < ntiles && ok && (kGatherSfa || lane == 0); t += t_step) {
-      const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
-      // Rows-ragged: B's scale atoms are those of the tile's expert.
+      const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+      // Rows-ragged: B's scale atoms are those of the tile's expert. SwiGLU:
+      // the second atom holds the up rows, N/256 atoms after the gate rows.
       const int64_t sfb_atom_row = (KIND == GEMM_GROUPED_M ? ti.group * p.b_ra : 0) + (ti.n0 >> 7);
+      const int64_t sfb_atom_step = kSwiGLU ? (p.N >> 8) : 1;
       for (int kb = 0; kb < ti.nkb; ++kb) {
         uint32_t good = 1;
         if (lane == 0) good = wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
@@ -907,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 2; ++j)
             tma_load_2d_pair(sSfb + stage * C::kSfbBytes + j * 512, &tmap_sfb, lfull, 0,
-                             static_cast<int32_t>((sfb_atom_row + j) * p.ka + katom));
+                             static_cast<int32_t>((sfb_atom_row + j * sfb_atom_step) * p.ka + katom));
         }
         ++issued;
         if (++stage == S) {
@@ -939,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
         if (!wait_or_abort<true>(acc_empty, acc_phase ^ 1, p, s_abort)) break;
         tc_fence_after_sync();
         for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -988,7 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort(&gfull[stage], phase, p, s_abort)) {
             ok = false;
@@ -1008,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort)) {
             ok = false;
@@ -1042,14 +1053,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lacc_empty = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t acc_phase = 0;
     for (int64_t t = t_first; t < ntiles; t += t_step) {
-      const Tile ti = get_pair_tile<KIND>(p, g, t, crank);
+      const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
       if (!wait_or_abort<true>(acc_full, acc_phase, p, s_abort)) break;
       tc_fence_after_sync();
       uint32_t r[kCols];
       if (ti.nkb > 0) {
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(col_off);
+        if (kSwiGLU) {
+          // Features [64 half, 64 half + 64): gate columns then the up columns
+          // 128 further on.
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(64 * half);
+          tmem_ld_32x32b_x32(taddr, r);
+          tmem_ld_32x32b_x32(taddr + 32, r + 32);
+          tmem_ld_32x32b_x32(taddr + 128, r + 64);
+          tmem_ld_32x32b_x32(taddr + 160, r + 96);
+        } else {
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(col_off);
 #pragma unroll
-        for (int ch = 0; ch < kCols / 32; ++ch) tmem_ld_32x32b_x32(taddr + ch * 32, r + ch * 32);
+          for (int ch = 0; ch < kCols / 32; ++ch) tmem_ld_32x32b_x32(taddr + ch * 32, r + ch * 32);
+        }
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -1059,7 +1080,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lacc_empty);  // the even CTA's MMAs may overwrite the accumulator
       acc_phase ^= 1;
-      store_tile<KIND, kCols, C::kEpiBufs>(p, ti, r, quarter, lane, kCols / 32, col_off, stg, &tmap_c);
+      if constexpr (kSwiGLU) {
+        // SwiGLU in FP32 on the FP32 accumulators, one rounding to BF16 at the store
+        // (the fast exponential's error stays below 1e-5 relative for |x| < 88).
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float gv = __uint_as_float(r[i]);
+          const float uv = __uint_as_float(r[64 + i]);
+          r[i] = __float_as_uint(gv / (1.0f + __expf(-gv)) * uv);
+        }
+        store_tile<KIND, 64, C::kEpiBufs>(p, ti, r, quarter, lane, 2, 64 * half, stg, &tmap_c);
+      } else {
+        store_tile<KIND, kCols, C::kEpiBufs>(p, ti, r, quarter, lane, kCols / 32, col_off, stg, &tmap_c);
+      }
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
@@ -1151,7 +1184,7 @@ void output_map(const GemmLaunch& L, GParams& p, CUtensorMap* mc, int kind) {
   p.c_tma = 0;
   if (p.c_vec) {
     const int64_t groups = (kind == GEMM_GROUPED_K) ? L.n_groups : 1;
-    if (make_out_map(mc, L.c, groups, L.M, L.N, L.ldc) == MX_OK) p.c_tma = 1;
+    if (make_out_map(mc, L.c, groups, L.M, L.swiglu ? L.N / 2 : L.N, L.ldc) == MX_OK) p.c_tma = 1;
   }
 }
 
@@ -1183,7 +1216,7 @@ int64_t pair_tiles_upper(const GemmLaunch& L) {
   return mu * nt;
 }
 
-template <int KIND>
+template <int KIND, bool kSwiGLU = false>
 mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) {
   GParams p = p_in;
   CUtensorMap ma, mb, msa, msb, mc;
@@ -1199,7 +1232,7 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   if (st != MX_OK) return st;
   output_map(L, p, &mc, KIND);
   const size_t smem = PairCfg::smem_bytes(KIND != GEMM_DENSE);
-  auto kern = mx_gemm_pair_kernel<KIND>;
+  auto kern = mx_gemm_pair_kernel<KIND, kSwiGLU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
   const int64_t pairs = pair_tiles_upper(L);
@@ -1303,6 +1336,7 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.b_scale = static_cast<const uint8_t*>(L.b_scale);
   p.M = L.M;
   p.N = L.N;
+  p.n_out = L.swiglu ? L.N / 2 : L.N;
   p.K = L.K;
   p.ka = (L.K + 127) / 128;
   p.a_ra = (L.M + 127) / 128;
@@ -1323,6 +1357,7 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.dev_status = L.dev_status;
   p.timeout_ns = wait_timeout_ns();
 
+  if (L.swiglu) return launch_pair<GEMM_GROUPED_M, true>(L, p, s);
   int bn;
   if (L.kind == GEMM_DENSE) {
     const int cfg = choose_dense_cfg(L);

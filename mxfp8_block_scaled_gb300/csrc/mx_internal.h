@@ -60,6 +60,7 @@ struct GemmLaunch {
   const int64_t* offsets;
   int n_groups;
   int* dev_status;
+  bool swiglu = false;  // rows-ragged only: C = SwiGLU(A . B^T), gate = B rows [0, N/2), up = [N/2, N)
 };
 mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
 

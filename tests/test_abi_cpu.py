@@ -169,3 +169,14 @@ def test_quantize_f32_rejects_bad_arguments_on_host(L):
     assert _status_of(q, x, 0, 64, 64, 64, 0, 3, None, None, None, None, None, None) == 0
     # a BF16-legal pitch of 66 elements is not a 16-byte FP32 pitch; 68 is
     assert _status_of(q, 0, 1, 64, 64, 68, 0, 1, 0x1000, 0x2000, None, None, None, None) == INVALID
+
+
+def test_grouped_gemm_swiglu_rejects_bad_arguments_on_host(L):
+    c, g = 0x4000, 0x8000
+    q = mx.mx_grouped_gemm_swiglu
+    assert _status_of(q, _op(rows=512), _op(rows=384), g, 2, c, 192, None, None) == SHAPE       # 2F % 256
+    assert _status_of(q, _op(rows=512), _op(rows=512, orient=mx.MX_COLWISE), g, 2, c, 256, None, None) == INVALID
+    assert _status_of(q, _op(rows=512), _op(rows=512), None, 2, c, 256, None, None) == INVALID
+    assert _status_of(q, _op(rows=512), _op(rows=512), g, 0, c, 256, None, None) == INVALID
+    assert _status_of(q, _op(rows=512, k=256), _op(rows=512, k=512), g, 2, c, 256, None, None) == INVALID
+    assert _status_of(q, _op(rows=512), _op(rows=512), g, 2, c, 100, None, None) == INVALID   # ldc < F
