@@ -41,6 +41,9 @@ Readings taken where the pages are silent (each is also pinned by a test):
   each group's segment is zero-padded to a multiple of 128 rows.
 * GEMM reference: the FP64 dot of the dequantised operands, kept unrounded,
   together with S = sum |a*b|; see ``within_tolerance`` for why.
+* Blockwise variant recipe (1x128 / 128x128 with FP32 multipliers): the
+  multiplier s = fl32(448 / amax) and the product fl32(s * x) are FP32
+  steps, then RNE to E4M3; an all-zero block takes s = 1.
 * SwiGLU after the grouped gate_up GEMM: gate = the first F output columns,
   up = the last F ([DSV3] §5 lays gate_up_proj out as [E, 2F, H]), computed in
   float64 on the unrounded dots; see ``swiglu_within_tolerance``.
@@ -417,6 +420,81 @@ def mx_grouped_gemm_ref_kragged(a_codes, a_scale, b_codes, b_scale, offsets):
 
 TOL_REL = 2.0 ** -8
 TOL_ABS_S = 1e-6
+
+
+# ----------------------------------------------------------------------------
+# Variant recipe: DeepSeek-V3 blockwise FP8 (1x128 activations, 128x128 weights)
+# ----------------------------------------------------------------------------
+
+FP8_BLOCK = 128
+
+
+def blockwise_scale(amax) -> np.ndarray:
+    """Per-block multiplier s = 448 / amax in FP32 ("浮点格式、数值稳定性与混合精度"
+    §七.2-§七.3: s = 448 / amax, x~ = fl_E4M3(s * x)); an all-zero block takes
+    s = 1 (the page leaves amax = 0 open)."""
+    a = np.asarray(amax, dtype=np.float32)
+    with np.errstate(divide="ignore"):
+        s = np.float32(E4M3_MAX) / a
+    return np.where(a > 0, s, np.float32(1.0)).astype(np.float32)
+
+
+def blockwise_encode(x, s) -> np.ndarray:
+    """E4M3 codes of fl32(s * x): the product rounded once to FP32, then RNE
+    to E4M3 (both sides of the comparison take the decision in FP32)."""
+    y = (np.asarray(x, dtype=np.float32) * np.asarray(s, dtype=np.float32)).astype(np.float32)
+    return e4m3_encode(y.astype(np.float64))
+
+
+def quantize_1x128(x) -> tuple[np.ndarray, np.ndarray]:
+    """Activation blocks of 1 x 128 along the last dim of x[R, C] (C % 128 == 0).
+    Returns codes [R, C] and the FP32 multipliers s [R, C/128]."""
+    x = np.asarray(x, dtype=np.float64)
+    R, C = x.shape
+    assert C % FP8_BLOCK == 0
+    b = x.reshape(R, C // FP8_BLOCK, FP8_BLOCK)
+    s = blockwise_scale(np.max(np.abs(b), axis=-1))
+    codes = blockwise_encode(b, s[..., None])
+    return codes.reshape(R, C), s
+
+
+def quantize_128x128(w) -> tuple[np.ndarray, np.ndarray]:
+    """Weight blocks of 128 x 128 over w[N, K] (K % 128 == 0; the last row block
+    may be short). Returns codes [N, K] and s [ceil(N/128), K/128]."""
+    w = np.asarray(w, dtype=np.float64)
+    N, K = w.shape
+    assert K % FP8_BLOCK == 0
+    nb = (N + FP8_BLOCK - 1) // FP8_BLOCK
+    amax = np.zeros((nb, K // FP8_BLOCK))
+    for i in range(nb):
+        blk = np.abs(w[i * FP8_BLOCK:(i + 1) * FP8_BLOCK]).reshape(-1, K // FP8_BLOCK, FP8_BLOCK)
+        amax[i] = blk.max(axis=(0, 2))
+    s = blockwise_scale(amax)
+    s_rows = np.repeat(s, FP8_BLOCK, axis=0)[:N]
+    codes = blockwise_encode(w.reshape(N, K // FP8_BLOCK, FP8_BLOCK), s_rows[..., None]).reshape(N, K)
+    return codes, s
+
+
+def gemm_blockwise_ref(a_codes, a_s, b_codes, b_s) -> tuple[np.ndarray, np.ndarray]:
+    """C = sum over 128-K blocks kb of (A_kb . B_kb^T) / (s_a[:, kb] s_b[nb, kb]),
+    the promotion of each block's partial sum with its two scales (same page,
+    §七.3), in float64. Returns (ref, S) with S = sum |a * b| of the dequantised
+    operands."""
+    a_codes, b_codes = np.asarray(a_codes), np.asarray(b_codes)
+    M, K = a_codes.shape
+    N = b_codes.shape[0]
+    A = e4m3_decode(a_codes)
+    B = e4m3_decode(b_codes)
+    sb_rows = np.repeat(np.asarray(b_s, dtype=np.float64), FP8_BLOCK, axis=0)[:N]
+    ref = np.zeros((M, N))
+    S = np.zeros((M, N))
+    for kb in range(K // FP8_BLOCK):
+        sl = slice(kb * FP8_BLOCK, (kb + 1) * FP8_BLOCK)
+        Ad = A[:, sl] / np.asarray(a_s, dtype=np.float64)[:, kb:kb + 1]
+        Bd = B[:, sl] / sb_rows[:, kb:kb + 1]
+        ref += Ad @ Bd.T
+        S += np.abs(Ad) @ np.abs(Bd).T
+    return ref, S
 
 
 # ----------------------------------------------------------------------------

@@ -474,6 +474,65 @@ def pin_grouped_gemm(O):
         assert np.array_equal(dw2[i], dw[p])
 
 
+def pin_blockwise_fp8(O):
+    """DeepSeek-V3 blockwise FP8 as the numerics page states it (§七.2-§七.3:
+    s = 448 / amax, x~ = fl_E4M3(s * x); 1x128 activation and 128x128 weight
+    blocks; each 128-K partial sum promoted with s_a and s_w). Hand-worked
+    blocks, block structure by explicit loops, and exact GEMM values."""
+    row = lambda vals: O.quantize_1x128(np.array([list(vals) + [0.0] * (128 - len(vals))]))
+    # amax 1 -> s = 448: 1 -> 448 = 0x7E, 0.5 -> 224 = 1.75 * 2**7 -> 0x76, -1 -> 0xFE
+    c, sc = row([1.0, 0.5, -1.0])
+    assert sc[0, 0] == 448.0 and c[0, :3].tolist() == [0x7E, 0x76, 0xFE]
+    # amax 3 -> s = fl32(448/3): 448/3 * 2**16 = 9786709.33 -> s = 9786709 * 2**-16
+    # = 149.33332824707031 (FP32 spacing 2**-16 on [128, 256)). x = 1: s lies in [144, 160)
+    # (E4M3 step 16 at 2**7), below the midpoint 152 -> 144 = 1.125 * 2**7 -> 0x71.
+    # x = 3: 3 s = 29360127 * 2**-16 = 448 - 2**-16, the FP32 midpoint of 448 - 2**-15 and
+    # 448 (spacing 2**-15 on [256, 512)); ties to even -> 448.0 -> 0x7E.
+    c, sc = row([1.0, 3.0])
+    assert float(sc[0, 0]) == 9786709 * 2.0 ** -16 and c[0, 0] == 0x71 and c[0, 1] == 0x7E
+    # amax 448 -> s = 1: the codes are the plain E4M3 codes (2.0 -> 0x40, -0.25 -> 0xA8)
+    c, sc = row([448.0, 2.0, -0.25])
+    assert sc[0, 0] == 1.0 and c[0, :3].tolist() == [0x7E, 0x40, 0xA8]
+    # all-zero block: s = 1 and the data keeps the sign
+    c, sc = O.quantize_1x128(np.concatenate([np.zeros((1, 128)), -np.zeros((1, 128))]))
+    assert np.all(sc == 1.0) and np.all(c[0] == 0x00) and np.all(c[1] == 0x80)
+    # block structure: 1x128 blocks per row; 128x128 blocks share one amax
+    g = np.random.Generator(np.random.Philox(21))
+    x = g.standard_normal((3, 256)) * np.array([1.0, 10.0, 0.01])[:, None]
+    c, sc = O.quantize_1x128(x)
+    for i in range(3):
+        for kb in range(2):
+            assert sc[i, kb] == np.float32(448.0) / np.float32(np.abs(x[i, kb * 128:(kb + 1) * 128]).max())
+    w = g.standard_normal((200, 256))
+    w[5, 3] = 1000.0          # one outlier: only block (0, 0) sees it
+    cw, sw = O.quantize_128x128(w)
+    assert sw.shape == (2, 2)
+    assert sw[0, 0] == np.float32(448.0) / np.float32(1000.0)
+    assert sw[1, 0] == np.float32(448.0) / np.float32(np.abs(w[128:, :128]).max())
+    assert sw[0, 1] == np.float32(448.0) / np.float32(np.abs(w[:128, 128:]).max())
+    # GEMM, one-hot: A row i = 1.0 (0x38) at k_i with s_a = 2, B = codes with s_b = 4:
+    # each output is (1/2) * b / 4
+    a = np.zeros((2, 256), dtype=np.uint8)
+    a[0, 5] = 0x38
+    a[1, 130] = 0x38
+    a_s = np.full((2, 2), 2.0, dtype=np.float32)
+    b = g.integers(0, 0x7E, size=(3, 256)).astype(np.uint8)
+    b_s = np.full((1, 2), 4.0, dtype=np.float32)
+    ref, S = O.gemm_blockwise_ref(a, a_s, b, b_s)
+    bv = O.e4m3_decode(b)
+    assert np.array_equal(ref[0], bv[:, 5] / 8.0) and np.array_equal(ref[1], bv[:, 130] / 8.0)
+    # two K blocks with different scales add: exact rational sum against brute force
+    a_s2 = np.array([[2.0, 0.5]], dtype=np.float32)
+    b_s2 = np.array([[4.0, 0.25]], dtype=np.float32)
+    a2 = g.integers(0, 0x7E, size=(1, 256)).astype(np.uint8)
+    b2 = g.integers(0, 0x7E, size=(1, 256)).astype(np.uint8)
+    r2, _ = O.gemm_blockwise_ref(a2, a_s2, b2, b_s2)
+    av, bv2 = O.e4m3_decode(a2)[0], O.e4m3_decode(b2)[0]
+    exact = sum(Fraction(av[k]) * Fraction(bv2[k]) / (Fraction(float(a_s2[0, k // 128])) * Fraction(float(b_s2[0, k // 128])))
+                for k in range(256))
+    assert abs(Fraction(r2[0, 0]) - exact) <= abs(exact) * Fraction(1, 2 ** 50)
+
+
 def pin_swiglu(O):
     """SiLU by its closed forms, SwiGLU's gate/up halves by explicit loops, and
     the grouped SwiGLU reference on one-hot operands whose dots are single
@@ -542,5 +601,6 @@ ALL_PINS = [
     pin_printed_values, pin_e4m3_closed_forms, pin_e4m3_census, pin_e4m3_roundtrip_and_ties,
     pin_e4m3_vs_torch, pin_e4m3_saturation, pin_bf16_vs_torch, pin_scale_hand_blocks,
     pin_fp32_master_blocks, pin_quant_error_bound, pin_row_col_blocking, pin_scale_layout, pin_grouped_quant,
-    pin_gemm_bruteforce, pin_gemm_single_block, pin_gemm_modes, pin_grouped_gemm, pin_swiglu, pin_tolerance,
+    pin_gemm_bruteforce, pin_gemm_single_block, pin_gemm_modes, pin_grouped_gemm, pin_blockwise_fp8, pin_swiglu,
+    pin_tolerance,
 ]

@@ -190,6 +190,25 @@ def m_silu_sign(O):
     O.silu = lambda x: np.asarray(x, dtype=np.float64) / (1.0 + np.exp(np.asarray(x, dtype=np.float64)))
 
 
+def m_blockwise_scale_inverted(O):
+    O.blockwise_scale = lambda amax: np.where(np.asarray(amax) > 0, np.asarray(amax, dtype=np.float32) / np.float32(448.0),
+                                              np.float32(1.0)).astype(np.float32)
+
+
+def m_blockwise_promote_multiplies(O):
+    orig = O.gemm_blockwise_ref
+    O.gemm_blockwise_ref = lambda a, sa, b, sb: orig(a, 1.0 / np.asarray(sa, dtype=np.float64), b,
+                                                     1.0 / np.asarray(sb, dtype=np.float64))
+
+
+def m_blockwise_weight_rows(O):
+    def q(w):
+        c, s = O.quantize_1x128(w)
+        nb = (w.shape[0] + 127) // 128
+        return c, s[::128][:nb]
+    O.quantize_128x128 = q
+
+
 def m_tolerance_loose(O):
     O.within_tolerance = lambda out, ref, S: np.abs(np.asarray(out) - ref) <= 2.0 ** -5 * np.abs(ref) + 1e-6 * S
 
@@ -198,7 +217,8 @@ MUTANTS = [m_scale_off_by_one, m_scale_ceil, m_zero_block_scale_one, m_ties_away
            m_no_saturation, m_drop_sign, m_decode_bias8, m_decode_subnormal_hidden_one,
            m_colwise_not_transposed, m_gemm_transposed, m_gemm_drop_b_scale, m_dequant_scale_sign,
            m_swizzle_swapped, m_group_blocks_not_restarting, m_group_pad_64, m_bf16_truncate,
-           m_tolerance_loose, m_input_bf16_prerounding, m_swiglu_halves_swapped, m_silu_sign]
+           m_tolerance_loose, m_input_bf16_prerounding, m_swiglu_halves_swapped, m_silu_sign,
+           m_blockwise_scale_inverted, m_blockwise_promote_multiplies, m_blockwise_weight_rows]
 
 
 def _caught(O):
