@@ -219,6 +219,36 @@ mx_status mx_grouped_gemm(int mode, const mx_operand* a, const mx_operand* b,
                           int* dev_status, void* stream);
 
 /*
+ * Variant recipe: DeepSeek-V3 blockwise FP8 ("浮点格式、数值稳定性与混合精度"
+ * §七.2-§七.3). E4M3 data with one FP32 multiplier per block, s = 448 / amax
+ * (an all-zero block takes s = 1), element = E4M3(s * x) with the product
+ * rounded to FP32 and then to E4M3 (nearest, ties to even, saturating).
+ * Blocks holding Inf or NaN are outside this recipe.
+ *
+ * mx_quantize_fp8_blockwise - x BF16 [rows, cols] (pitch ldx, a multiple of 8;
+ * 16-byte aligned), cols % 128 == 0; data E4M3 [rows, cols] (pitch cols).
+ *   block = 1:   1 x 128 activation blocks; scale FP32 [cols/128][rows] (one
+ *                row of multipliers per 128-column block, transposed so a
+ *                GEMM tile's rows are contiguous).
+ *   block = 128: 128 x 128 weight blocks (the last row block may be short);
+ *                scale FP32 [ceil(rows/128)][cols/128].
+ */
+mx_status mx_quantize_fp8_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,
+                                    float* scale, int* dev_status, void* stream);
+
+/*
+ * mx_gemm_fp8_blockwise - C[M, N] = sum over 128-K blocks kb of
+ * (A_kb . B_kb^T) / (a_scale[kb][m] * b_scale[n/128][kb]): each block's partial
+ * sum is promoted to FP32 with its two multipliers (same page, §七.3). a_data
+ * E4M3 [M, K] from block = 1, b_data E4M3 [N, K] from block = 128 (both dense,
+ * pitch K, 16-byte aligned), K % 128 == 0; C BF16 [M, N] pitch ldc, round to
+ * nearest even. Errors as mx_gemm.
+ */
+mx_status mx_gemm_fp8_blockwise(const void* a_data, const float* a_scale, int64_t M, const void* b_data,
+                                const float* b_scale, int64_t N, int64_t K, void* c, int64_t ldc, int* dev_status,
+                                void* stream);
+
+/*
  * mx_grouped_gemm_swiglu - the routed experts' gate_up fprop with the grouped
  * SwiGLU fused into its epilogue ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计"
  * §5: gate_up_proj [E, 2F, H] and the grouped SwiGLU between gate_up and

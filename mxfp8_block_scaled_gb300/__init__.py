@@ -29,8 +29,8 @@ STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAP
 
 # Symbols the header declares (the CPU tests check the library exports them).
 EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quantize_batched", "mx_quantize_f32",
-            "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_status_string", "mx_last_error",
-            "mx_abi_version")
+            "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_quantize_fp8_blockwise",
+            "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version")
 
 
 class MXError(RuntimeError):
@@ -75,6 +75,10 @@ def lib() -> ctypes.CDLL:
     L.mx_grouped_gemm_swiglu.argtypes = [ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
                                          vp, vp]
     L.mx_grouped_gemm_swiglu.restype = i32
+    L.mx_quantize_fp8_blockwise.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp]
+    L.mx_quantize_fp8_blockwise.restype = i32
+    L.mx_gemm_fp8_blockwise.argtypes = [vp, vp, i64, vp, vp, i64, i64, vp, i64, vp, vp]
+    L.mx_gemm_fp8_blockwise.restype = i32
     L.mx_status_string.argtypes = [i32]
     L.mx_status_string.restype = ctypes.c_char_p
     L.mx_last_error.argtypes = []
@@ -132,6 +136,16 @@ def mx_quantize_f32(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, r
                     dev_status, stream) -> None:
     _check(lib().mx_quantize_f32(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, row_scale, col_data,
                                  col_scale, dev_status, stream), "mx_quantize_f32")
+
+
+def mx_quantize_fp8_blockwise(x, rows, cols, ldx, block, data, scale, dev_status, stream) -> None:
+    _check(lib().mx_quantize_fp8_blockwise(x, rows, cols, ldx, block, data, scale, dev_status, stream),
+           "mx_quantize_fp8_blockwise")
+
+
+def mx_gemm_fp8_blockwise(a_data, a_scale, M, b_data, b_scale, N, K, c, ldc, dev_status, stream) -> None:
+    _check(lib().mx_gemm_fp8_blockwise(a_data, a_scale, M, b_data, b_scale, N, K, c, ldc, dev_status, stream),
+           "mx_gemm_fp8_blockwise")
 
 
 def _ref(op):
@@ -310,4 +324,39 @@ def grouped_gemm_swiglu(a, b, group_offsets, out=None, status=None, stream=None)
         out = torch.empty((a.rows, b.rows // 2), dtype=torch.bfloat16, device=a.data.device)
     mx_grouped_gemm_swiglu(a.c_operand(), b.c_operand(), group_offsets.data_ptr(), E, out.data_ptr(), out.stride(0),
                            _ptr(status), _stream(stream))
+    return out
+
+
+@dataclass
+class FP8Blockwise:
+    """E4M3 data [rows, k] with FP32 block multipliers: block 1 -> scale
+    [k/128, rows] (1 x 128 blocks), block 128 -> scale [ceil(rows/128), k/128]."""
+    data: "object"
+    scale: "object"
+    rows: int
+    k: int
+    block: int
+
+
+def quantize_fp8_blockwise(x, block: int, status=None, stream=None) -> FP8Blockwise:
+    """DeepSeek-V3 blockwise FP8 quantisation of a 2-D BF16 CUDA tensor."""
+    torch = _torch()
+    assert x.dim() == 2 and x.dtype == torch.bfloat16 and x.is_cuda and x.stride(1) == 1
+    R, C = x.shape
+    data = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    shape = (C // 128, R) if block == 1 else ((R + 127) // 128, C // 128)
+    scale = torch.empty(shape, dtype=torch.float32, device=x.device)
+    mx_quantize_fp8_blockwise(x.data_ptr(), R, C, x.stride(0), block, data.data_ptr(), scale.data_ptr(),
+                              _ptr(status), _stream(stream))
+    return FP8Blockwise(data, scale, R, C, block)
+
+
+def gemm_fp8_blockwise(a: FP8Blockwise, b: FP8Blockwise, out=None, status=None, stream=None):
+    """C[M, N] = A . B^T for an activation (block 1) and a weight (block 128)."""
+    torch = _torch()
+    assert a.block == 1 and b.block == 128 and a.k == b.k
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
+    mx_gemm_fp8_blockwise(a.data.data_ptr(), a.scale.data_ptr(), a.rows, b.data.data_ptr(), b.scale.data_ptr(),
+                          b.rows, a.k, out.data_ptr(), out.stride(0), _ptr(status), _stream(stream))
     return out

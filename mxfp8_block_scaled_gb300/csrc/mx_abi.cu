@@ -413,6 +413,88 @@ mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, i
   return launch_gemm(L, s);
 }
 
+mx_status mx_quantize_fp8_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,
+                                    float* scale, int* dev_status, void* stream) {
+  (void)dev_status;
+  if (block != 1 && block != 128) {
+    set_error("mx_quantize_fp8_blockwise: block must be 1 (1 x 128 blocks) or 128 (128 x 128 blocks)");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (rows < 0 || cols < 0 || ldx < cols) {
+    set_error("mx_quantize_fp8_blockwise: bad sizes");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (cols % 128 != 0) {
+    set_error("mx_quantize_fp8_blockwise: cols must be a multiple of 128");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (rows == 0 || cols == 0) return MX_OK;
+  if (!x || !data || !scale) {
+    set_error("mx_quantize_fp8_blockwise: null pointer");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (!aligned16(x) || ldx % 8 != 0 || !aligned16(data) || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0) {
+    set_error("mx_quantize_fp8_blockwise: x and data must be 16-byte aligned, ldx a multiple of 8, scale 4-byte aligned");
+    return MX_ERR_ALIGNMENT;
+  }
+  mx_status st = check_device();
+  if (st != MX_OK) return st;
+  return launch_quantize_blockwise(x, rows, cols, ldx, block, data, scale, static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_gemm_fp8_blockwise(const void* a_data, const float* a_scale, int64_t M, const void* b_data,
+                                const float* b_scale, int64_t N, int64_t K, void* c, int64_t ldc, int* dev_status,
+                                void* stream) {
+  if (M < 0 || N < 0 || K < 0) {
+    set_error("mx_gemm_fp8_blockwise: negative size");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (K % 128 != 0) {
+    set_error("mx_gemm_fp8_blockwise: K must be a multiple of 128");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL) {
+    set_error("mx_gemm_fp8_blockwise: sizes must be < 2^31");
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  mx_status st = check_output(c, ldc, N, M);
+  if (st != MX_OK) return st;
+  if (M == 0 || N == 0) return MX_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K > 0 && (!a_data || !b_data || !a_scale || !b_scale)) {
+    set_error("mx_gemm_fp8_blockwise: null operand");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (K > 0 && (!aligned16(a_data) || !aligned16(b_data) || (reinterpret_cast<uintptr_t>(a_scale) & 3u) != 0 ||
+                (reinterpret_cast<uintptr_t>(b_scale) & 3u) != 0)) {
+    set_error("mx_gemm_fp8_blockwise: data must be 16-byte aligned, scales 4-byte aligned");
+    return MX_ERR_ALIGNMENT;
+  }
+  st = check_device();
+  if (st != MX_OK) return st;
+  if (K == 0) return zero_output(c, ldc, N, M, s);
+  GemmLaunch L;
+  L.kind = GEMM_DENSE;
+  L.a_data = a_data;
+  L.a_scale = nullptr;
+  L.a_ld = K;
+  L.b_data = b_data;
+  L.b_scale = nullptr;
+  L.b_ld = K;
+  L.M = M;
+  L.N = N;
+  L.K = K;
+  L.b_rows_total = N;
+  L.c = c;
+  L.ldc = ldc;
+  L.offsets = nullptr;
+  L.n_groups = 0;
+  L.dev_status = dev_status;
+  L.bw_a_scale = a_scale;
+  L.bw_b_scale = b_scale;
+  return launch_gemm(L, s);
+}
+
 mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
                                  int n_groups, void* c, int64_t ldc, int* dev_status, void* stream) {
   mx_status st = check_operand(a, "a");

@@ -1109,6 +1109,232 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ===========================================================================
+// Blockwise FP8 variant (DeepSeek-V3 recipe): C = sum over 128-K blocks of
+// (A_kb . B_kb^T) / (s_a[kb][m] * s_b[n/128][kb])
+// ===========================================================================
+//
+// "浮点格式、数值稳定性与混合精度" §七.3: the block scales change along K, so
+// each 128-K block's partial sum is promoted to FP32 with its two scales. Here
+// the tensor core computes each block's partial sum (the block-scaled MMA with
+// unit E8M0 scales, loaded into TMEM once) into one of two TMEM buffers, and
+// the epilogue warps fold it into FP32 registers while the MMAs fill the other
+// buffer. 128 x 128 tiles: two 128-column partial buffers plus the unit
+// scales fit TMEM.
+
+struct BwCfg {
+  static constexpr int BN = 128;
+  static constexpr int kStages = 6;
+  static constexpr int kParts = 2;  // partial-sum buffers in TMEM (a third measured no faster)
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr uint32_t kSfCol0 = kParts * BN;  // unit scales after the partial buffers
+  static_assert(kSfCol0 + 8 <= kTmemCols, "TMEM budget");
+  static constexpr int kBarBytes = (2 * kStages + 2 * kParts + 1) * 8 + 16;
+  static constexpr size_t smem_bytes() {
+    return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kEpiBytes + 512 + kBarBytes;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                             const __grid_constant__ CUtensorMap tmap_c, const GParams p,
+                             const float* __restrict__ sa, const float* __restrict__ sb) {
+  using C = BwCfg;
+  constexpr int S = C::kStages;
+  constexpr int BN = C::BN;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * C::kABytes;
+  uint8_t* sEpi = sB + S * C::kBBytes;
+  uint8_t* sUnit = sEpi + kEpiBytes;  // a scale atom of 0x7F bytes (E8M0 1.0)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sUnit + 512);
+  uint64_t* empty_bar = full_bar + S;
+  constexpr int P = C::kParts;
+  uint64_t* part_full = empty_bar + S;   // [P] a partial sum is in TMEM
+  uint64_t* part_empty = part_full + P;  // [P] the epilogue has read it
+  uint64_t* drain_bar = part_empty + P;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(s_tmem + 1);
+  GroupInfo g{};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 128) {
+    reinterpret_cast<uint32_t*>(sUnit)[threadIdx.x] = 0x7F7F7F7Fu;
+    fence_proxy_async_smem();  // read by the tensor-core copy (async proxy)
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < P; ++b) {
+      mbar_init(&part_full[b], 1);
+      mbar_init(&part_empty[b], kEpiThreads);
+    }
+    mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
+  const int64_t ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
+  const int64_t kbs = (p.K + kBK - 1) / kBK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const Tile ti = get_tile<BN, GEMM_DENSE>(p, g, t);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!wait_or_abort(&empty_bar[stage], phase ^ 1, p, s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], C::kABytes + C::kBBytes);
+          const int32_t kx = kb * kBK;
+          tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full_bar[stage], kx, static_cast<int32_t>(ti.a_row));
+          tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full_bar[stage], kx, static_cast<int32_t>(ti.b_row));
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (*s_abort) {
+        int st = stage;
+        uint32_t ph = phase;
+        for (int64_t i = 0; i < min64(issued, S); ++i) {
+          if (--st < 0) {
+            st = S - 1;
+            ph ^= 1;
+          }
+          mbar_wait(&full_bar[st], ph, p.timeout_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_mxf8_e4m3(kBM, BN);
+      const uint32_t sf_t = tmem_base + C::kSfCol0;
+      // Unit scales for A and B, once; later MMAs of this thread see them in order.
+      tc_cp_32x128b_warpx4(sf_t, sdesc_scale_atom(smem_u32(sUnit)));
+      tc_cp_32x128b_warpx4(sf_t + 4, sdesc_scale_atom(smem_u32(sUnit)));
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t gk = 0;  // k blocks issued so far: buffer gk % P, its use count gk / P
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const Tile ti = get_tile<BN, GEMM_DENSE>(p, g, t);
+        for (int kb = 0; kb < ti.nkb; ++kb, ++gk) {
+          const int buf = static_cast<int>(gk % P);
+          if (!wait_or_abort(&full_bar[stage], phase, p, s_abort) ||
+              !wait_or_abort(&part_empty[buf], static_cast<uint32_t>(((gk / P) & 1) ^ 1), p, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::kABytes));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::kBBytes));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc_mma_mxf8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_id(idesc, k, k), sf_t, sf_t + 4,
+                        k != 0 ? 1u : 0u);
+          tc_commit(&empty_bar[stage]);
+          tc_commit(&part_full[buf]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      tc_commit(drain_bar);
+      mbar_wait(drain_bar, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp < 2 + kEpiThreads / 32) {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int col_off = half * 64;
+    uint8_t* stg = sEpi + (warp - 2) * kEpiWarpBytes;
+    int64_t gk = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile ti = get_tile<BN, GEMM_DENSE>(p, g, t);
+      const int64_t grow = ti.m0 + quarter * 32 + lane;
+      const int64_t nb = ti.n0 / 128;
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+      bool ok = true;
+      // The blocks' two multipliers, fetched one block ahead so their latency
+      // hides behind the previous block's promotion; rows past the end hold
+      // zeros, give them 1.
+      float a_s = (ti.nkb > 0 && grow < p.M) ? sa[grow] : 1.0f;
+      float b_s = ti.nkb > 0 ? sb[nb * kbs] : 1.0f;
+      for (int kb = 0; kb < ti.nkb; ++kb, ++gk) {
+        const int buf = static_cast<int>(gk % P);
+        float a_next = 1.0f, b_next = 1.0f;
+        if (kb + 1 < ti.nkb) {
+          a_next = grow < p.M ? sa[(kb + 1) * p.M + grow] : 1.0f;
+          b_next = sb[nb * kbs + kb + 1];
+        }
+        if (!wait_or_abort(&part_full[buf], static_cast<uint32_t>((gk / P) & 1), p, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t pr[64];
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN + col_off);
+        tmem_ld_32x32b_x32(taddr, pr);
+        tmem_ld_32x32b_x32(taddr + 32, pr + 32);
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&part_empty[buf]);
+        const float f = 1.0f / (a_s * b_s);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = fmaf(__uint_as_float(pr[i]), f, acc[i]);
+        a_s = a_next;
+        b_s = b_next;
+      }
+      if (!ok) break;
+      store_tile<GEMM_DENSE, 64>(p, ti, reinterpret_cast<const uint32_t*>(acc), quarter, lane, 2, col_off, stg,
+                                 &tmap_c);
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -1324,6 +1550,24 @@ bool use_pairs(const GemmLaunch& L) {
   return pair_tiles_upper(L) >= sm_count() / 2;
 }
 
+mx_status launch_blockwise(const GemmLaunch& L, GParams p, cudaStream_t s) {
+  CUtensorMap ma, mb, mc;
+  mx_status st = make_map(&ma, L.a_data, L.M, L.K, L.a_ld, kBM);
+  if (st != MX_OK) return st;
+  st = make_map(&mb, L.b_data, L.N, L.K, L.b_ld, BwCfg::BN);
+  if (st != MX_OK) return st;
+  output_map(L, p, &mc, GEMM_DENSE);
+  const size_t smem = BwCfg::smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(mx_gemm_blockwise_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(blockwise smem)");
+  const int64_t tiles = (L.M + kBM - 1) / kBM * ((L.N + BwCfg::BN - 1) / BwCfg::BN);
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count()));
+  mx_gemm_blockwise_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(ma, mb, mc, p, L.bw_a_scale,
+                                                                              L.bw_b_scale);
+  return cuda_status(cudaGetLastError(), "mx_gemm_fp8_blockwise launch");
+}
+
 }  // namespace
 
 mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
@@ -1359,6 +1603,7 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.dev_status = L.dev_status;
   p.timeout_ns = wait_timeout_ns();
 
+  if (L.bw_a_scale) return launch_blockwise(L, p, s);
   if (L.swiglu) return launch_pair<GEMM_GROUPED_M, true>(L, p, s);
   int bn;
   if (L.kind == GEMM_DENSE) {

@@ -39,6 +39,10 @@ struct QuantLaunch {
   int* dev_status;
 };
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s);
+// Blockwise FP8 variant: block = 1 (1 x 128 activation blocks, scale[kb][rows])
+// or 128 (128 x 128 weight blocks, scale[row block][kb]).
+mx_status launch_quantize_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,
+                                    float* scale, cudaStream_t s);
 
 // --- GEMM ------------------------------------------------------------------
 enum GemmKind { GEMM_DENSE = 0, GEMM_GROUPED_M = 1, GEMM_GROUPED_K = 2 };
@@ -61,6 +65,11 @@ struct GemmLaunch {
   int n_groups;
   int* dev_status;
   bool swiglu = false;  // rows-ragged only: C = SwiGLU(A . B^T), gate = B rows [0, N/2), up = [N/2, N)
+  // Blockwise FP8 variant (dense): FP32 multipliers of A's 1 x 128 blocks
+  // ([K/128][M]) and B's 128 x 128 blocks ([ceil(N/128)][K/128]); a_scale /
+  // b_scale unused.
+  const float* bw_a_scale = nullptr;
+  const float* bw_b_scale = nullptr;
 };
 mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
 

@@ -716,6 +716,97 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   }
 }
 
+// ===========================================================================
+// Variant recipe: DeepSeek-V3 blockwise FP8 (FP32 multipliers per block)
+// ===========================================================================
+//
+// "浮点格式、数值稳定性与混合精度" §七.2-§七.3: a block's multiplier is
+// s = 448 / amax and its elements are E4M3(s * x); activations use 1 x 128
+// blocks along the row, weights 128 x 128 blocks. Both steps are FP32 IEEE
+// operations (division and product correctly rounded) followed by the
+// round-to-nearest-even satfinite E4M3 conversion; an all-zero block takes
+// s = 1.
+
+__device__ __forceinline__ float blockwise_s(float amax) { return amax > 0.0f ? 448.0f / amax : 1.0f; }
+
+// Four BF16 values (two words) times s -> four E4M3 bytes.
+__device__ __forceinline__ uint32_t blockwise_quad(uint32_t w0, uint32_t w1, float s) {
+  return cvt_pair(__fmul_rn(lo_f(w0), s), __fmul_rn(hi_f(w0), s)) |
+         (cvt_pair(__fmul_rn(lo_f(w1), s), __fmul_rn(hi_f(w1), s)) << 16);
+}
+
+// 1 x 128 blocks: a half-warp per block (lane = 8 consecutive elements, one
+// 16-byte load), each warp on two consecutive blocks of a row per step.
+// s is stored transposed, scale[kb * rows + r].
+__global__ void __launch_bounds__(256) fp8_quant_1x128_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+                                                              int64_t cols, int64_t ldx, uint8_t* __restrict__ data,
+                                                              float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int hl = lane & 15;
+  const int64_t kbs = cols / 128;
+  const int64_t nblocks = rows * kbs;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t b2 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); 2 * b2 < nblocks;
+       b2 += warps) {
+    const int64_t b = 2 * b2 + (lane >> 4);  // this half-warp's block (kbs is even or the row ends)
+    const bool in = b < nblocks;
+    const int64_t r = in ? b / kbs : 0, kb = in ? b - (b / kbs) * kbs : 0;
+    const uint4 v = in ? *reinterpret_cast<const uint4*>(x + r * ldx + kb * 128 + hl * 8) : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t m = max(max(half_max(v.x & 0x7FFF7FFFu), half_max(v.y & 0x7FFF7FFFu)),
+                     max(half_max(v.z & 0x7FFF7FFFu), half_max(v.w & 0x7FFF7FFFu)));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));  // within the half-warp
+    const float s = blockwise_s(__uint_as_float(m << 16));
+    if (in) {
+      *reinterpret_cast<uint2*>(data + r * cols + kb * 128 + hl * 8) =
+          make_uint2(blockwise_quad(v.x, v.y, s), blockwise_quad(v.z, v.w, s));
+      if (hl == 0) scale[kb * rows + r] = s;
+    }
+  }
+}
+
+// 128 x 128 blocks: one CTA per block; thread t holds 64 elements of row t/2.
+__global__ void __launch_bounds__(256) fp8_quant_128x128_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+                                                                int64_t cols, int64_t ldx,
+                                                                uint8_t* __restrict__ data,
+                                                                float* __restrict__ scale) {
+  __shared__ uint32_t warp_max[8];
+  const int tid = threadIdx.x;
+  const int64_t kbs = cols / 128;
+  const int64_t rbs = (rows + 127) / 128;
+  for (int64_t b = blockIdx.x; b < rbs * kbs; b += gridDim.x) {
+    const int64_t rb = b / kbs, kb = b - rb * kbs;
+    const int64_t r = rb * 128 + (tid >> 1);
+    const bool in = r < rows;
+    uint4 v[8];  // 64 BF16 values of row r: columns (tid & 1) * 64 .. + 63 of the block
+    uint32_t m = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[q] = in ? *reinterpret_cast<const uint4*>(x + r * ldx + kb * 128 + (tid & 1) * 64 + q * 8)
+                : make_uint4(0u, 0u, 0u, 0u);
+      m = max(m, max(max(half_max(v[q].x & 0x7FFF7FFFu), half_max(v[q].y & 0x7FFF7FFFu)),
+                     max(half_max(v[q].z & 0x7FFF7FFFu), half_max(v[q].w & 0x7FFF7FFFu))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((tid & 31) == 0) warp_max[tid >> 5] = m;
+    __syncthreads();
+    uint32_t bm = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) bm = max(bm, warp_max[w]);
+    __syncthreads();  // warp_max is rewritten by the next block
+    const float s = blockwise_s(__uint_as_float(bm << 16));
+    if (in) {
+      uint4* dst = reinterpret_cast<uint4*>(data + r * cols + kb * 128 + (tid & 1) * 64);
+#pragma unroll
+      for (int q = 0; q < 8; q += 2)
+        dst[q >> 1] = make_uint4(blockwise_quad(v[q].x, v[q].y, s), blockwise_quad(v[q].z, v[q].w, s),
+                                 blockwise_quad(v[q + 1].x, v[q + 1].y, s), blockwise_quad(v[q + 1].z, v[q + 1].w, s));
+    }
+    if (tid == 0) scale[rb * kbs + kb] = s;
+  }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -795,6 +886,22 @@ mx_status launch_f32(const QuantLaunch& q, const QParams& p, bool do_row, bool d
 }
 
 }  // namespace
+
+mx_status launch_quantize_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,
+                                    float* scale, cudaStream_t s) {
+  const int64_t blocks = block == 1 ? rows * (cols / 128) : (rows + 127) / 128 * (cols / 128);
+  if (blocks == 0) return MX_OK;
+  if (block == 1) {
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((blocks + 15) / 16, 16LL * sm_count()));
+    fp8_quant_1x128_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, cols, ldx, static_cast<uint8_t*>(data), scale);
+  } else {
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(blocks, 8LL * sm_count()));
+    fp8_quant_128x128_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, cols, ldx, static_cast<uint8_t*>(data), scale);
+  }
+  return cuda_status(cudaGetLastError(), "mx_quantize_fp8_blockwise launch");
+}
 
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s) {
   QParams p;

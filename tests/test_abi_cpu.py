@@ -180,3 +180,21 @@ def test_grouped_gemm_swiglu_rejects_bad_arguments_on_host(L):
     assert _status_of(q, _op(rows=512), _op(rows=512), g, 0, c, 256, None, None) == INVALID
     assert _status_of(q, _op(rows=512, k=256), _op(rows=512, k=512), g, 2, c, 256, None, None) == INVALID
     assert _status_of(q, _op(rows=512), _op(rows=512), g, 2, c, 100, None, None) == INVALID   # ldc < F
+
+
+def test_blockwise_rejects_bad_arguments_on_host(L):
+    q = mx.mx_quantize_fp8_blockwise
+    x, d, sc = 0x10000, 0x20000, 0x30000
+    assert _status_of(q, x, 64, 128, 128, 2, d, sc, None, None) == INVALID          # block
+    assert _status_of(q, x, 64, 96, 96, 1, d, sc, None, None) == SHAPE              # cols % 128
+    assert _status_of(q, x + 8, 64, 128, 128, 1, d, sc, None, None) == ALIGN
+    assert _status_of(q, x, 64, 128, 132, 1, d, sc, None, None) == ALIGN           # ldx % 8
+    assert _status_of(q, x, 64, 128, 128, 1, None, sc, None, None) == INVALID
+    assert _status_of(q, x, 0, 128, 128, 1, None, None, None, None) == 0
+    g = mx.mx_gemm_fp8_blockwise
+    c = 0x40000
+    assert _status_of(g, x, sc, 64, d, sc, 64, 192, c, 64, None, None) == SHAPE    # K % 128
+    assert _status_of(g, x, sc, 64, d, sc, 64, 128, c, 32, None, None) == INVALID  # ldc < N
+    assert _status_of(g, x + 4, sc, 64, d, sc, 64, 128, c, 64, None, None) == ALIGN
+    assert _status_of(g, x, sc + 2, 64, d, sc, 64, 128, c, 64, None, None) == ALIGN
+    assert _status_of(g, None, sc, 64, d, sc, 64, 128, c, 64, None, None) == INVALID
