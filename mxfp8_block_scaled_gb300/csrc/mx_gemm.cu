@@ -70,6 +70,8 @@ constexpr int kBM = 128;       // tile rows per CTA (MMA M of one CTA)
 constexpr int kBK = 128;       // K elements (= bytes) per stage: four K=32 MMAs
 constexpr int kThreads = 352;  // producer, MMA, 8 epilogue warps, scale copier
 constexpr int kCopierWarp = 10;
+constexpr int kPairThreads = 384;  // the pair kernel adds a scale-gather warp
+constexpr int kGatherWarp = 11;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 512;
 constexpr uint32_t kTmemCols = 512;
@@ -784,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 
 template <int KIND, bool kSwiGLU = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                         const __grid_constant__ CUtensorMap tmap_c, const GParams p) {
@@ -874,40 +876,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    // Only the scale gather needs the whole warp; otherwise lane 0 alone runs
-    // the loop (a per-stage warp shuffle cost ~5% of GEMM throughput).
-    for (int64_t t = t_first; t < ntiles && ok && (kGatherSfa || lane == 0); t += t_step) {
+    // Lane 0 alone runs the loop (the rows-ragged scale gather has a warp of
+    // its own: a per-stage warp shuffle here cost ~5% of GEMM throughput).
+    for (int64_t t = t_first; t < ntiles && ok && lane == 0; t += t_step) {
       const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
       // Rows-ragged: B's scale atoms are those of the tile's expert. SwiGLU:
       // the second atom holds the up rows, N/256 atoms after the gate rows.
       const int64_t sfb_atom_row = (KIND == GEMM_GROUPED_M ? ti.group * p.b_ra : 0) + (ti.n0 >> 7);
       const int64_t sfb_atom_step = kSwiGLU ? (p.N >> 8) : 1;
       for (int kb = 0; kb < ti.nkb; ++kb) {
-        uint32_t good = 1;
-        if (lane == 0) good = wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
-        if constexpr (kGatherSfa) good = __shfl_sync(0xFFFFFFFFu, good, 0);
-        if (!good) {
+        if (!wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort)) {
           ok = false;
           break;
         }
         const int64_t katom = ti.k_atom0 + kb;
-        if constexpr (kGatherSfa) {
-          // Scale words of A rows m0 .. m0+127 gathered into one atom with
-          // 4-byte asynchronous copies; the odd CTA counts them on a local
-          // barrier that its relay warp forwards to the leader.
-          uint8_t* dst = sSfa + stage * 512 + lane * 16;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int64_t r = ti.a_row + lane + 32 * q;
-            const bool in = r < p.a_ra * 128;  // rows past the scale buffer read as zero
-            cp_async_4(dst + 4 * q,
-                       in ? p.a_scale + (((r >> 7) * p.ka + katom) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2)
-                          : p.a_scale,
-                       in ? 4u : 0u);
-          }
-          cp_async_arrive_noinc(leader ? &full_bar[stage] : &gfull[stage]);
-        }
-        if (lane == 0) {
+        {
           const uint32_t lfull = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * (C::kStageTx - (kGatherSfa ? 512 : 0)));
           const int32_t kx = static_cast<int32_t>(katom * kBK);
@@ -929,7 +912,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if constexpr (kGatherSfa) cp_async_wait_all();  // no copy into this CTA's memory outlives it
     if (*s_abort && leader && lane == 0) {
       // The leader's full barriers count both CTAs' copies: let them land.
       int st = stage;
@@ -1043,6 +1025,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit_pair_multicast(sf_drain, static_cast<uint16_t>(0x1));
       mbar_wait(sf_drain, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == kGatherWarp) {
+    // ----------------------------------------- A scale gather (rows-ragged)
+    // Scale words of A rows m0 .. m0+127 gathered into the stage's atom with
+    // 4-byte asynchronous copies; each lane's arrival fires when its copies
+    // have landed (the leader's full barrier, or the odd CTA's local barrier
+    // that its relay warp forwards to the leader).
+    if constexpr (kGatherSfa) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          uint32_t good = 1;
+          if (lane == 0) good = wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
+          good = __shfl_sync(0xFFFFFFFFu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
+          const int64_t katom = ti.k_atom0 + kb;
+          uint8_t* dst = sSfa + stage * 512 + lane * 16;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t r = ti.a_row + lane + 32 * q;
+            const bool in = r < p.a_ra * 128;  // rows past the scale buffer read as zero
+            cp_async_4(dst + 4 * q,
+                       in ? p.a_scale + (((r >> 7) * p.ka + katom) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2)
+                          : p.a_scale,
+                       in ? 4u : 0u);
+          }
+          cp_async_arrive_noinc(leader ? &full_bar[stage] : &gfull[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      cp_async_wait_all();  // no copy into this CTA's memory outlives it
     }
     __syncwarp();
   } else {
@@ -1468,7 +1491,7 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
