@@ -581,14 +581,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    // The whole warp only where it gathers scale words; otherwise lane 0 alone
+    // (a per-stage warp shuffle slows the stage issue).
+    for (int64_t t = blockIdx.x; t < ntiles && ok && (kGatherSfa || lane == 0); t += gridDim.x) {
       const Tile ti = get_tile<BN, KIND>(p, g, t);
       const int64_t sfb_row_atom0 = ti.n0 / 128;
       for (int kb = 0; kb < ti.nkb; ++kb) {
         const int64_t katom = ti.k_atom0 + kb;
         uint32_t good = 1;
         if (lane == 0) good = wait_or_abort(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
-        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        if constexpr (kGatherSfa) good = __shfl_sync(0xFFFFFFFFu, good, 0);
         if (!good) {
           ok = false;
           break;
