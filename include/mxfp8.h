@@ -277,6 +277,20 @@ const char* mx_last_error(void);
 /* MXFP8_ABI_VERSION of the loaded library. */
 int mx_abi_version(void);
 
+/*
+ * mx_selftest_wait_timeout - failure-reporting self test: launches one CTA
+ * whose thread waits, through the same bounded mbarrier wait every kernel of
+ * the library uses, on a barrier that nothing ever signals. When timeout_ns
+ * expires the kernel writes MX_ERR_TIMEOUT to *dev_status and returns; the
+ * context stays usable. dev_status must be a device int (0 before the call);
+ * 0 < timeout_ns <= 10 s. Asynchronous on stream.
+ *
+ * (Every kernel's waits are bounded by MXFP8_WAIT_TIMEOUT_NS nanoseconds,
+ * default 2 s, at least 1 ms; on expiry the kernel records MX_ERR_TIMEOUT,
+ * lets its own copies and MMAs land, frees its tensor memory and returns.)
+ */
+mx_status mx_selftest_wait_timeout(uint64_t timeout_ns, int* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

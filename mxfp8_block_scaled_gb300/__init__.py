@@ -30,7 +30,8 @@ STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAP
 # Symbols the header declares (the CPU tests check the library exports them).
 EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quantize_batched", "mx_quantize_f32",
             "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_quantize_fp8_blockwise",
-            "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version")
+            "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version",
+            "mx_selftest_wait_timeout")
 
 
 class MXError(RuntimeError):
@@ -79,6 +80,8 @@ def lib() -> ctypes.CDLL:
     L.mx_quantize_fp8_blockwise.restype = i32
     L.mx_gemm_fp8_blockwise.argtypes = [vp, vp, i64, vp, vp, i64, i64, vp, i64, vp, vp]
     L.mx_gemm_fp8_blockwise.restype = i32
+    L.mx_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
+    L.mx_selftest_wait_timeout.restype = i32
     L.mx_status_string.argtypes = [i32]
     L.mx_status_string.restype = ctypes.c_char_p
     L.mx_last_error.argtypes = []
@@ -146,6 +149,10 @@ def mx_quantize_fp8_blockwise(x, rows, cols, ldx, block, data, scale, dev_status
 def mx_gemm_fp8_blockwise(a_data, a_scale, M, b_data, b_scale, N, K, c, ldc, dev_status, stream) -> None:
     _check(lib().mx_gemm_fp8_blockwise(a_data, a_scale, M, b_data, b_scale, N, K, c, ldc, dev_status, stream),
            "mx_gemm_fp8_blockwise")
+
+
+def mx_selftest_wait_timeout(timeout_ns, dev_status, stream) -> None:
+    _check(lib().mx_selftest_wait_timeout(timeout_ns, dev_status, stream), "mx_selftest_wait_timeout")
 
 
 def _ref(op):

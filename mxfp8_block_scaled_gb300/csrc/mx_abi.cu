@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -11,6 +12,7 @@
 #include <mutex>
 
 #include "mx_internal.h"
+#include "mx_ptx.cuh"
 
 namespace mx {
 
@@ -129,11 +131,13 @@ mx_status cuda_status(cudaError_t e, const char* what) {
 }
 
 uint64_t wait_timeout_ns() {
+  // At least 1 ms: the drain after an abort waits for copies and MMAs already
+  // in flight (they finish within microseconds) under the same bound.
   static uint64_t v = [] {
     const char* s = std::getenv("MXFP8_WAIT_TIMEOUT_NS");
     if (s && *s) {
       const unsigned long long x = std::strtoull(s, nullptr, 10);
-      if (x > 0) return static_cast<uint64_t>(x);
+      if (x > 0) return std::max<uint64_t>(static_cast<uint64_t>(x), 1000000ull);
     }
     return static_cast<uint64_t>(2000000000ull);
   }();
@@ -236,9 +240,33 @@ static mx_status quantize_stacked(const char* fn, int elem, const void* x, int64
   return launch_quantize(q, do_row, do_col, static_cast<cudaStream_t>(stream));
 }
 
+// One thread waits, through the library's bounded wait, on an mbarrier that
+// nothing ever arrives on; when the bound expires it reports MX_ERR_TIMEOUT
+// the way every kernel of the library does.
+__global__ void selftest_wait_kernel(uint64_t timeout_ns, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, timeout_ns)) atomicExch(status, static_cast<int>(MX_ERR_TIMEOUT));
+}
+
 extern "C" {
 
 int mx_abi_version(void) { return MXFP8_ABI_VERSION; }
+
+mx_status mx_selftest_wait_timeout(uint64_t timeout_ns, int* dev_status, void* stream) {
+  if (!dev_status || timeout_ns == 0 || timeout_ns > 10000000000ull) {
+    set_error("mx_selftest_wait_timeout: dev_status must be non-null and 0 < timeout_ns <= 10 s");
+    return MX_ERR_INVALID_ARG;
+  }
+  mx_status st = check_device();
+  if (st != MX_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns, dev_status);
+  return cuda_status(cudaGetLastError(), "mx_selftest_wait_timeout launch");
+}
 
 const char* mx_last_error(void) { return g_err; }
 

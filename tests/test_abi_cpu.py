@@ -198,3 +198,9 @@ def test_blockwise_rejects_bad_arguments_on_host(L):
     assert _status_of(g, x + 4, sc, 64, d, sc, 64, 128, c, 64, None, None) == ALIGN
     assert _status_of(g, x, sc + 2, 64, d, sc, 64, 128, c, 64, None, None) == ALIGN
     assert _status_of(g, None, sc, 64, d, sc, 64, 128, c, 64, None, None) == INVALID
+
+
+def test_selftest_rejects_bad_arguments_on_host(L):
+    assert _status_of(mx.mx_selftest_wait_timeout, 0, 0x1000, None) == INVALID
+    assert _status_of(mx.mx_selftest_wait_timeout, 1000000, None, None) == INVALID
+    assert _status_of(mx.mx_selftest_wait_timeout, 20 * 10 ** 9, 0x1000, None) == INVALID
