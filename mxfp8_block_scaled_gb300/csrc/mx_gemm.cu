@@ -1435,9 +1435,13 @@ mx_status make_out_map(CUtensorMap* map, void* c, int64_t groups, int64_t rows, 
 void output_map(const GemmLaunch& L, GParams& p, CUtensorMap* mc, int kind) {
   std::memset(mc, 0, sizeof(*mc));
   p.c_tma = 0;
-  if (p.c_vec) {
+  const int64_t n_out = L.swiglu ? L.N / 2 : L.N;
+  // TMA stores clip a row at 16-byte granularity: with a row width that is not
+  // a multiple of 8 elements they would also write the first elements of the
+  // pitch gap, so such outputs take the plain bounded stores.
+  if (p.c_vec && n_out % 8 == 0) {
     const int64_t groups = (kind == GEMM_GROUPED_K) ? L.n_groups : 1;
-    if (make_out_map(mc, L.c, groups, L.M, L.swiglu ? L.N / 2 : L.N, L.ldc) == MX_OK) p.c_tma = 1;
+    if (make_out_map(mc, L.c, groups, L.M, n_out, L.ldc) == MX_OK) p.c_tma = 1;
   }
 }
 
