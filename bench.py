@@ -370,7 +370,7 @@ def run_reference(args, rank, world):
         flops_total += fl
     v = flops_total / t_total / 1e12
     line = {"impl": "reference", "metric": "MXFP8 GEMM TFLOPS (fprop+dgrad+wgrad step, dense FFN up-proj)",
-            "value": v, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "value": v, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * t_total / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "dense_ffn_up_proj M=8192 K=2048 N=10944 (fprop+dgrad+wgrad)",
