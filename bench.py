@@ -25,6 +25,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -96,7 +97,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples go to the temp directory; the line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"mxfp8_bench_clocks_gpu{gpu_index}.csv")
 
     def start(self):
         try:
