@@ -182,6 +182,41 @@ mx_status mx_quantize_f32(const float* x, int64_t batch, int64_t rows, int64_t c
                           int64_t x_batch_stride, int axis, void* row_data, void* row_scale, void* col_data,
                           void* col_scale, int* dev_status, void* stream);
 
+/* One BF16 matrix of an mx_quantize_multi call: the arguments of the dense
+ * mx_quantize (no groups), gathered in a struct. */
+typedef struct mx_quant_tensor {
+  const void* x;    /* BF16 [rows, cols], row pitch ldx elements */
+  int64_t rows;
+  int64_t cols;
+  int64_t ldx;
+  void* row_data;   /* [rows, cols] E4M3, or NULL when the row copy is not asked for */
+  void* row_scale;  /* mx_scale_bytes(rows, cols) bytes */
+  void* col_data;   /* [cols, rows] E4M3, or NULL when the column copy is not asked for */
+  void* col_scale;  /* mx_scale_bytes(cols, rows) bytes */
+} mx_quant_tensor;
+
+/*
+ * mx_quantize_multi - the dense mx_quantize of up to MX_MAX_MULTI unrelated
+ * BF16 matrices (different shapes and buffers) in one launch, e.g. the
+ * activation X and the weight W that one Linear's forward GEMM reads ([DSV3]
+ * §8.1: X and W are both quantised into row and column copies before the
+ * forward GEMM; §10, the step data flow). One launch shares the persistent
+ * grid's ramp and tail between the matrices; each matrix's results are
+ * exactly those of mx_quantize on it alone.
+ *
+ *   tensors  host array of n descriptors (host pointer; read before return).
+ *   n        0 .. MX_MAX_MULTI; n == 0 and matrices with rows == 0 or
+ *            cols == 0 are no-ops.
+ *   axis     one axis for every matrix (MX_ROWWISE, MX_COLWISE or MX_BOTH).
+ *   Requirements per matrix are those of the dense mx_quantize: cols % 32 ==
+ *   0, rows % 32 == 0 for the column copy, x 16-byte aligned with ldx % 8 ==
+ *   0, outputs 16-byte aligned. Any violation fails the whole call before
+ *   anything is launched, with the index of the matrix in mx_last_error().
+ *   Output buffers must not overlap one another or any input.
+ */
+#define MX_MAX_MULTI 8
+mx_status mx_quantize_multi(const mx_quant_tensor* tensors, int n, int axis, int* dev_status, void* stream);
+
 /*
  * mx_gemm - block-scaled GEMM C[M,N] = A[M,K] . B[N,K]^T with FP32 accumulation
  * and BF16 output rounded to nearest even ([DSV3] §8 and §13.4

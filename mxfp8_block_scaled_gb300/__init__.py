@@ -24,11 +24,13 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmxfp8_gb300.so")
 
 MX_ROWWISE, MX_COLWISE, MX_BOTH = 1, 2, 3
 MX_FPROP, MX_DGRAD, MX_WGRAD = 0, 1, 2
+MX_MAX_MULTI = 8
 STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAPE", 3: "MX_ERR_ALIGNMENT",
                 4: "MX_ERR_CUDA", 5: "MX_ERR_DEVICE_CHECK", 6: "MX_ERR_TIMEOUT", 7: "MX_ERR_NO_DEVICE"}
 
 # Symbols the header declares (the CPU tests check the library exports them).
 EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quantize_batched", "mx_quantize_f32",
+            "mx_quantize_multi",
             "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_quantize_fp8_blockwise",
             "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version",
             "mx_selftest_wait_timeout")
@@ -44,6 +46,12 @@ class MXOperandC(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
                 ("k", ctypes.c_int64), ("ld", ctypes.c_int64), ("orient", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class MXQuantTensorC(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("ldx", ctypes.c_int64),
+                ("row_data", ctypes.c_void_p), ("row_scale", ctypes.c_void_p), ("col_data", ctypes.c_void_p),
+                ("col_scale", ctypes.c_void_p)]
 
 
 _lib = None
@@ -68,6 +76,8 @@ def lib() -> ctypes.CDLL:
     L.mx_quantize_batched.restype = i32
     L.mx_quantize_f32.argtypes = [vp, i64, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp]
     L.mx_quantize_f32.restype = i32
+    L.mx_quantize_multi.argtypes = [ctypes.POINTER(MXQuantTensorC), i32, i32, vp, vp]
+    L.mx_quantize_multi.restype = i32
     L.mx_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp, vp]
     L.mx_gemm.restype = i32
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
@@ -139,6 +149,12 @@ def mx_quantize_f32(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, r
                     dev_status, stream) -> None:
     _check(lib().mx_quantize_f32(x, batch, rows, cols, ldx, x_batch_stride, axis, row_data, row_scale, col_data,
                                  col_scale, dev_status, stream), "mx_quantize_f32")
+
+
+def mx_quantize_multi(tensors, axis, dev_status, stream) -> None:
+    """``tensors``: a sequence of MXQuantTensorC."""
+    arr = (MXQuantTensorC * max(len(tensors), 1))(*tensors)
+    _check(lib().mx_quantize_multi(arr, len(tensors), axis, dev_status, stream), "mx_quantize_multi")
 
 
 def mx_quantize_fp8_blockwise(x, rows, cols, ldx, block, data, scale, dev_status, stream) -> None:
@@ -255,6 +271,33 @@ def quantize(x, axis: int = MX_BOTH, group_offsets=None, col_capacity: Optional[
                 _ptr(col.data) if col else None, _ptr(col.scale) if col else None,
                 _ptr(group_offsets), n_groups, cap, _ptr(status), _stream(stream))
     return row, col
+
+
+def quantize_multi(xs, axis: int = MX_BOTH, status=None, stream=None):
+    """MX-quantise up to MX_MAX_MULTI 2-D BF16 CUDA tensors of any shapes in
+    one launch. Returns a list of (row_copy, col_copy), one per input, each
+    exactly what ``quantize`` gives for that input alone."""
+    torch = _torch()
+    outs, descs = [], []
+    for x in xs:
+        assert x.dim() == 2 and x.dtype == torch.bfloat16 and x.is_cuda
+        assert x.numel() == 0 or x.stride(1) == 1
+        R, C = x.shape
+        dev = x.device
+        row = col = None
+        if axis & MX_ROWWISE:
+            row = MXTensor(torch.empty((R, C), dtype=torch.uint8, device=dev),
+                           torch.empty(mx_scale_bytes(R, C), dtype=torch.uint8, device=dev), R, C, MX_ROWWISE)
+        if axis & MX_COLWISE:
+            col = MXTensor(torch.empty((C, R), dtype=torch.uint8, device=dev),
+                           torch.empty(mx_scale_bytes(C, R), dtype=torch.uint8, device=dev), C, R, MX_COLWISE)
+        outs.append((row, col))
+        ldx = x.stride(0) if x.numel() else C  # an empty matrix's strides carry no pitch
+        descs.append(MXQuantTensorC(x.data_ptr(), R, C, ldx,
+                                    _ptr(row.data) if row else None, _ptr(row.scale) if row else None,
+                                    _ptr(col.data) if col else None, _ptr(col.scale) if col else None))
+    mx_quantize_multi(descs, axis, _ptr(status), _stream(stream))
+    return outs
 
 
 def gemm(mode: int, a: MXTensor, b: MXTensor, out=None, status=None, stream=None):

@@ -398,6 +398,77 @@ mx_status mx_quantize_f32(const float* x, int64_t batch, int64_t rows, int64_t c
                           row_scale, col_data, col_scale, dev_status, stream);
 }
 
+mx_status mx_quantize_multi(const mx_quant_tensor* tensors, int n, int axis, int* dev_status, void* stream) {
+  if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) {
+    set_error("mx_quantize_multi: axis must be MX_ROWWISE, MX_COLWISE or MX_BOTH");
+    return MX_ERR_INVALID_ARG;
+  }
+  if (n < 0 || n > MX_MAX_MULTI) {
+    set_error("mx_quantize_multi: n = %d is outside 0 .. %d", n, MX_MAX_MULTI);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (n == 0) return MX_OK;
+  if (!tensors) {
+    set_error("mx_quantize_multi: tensors is null");
+    return MX_ERR_INVALID_ARG;
+  }
+  const bool do_row = (axis & MX_ROWWISE) != 0;
+  const bool do_col = (axis & MX_COLWISE) != 0;
+  QuantLaunch qs[MX_MAX_MULTI];
+  int m = 0;
+  // Every matrix is checked before anything is launched.
+  for (int i = 0; i < n; ++i) {
+    const mx_quant_tensor& t = tensors[i];
+    if (t.rows < 0 || t.cols < 0 || t.ldx < t.cols) {
+      set_error("mx_quantize_multi: tensor %d: bad sizes rows=%lld cols=%lld ldx=%lld", i,
+                static_cast<long long>(t.rows), static_cast<long long>(t.cols), static_cast<long long>(t.ldx));
+      return MX_ERR_INVALID_ARG;
+    }
+    if (t.rows > 0x7FFFFFFFLL) {
+      set_error("mx_quantize_multi: tensor %d: rows must be < 2^31", i);
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (t.cols % 32 != 0 || (do_col && t.rows % 32 != 0)) {
+      set_error("mx_quantize_multi: tensor %d: cols (and rows for the column copy) must be multiples of 32", i);
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (t.rows == 0 || t.cols == 0) continue;
+    if (!t.x || !aligned16(t.x) || t.ldx % 8 != 0) {
+      set_error("mx_quantize_multi: tensor %d: x must be non-null, 16-byte aligned, ldx a multiple of 8", i);
+      return t.x ? MX_ERR_ALIGNMENT : MX_ERR_INVALID_ARG;
+    }
+    if ((do_row && (!t.row_data || !t.row_scale)) || (do_col && (!t.col_data || !t.col_scale))) {
+      set_error("mx_quantize_multi: tensor %d: a requested output is null", i);
+      return MX_ERR_INVALID_ARG;
+    }
+    if ((do_row && (!aligned16(t.row_data) || !aligned16(t.row_scale))) ||
+        (do_col && (!aligned16(t.col_data) || !aligned16(t.col_scale)))) {
+      set_error("mx_quantize_multi: tensor %d: outputs must be 16-byte aligned", i);
+      return MX_ERR_ALIGNMENT;
+    }
+    QuantLaunch& q = qs[m++];
+    q = QuantLaunch();
+    q.x = t.x;
+    q.rows = t.rows;
+    q.cols = t.cols;
+    q.ldx = t.ldx;
+    q.row_data = t.row_data;
+    q.row_scale = t.row_scale;
+    q.col_data = t.col_data;
+    q.col_scale = t.col_scale;
+    q.offsets = nullptr;
+    q.n_groups = 0;
+    q.col_pitch = t.rows;
+    q.batch = 1;
+    q.x_batch_stride = 0;
+    q.dev_status = dev_status;
+  }
+  if (m == 0) return MX_OK;
+  mx_status st = check_device();
+  if (st != MX_OK) return st;
+  return launch_quantize_multi(qs, m, do_row, do_col, static_cast<cudaStream_t>(stream));
+}
+
 mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,
                   void* stream) {
   mx_status st = check_operand(a, "a");

@@ -39,6 +39,8 @@ struct QuantLaunch {
   int* dev_status;
 };
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s);
+// Several dense BF16 matrices (batch 1 each, no groups) in one launch.
+mx_status launch_quantize_multi(const QuantLaunch* qs, int n, bool do_row, bool do_col, cudaStream_t s);
 // Blockwise FP8 variant: block = 1 (1 x 128 activation blocks, scale[kb][rows])
 // or 128 (128 x 128 weight blocks, scale[row block][kb]).
 mx_status launch_quantize_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,

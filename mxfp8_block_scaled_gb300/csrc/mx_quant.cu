@@ -79,6 +79,16 @@ struct QParams {
   uint64_t timeout_ns;
 };
 
+// Up to kMaxTensors independent matrices per launch (dense quantisation of
+// several operands at once); the grouped and single-matrix calls use one.
+constexpr int kMaxTensors = MX_MAX_MULTI;
+struct QuantArgs {
+  CUtensorMap map[kMaxTensors];
+  QParams p[kMaxTensors];
+  int64_t tile0[kMaxTensors + 1];  // first launch-wide tile of each tensor; tile0[n] = all tiles
+  int n;
+};
+
 // Byte offset of logical scale (r, kb) in the swizzled layout with `ka`
 // scale-column atoms per 128-row band.
 __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t kb, int64_t ka) {
@@ -221,9 +231,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 #define MX_QUANT_MIN_BLOCKS 2
 #endif
 
-template <bool kRow, bool kCol, bool kGrouped>
+// kMulti: the launch holds several matrices and each tile looks up its own;
+// otherwise every tile belongs to matrix 0 and its fields stay fixed
+// parameter operands.
+template <bool kRow, bool kCol, bool kGrouped, bool kMulti>
 __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
-    mx_quant_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams p) {
+    mx_quant_kernel(const __grid_constant__ QuantArgs qa) {
+  const QParams& p = qa.p[0];  // grouped and shared fields (status word, bound)
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the unit of the 128-byte swizzle pattern.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -282,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     }
   }
 
-  const int64_t ntiles = row_tiles * col_tiles * p.batch;
+  // Grouped launches hold one matrix and take their tile grid from the groups.
+  const int64_t ntiles = kGrouped ? row_tiles * col_tiles : qa.tile0[qa.n];
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -296,8 +311,9 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   if (warp == kConsumers / 32) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_x);
+      for (int i = 0; i < qa.n; ++i) tma_prefetch_desc(&qa.map[i]);
       int j = 0;
+      int ti = 0;  // tensor of tile t (t only grows)
       int last_phase_issued[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_phase_issued[s] = -1;
@@ -305,11 +321,17 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
         const int s = j % kStages;
         const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
         if (!wait_or_abort(&empty[s], ph ^ 1u, p, &s_abort)) break;
-        const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile);
+        if constexpr (kMulti)
+          while (t >= qa.tile0[ti + 1]) ++ti;
+        const QParams& pt = qa.p[ti];
+        const TileGeo g =
+            kGrouped ? tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile)
+                     : tile_geo<kGrouped>(pt, t - qa.tile0[ti], (pt.cols + kTileCols - 1) / kTileCols,
+                                          (pt.rows + kTileRows - 1) / kTileRows, g_off, g_tile);
         mbar_arrive_expect_tx(&full[s], kTileBytes);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(tiles + s * kTileBytes + h * (kTileBytes / 2), &tmap_x, &full[s],
+          tma_load_3d(tiles + s * kTileBytes + h * (kTileBytes / 2), &qa.map[ti], &full[s],
                       static_cast<int32_t>(g.c0 + h * kHalfCols), static_cast<int32_t>(g.row0),
                       static_cast<int32_t>(g.b));
 #pragma unroll
@@ -326,10 +348,17 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   } else {
     // ----------------------------------------------------------- consumers
     int j = 0;
+    int ti = 0;  // tensor of tile t (t only grows)
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
       const int s = j % kStages;
       const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
-      const TileGeo g = tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile);
+      if constexpr (kMulti)
+        while (t >= qa.tile0[ti + 1]) ++ti;
+      const QParams& p = qa.p[ti];
+      const TileGeo g =
+          kGrouped ? tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile)
+                   : tile_geo<kGrouped>(p, t - qa.tile0[ti], (p.cols + kTileCols - 1) / kTileCols,
+                                        (p.rows + kTileRows - 1) / kTileRows, g_off, g_tile);
       uint8_t* const row_data = p.row_data + g.b * p.row_data_bs;
       uint8_t* const row_scale = p.row_scale + g.b * p.row_scale_bs;
       uint8_t* const col_data = p.col_data + g.b * p.col_data_bs;
@@ -825,11 +854,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <bool R, bool C, bool G>
-mx_status launch_one(const CUtensorMap& map, const QParams& p, int64_t tiles_upper, cudaStream_t s) {
+template <bool R, bool C, bool G, bool M = false>
+mx_status launch_one(const QuantArgs& qa, int64_t tiles_upper, cudaStream_t s) {
   const size_t smem = 1024 + static_cast<size_t>(kStages) * kTileBytes + 2 * kColStageBytes + 1024 + 2 * kStages * 8 +
                       (G ? 2 * (kMaxGroups + 1) * sizeof(int32_t) : 0);
-  auto kern = mx_quant_kernel<R, C, G>;
+  auto kern = mx_quant_kernel<R, C, G, M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(quant smem)");
   int per_sm = 0;
@@ -837,7 +866,7 @@ mx_status launch_one(const CUtensorMap& map, const QParams& p, int64_t tiles_upp
   if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   const int64_t grid =
       std::max<int64_t>(1, std::min<int64_t>(tiles_upper, static_cast<int64_t>(std::max(per_sm, 1)) * sm_count()));
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(map, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(qa);
   return cuda_status(cudaGetLastError(), "mx_quantize launch");
 }
 
@@ -903,7 +932,9 @@ mx_status launch_quantize_blockwise(const void* x, int64_t rows, int64_t cols, i
   return cuda_status(cudaGetLastError(), "mx_quantize_fp8_blockwise launch");
 }
 
-mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s) {
+namespace {
+
+QParams make_qparams(const QuantLaunch& q) {
   QParams p;
   p.rows = q.rows;
   p.cols = q.cols;
@@ -923,6 +954,51 @@ mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaSt
   p.col_data_bs = q.cols * q.col_pitch;
   p.col_scale_bs = static_cast<int64_t>(mx_scale_bytes(q.cols, q.col_pitch));
   p.timeout_ns = wait_timeout_ns();
+  return p;
+}
+
+// [batch, rows, cols] view of a BF16 input (a single matrix is a batch of one),
+// 64-column boxes in the 128-byte swizzle.
+mx_status make_bf16_input_map(const QuantLaunch& q, CUtensorMap* map) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return MX_ERR_CUDA;
+  }
+  std::memset(map, 0, sizeof(*map));
+  const int64_t bstride = q.batch > 1 ? q.x_batch_stride : q.rows * q.ldx;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.cols), static_cast<cuuint64_t>(q.rows),
+                        static_cast<cuuint64_t>(q.batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.ldx * 2), static_cast<cuuint64_t>(bstride * 2)};
+  cuuint32_t box[3] = {kHalfCols, kTileRows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q.x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (quantiser input) failed (%d)", static_cast<int>(r));
+    return MX_ERR_CUDA;
+  }
+  return MX_OK;
+}
+
+mx_status launch_by_axis(const QuantArgs& qa, int64_t tiles, bool do_row, bool do_col, bool grouped, cudaStream_t s) {
+  if (grouped)
+    return do_row ? launch_one<true, true, true>(qa, tiles, s) : launch_one<false, true, true>(qa, tiles, s);
+  if (qa.n > 1) {
+    if (do_row && do_col) return launch_one<true, true, false, true>(qa, tiles, s);
+    if (do_row) return launch_one<true, false, false, true>(qa, tiles, s);
+    return launch_one<false, true, false, true>(qa, tiles, s);
+  }
+  if (do_row && do_col) return launch_one<true, true, false>(qa, tiles, s);
+  if (do_row) return launch_one<true, false, false>(qa, tiles, s);
+  return launch_one<false, true, false>(qa, tiles, s);
+}
+
+}  // namespace
+
+mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s) {
+  const QParams p = make_qparams(q);
   const bool grouped = q.offsets != nullptr && do_col;
   if (grouped && q.n_groups > kMaxGroups) {
     set_error("mx_quantize: at most %d groups", kMaxGroups);
@@ -933,35 +1009,42 @@ mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaSt
   int64_t row_tiles = (q.rows + kTileRows - 1) / kTileRows;
   if (grouped) row_tiles += q.n_groups;  // upper bound of sum ceil(m_e / 128)
   if (row_tiles == 0 || col_tiles == 0) return MX_OK;
-
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) {
-    set_error("cuTensorMapEncodeTiled is not available from the driver");
-    return MX_ERR_CUDA;
-  }
-  CUtensorMap map;
-  std::memset(&map, 0, sizeof(map));
-  // [batch, rows, cols] view; a single matrix is a batch of one.
-  const int64_t bstride = q.batch > 1 ? q.x_batch_stride : q.rows * q.ldx;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.cols), static_cast<cuuint64_t>(q.rows),
-                        static_cast<cuuint64_t>(q.batch)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.ldx * 2), static_cast<cuuint64_t>(bstride * 2)};
-  cuuint32_t box[3] = {kHalfCols, kTileRows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q.x), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    set_error("cuTensorMapEncodeTiled (quantiser input) failed (%d)", static_cast<int>(r));
-    return MX_ERR_CUDA;
-  }
+  QuantArgs qa;
+  std::memset(&qa, 0, sizeof(qa));
+  mx_status st = make_bf16_input_map(q, &qa.map[0]);
+  if (st != MX_OK) return st;
+  qa.p[0] = p;
+  qa.n = 1;
   const int64_t tiles = row_tiles * col_tiles * q.batch;
-  if (grouped) {
-    return do_row ? launch_one<true, true, true>(map, p, tiles, s) : launch_one<false, true, true>(map, p, tiles, s);
+  qa.tile0[0] = 0;
+  qa.tile0[1] = tiles;
+  return launch_by_axis(qa, tiles, do_row, do_col, grouped, s);
+}
+
+mx_status launch_quantize_multi(const QuantLaunch* qs, int n, bool do_row, bool do_col, cudaStream_t s) {
+  if (n < 1 || n > kMaxTensors) {
+    set_error("mx_quantize_multi: 1 to %d tensors", kMaxTensors);
+    return MX_ERR_INVALID_ARG;
   }
-  if (do_row && do_col) return launch_one<true, true, false>(map, p, tiles, s);
-  if (do_row) return launch_one<true, false, false>(map, p, tiles, s);
-  return launch_one<false, true, false>(map, p, tiles, s);
+  QuantArgs qa;
+  std::memset(&qa, 0, sizeof(qa));
+  int64_t tiles = 0;
+  int m = 0;
+  for (int i = 0; i < n; ++i) {
+    const QuantLaunch& q = qs[i];
+    const int64_t t = (q.rows + kTileRows - 1) / kTileRows * ((q.cols + kTileCols - 1) / kTileCols);
+    if (t == 0) continue;  // an empty matrix has nothing to write
+    mx_status st = make_bf16_input_map(q, &qa.map[m]);
+    if (st != MX_OK) return st;
+    qa.p[m] = make_qparams(q);
+    qa.tile0[m] = tiles;
+    tiles += t;
+    ++m;
+  }
+  if (m == 0) return MX_OK;
+  qa.n = m;
+  qa.tile0[m] = tiles;
+  return launch_by_axis(qa, tiles, do_row, do_col, false, s);
 }
 
 }  // namespace mx

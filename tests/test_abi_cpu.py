@@ -171,6 +171,31 @@ def test_quantize_f32_rejects_bad_arguments_on_host(L):
     assert _status_of(q, 0, 1, 64, 64, 68, 0, 1, 0x1000, 0x2000, None, None, None, None) == INVALID
 
 
+def _qt(x=0x10000, rows=64, cols=64, ldx=None, rd=0x1000, rs=0x2000, cd=0x3000, cs=0x4000):
+    return mx.MXQuantTensorC(x, rows, cols, cols if ldx is None else ldx, rd, rs, cd, cs)
+
+
+def test_quantize_multi_rejects_bad_arguments_on_host(L):
+    q = mx.mx_quantize_multi
+    good = _qt()
+    assert _status_of(q, [good, _qt(cols=48)], 3, None, None) == SHAPE          # cols % 32
+    assert _status_of(q, [good, _qt(rows=48)], 3, None, None) == SHAPE          # rows % 32, column copy
+    assert _status_of(q, [_qt(rows=-1)], 3, None, None) == INVALID
+    assert _status_of(q, [_qt(ldx=32)], 3, None, None) == INVALID               # ldx < cols
+    assert _status_of(q, [_qt(ldx=68)], 3, None, None) == ALIGN                 # ldx % 8
+    assert _status_of(q, [_qt(x=0x10008)], 3, None, None) == ALIGN
+    assert _status_of(q, [_qt(x=0)], 3, None, None) == INVALID
+    assert _status_of(q, [good, _qt(cd=None)], 3, None, None) == INVALID        # requested output null
+    assert _status_of(q, [_qt(rs=0x2008)], 1, None, None) == ALIGN
+    assert _status_of(q, [good], 0, None, None) == INVALID                      # axis
+    assert _status_of(q, [good] * (mx.MX_MAX_MULTI + 1), 3, None, None) == INVALID
+    # rows % 32 only binds the column copy; empty matrices and n == 0 are no-ops
+    assert _status_of(q, [_qt(rows=48, x=0, cd=None, cs=None, ldx=64)], 1, None, None) == INVALID  # null x
+    assert _status_of(q, [_qt(rows=0, x=0, rd=None, rs=None, cd=None, cs=None)], 3, None, None) == 0
+    assert _status_of(q, [], 3, None, None) == 0
+    assert _status_of(q, [_qt(cols=0, x=0, rd=None, rs=None, cd=None, cs=None)], 3, None, None) == 0
+
+
 def test_grouped_gemm_swiglu_rejects_bad_arguments_on_host(L):
     c, g = 0x4000, 0x8000
     q = mx.mx_grouped_gemm_swiglu
