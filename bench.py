@@ -206,7 +206,9 @@ class DenseFFN:
         return {k: (2 + 1 + 1 + 2 / 32) * r.rows * r.k for k, (r, _) in self.q.items()}
 
     def launches_per_step(self):
-        return 5
+        (xr, xc), (wr, wc), (dr, dc) = self.q["X"], self.q["W"], self.q["dY"]
+        return 2 + sum(gemm_launches(self.mx, mode, a, b) for mode, a, b in
+                       ((self.mx.MX_FPROP, xr, wr), (self.mx.MX_DGRAD, dr, wc), (self.mx.MX_WGRAD, dc, xc)))
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.host.values())
@@ -614,6 +616,12 @@ def _linear_step(layers, mx, stream, timers=None):
                 e.record(stream)
 
 
+def gemm_launches(mx, mode, a, b):
+    """Kernel launches of one dense mx_gemm call: the GEMM, plus the split-tail
+    reduction when the library splits this GEMM's last round."""
+    return 1 + (1 if mx.mx_gemm_workspace_bytes(mode, a.c_operand(), b.c_operand()) > 0 else 0)
+
+
 def _gemm_shapes(ly):
     """(label, M, N, K) of the three GEMMs of one Linear layer."""
     M, N, K = ly["M"], ly["N"], ly["K"]
@@ -684,7 +692,12 @@ def run_mla(args, rank, world, peaks, peak_src):
                          "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8, "traffic": None,
                          "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}",
                          "roofline_time_frac": sum(g["roofline_ms"] for g in per_gemm) / gemm_ms_total},
-            "gpu_launches": 6 * len(layers) * args.steps, "clocks": clk}
+            "gpu_launches": sum(3 + sum(gemm_launches(mx, mode, a, b) for mode, a, b in
+                                         ((mx.MX_FPROP, ly["q"][0][0], ly["q"][1][0]),
+                                          (mx.MX_DGRAD, ly["q"][2][0], ly["q"][1][1]),
+                                          (mx.MX_WGRAD, ly["q"][2][1], ly["q"][0][1])))
+                                for ly in layers) * args.steps,
+            "clocks": clk}
     if rank == 0:
         print(json.dumps(line))
 
@@ -732,7 +745,7 @@ def run_single(args, rank, world, peaks, peak_src):
                        "l2": "inputs stay in L2 (launch-latency bound; no roofline fraction)"},
             "per_kernel_us": {"quant": timers.total_ms("quant") / timers.count("quant") * 1e3,
                               "gemm": timers.total_ms("gemm") / timers.count("gemm") * 1e3},
-            "gpu_launches": 3 * args.steps, "clocks": clk}
+            "gpu_launches": (2 + gemm_launches(mx, mx.MX_FPROP, xr, wr)) * args.steps, "clocks": clk}
     if rank == 0:
         print(json.dumps(line))
 

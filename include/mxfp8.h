@@ -11,9 +11,12 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- * - All pointers named *_data, *_scale, x, c and group_offsets are DEVICE
- *   pointers, allocated and owned by the caller. The library never allocates,
- *   frees or keeps device memory, and keeps no state between calls.
+ * - All pointers named *_data, *_scale, x, c, workspace and group_offsets are
+ *   DEVICE pointers, allocated and owned by the caller. One exception to "the
+ *   caller owns all memory": mx_gemm takes its split-tail scratch from a
+ *   stream-ordered pool the library keeps per device (see
+ *   mx_gemm_workspace_bytes); mx_gemm_with_workspace and every other call
+ *   allocate nothing. No other state is kept between calls.
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *   void*; NULL is the legacy default stream) on the current device, which must
  *   be an sm_103 GPU. Nothing is synchronised.
@@ -233,6 +236,34 @@ mx_status mx_quantize_multi(const mx_quant_tensor* tensors, int n, int axis, int
  */
 mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,
                   int* dev_status, void* stream);
+
+/*
+ * Scratch memory of the dense GEMM. When the 256 x 256 tiles leave the last
+ * round over the GPU's SM pairs partly empty, the contraction of those last
+ * tiles is cut into equal runs of 128-K blocks, one run per SM pair; each run
+ * leaves FP32 partial tiles in a workspace, and a second kernel adds a tile's
+ * partials in a fixed order and rounds once to BF16 (so results stay
+ * bit-identical from call to call, and within the same error bound as the
+ * whole-tile path: FP32 accumulation throughout). mx_gemm takes that workspace
+ * from a stream-ordered memory pool the library owns (created on first use,
+ * kept for the process). The two calls below never allocate.
+ *
+ * mx_gemm_workspace_bytes - bytes of workspace mx_gemm_with_workspace would use
+ * for these operands on the current device (0: this GEMM does not split).
+ *   Same operand checks as mx_gemm; *bytes is a host pointer.
+ *
+ * mx_gemm_with_workspace - mx_gemm with caller-owned scratch memory.
+ *   workspace        device memory, 16-byte aligned, owned by the caller; it
+ *                    must stay untouched until the GEMM's work on `stream`
+ *                    has finished. May be NULL when workspace_bytes == 0.
+ *   workspace_bytes  its size. With less than mx_gemm_workspace_bytes the
+ *                    GEMM runs whole tiles only: same results up to FP32
+ *                    summation order, never an error.
+ *   Everything else is exactly mx_gemm.
+ */
+mx_status mx_gemm_workspace_bytes(int mode, const mx_operand* a, const mx_operand* b, size_t* bytes);
+mx_status mx_gemm_with_workspace(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,
+                                 void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
 /*
  * mx_grouped_gemm - per-expert block-scaled GEMMs over contiguous token ranges

@@ -33,7 +33,7 @@ EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quant
             "mx_quantize_multi",
             "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_quantize_fp8_blockwise",
             "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version",
-            "mx_selftest_wait_timeout")
+            "mx_selftest_wait_timeout", "mx_gemm_workspace_bytes", "mx_gemm_with_workspace")
 
 
 class MXError(RuntimeError):
@@ -80,6 +80,12 @@ def lib() -> ctypes.CDLL:
     L.mx_quantize_multi.restype = i32
     L.mx_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp, vp]
     L.mx_gemm.restype = i32
+    L.mx_gemm_workspace_bytes.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC),
+                                          ctypes.POINTER(ctypes.c_size_t)]
+    L.mx_gemm_workspace_bytes.restype = i32
+    L.mx_gemm_with_workspace.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp,
+                                         ctypes.c_size_t, vp, vp]
+    L.mx_gemm_with_workspace.restype = i32
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
                                   vp, vp]
     L.mx_grouped_gemm.restype = i32
@@ -177,6 +183,18 @@ def _ref(op):
 
 def mx_gemm(mode, a: MXOperandC, b: MXOperandC, c, ldc, dev_status, stream) -> None:
     _check(lib().mx_gemm(mode, _ref(a), _ref(b), c, ldc, dev_status, stream), "mx_gemm")
+
+
+def mx_gemm_workspace_bytes(mode, a: MXOperandC, b: MXOperandC) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().mx_gemm_workspace_bytes(mode, _ref(a), _ref(b), ctypes.byref(out)), "mx_gemm_workspace_bytes")
+    return int(out.value)
+
+
+def mx_gemm_with_workspace(mode, a: MXOperandC, b: MXOperandC, c, ldc, workspace, workspace_bytes, dev_status,
+                           stream) -> None:
+    _check(lib().mx_gemm_with_workspace(mode, _ref(a), _ref(b), c, ldc, workspace, workspace_bytes, dev_status,
+                                        stream), "mx_gemm_with_workspace")
 
 
 def mx_grouped_gemm(mode, a: MXOperandC, b: MXOperandC, group_offsets, n_groups, c, ldc, dev_status,

@@ -469,8 +469,9 @@ mx_status mx_quantize_multi(const mx_quant_tensor* tensors, int n, int axis, int
   return launch_quantize_multi(qs, m, do_row, do_col, static_cast<cudaStream_t>(stream));
 }
 
-mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,
-                  void* stream) {
+// Dense GEMM checks shared by the entry points; fills L (dense, no workspace).
+static mx_status dense_gemm_setup(const char* fn, int mode, const mx_operand* a, const mx_operand* b, void* c,
+                                  int64_t ldc, int* dev_status, bool check_c, GemmLaunch* L) {
   mx_status st = check_operand(a, "a");
   if (st != MX_OK) return st;
   st = check_operand(b, "b");
@@ -478,38 +479,83 @@ mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, i
   st = check_mode(mode, a, b);
   if (st != MX_OK) return st;
   if (a->k != b->k) {
-    set_error("mx_gemm: a.k (%lld) != b.k (%lld)", static_cast<long long>(a->k), static_cast<long long>(b->k));
+    set_error("%s: a.k (%lld) != b.k (%lld)", fn, static_cast<long long>(a->k), static_cast<long long>(b->k));
     return MX_ERR_INVALID_ARG;
   }
   if (a->rows > 0x7FFFFFFFLL || b->rows > 0x7FFFFFFFLL || a->k > 0x7FFFFFFFLL) {
-    set_error("mx_gemm: sizes must be < 2^31");
+    set_error("%s: sizes must be < 2^31", fn);
     return MX_ERR_UNSUPPORTED_SHAPE;
   }
-  st = check_output(c, ldc, b->rows, a->rows);
-  if (st != MX_OK) return st;
-  if (a->rows == 0 || b->rows == 0) return MX_OK;
-  st = check_device();
+  if (check_c) {
+    st = check_output(c, ldc, b->rows, a->rows);
+    if (st != MX_OK) return st;
+  }
+  L->kind = GEMM_DENSE;
+  L->a_data = a->data;
+  L->a_scale = a->scale;
+  L->a_ld = a->ld ? a->ld : a->k;
+  L->b_data = b->data;
+  L->b_scale = b->scale;
+  L->b_ld = b->ld ? b->ld : b->k;
+  L->M = a->rows;
+  L->N = b->rows;
+  L->K = a->k;
+  L->b_rows_total = b->rows;
+  L->c = c;
+  L->ldc = ldc;
+  L->offsets = nullptr;
+  L->n_groups = 0;
+  L->dev_status = dev_status;
+  return MX_OK;
+}
+
+static mx_status dense_gemm_run(GemmLaunch& L, void* stream) {
+  if (L.M == 0 || L.N == 0) return MX_OK;
+  mx_status st = check_device();
   if (st != MX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a->k == 0) return zero_output(c, ldc, b->rows, a->rows, s);
-  GemmLaunch L;
-  L.kind = GEMM_DENSE;
-  L.a_data = a->data;
-  L.a_scale = a->scale;
-  L.a_ld = a->ld ? a->ld : a->k;
-  L.b_data = b->data;
-  L.b_scale = b->scale;
-  L.b_ld = b->ld ? b->ld : b->k;
-  L.M = a->rows;
-  L.N = b->rows;
-  L.K = a->k;
-  L.b_rows_total = b->rows;
-  L.c = c;
-  L.ldc = ldc;
-  L.offsets = nullptr;
-  L.n_groups = 0;
-  L.dev_status = dev_status;
+  if (L.K == 0) return zero_output(L.c, L.ldc, L.N, L.M, s);
   return launch_gemm(L, s);
+}
+
+mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,
+                  void* stream) {
+  GemmLaunch L;
+  mx_status st = dense_gemm_setup("mx_gemm", mode, a, b, c, ldc, dev_status, true, &L);
+  if (st != MX_OK) return st;
+  L.ws_alloc = true;
+  return dense_gemm_run(L, stream);
+}
+
+mx_status mx_gemm_workspace_bytes(int mode, const mx_operand* a, const mx_operand* b, size_t* bytes) {
+  if (!bytes) {
+    set_error("mx_gemm_workspace_bytes: bytes is null");
+    return MX_ERR_INVALID_ARG;
+  }
+  *bytes = 0;
+  GemmLaunch L;
+  mx_status st = dense_gemm_setup("mx_gemm_workspace_bytes", mode, a, b, nullptr, 0, nullptr, false, &L);
+  if (st != MX_OK) return st;
+  if (L.M == 0 || L.N == 0 || L.K == 0) return MX_OK;
+  st = check_device();
+  if (st != MX_OK) return st;
+  *bytes = gemm_workspace_bytes(L);
+  return MX_OK;
+}
+
+mx_status mx_gemm_with_workspace(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,
+                                 void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+  GemmLaunch L;
+  mx_status st = dense_gemm_setup("mx_gemm_with_workspace", mode, a, b, c, ldc, dev_status, true, &L);
+  if (st != MX_OK) return st;
+  if (workspace_bytes > 0 && (!workspace || !aligned16(workspace))) {
+    set_error("mx_gemm_with_workspace: workspace must be non-null and 16-byte aligned when workspace_bytes > 0");
+    return workspace ? MX_ERR_ALIGNMENT : MX_ERR_INVALID_ARG;
+  }
+  L.ws = workspace_bytes > 0 ? workspace : nullptr;
+  L.ws_bytes = workspace_bytes;
+  L.ws_alloc = false;
+  return dense_gemm_run(L, stream);
 }
 
 mx_status mx_quantize_fp8_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,

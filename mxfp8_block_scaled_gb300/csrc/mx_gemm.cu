@@ -157,7 +157,21 @@ struct GParams {
   int n_groups;
   int* dev_status;
   uint64_t timeout_ns;
+  // Dense pair kernel, split tail (sk_w > 0): tiles [sk_first, mu*nt) are the
+  // last partial wave. Their K blocks, laid end to end (sk_total of them), are
+  // cut into sk_slots runs of sk_w blocks, one run per pair of SMs; a run
+  // covers at most two tiles (two segments), and each segment leaves an FP32
+  // partial tile in ws for the reduction kernel.
+  int64_t sk_first;
+  int64_t sk_total;
+  int32_t sk_w;
+  int32_t sk_slots;
+  float* ws;
 };
+
+// One segment's partial tile in the workspace: [unit][cta of the pair][epilogue
+// warp][32 float4 columns][32 lanes], so each warp store covers 512 bytes.
+constexpr int64_t kPartialFloats = 2LL * 8 * 32 * 32 * 4;  // 256 x 256
 
 struct Tile {
   int64_t m0, n0;      // output tile origin (this CTA's rows) within the (per-expert) C
@@ -167,6 +181,7 @@ struct Tile {
   int32_t nkb;         // number of 128-K blocks
   int32_t valid_m;     // rows of the tile that exist (may be <= 0 for a pair's spare tile)
   int32_t group;       // expert (grouped kinds)
+  int32_t part;        // -1: whole tile; >= 0: split-tail segment (workspace unit); -2: empty segment
   const uint8_t* sfb;  // base of B's scales for this tile's expert
   __nv_bfloat16* cbase;  // C element (m0, n0)
 };
@@ -199,6 +214,7 @@ __device__ __forceinline__ int64_t num_tiles(const GParams& p, const GroupInfo& 
 template <int BN, int KIND>
 __device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, int64_t t) {
   Tile ti;
+  ti.part = -1;
   const int64_t nt = (p.N + BN - 1) / BN;
   const int64_t mt = (p.M + kBM - 1) / kBM;
   if (KIND == GEMM_DENSE) {
@@ -257,6 +273,7 @@ __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo&
   const int64_t nt = (p.N + BN - 1) / BN;
   const int64_t mu = ((p.M + kBM - 1) / kBM + 1) / 2;
   Tile ti;
+  ti.part = -1;
   int64_t mp, nb;
   if (KIND == GEMM_GROUPED_M) {
     // Pair row tiles of 256 inside one expert, N-fastest; the odd CTA's half
@@ -284,10 +301,34 @@ __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo&
     return ti;
   }
   if (KIND == GEMM_DENSE) {
-    mp = p.n_fast ? t / nt : t % mu;
-    nb = p.n_fast ? t % nt : t / mu;
+    const int64_t nkb = (p.K + kBK - 1) / kBK;
+    int64_t tt = t;
     ti.k_atom0 = 0;
-    ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
+    ti.nkb = static_cast<int32_t>(nkb);
+    if (p.sk_w > 0 && t >= p.sk_first) {
+      // Split tail: run `slot` is K blocks [slot*w, slot*w + w) of the tail
+      // tiles laid end to end; segment 0 ends with its first tile, segment 1
+      // is the remainder in the next tile.
+      const int64_t v = t - p.sk_first;
+      const int64_t slot = v % p.sk_slots, seg = v / p.sk_slots;
+      const int64_t g0 = slot * p.sk_w, g1 = min64(g0 + p.sk_w, p.sk_total);
+      const int64_t tile_end = (g0 / nkb + 1) * nkb;
+      const int64_t lo = seg == 0 ? g0 : tile_end;
+      const int64_t hi = seg == 0 ? min64(g1, tile_end) : g1;
+      tt = p.sk_first;
+      if (lo >= hi) {
+        ti.part = -2;
+        ti.nkb = 0;
+      } else {
+        const int64_t j = lo / nkb;
+        tt = p.sk_first + j;
+        ti.k_atom0 = lo - j * nkb;
+        ti.nkb = static_cast<int32_t>(hi - lo);
+        ti.part = static_cast<int32_t>(slot * 2 + seg);
+      }
+    }
+    mp = p.n_fast ? tt / nt : tt % mu;
+    nb = p.n_fast ? tt % nt : tt / mu;
     ti.group = 0;
   } else {
     const int64_t per = mu * nt;
@@ -866,9 +907,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *s_tmem;
   const int64_t nt = (p.N + BN - 1) / BN;
-  const int64_t ntiles = (KIND == GEMM_GROUPED_M)
-                             ? static_cast<int64_t>(g.total) * nt
-                             : (((p.M + kBM - 1) / kBM + 1) / 2) * nt * (KIND == GEMM_GROUPED_K ? p.n_groups : 1);
+  int64_t ntiles = (KIND == GEMM_GROUPED_M)
+                       ? static_cast<int64_t>(g.total) * nt
+                       : (((p.M + kBM - 1) / kBM + 1) / 2) * nt * (KIND == GEMM_GROUPED_K ? p.n_groups : 1);
+  if (KIND == GEMM_DENSE && p.sk_w > 0) ntiles = p.sk_first + 2 * static_cast<int64_t>(p.sk_slots);
   const int64_t t_first = blockIdx.x >> 1;
   const int64_t t_step = gridDim.x >> 1;
 
@@ -937,6 +979,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
         const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+        if (ti.part == -2) continue;  // an empty split-tail segment
         if (!wait_or_abort<true>(acc_empty, acc_phase ^ 1, p, s_abort)) break;
         tc_fence_after_sync();
         for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -1081,6 +1124,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint32_t acc_phase = 0;
     for (int64_t t = t_first; t < ntiles; t += t_step) {
       const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+      if (ti.part == -2) continue;
       if (!wait_or_abort<true>(acc_full, acc_phase, p, s_abort)) break;
       tc_fence_after_sync();
       uint32_t r[kCols];
@@ -1107,6 +1151,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lacc_empty);  // the even CTA's MMAs may overwrite the accumulator
       acc_phase ^= 1;
+      if (KIND == GEMM_DENSE && ti.part >= 0) {
+        // Split-tail segment: the FP32 partial goes to the workspace.
+        float4* dst = reinterpret_cast<float4*>(p.ws) +
+                      ((static_cast<int64_t>(ti.part) * 2 + crank) * 8 + (warp - 2)) * (32 * 32) + lane;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          dst[j * 32] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        continue;
+      }
       if constexpr (kSwiGLU) {
         // SwiGLU in FP32 on the FP32 accumulators, one rounding to BF16 at the store
         // (the fast exponential's error stays below 1e-5 relative for |x| < 88).
@@ -1131,6 +1185,76 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// ===========================================================================
+// Split-tail reduction
+// ===========================================================================
+//
+// Tail tile j's FP32 partials, one per run of K blocks that touched it, are
+// added in run order (so repeated calls give identical bits) and rounded to
+// BF16 once, as the GEMM epilogue does. Block (2j + r) * 16 + c handles the
+// r-th CTA's 128 rows and the 8-column chunk c of each epilogue warp's half:
+// thread (w, lane) holds row `lane` of epilogue warp w + 2, so its partials
+// are two float4 of every unit, and the loads of up to four units are in
+// flight at once.
+__global__ void __launch_bounds__(256) mx_gemm_sk_reduce_kernel(const GParams p) {
+  const int64_t nkb = (p.K + kBK - 1) / kBK;
+  const int c = blockIdx.x & 15;
+  const int crank = (blockIdx.x >> 4) & 1;
+  const int64_t j = blockIdx.x >> 5;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = (w + 2) & 3, half = w >> 2;
+  const int64_t nt = (p.N + PairCfg::BN - 1) / PairCfg::BN;
+  const int64_t mu = ((p.M + kBM - 1) / kBM + 1) / 2;
+  const int64_t tt = p.sk_first + j;
+  const int64_t mp = p.n_fast ? tt / nt : tt % mu;
+  const int64_t nb = p.n_fast ? tt % nt : tt / mu;
+  const int64_t row = (2 * mp + crank) * kBM + quarter * 32 + lane;
+  const int64_t col = nb * PairCfg::BN + half * 128 + 8 * c;
+  const int64_t s_lo = j * nkb / p.sk_w, s_hi = ((j + 1) * nkb - 1) / p.sk_w;
+  const float4* base = reinterpret_cast<const float4*>(p.ws) + (crank * 8 + w) * (32 * 32) + (2 * c) * 32 + lane;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int64_t s0 = s_lo; s0 <= s_hi; s0 += 4) {
+    float4 v[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t slot = s0 + u;
+      if (slot <= s_hi) {
+        const int64_t unit = slot * 2 + (slot * p.sk_w >= j * nkb ? 0 : 1);
+        const float4* src = base + unit * (kPartialFloats / 4);
+        v[u][0] = __ldcs(src);
+        v[u][1] = __ldcs(src + 32);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (s0 + u <= s_hi) {  // in run order
+        acc[0] += v[u][0].x;
+        acc[1] += v[u][0].y;
+        acc[2] += v[u][0].z;
+        acc[3] += v[u][0].w;
+        acc[4] += v[u][1].x;
+        acc[5] += v[u][1].y;
+        acc[6] += v[u][1].z;
+        acc[7] += v[u][1].w;
+      }
+    }
+  }
+  if (row < p.M && col < p.n_out) {
+    __nv_bfloat16* dst = p.c + row * p.ldc + col;
+    const uint32_t wv[4] = {pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                            pack_bf16(acc[6], acc[7])};
+    if (p.c_vec && col + 8 <= p.n_out) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (col + e < p.n_out) reinterpret_cast<uint16_t*>(dst)[e] = static_cast<uint16_t>(wv[e >> 1] >> ((e & 1) * 16));
+    }
   }
 }
 
@@ -1473,6 +1597,82 @@ int64_t pair_tiles_upper(const GemmLaunch& L) {
   return mu * nt;
 }
 
+// Dense pair schedule: whole 256 x 256 tiles round by round and, when the last
+// round is partial, optionally the split tail (see GParams). Times are
+// estimates from the per-SM-pair MXFP8 rate (19 TFLOP/s per SM) and a fixed
+// ~1 us per tile (accumulator drain, epilogue). The split costs ~16 us on top
+// of its runs (up to two segments per run, each starting its pipeline cold and
+// storing a 256 KB FP32 partial; the reduction launch) plus ~0.06 us per
+// partial read back, as measured on GB300; runs are at least four K blocks
+// long. It therefore pays for few-tile, long-K GEMMs (weight gradients over
+// many tokens), not for a short tail of a many-round GEMM.
+struct PairPlan {
+  int64_t clusters = 1;
+  int64_t sk_first = 0, sk_total = 0, tail_tiles = 0;
+  int32_t sk_w = 0, sk_slots = 0;
+  double est_us = 0.0;
+  size_t ws_bytes = 0;
+};
+
+int env_int(const char* name, int dflt);
+
+PairPlan plan_pair_dense(const GemmLaunch& L, bool allow_split) {
+  static const int split_mode = env_int("MXFP8_GEMM_SPLIT", 1);  // 0: whole tiles only
+  if (split_mode == 0) allow_split = false;
+  PairPlan pl;
+  const int64_t slots = std::max(1, sm_count() / 2);
+  const int64_t nt = (L.N + PairCfg::BN - 1) / PairCfg::BN;
+  const int64_t tiles = ((L.M + kBM - 1) / kBM + 1) / 2 * nt;
+  const int64_t nkb = (L.K + kBK - 1) / kBK;
+  const double t_kb = 2.0 * PairCfg::BN * PairCfg::BN * kBK / (2 * 19.0e12) * 1e6;
+  const double c_tile = 1.0;
+  const int64_t full = tiles / slots, rem = tiles % slots;
+  pl.clusters = std::max<int64_t>(1, std::min(tiles, slots));
+  pl.est_us = static_cast<double>(full + (rem ? 1 : 0)) * (nkb * t_kb + c_tile);
+  if (!allow_split || rem == 0 || nkb < 2) return pl;
+  const int64_t total = rem * nkb;
+  // <= nkb (rem < slots; a run spans at most two tiles)
+  const int64_t w = std::min(nkb, std::max<int64_t>(4, (total + slots - 1) / slots));
+  const int64_t runs = (total + w - 1) / w;
+  const double split_tail = w * t_kb + 16.0 + 0.06 * static_cast<double>(runs + rem);
+  const double whole_tail = nkb * t_kb + c_tile;
+  if (split_tail + 4.0 >= whole_tail) return pl;
+  pl.clusters = slots;  // runs past `runs` are empty
+  pl.sk_first = full * slots;
+  pl.sk_total = total;
+  pl.tail_tiles = rem;
+  pl.sk_w = static_cast<int32_t>(w);
+  pl.sk_slots = static_cast<int32_t>(slots);
+  pl.est_us = static_cast<double>(full) * (nkb * t_kb + c_tile) + split_tail;
+  pl.ws_bytes = static_cast<size_t>(2 * slots) * kPartialFloats * sizeof(float);
+  return pl;
+}
+
+// Stream-ordered workspace from a pool the library owns (one per device,
+// never trimmed), so a call needs no synchronous allocation and can be
+// captured in a CUDA graph.
+cudaMemPool_t workspace_pool(int dev) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = UINT64_MAX;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[dev] = pool;
+  }
+  return pools[dev];
+}
+
+bool split_allowed(const GemmLaunch& L, size_t need) { return L.ws_alloc || (L.ws && L.ws_bytes >= need); }
+
 template <int KIND, bool kSwiGLU = false>
 mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) {
   GParams p = p_in;
@@ -1492,8 +1692,34 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   auto kern = mx_gemm_pair_kernel<KIND, kSwiGLU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
-  const int64_t pairs = pair_tiles_upper(L);
-  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pairs, sm_count() / 2));
+  int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pair_tiles_upper(L), sm_count() / 2));
+  PairPlan pl;
+  void* pooled = nullptr;
+  if constexpr (KIND == GEMM_DENSE) {
+    pl = plan_pair_dense(L, true);
+    if (pl.sk_w > 0 && !split_allowed(L, pl.ws_bytes)) pl = plan_pair_dense(L, false);
+    if (pl.sk_w > 0) {
+      if (L.ws && L.ws_bytes >= pl.ws_bytes) {
+        p.ws = static_cast<float*>(L.ws);
+      } else {
+        int dev = 0;
+        cudaMemPool_t pool = cudaGetDevice(&dev) == cudaSuccess ? workspace_pool(dev) : nullptr;
+        if (pool && cudaMallocFromPoolAsync(&pooled, pl.ws_bytes, pool, s) == cudaSuccess) {
+          p.ws = static_cast<float*>(pooled);
+        } else {
+          (void)cudaGetLastError();  // no workspace: whole tiles only
+          pl = plan_pair_dense(L, false);
+        }
+      }
+    }
+    if (pl.sk_w > 0) {
+      p.sk_first = pl.sk_first;
+      p.sk_total = pl.sk_total;
+      p.sk_w = pl.sk_w;
+      p.sk_slots = pl.sk_slots;
+    }
+    clusters = pl.clusters;
+  }
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
@@ -1507,7 +1733,16 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, mc, p), "mx_gemm launch (CTA pairs)");
+  st = cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, mc, p), "mx_gemm launch (CTA pairs)");
+  if (st == MX_OK && p.sk_w > 0) {
+    mx_gemm_sk_reduce_kernel<<<static_cast<unsigned>(32 * pl.tail_tiles), 256, 0, s>>>(p);
+    st = cuda_status(cudaGetLastError(), "mx_gemm split-tail reduction launch");
+  }
+  if (pooled) {
+    const mx_status fst = cuda_status(cudaFreeAsync(pooled, s), "cudaFreeAsync(workspace)");
+    if (st == MX_OK) st = fst;
+  }
+  return st;
 }
 
 int env_int(const char* name, int dflt) {
@@ -1529,10 +1764,8 @@ double dense_cfg_time_us(const GemmLaunch& L, int cfg) {
   int64_t tiles, slots;
   double tile_flops, rate;
   if (cfg == CFG_PAIR) {
-    tiles = (mt + 1) / 2 * ((L.N + 255) / 256);
-    slots = sms / 2;
-    tile_flops = 2.0 * 256 * 256 * kpad;
-    rate = 2 * 19.0e12;
+    const PairPlan pl = plan_pair_dense(L, true);
+    return (pl.sk_w > 0 && split_allowed(L, pl.ws_bytes)) ? pl.est_us : plan_pair_dense(L, false).est_us;
   } else {
     const int bn = cfg == CFG_BN256 ? 256 : 128;
     tiles = mt * ((L.N + bn - 1) / bn);
@@ -1599,6 +1832,15 @@ mx_status launch_blockwise(const GemmLaunch& L, GParams p, cudaStream_t s) {
 
 }  // namespace
 
+size_t gemm_workspace_bytes(const GemmLaunch& L) {
+  if (L.kind != GEMM_DENSE || L.swiglu || L.bw_a_scale || L.M == 0 || L.N == 0 || L.K == 0) return 0;
+  GemmLaunch q = L;
+  q.ws_alloc = true;  // the size a split would need
+  if (choose_dense_cfg(q) != CFG_PAIR) return 0;
+  const PairPlan pl = plan_pair_dense(q, true);
+  return pl.sk_w > 0 ? pl.ws_bytes : 0;
+}
+
 mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   if (L.M == 0 || L.N == 0) return MX_OK;
   if (L.kind != GEMM_DENSE && L.n_groups > kMaxGroups) {
@@ -1631,6 +1873,11 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.n_groups = L.n_groups;
   p.dev_status = L.dev_status;
   p.timeout_ns = wait_timeout_ns();
+  p.sk_first = 0;
+  p.sk_total = 0;
+  p.sk_w = 0;
+  p.sk_slots = 0;
+  p.ws = nullptr;
 
   if (L.bw_a_scale) return launch_blockwise(L, p, s);
   if (L.swiglu) return launch_pair<GEMM_GROUPED_M, true>(L, p, s);

@@ -72,7 +72,15 @@ struct GemmLaunch {
   // b_scale unused.
   const float* bw_a_scale = nullptr;
   const float* bw_b_scale = nullptr;
+  // Workspace for the dense split tail: the caller's (ws, ws_bytes), else,
+  // with ws_alloc, the library's stream-ordered pool; with neither the GEMM
+  // runs whole tiles only.
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  bool ws_alloc = false;
 };
 mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
+// Bytes of workspace the dense GEMM L would use for its split tail (0: none).
+size_t gemm_workspace_bytes(const GemmLaunch& L);
 
 }  // namespace mx

@@ -108,6 +108,27 @@ def test_gemm_rejects_bad_arguments_on_host(L):
     assert _status_of(mx.mx_gemm, mx.MX_FPROP, None, _op(), c, 128, None, None) != 0
 
 
+def test_gemm_workspace_entry_points_validate_on_host(L):
+    c, ws = 0x4000, 0x100000
+    q = mx.mx_gemm_with_workspace
+    # the operand checks are mx_gemm's
+    assert _status_of(q, mx.MX_DGRAD, _op(), _op(), c, 128, ws, 1 << 20, None, None) == INVALID
+    assert _status_of(q, mx.MX_FPROP, _op(k=48), _op(k=48), c, 128, ws, 1 << 20, None, None) == SHAPE
+    assert _status_of(q, mx.MX_FPROP, _op(), _op(), c, 100, ws, 1 << 20, None, None) == INVALID
+    # a workspace of non-zero size must be a 16-byte aligned pointer
+    assert _status_of(q, mx.MX_FPROP, _op(), _op(), c, 128, None, 1 << 20, None, None) == INVALID
+    assert _status_of(q, mx.MX_FPROP, _op(), _op(), c, 128, ws + 8, 1 << 20, None, None) == ALIGN
+    # empty problems are no-ops with or without a workspace
+    assert _status_of(q, mx.MX_FPROP, _op(rows=0), _op(), c, 128, None, 0, None, None) == 0
+    w = mx.mx_gemm_workspace_bytes
+    assert _status_of(w, mx.MX_FPROP, _op(), _op(orient=mx.MX_COLWISE)) == INVALID
+    assert _status_of(w, mx.MX_FPROP, _op(k=48), _op(k=48)) == SHAPE
+    assert w(mx.MX_FPROP, _op(rows=0), _op()) == 0
+    assert L.mx_gemm_workspace_bytes(mx.MX_FPROP, _op(), _op(), None) == INVALID  # null result pointer
+    # a valid query needs the device's SM count: an error status without a GPU
+    assert _status_of(w, mx.MX_FPROP, _op(), _op()) in (0, 4, 7)
+
+
 def test_grouped_gemm_rejects_bad_arguments_on_host(L):
     c = 0x4000
     g = 0x8000
