@@ -206,9 +206,9 @@ class DenseFFN:
         return {k: (2 + 1 + 1 + 2 / 32) * r.rows * r.k for k, (r, _) in self.q.items()}
 
     def launches_per_step(self):
-        (xr, xc), (wr, wc), (dr, dc) = self.q["X"], self.q["W"], self.q["dY"]
-        return 2 + sum(gemm_launches(self.mx, mode, a, b) for mode, a, b in
-                       ((self.mx.MX_FPROP, xr, wr), (self.mx.MX_DGRAD, dr, wc), (self.mx.MX_WGRAD, dc, xc)))
+        # two quantiser launches, fprop, and dgrad + wgrad in one launch
+        (xr, xc), (wr, wc) = self.q["X"], self.q["W"]
+        return 2 + gemm_launches(self.mx, self.mx.MX_FPROP, xr, wr) + 1
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.host.values())
@@ -234,12 +234,17 @@ class DenseFFN:
             if e is not None:
                 e.record(stream)
         (xr, xc), (wr, wc), (dr, dc) = self.q["X"], self.q["W"], self.q["dY"]
-        for mode, a, b, out in ((mx.MX_FPROP, xr, wr, out_t["Y"]), (mx.MX_DGRAD, dr, wc, out_t["dX"]),
-                                (mx.MX_WGRAD, dc, xc, out_t["dW"])):
-            e = timers.span("gemm", stream) if timers else None
-            mx.mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), None, sp)
-            if e is not None:
-                e.record(stream)
+        # fprop; then the backward pass's dgrad and wgrad, independent of each
+        # other, in one launch
+        e = timers.span("gemm", stream) if timers else None
+        mx.mx_gemm(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), out_t["Y"].data_ptr(), out_t["Y"].stride(0), None,
+                   sp)
+        mx.mx_gemm_multi([mx.MXGemmProblemC(dr.c_operand(), wc.c_operand(), out_t["dX"].data_ptr(),
+                                            out_t["dX"].stride(0), mx.MX_DGRAD, 0),
+                          mx.MXGemmProblemC(dc.c_operand(), xc.c_operand(), out_t["dW"].data_ptr(),
+                                            out_t["dW"].stride(0), mx.MX_WGRAD, 0)], None, sp)
+        if e is not None:
+            e.record(stream)
 
     def run_e2e(self, stream, steps):
         """`steps` end-to-end steps: each copies its inputs from pinned host memory,
@@ -348,8 +353,9 @@ def cpu_threads():
 # ---------------------------------------------------------------------------
 
 def profile_traffic(kernel: str):
-    """DRAM traffic per launch from a committed ncu summary, if it was taken
-    from the current kernel source (else None)."""
+    """DRAM traffic of the dense step's launches of `kernel` (bytes per step,
+    as the roofline entries count their time) from a committed ncu summary,
+    if it was taken from the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -362,7 +368,7 @@ def profile_traffic(kernel: str):
     if not os.path.exists(src):
         return None
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return ent.get("bytes_per_launch") if h == ent.get("source_sha256_16") else None
+    return ent.get("bytes_per_step") if h == ent.get("source_sha256_16") else None
 
 
 def run_reference(args, rank, world):
@@ -574,7 +580,7 @@ def run_quant_sweep(args, rank, world, peaks, peak_src):
             "per_M_gbs": per_m,
             "roofline": {"bound": "hbm", "kernel": "mx_quant_kernel", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": profile_traffic("mx_quant_kernel"), "bytes_per_launch": per_elem * big * C,
+                         "traffic": profile_traffic("mx_quant_kernel:quant_sweep_M32768"), "bytes_per_launch": per_elem * big * C,
                          "peak_source": f"{peak_src} hbm_gbs", "launch": f"M={big}"},
             "gpu_launches": len(xs) * args.steps, "clocks": clk}
     if rank == 0:
@@ -925,9 +931,9 @@ def main():
     ms_max = max_over_ranks(ms, world)
     value = world * args.steps * wl.step_flops() / (ms_max / 1e3) / 1e12
 
-    gemm_ms = timers.total_ms("gemm") / timers.count("gemm")
+    gemm_ms = timers.total_ms("gemm") / args.steps            # fprop + the fused dgrad/wgrad launch
     quant_ms = timers.total_ms("quant") / args.steps          # both quantiser launches of a step
-    achieved = wl.gemm_flops() / (gemm_ms / 1e3) / 1e12
+    achieved = wl.step_flops() / (gemm_ms / 1e3) / 1e12
     peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     qbytes = sum(wl.quant_bytes().values())                    # X, W and dY per step
     q_gbs = qbytes / (quant_ms / 1e3) / 1e9
@@ -962,7 +968,9 @@ def main():
                      "traffic": profile_traffic("mx_gemm_pair_kernel"),
                      "peak_source": f"{peak_src} bf16 sustained {peaks['bf16_tflops_sustained']} x nominal fp8/bf16 "
                                     f"ratio {FP8_OVER_BF16}",
-                     "flops_per_launch": wl.gemm_flops(), "avg_launch_ms": gemm_ms},
+                     "flops_per_step": wl.step_flops(), "ms_per_step": gemm_ms, "launches_per_step": 2,
+                     "basis": "fprop, dgrad and wgrad FLOPs (2MNK each) over the summed duration of the step's "
+                              "two GEMM launches (fprop; dgrad + wgrad in one launch)"},
         "quant_roofline": {"bound": "hbm", "kernel": "mx_quant_kernel", "achieved": q_gbs,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": q_gbs / peaks["hbm_gbs"],
                            "traffic": profile_traffic("mx_quant_kernel"), "bytes_per_step": qbytes,

@@ -265,6 +265,36 @@ mx_status mx_gemm_workspace_bytes(int mode, const mx_operand* a, const mx_operan
 mx_status mx_gemm_with_workspace(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,
                                  void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
+/* One GEMM of an mx_gemm_multi call: the arguments of mx_gemm. */
+typedef struct mx_gemm_problem {
+  mx_operand a;
+  mx_operand b;
+  void* c;          /* BF16 [a.rows, b.rows], row pitch ldc elements */
+  int64_t ldc;
+  int32_t mode;     /* MX_FPROP, MX_DGRAD or MX_WGRAD */
+  int32_t reserved; /* must be 0 */
+} mx_gemm_problem;
+
+/*
+ * mx_gemm_multi - up to MX_MAX_GEMM_MULTI independent dense GEMMs in one
+ * launch, e.g. the dgrad and wgrad of one Linear layer's backward pass
+ * ([DSV3] §8: both read the quantised dY, dgrad with W's column copy and
+ * wgrad with X's; §10, the step data flow). One persistent grid walks the
+ * tiles of all of them, so the GPU fills up across the GEMMs' last partial
+ * rounds and pays one launch. Each output equals mx_gemm's for that problem
+ * up to FP32 summation order (whole tiles; no split tail), within the same
+ * bound; results are bit-identical from call to call.
+ *
+ *   problems  host array of n descriptors (read before return).
+ *   n         0 .. MX_MAX_GEMM_MULTI.
+ *   Requirements per problem are mx_gemm's; any violation fails the whole
+ *   call before anything is launched (mx_last_error names the problem).
+ *   No output may overlap another output or any operand: the GEMMs run
+ *   concurrently.
+ */
+#define MX_MAX_GEMM_MULTI 4
+mx_status mx_gemm_multi(const mx_gemm_problem* problems, int n, int* dev_status, void* stream);
+
 /*
  * mx_grouped_gemm - per-expert block-scaled GEMMs over contiguous token ranges
  * ([DSV3] §5.2 routed experts and §13.4 low_precision_grouped_matmul with

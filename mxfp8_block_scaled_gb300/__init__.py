@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmxfp8_gb300.so")
 MX_ROWWISE, MX_COLWISE, MX_BOTH = 1, 2, 3
 MX_FPROP, MX_DGRAD, MX_WGRAD = 0, 1, 2
 MX_MAX_MULTI = 8
+MX_MAX_GEMM_MULTI = 4
 STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAPE", 3: "MX_ERR_ALIGNMENT",
                 4: "MX_ERR_CUDA", 5: "MX_ERR_DEVICE_CHECK", 6: "MX_ERR_TIMEOUT", 7: "MX_ERR_NO_DEVICE"}
 
@@ -33,7 +34,7 @@ EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quant
             "mx_quantize_multi",
             "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_quantize_fp8_blockwise",
             "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version",
-            "mx_selftest_wait_timeout", "mx_gemm_workspace_bytes", "mx_gemm_with_workspace")
+            "mx_selftest_wait_timeout", "mx_gemm_workspace_bytes", "mx_gemm_with_workspace", "mx_gemm_multi")
 
 
 class MXError(RuntimeError):
@@ -46,6 +47,11 @@ class MXOperandC(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
                 ("k", ctypes.c_int64), ("ld", ctypes.c_int64), ("orient", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class MXGemmProblemC(ctypes.Structure):
+    _fields_ = [("a", MXOperandC), ("b", MXOperandC), ("c", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("mode", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class MXQuantTensorC(ctypes.Structure):
@@ -86,6 +92,8 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm_with_workspace.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp,
                                          ctypes.c_size_t, vp, vp]
     L.mx_gemm_with_workspace.restype = i32
+    L.mx_gemm_multi.argtypes = [ctypes.POINTER(MXGemmProblemC), i32, vp, vp]
+    L.mx_gemm_multi.restype = i32
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
                                   vp, vp]
     L.mx_grouped_gemm.restype = i32
@@ -195,6 +203,12 @@ def mx_gemm_with_workspace(mode, a: MXOperandC, b: MXOperandC, c, ldc, workspace
                            stream) -> None:
     _check(lib().mx_gemm_with_workspace(mode, _ref(a), _ref(b), c, ldc, workspace, workspace_bytes, dev_status,
                                         stream), "mx_gemm_with_workspace")
+
+
+def mx_gemm_multi(problems, dev_status, stream) -> None:
+    """``problems``: a sequence of MXGemmProblemC."""
+    arr = (MXGemmProblemC * max(len(problems), 1))(*problems)
+    _check(lib().mx_gemm_multi(arr, len(problems), dev_status, stream), "mx_gemm_multi")
 
 
 def mx_grouped_gemm(mode, a: MXOperandC, b: MXOperandC, group_offsets, n_groups, c, ldc, dev_status,
@@ -325,6 +339,21 @@ def gemm(mode: int, a: MXTensor, b: MXTensor, out=None, status=None, stream=None
         out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
     mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), _ptr(status), _stream(stream))
     return out
+
+
+def gemm_multi(problems, status=None, stream=None):
+    """Several independent GEMMs (mode, a, b[, out]) in one launch; returns the
+    outputs (BF16 [a.rows, b.rows], allocated where not given)."""
+    torch = _torch()
+    outs, descs = [], []
+    for pr in problems:
+        mode, a, b = pr[0], pr[1], pr[2]
+        out = pr[3] if len(pr) > 3 and pr[3] is not None else \
+            torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
+        outs.append(out)
+        descs.append(MXGemmProblemC(a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), mode, 0))
+    mx_gemm_multi(descs, _ptr(status), _stream(stream))
+    return outs
 
 
 @dataclass

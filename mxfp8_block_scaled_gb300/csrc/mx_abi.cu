@@ -558,6 +558,52 @@ mx_status mx_gemm_with_workspace(int mode, const mx_operand* a, const mx_operand
   return dense_gemm_run(L, stream);
 }
 
+mx_status mx_gemm_multi(const mx_gemm_problem* problems, int n, int* dev_status, void* stream) {
+  if (n < 0 || n > MX_MAX_GEMM_MULTI) {
+    set_error("mx_gemm_multi: n = %d is outside 0 .. %d", n, MX_MAX_GEMM_MULTI);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (n == 0) return MX_OK;
+  if (!problems) {
+    set_error("mx_gemm_multi: problems is null");
+    return MX_ERR_INVALID_ARG;
+  }
+  GemmLaunch Ls[MX_MAX_GEMM_MULTI];
+  bool any = false;
+  for (int i = 0; i < n; ++i) {
+    const mx_gemm_problem& pr = problems[i];
+    if (pr.reserved != 0) {
+      set_error("mx_gemm_multi: problem %d: reserved must be 0", i);
+      return MX_ERR_INVALID_ARG;
+    }
+    mx_status st = dense_gemm_setup("mx_gemm_multi", pr.mode, &pr.a, &pr.b, pr.c, pr.ldc, dev_status, true, &Ls[i]);
+    if (st != MX_OK) {
+      char msg[512];
+      std::snprintf(msg, sizeof(msg), "%s", mx_last_error());
+      set_error("problem %d: %s", i, msg);
+      return st;
+    }
+    if (Ls[i].M > 0 && Ls[i].N > 0) any = true;
+  }
+  if (!any) return MX_OK;
+  mx_status st = check_device();
+  if (st != MX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // K = 0: C = 0, no tensor-core work.
+  GemmLaunch live[MX_MAX_GEMM_MULTI];
+  int m = 0;
+  for (int i = 0; i < n; ++i) {
+    if (Ls[i].M == 0 || Ls[i].N == 0) continue;
+    if (Ls[i].K == 0) {
+      st = zero_output(Ls[i].c, Ls[i].ldc, Ls[i].N, Ls[i].M, s);
+      if (st != MX_OK) return st;
+      continue;
+    }
+    live[m++] = Ls[i];
+  }
+  return m ? launch_gemm_multi(live, m, s) : MX_OK;
+}
+
 mx_status mx_quantize_fp8_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,
                                     float* scale, int* dev_status, void* stream) {
   (void)dev_status;

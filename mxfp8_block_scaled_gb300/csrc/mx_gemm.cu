@@ -828,12 +828,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 // cta_group::2, M = 256
 // ===========================================================================
 
-template <int KIND, bool kSwiGLU = false>
+// Parameters of one pair-kernel launch: up to kMaxProblems independent dense
+// GEMMs whose tiles one persistent grid walks in turn (problem i owns launch
+// tiles [tile0[i], tile0[i+1])), or a single GEMM of any kind (n = 1).
+constexpr int kMaxProblems = MX_MAX_GEMM_MULTI;
+struct PairProblem {
+  CUtensorMap a, b, sfa, sfb, c;
+  GParams p;
+};
+struct PairArgs {
+  PairProblem prob[kMaxProblems];
+  int64_t tile0[kMaxProblems + 1];
+  int n;
+};
+static_assert(sizeof(PairArgs) <= 4096, "kernel parameter space");
+
+template <bool kMulti>
+__device__ __forceinline__ int problem_of(const PairArgs& args, int64_t t) {
+  int i = 0;
+  if constexpr (kMulti)
+    while (i + 1 < args.n && t >= args.tile0[i + 1]) ++i;
+  return i;
+}
+
+template <int KIND, bool kSwiGLU = false, bool kMulti = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
-    mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
-                        const __grid_constant__ CUtensorMap tmap_c, const GParams p) {
+    mx_gemm_pair_kernel(const __grid_constant__ PairArgs args) {
   using C = PairCfg;
+  static_assert(!kMulti || (KIND == GEMM_DENSE && !kSwiGLU), "several problems per launch: dense GEMMs only");
+  // Problem 0 holds the fields every problem shares (status word, wait bound)
+  // and, unless kMulti, the whole GEMM.
+  const GParams& p = args.prob[0].p;
   static_assert(!kSwiGLU || KIND == GEMM_GROUPED_M, "the SwiGLU epilogue follows the grouped gate_up fprop");
   // Rows-ragged tiles start at any row: each CTA gathers its A scale atom.
   constexpr bool kGatherSfa = (KIND == GEMM_GROUPED_M);
@@ -892,10 +917,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmap_a);
-    tma_prefetch_desc(&tmap_b);
-    tma_prefetch_desc(&tmap_sfa);
-    tma_prefetch_desc(&tmap_sfb);
+    for (int i = 0; i < (kMulti ? args.n : 1); ++i) {
+      tma_prefetch_desc(&args.prob[i].a);
+      tma_prefetch_desc(&args.prob[i].b);
+      tma_prefetch_desc(&args.prob[i].sfa);
+      tma_prefetch_desc(&args.prob[i].sfb);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(s_tmem, kTmemCols);
@@ -911,6 +938,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                        ? static_cast<int64_t>(g.total) * nt
                        : (((p.M + kBM - 1) / kBM + 1) / 2) * nt * (KIND == GEMM_GROUPED_K ? p.n_groups : 1);
   if (KIND == GEMM_DENSE && p.sk_w > 0) ntiles = p.sk_first + 2 * static_cast<int64_t>(p.sk_slots);
+  if (kMulti) ntiles = args.tile0[args.n];
   const int64_t t_first = blockIdx.x >> 1;
   const int64_t t_step = gridDim.x >> 1;
 
@@ -923,11 +951,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // Lane 0 alone runs the loop (the rows-ragged scale gather has a warp of
     // its own: a per-stage warp shuffle here cost ~5% of GEMM throughput).
     for (int64_t t = t_first; t < ntiles && ok && lane == 0; t += t_step) {
-      const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+      const int pi = problem_of<kMulti>(args, t);
+        const GParams& pp = args.prob[pi].p;
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
       // Rows-ragged: B's scale atoms are those of the tile's expert. SwiGLU:
       // the second atom holds the up rows, N/256 atoms after the gate rows.
-      const int64_t sfb_atom_row = (KIND == GEMM_GROUPED_M ? ti.group * p.b_ra : 0) + (ti.n0 >> 7);
-      const int64_t sfb_atom_step = kSwiGLU ? (p.N >> 8) : 1;
+      const int64_t sfb_atom_row = (KIND == GEMM_GROUPED_M ? ti.group * pp.b_ra : 0) + (ti.n0 >> 7);
+      const int64_t sfb_atom_step = kSwiGLU ? (pp.N >> 8) : 1;
       for (int kb = 0; kb < ti.nkb; ++kb) {
         if (!wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort)) {
           ok = false;
@@ -938,16 +968,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const uint32_t lfull = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * (C::kStageTx - (kGatherSfa ? 512 : 0)));
           const int32_t kx = static_cast<int32_t>(katom * kBK);
-          tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, lfull, kx, static_cast<int32_t>(ti.a_row));
-          tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, lfull, kx, static_cast<int32_t>(ti.b_row));
+          tma_load_2d_pair(sA + stage * C::kABytes, &args.prob[pi].a, lfull, kx, static_cast<int32_t>(ti.a_row));
+          tma_load_2d_pair(sB + stage * C::kBBytes, &args.prob[pi].b, lfull, kx, static_cast<int32_t>(ti.b_row));
           // Scale atoms through [atoms][128 words] views (rows past the end read as zero).
           if constexpr (!kGatherSfa)
-            tma_load_2d_pair(sSfa + stage * 512, &tmap_sfa, lfull, 0,
-                             static_cast<int32_t>((ti.m0 >> 7) * p.ka + katom));
+            tma_load_2d_pair(sSfa + stage * 512, &args.prob[pi].sfa, lfull, 0,
+                             static_cast<int32_t>((ti.m0 >> 7) * pp.ka + katom));
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            tma_load_2d_pair(sSfb + stage * C::kSfbBytes + j * 512, &tmap_sfb, lfull, 0,
-                             static_cast<int32_t>((sfb_atom_row + j * sfb_atom_step) * p.ka + katom));
+            tma_load_2d_pair(sSfb + stage * C::kSfbBytes + j * 512, &args.prob[pi].sfb, lfull, 0,
+                             static_cast<int32_t>((sfb_atom_row + j * sfb_atom_step) * pp.ka + katom));
         }
         ++issued;
         if (++stage == S) {
@@ -978,7 +1008,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+        const int pi = problem_of<kMulti>(args, t);
+        const GParams& pp = args.prob[pi].p;
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
         if (ti.part == -2) continue;  // an empty split-tail segment
         if (!wait_or_abort<true>(acc_empty, acc_phase ^ 1, p, s_abort)) break;
         tc_fence_after_sync();
@@ -1028,7 +1060,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+        const int pi = problem_of<kMulti>(args, t);
+        const GParams& pp = args.prob[pi].p;
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort(&gfull[stage], phase, p, s_abort)) {
             ok = false;
@@ -1048,7 +1082,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+        const int pi = problem_of<kMulti>(args, t);
+        const GParams& pp = args.prob[pi].p;
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort)) {
             ok = false;
@@ -1083,7 +1119,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+        const int pi = problem_of<kMulti>(args, t);
+        const GParams& pp = args.prob[pi].p;
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           uint32_t good = 1;
           if (lane == 0) good = wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
@@ -1097,10 +1135,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int64_t r = ti.a_row + lane + 32 * q;
-            const bool in = r < p.a_ra * 128;  // rows past the scale buffer read as zero
+            const bool in = r < pp.a_ra * 128;  // rows past the scale buffer read as zero
             cp_async_4(dst + 4 * q,
-                       in ? p.a_scale + (((r >> 7) * p.ka + katom) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2)
-                          : p.a_scale,
+                       in ? pp.a_scale + (((r >> 7) * pp.ka + katom) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2)
+                          : pp.a_scale,
                        in ? 4u : 0u);
           }
           cp_async_arrive_noinc(leader ? &full_bar[stage] : &gfull[stage]);
@@ -1123,7 +1161,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const uint32_t lacc_empty = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t acc_phase = 0;
     for (int64_t t = t_first; t < ntiles; t += t_step) {
-      const Tile ti = get_pair_tile<KIND, kSwiGLU>(p, g, t, crank);
+      const int pi = problem_of<kMulti>(args, t);
+        const GParams& pp = args.prob[pi].p;
+        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
       if (ti.part == -2) continue;
       if (!wait_or_abort<true>(acc_full, acc_phase, p, s_abort)) break;
       tc_fence_after_sync();
@@ -1153,7 +1193,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       acc_phase ^= 1;
       if (KIND == GEMM_DENSE && ti.part >= 0) {
         // Split-tail segment: the FP32 partial goes to the workspace.
-        float4* dst = reinterpret_cast<float4*>(p.ws) +
+        float4* dst = reinterpret_cast<float4*>(pp.ws) +
                       ((static_cast<int64_t>(ti.part) * 2 + crank) * 8 + (warp - 2)) * (32 * 32) + lane;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -1170,9 +1210,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const float uv = __uint_as_float(r[64 + i]);
           r[i] = __float_as_uint(gv / (1.0f + __expf(-gv)) * uv);
         }
-        store_tile<KIND, 64, C::kEpiBufs>(p, ti, r, quarter, lane, 2, 64 * half, stg, &tmap_c);
+        store_tile<KIND, 64, C::kEpiBufs>(pp, ti, r, quarter, lane, 2, 64 * half, stg, &args.prob[pi].c);
       } else {
-        store_tile<KIND, kCols, C::kEpiBufs>(p, ti, r, quarter, lane, kCols / 32, col_off, stg, &tmap_c);
+        store_tile<KIND, kCols, C::kEpiBufs>(pp, ti, r, quarter, lane, kCols / 32, col_off, stg, &args.prob[pi].c);
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -1673,6 +1713,13 @@ cudaMemPool_t workspace_pool(int dev) {
 
 bool split_allowed(const GemmLaunch& L, size_t need) { return L.ws_alloc || (L.ws && L.ws_bytes >= need); }
 
+// The launch arguments live in a per-thread buffer (about 4 KB) rather than
+// on the host stack; cudaLaunchKernelEx copies them at the call.
+PairArgs* pair_args_scratch() {
+  static thread_local PairArgs args;
+  return &args;
+}
+
 template <int KIND, bool kSwiGLU = false>
 mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) {
   GParams p = p_in;
@@ -1689,7 +1736,7 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   if (st != MX_OK) return st;
   output_map(L, p, &mc, KIND);
   const size_t smem = PairCfg::smem_bytes(KIND != GEMM_DENSE);
-  auto kern = mx_gemm_pair_kernel<KIND, kSwiGLU>;
+  auto kern = mx_gemm_pair_kernel<KIND, kSwiGLU, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
   int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pair_tiles_upper(L), sm_count() / 2));
@@ -1733,7 +1780,11 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  st = cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, mc, p), "mx_gemm launch (CTA pairs)");
+  PairArgs* args = pair_args_scratch();
+  std::memset(args, 0, sizeof(PairArgs));
+  args->prob[0] = PairProblem{ma, mb, msa, msb, mc, p};
+  args->n = 1;
+  st = cuda_status(cudaLaunchKernelEx(&cfg, kern, *args), "mx_gemm launch (CTA pairs)");
   if (st == MX_OK && p.sk_w > 0) {
     mx_gemm_sk_reduce_kernel<<<static_cast<unsigned>(32 * pl.tail_tiles), 256, 0, s>>>(p);
     st = cuda_status(cudaGetLastError(), "mx_gemm split-tail reduction launch");
@@ -1841,13 +1892,9 @@ size_t gemm_workspace_bytes(const GemmLaunch& L) {
   return pl.sk_w > 0 ? pl.ws_bytes : 0;
 }
 
-mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
-  if (L.M == 0 || L.N == 0) return MX_OK;
-  if (L.kind != GEMM_DENSE && L.n_groups > kMaxGroups) {
-    set_error("mx_grouped_gemm: at most %d groups", kMaxGroups);
-    return MX_ERR_UNSUPPORTED_SHAPE;
-  }
-  if (L.kind == GEMM_GROUPED_K && L.n_groups == 0) return MX_OK;
+namespace {
+
+GParams make_gparams(const GemmLaunch& L) {
   GParams p;
   p.a_scale = static_cast<const uint8_t*>(L.a_scale);
   p.b_scale = static_cast<const uint8_t*>(L.b_scale);
@@ -1878,6 +1925,63 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.sk_w = 0;
   p.sk_slots = 0;
   p.ws = nullptr;
+  return p;
+}
+
+// Several dense GEMMs in one launch of the pair kernel.
+mx_status launch_pair_multi(const GemmLaunch* Ls, int n, cudaStream_t s) {
+  PairArgs* args = pair_args_scratch();
+  std::memset(args, 0, sizeof(PairArgs));
+  int64_t tiles = 0;
+  for (int i = 0; i < n; ++i) {
+    const GemmLaunch& L = Ls[i];
+    PairProblem& pr = args->prob[i];
+    pr.p = make_gparams(L);
+    mx_status st = make_map(&pr.a, L.a_data, L.M, L.K, L.a_ld, kBM);
+    if (st != MX_OK) return st;
+    st = make_map(&pr.b, L.b_data, L.b_rows_total, L.K, L.b_ld, PairCfg::BN / 2);
+    if (st != MX_OK) return st;
+    st = make_scale_map(&pr.sfa, L.a_scale, L.M, L.K);
+    if (st != MX_OK) return st;
+    st = make_scale_map(&pr.sfb, L.b_scale, L.N, L.K);
+    if (st != MX_OK) return st;
+    output_map(L, pr.p, &pr.c, GEMM_DENSE);
+    args->tile0[i] = tiles;
+    tiles += pair_tiles_upper(L);
+  }
+  args->tile0[n] = tiles;
+  args->n = n;
+  const size_t smem = PairCfg::smem_bytes(false);
+  auto kern = mx_gemm_pair_kernel<GEMM_DENSE, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count() / 2));
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, *args), "mx_gemm_multi launch (CTA pairs)");
+}
+
+}  // namespace
+
+mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
+  if (L.M == 0 || L.N == 0) return MX_OK;
+  if (L.kind != GEMM_DENSE && L.n_groups > kMaxGroups) {
+    set_error("mx_grouped_gemm: at most %d groups", kMaxGroups);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (L.kind == GEMM_GROUPED_K && L.n_groups == 0) return MX_OK;
+  GParams p = make_gparams(L);
 
   if (L.bw_a_scale) return launch_blockwise(L, p, s);
   if (L.swiglu) return launch_pair<GEMM_GROUPED_M, true>(L, p, s);
@@ -1908,6 +2012,30 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
       return bn == 256 ? launch_cfg<256, GEMM_GROUPED_K>(L, p, tiles_upper, s)
                        : launch_cfg<128, GEMM_GROUPED_K>(L, p, tiles_upper, s);
   }
+}
+
+mx_status launch_gemm_multi(const GemmLaunch* Ls, int n, cudaStream_t s) {
+  // Problems with nothing to compute drop out; K = 0 is the caller's memset.
+  GemmLaunch live[kMaxProblems];
+  int m = 0;
+  int64_t tiles = 0;
+  bool pairs = true;
+  for (int i = 0; i < n; ++i) {
+    if (Ls[i].M == 0 || Ls[i].N == 0) continue;
+    live[m] = Ls[i];
+    tiles += pair_tiles_upper(Ls[i]);
+    if (Ls[i].kind != GEMM_DENSE || Ls[i].N <= 128) pairs = false;
+    ++m;
+  }
+  if (m == 0) return MX_OK;
+  // One pair launch when the problems together fill the SM pairs at least
+  // once; otherwise each GEMM on its own best configuration.
+  if (m > 1 && pairs && tiles >= sm_count() / 2) return launch_pair_multi(live, m, s);
+  for (int i = 0; i < m; ++i) {
+    mx_status st = launch_gemm(live[i], s);
+    if (st != MX_OK) return st;
+  }
+  return MX_OK;
 }
 
 }  // namespace mx

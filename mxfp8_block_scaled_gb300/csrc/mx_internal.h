@@ -82,5 +82,8 @@ struct GemmLaunch {
 mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // Bytes of workspace the dense GEMM L would use for its split tail (0: none).
 size_t gemm_workspace_bytes(const GemmLaunch& L);
+// Up to MX_MAX_GEMM_MULTI independent dense GEMMs; one launch of the pair
+// kernel when they fill the GPU together, else one launch each.
+mx_status launch_gemm_multi(const GemmLaunch* Ls, int n, cudaStream_t s);
 
 }  // namespace mx

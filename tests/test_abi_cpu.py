@@ -129,6 +129,26 @@ def test_gemm_workspace_entry_points_validate_on_host(L):
     assert _status_of(w, mx.MX_FPROP, _op(), _op()) in (0, 4, 7)
 
 
+def _gp(mode=mx.MX_FPROP, a=None, b=None, c=0x4000, ldc=128):
+    return mx.MXGemmProblemC(a or _op(), b or _op(), c, ldc, mode, 0)
+
+
+def test_gemm_multi_rejects_bad_arguments_on_host(L):
+    q = mx.mx_gemm_multi
+    good = _gp()
+    assert _status_of(q, [good, _gp(mode=mx.MX_DGRAD)], None, None) == INVALID      # orientation vs mode
+    assert _status_of(q, [good, _gp(a=_op(k=48), b=_op(k=48))], None, None) == SHAPE
+    assert _status_of(q, [_gp(c=0x4001)], None, None) == ALIGN
+    assert _status_of(q, [_gp(ldc=100)], None, None) == INVALID
+    bad = _gp()
+    bad.reserved = 1
+    assert _status_of(q, [good, bad], None, None) == INVALID
+    assert _status_of(q, [good] * (mx.MX_MAX_GEMM_MULTI + 1), None, None) == INVALID
+    assert _status_of(q, [], None, None) == 0
+    assert _status_of(q, [_gp(a=_op(rows=0)), _gp(b=_op(rows=0))], None, None) == 0   # empty problems
+    assert "problem 1" in (lambda: (_status_of(q, [good, _gp(ldc=100)], None, None), mx.mx_last_error())[1])()
+
+
 def test_grouped_gemm_rejects_bad_arguments_on_host(L):
     c = 0x4000
     g = 0x8000
