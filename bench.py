@@ -986,10 +986,10 @@ def main():
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        fl, dt = oracle_dense_sample(256, 256)
+        fl, dt = oracle_dense_sample(1536, 1536)
         line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
                                 "kind": "oracle", "seconds": dt,
-                                "sample": "256x256 output block of each of fprop/dgrad/wgrad (dense FFN "
+                                "sample": "1536x1536 output block of each of fprop/dgrad/wgrad (dense FFN "
                                           "up-proj), with the oracle quantisation of the operand rows it reads"}
     if rank == 0:
         print(json.dumps(line))
