@@ -709,29 +709,34 @@ def run_mla(args, rank, world, peaks, peak_src):
 
 
 def run_single(args, rank, world, peaks, peak_src):
-    """Single MXFP8 Linear (X[256, 512], W[256, 512]): quantise X and W (both
-    copies), then fprop. Launch-latency bound, so the line reports time."""
+    """Single MXFP8 Linear fprop (X[256, 512], W[256, 512]): X and W quantised
+    1x32 along K in one launch, then the GEMM. Launch-latency bound, so the
+    line reports time per step. `value` replays the step from a CUDA graph
+    (its two launches recorded once, as a serving loop would); the same step
+    issued call by call through the C ABI is reported as `eager_us`."""
     import workloads
     import mxfp8_block_scaled_gb300 as mx
     d = workloads.single_linear()
     X, W = d["X"].cuda(), d["W"].cuda()
-    (xr, xc), (wr, wc) = mx.quantize(X, mx.MX_BOTH), mx.quantize(W, mx.MX_BOTH)
+    xr, _ = mx.quantize(X, mx.MX_ROWWISE)
+    wr, _ = mx.quantize(W, mx.MX_ROWWISE)
     out = torch.empty((X.shape[0], W.shape[0]), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.Stream()
     sp = stream.cuda_stream
+    descs = [mx.MXQuantTensorC(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), r.data.data_ptr(),
+                               r.scale.data_ptr(), None, None) for x, r in ((X, xr), (W, wr))]
 
     def step(timers):
-        for x, r, c in ((X, xr, xc), (W, wr, wc)):
-            e = timers.span("quant", stream) if timers else None
-            mx.mx_quantize(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), mx.MX_BOTH, r.data.data_ptr(),
-                           r.scale.data_ptr(), c.data.data_ptr(), c.scale.data_ptr(), None, 0, 0, None, sp)
-            if e is not None:
-                e.record(stream)
+        e = timers.span("quant", stream) if timers else None
+        mx.mx_quantize_multi(descs, mx.MX_ROWWISE, None, sp)
+        if e is not None:
+            e.record(stream)
         e = timers.span("gemm", stream) if timers else None
         mx.mx_gemm(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), out.data_ptr(), out.stride(0), None, sp)
         if e is not None:
             e.record(stream)
 
+    # eager: every call through the C ABI, per-kernel spans on the stream
     timers, clocks = _timed(step, args, world)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -740,18 +745,44 @@ def run_single(args, rank, world, peaks, peak_src):
         step(timers)
     t1.record(stream)
     torch.cuda.synchronize()
+    eager_us = max_over_ranks(t0.elapsed_time(t1), world) / args.steps * 1e3
+    eager_out = out.clone()
+
+    # the same step recorded once into a CUDA graph and replayed; its output
+    # must equal the eager step's bit for bit
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        step(None)
+    with torch.cuda.stream(stream):
+        out.zero_()
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager_out.view(torch.int16), out.view(torch.int16)), "graph replay differs from eager"
+    barrier(world)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+    torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms = max_over_ranks(g0.elapsed_time(g1), world)
     us = ms / args.steps * 1e3
     line = {"metric": "single MXFP8 Linear fprop latency (quantise X and W, GEMM)", "value": us, "unit": "us",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": "single_linear M=256 N=256 K=512", "parallelism": f"replicas{world}",
+            "config": {"workload": "single_linear M=256 N=256 K=512, X and W quantised 1x32 along K",
+                       "launch": "CUDA graph of the step's two launches, replayed; eager_us = the same step "
+                                 "issued call by call", "parallelism": f"replicas{world}",
                        "l2": "inputs stay in L2 (launch-latency bound; no roofline fraction)"},
-            "per_kernel_us": {"quant": timers.total_ms("quant") / timers.count("quant") * 1e3,
+            "eager_us": eager_us,
+            "per_kernel_us": {"quant_x_and_w": timers.total_ms("quant") / timers.count("quant") * 1e3,
                               "gemm": timers.total_ms("gemm") / timers.count("gemm") * 1e3},
-            "gpu_launches": (2 + gemm_launches(mx, mx.MX_FPROP, xr, wr)) * args.steps, "clocks": clk}
+            "gpu_launches": (1 + gemm_launches(mx, mx.MX_FPROP, xr, wr)) * args.steps, "clocks": clk}
     if rank == 0:
         print(json.dumps(line))
 
