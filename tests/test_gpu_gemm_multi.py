@@ -127,3 +127,23 @@ def test_k_zero_and_pitch_gap():
     assert np.all(h2[:, 1008:1016] == 0), "K = 0 problem did not write zeros"
     for out in (big[:, :N], big2[:, :N]):
         check_gemm_full(out, *oracle.mx_quantize_rowwise(f64(a)), *oracle.mx_quantize_rowwise(f64(b)), "pitch gap")
+
+
+def test_multi_captured_in_cuda_graph():
+    """dgrad + wgrad in one launch, recorded into a CUDA graph and replayed:
+    the eager call's bits."""
+    X, W, dY, probs = linear_backward(2048, 1536, 2048, 60)
+    dX, dW = run_multi(probs)
+    gX, gW = torch.zeros_like(dX), torch.zeros_like(dW)
+    descs = [mx.MXGemmProblemC(a.c_operand(), b.c_operand(), o.data_ptr(), o.stride(0), mode, 0)
+             for (mode, a, b), o in zip(probs, (gX, gW))]
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        mx.mx_gemm_multi(descs, None, stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(gX.view(torch.int16), dX.view(torch.int16))
+    assert torch.equal(gW.view(torch.int16), dW.view(torch.int16))

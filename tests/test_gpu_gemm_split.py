@@ -130,3 +130,23 @@ def test_split_tail_pitch_gap_and_unaligned_output(aligned):
     assert np.all(np.isnan(h[:, :c0])) and np.all(np.isnan(h[:, c0 + N:])), "wrote outside C"
     check_gemm_full(view, *oracle.mx_quantize_rowwise(f64(x)), *oracle.mx_quantize_rowwise(f64(w)),
                     f"split pitch aligned={aligned}")
+
+
+def test_split_tail_captured_in_cuda_graph():
+    """The split tail takes its workspace from a stream-ordered pool, so a call
+    can be recorded into a CUDA graph: replays give the eager call's bits."""
+    M, N, K = 512, 512, 16384
+    _, _, xr, wr = operands(M, N, K, 13)
+    assert ws_bytes(xr, wr) > 0
+    y_eager = gemm(xr, wr)
+    out = torch.zeros_like(y_eager)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        mx.mx_gemm(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), out.data_ptr(), out.stride(0), None,
+                   stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), y_eager.view(torch.int16))
