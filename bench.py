@@ -598,7 +598,11 @@ def _linear_set(projs, mx):
         M, K = X.shape
         N = W.shape[0]
         bf = dict(dtype=torch.bfloat16, device="cuda")
+        gemms = ((mx.MX_FPROP, xr, wr), (mx.MX_DGRAD, dr, wc), (mx.MX_WGRAD, dc, xc))
+        # one scratch buffer per layer for the GEMMs that split their last round
+        need = max(mx.mx_gemm_workspace_bytes(m, a.c_operand(), b.c_operand()) for m, a, b in gemms)
         layers.append(dict(name=name, M=M, N=N, K=K, src=(X, W, dY), q=((xr, xc), (wr, wc), (dr, dc)),
+                           ws=torch.empty(max(need, 16), dtype=torch.uint8, device="cuda"), ws_bytes=need,
                            out=(torch.empty((M, N), **bf), torch.empty((M, K), **bf), torch.empty((N, K), **bf))))
     return layers
 
@@ -617,15 +621,16 @@ def _linear_step(layers, mx, stream, timers=None):
         for j, (mode, a, b) in enumerate(((mx.MX_FPROP, xr, wr), (mx.MX_DGRAD, dr, wc), (mx.MX_WGRAD, dc, xc))):
             out = ly["out"][j]
             e = timers.span((ly["name"], j), stream) if timers else None
-            mx.mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), None, sp)
+            mx.mx_gemm_with_workspace(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0),
+                                      ly["ws"].data_ptr(), ly["ws_bytes"], None, sp)
             if e is not None:
                 e.record(stream)
 
 
-def gemm_launches(mx, mode, a, b):
-    """Kernel launches of one dense mx_gemm call: the GEMM, plus the split-tail
-    reduction when the library splits this GEMM's last round."""
-    return 1 + (1 if mx.mx_gemm_workspace_bytes(mode, a.c_operand(), b.c_operand()) > 0 else 0)
+def gemm_launches(mx, mode, a, b, workspace=False):
+    """Kernel launches of one dense GEMM call: the GEMM, plus the split-tail
+    reduction when a workspace is passed and the GEMM splits its last round."""
+    return 1 + (1 if workspace and mx.mx_gemm_workspace_bytes(mode, a.c_operand(), b.c_operand()) > 0 else 0)
 
 
 def _gemm_shapes(ly):
@@ -698,7 +703,7 @@ def run_mla(args, rank, world, peaks, peak_src):
                          "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8, "traffic": None,
                          "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}",
                          "roofline_time_frac": sum(g["roofline_ms"] for g in per_gemm) / gemm_ms_total},
-            "gpu_launches": sum(3 + sum(gemm_launches(mx, mode, a, b) for mode, a, b in
+            "gpu_launches": sum(3 + sum(gemm_launches(mx, mode, a, b, workspace=True) for mode, a, b in
                                          ((mx.MX_FPROP, ly["q"][0][0], ly["q"][1][0]),
                                           (mx.MX_DGRAD, ly["q"][2][0], ly["q"][1][1]),
                                           (mx.MX_WGRAD, ly["q"][2][1], ly["q"][0][1])))

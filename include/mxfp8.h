@@ -12,11 +12,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - All pointers named *_data, *_scale, x, c, workspace and group_offsets are
- *   DEVICE pointers, allocated and owned by the caller. One exception to "the
- *   caller owns all memory": mx_gemm takes its split-tail scratch from a
- *   stream-ordered pool the library keeps per device (see
- *   mx_gemm_workspace_bytes); mx_gemm_with_workspace and every other call
- *   allocate nothing. No other state is kept between calls.
+ *   DEVICE pointers, allocated and owned by the caller. The library never
+ *   allocates, frees or keeps device memory: the one scratch buffer any call
+ *   can use (mx_gemm_with_workspace) is the caller's, sized by a query
+ *   (mx_gemm_workspace_bytes). No state is kept between calls.
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *   void*; NULL is the legacy default stream) on the current device, which must
  *   be an sm_103 GPU. Nothing is synchronised.
@@ -239,14 +238,15 @@ mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, i
 
 /*
  * Scratch memory of the dense GEMM. When the 256 x 256 tiles leave the last
- * round over the GPU's SM pairs partly empty, the contraction of those last
- * tiles is cut into equal runs of 128-K blocks, one run per SM pair; each run
- * leaves FP32 partial tiles in a workspace, and a second kernel adds a tile's
+ * round over the GPU's SM pairs mostly empty and the contraction is long
+ * (weight gradients over many tokens), the contraction of those last tiles can
+ * be cut into equal runs of 128-K blocks, one run per SM pair; each run leaves
+ * FP32 partial tiles in a workspace, and a second kernel adds a tile's
  * partials in a fixed order and rounds once to BF16 (so results stay
  * bit-identical from call to call, and within the same error bound as the
- * whole-tile path: FP32 accumulation throughout). mx_gemm takes that workspace
- * from a stream-ordered memory pool the library owns (created on first use,
- * kept for the process). The two calls below never allocate.
+ * whole-tile path: FP32 accumulation throughout). mx_gemm never splits;
+ * mx_gemm_with_workspace splits when the caller's workspace is large enough
+ * and the split is estimated to be faster.
  *
  * mx_gemm_workspace_bytes - bytes of workspace mx_gemm_with_workspace would use
  * for these operands on the current device (0: this GEMM does not split).
@@ -257,9 +257,10 @@ mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, i
  *                    must stay untouched until the GEMM's work on `stream`
  *                    has finished. May be NULL when workspace_bytes == 0.
  *   workspace_bytes  its size. With less than mx_gemm_workspace_bytes the
- *                    GEMM runs whole tiles only: same results up to FP32
- *                    summation order, never an error.
- *   Everything else is exactly mx_gemm.
+ *                    GEMM runs whole tiles only: mx_gemm's result, never an
+ *                    error.
+ *   Everything else is exactly mx_gemm. The split adds one kernel launch on
+ *   `stream`; both calls can be recorded into a CUDA graph.
  */
 mx_status mx_gemm_workspace_bytes(int mode, const mx_operand* a, const mx_operand* b, size_t* bytes);
 mx_status mx_gemm_with_workspace(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,

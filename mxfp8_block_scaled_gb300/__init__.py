@@ -332,13 +332,27 @@ def quantize_multi(xs, axis: int = MX_BOTH, status=None, stream=None):
     return outs
 
 
-def gemm(mode: int, a: MXTensor, b: MXTensor, out=None, status=None, stream=None):
-    """C[M, N] = A . B^T in BF16 (FP32 accumulation)."""
+def gemm(mode: int, a: MXTensor, b: MXTensor, out=None, status=None, stream=None, workspace=None):
+    """C[M, N] = A . B^T in BF16 (FP32 accumulation). With `workspace` (a CUDA
+    uint8 tensor, see gemm_workspace) the GEMM may split its last round."""
     torch = _torch()
     if out is None:
         out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
-    mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), _ptr(status), _stream(stream))
+    if workspace is None:
+        mx_gemm(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), _ptr(status), _stream(stream))
+    else:
+        mx_gemm_with_workspace(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0),
+                               workspace.data_ptr() if workspace.numel() else None, workspace.numel(),
+                               _ptr(status), _stream(stream))
     return out
+
+
+def gemm_workspace(mode: int, a: MXTensor, b: MXTensor):
+    """A workspace of the size mx_gemm_with_workspace uses for these operands
+    (an empty tensor when the GEMM does not split)."""
+    torch = _torch()
+    n = mx_gemm_workspace_bytes(mode, a.c_operand(), b.c_operand())
+    return torch.empty(n, dtype=torch.uint8, device=a.data.device)
 
 
 def gemm_multi(problems, status=None, stream=None):

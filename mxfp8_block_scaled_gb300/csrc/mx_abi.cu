@@ -523,7 +523,6 @@ mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, i
   GemmLaunch L;
   mx_status st = dense_gemm_setup("mx_gemm", mode, a, b, c, ldc, dev_status, true, &L);
   if (st != MX_OK) return st;
-  L.ws_alloc = true;
   return dense_gemm_run(L, stream);
 }
 
@@ -554,7 +553,6 @@ mx_status mx_gemm_with_workspace(int mode, const mx_operand* a, const mx_operand
   }
   L.ws = workspace_bytes > 0 ? workspace : nullptr;
   L.ws_bytes = workspace_bytes;
-  L.ws_alloc = false;
   return dense_gemm_run(L, stream);
 }
 

@@ -1688,30 +1688,8 @@ PairPlan plan_pair_dense(const GemmLaunch& L, bool allow_split) {
   return pl;
 }
 
-// Stream-ordered workspace from a pool the library owns (one per device,
-// never trimmed), so a call needs no synchronous allocation and can be
-// captured in a CUDA graph.
-cudaMemPool_t workspace_pool(int dev) {
-  static std::mutex mu;
-  static cudaMemPool_t pools[64] = {};
-  if (dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!pools[dev]) {
-    cudaMemPoolProps props;
-    std::memset(&props, 0, sizeof(props));
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t pool = nullptr;
-    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
-    uint64_t keep = UINT64_MAX;
-    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    pools[dev] = pool;
-  }
-  return pools[dev];
-}
-
-bool split_allowed(const GemmLaunch& L, size_t need) { return L.ws_alloc || (L.ws && L.ws_bytes >= need); }
+// The split tail runs only in a workspace the caller passed (large enough).
+bool split_allowed(const GemmLaunch& L, size_t need) { return L.ws && L.ws_bytes >= need; }
 
 // The launch arguments live in a per-thread buffer (about 4 KB) rather than
 // on the host stack; cudaLaunchKernelEx copies them at the call.
@@ -1741,25 +1719,11 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
   int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pair_tiles_upper(L), sm_count() / 2));
   PairPlan pl;
-  void* pooled = nullptr;
   if constexpr (KIND == GEMM_DENSE) {
     pl = plan_pair_dense(L, true);
     if (pl.sk_w > 0 && !split_allowed(L, pl.ws_bytes)) pl = plan_pair_dense(L, false);
     if (pl.sk_w > 0) {
-      if (L.ws && L.ws_bytes >= pl.ws_bytes) {
-        p.ws = static_cast<float*>(L.ws);
-      } else {
-        int dev = 0;
-        cudaMemPool_t pool = cudaGetDevice(&dev) == cudaSuccess ? workspace_pool(dev) : nullptr;
-        if (pool && cudaMallocFromPoolAsync(&pooled, pl.ws_bytes, pool, s) == cudaSuccess) {
-          p.ws = static_cast<float*>(pooled);
-        } else {
-          (void)cudaGetLastError();  // no workspace: whole tiles only
-          pl = plan_pair_dense(L, false);
-        }
-      }
-    }
-    if (pl.sk_w > 0) {
+      p.ws = static_cast<float*>(L.ws);
       p.sk_first = pl.sk_first;
       p.sk_total = pl.sk_total;
       p.sk_w = pl.sk_w;
@@ -1788,10 +1752,6 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   if (st == MX_OK && p.sk_w > 0) {
     mx_gemm_sk_reduce_kernel<<<static_cast<unsigned>(32 * pl.tail_tiles), 256, 0, s>>>(p);
     st = cuda_status(cudaGetLastError(), "mx_gemm split-tail reduction launch");
-  }
-  if (pooled) {
-    const mx_status fst = cuda_status(cudaFreeAsync(pooled, s), "cudaFreeAsync(workspace)");
-    if (st == MX_OK) st = fst;
   }
   return st;
 }
@@ -1886,7 +1846,8 @@ mx_status launch_blockwise(const GemmLaunch& L, GParams p, cudaStream_t s) {
 size_t gemm_workspace_bytes(const GemmLaunch& L) {
   if (L.kind != GEMM_DENSE || L.swiglu || L.bw_a_scale || L.M == 0 || L.N == 0 || L.K == 0) return 0;
   GemmLaunch q = L;
-  q.ws_alloc = true;  // the size a split would need
+  q.ws = reinterpret_cast<void*>(uintptr_t{16});  // any workspace: the size a split would need
+  q.ws_bytes = SIZE_MAX;
   if (choose_dense_cfg(q) != CFG_PAIR) return 0;
   const PairPlan pl = plan_pair_dense(q, true);
   return pl.sk_w > 0 ? pl.ws_bytes : 0;

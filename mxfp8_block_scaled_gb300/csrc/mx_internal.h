@@ -72,12 +72,10 @@ struct GemmLaunch {
   // b_scale unused.
   const float* bw_a_scale = nullptr;
   const float* bw_b_scale = nullptr;
-  // Workspace for the dense split tail: the caller's (ws, ws_bytes), else,
-  // with ws_alloc, the library's stream-ordered pool; with neither the GEMM
-  // runs whole tiles only.
+  // The caller's workspace for the dense split tail; without one (or with
+  // too small a one) the GEMM runs whole tiles only.
   void* ws = nullptr;
   size_t ws_bytes = 0;
-  bool ws_alloc = false;
 };
 mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // Bytes of workspace the dense GEMM L would use for its split tail (0: none).

@@ -34,8 +34,9 @@ def operands(M, N, K, seed):
 
 
 def gemm(xr, wr, out=None):
+    """The GEMM with a workspace of the queried size (so it may split)."""
     st = mx.new_status()
-    y = mx.gemm(mx.MX_FPROP, xr, wr, out=out, status=st)
+    y = mx.gemm(mx.MX_FPROP, xr, wr, out=out, status=st, workspace=mx.gemm_workspace(mx.MX_FPROP, xr, wr))
     torch.cuda.synchronize()
     assert mx.read_status(st) == 0
     return y
@@ -90,7 +91,12 @@ def test_split_tail_deterministic_and_workspace_entry_point():
     torch.cuda.synchronize()
     assert mx.read_status(st) == 0
     assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
-    # too small a workspace (or none): whole tiles only, still within the bound
+    # mx_gemm (no workspace) and too small a workspace: whole tiles only,
+    # still within the bound
+    y5 = mx.gemm(mx.MX_FPROP, xr, wr, status=st)
+    torch.cuda.synchronize()
+    assert mx.read_status(st) == 0
+    check_gemm_full(y5, *oracle.mx_quantize_rowwise(f64(x)), *oracle.mx_quantize_rowwise(f64(w)), "mx_gemm")
     for size in (0, need - 16):
         y4 = torch.empty_like(y1)
         mx.mx_gemm_with_workspace(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), y4.data_ptr(), y4.stride(0),
@@ -122,7 +128,9 @@ def test_split_tail_pitch_gap_and_unaligned_output(aligned):
     big = torch.full((M, ldc + 8), float("nan"), dtype=torch.bfloat16, device="cuda")
     view = big[:, :N] if aligned else big[:, 1:N + 1]
     st = mx.new_status()
-    mx.mx_gemm(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), view.data_ptr(), big.stride(0), st.data_ptr(), None)
+    ws = mx.gemm_workspace(mx.MX_FPROP, xr, wr)
+    mx.mx_gemm_with_workspace(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), view.data_ptr(), big.stride(0),
+                              ws.data_ptr(), ws.numel(), st.data_ptr(), None)
     torch.cuda.synchronize()
     assert mx.read_status(st) == 0
     h = big.float().cpu().numpy()
@@ -133,18 +141,20 @@ def test_split_tail_pitch_gap_and_unaligned_output(aligned):
 
 
 def test_split_tail_captured_in_cuda_graph():
-    """The split tail takes its workspace from a stream-ordered pool, so a call
-    can be recorded into a CUDA graph: replays give the eager call's bits."""
+    """A split-tail GEMM (its partial tiles in the caller's workspace, then the
+    reduction launch) recorded into a CUDA graph: replays give the eager call's
+    bits."""
     M, N, K = 512, 512, 16384
     _, _, xr, wr = operands(M, N, K, 13)
     assert ws_bytes(xr, wr) > 0
     y_eager = gemm(xr, wr)
     out = torch.zeros_like(y_eager)
+    ws = mx.gemm_workspace(mx.MX_FPROP, xr, wr)
     stream = torch.cuda.Stream()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-        mx.mx_gemm(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), out.data_ptr(), out.stride(0), None,
-                   stream.cuda_stream)
+        mx.mx_gemm_with_workspace(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), out.data_ptr(), out.stride(0),
+                                  ws.data_ptr(), ws.numel(), None, stream.cuda_stream)
     with torch.cuda.stream(stream):
         for _ in range(3):
             graph.replay()
