@@ -583,8 +583,28 @@ def run_quant_sweep(args, rank, world, peaks, peak_src):
                          "traffic": profile_traffic("mx_quant_kernel:quant_sweep_M32768"), "bytes_per_launch": per_elem * big * C,
                          "peak_source": f"{peak_src} hbm_gbs", "launch": f"M={big}"},
             "gpu_launches": len(xs) * args.steps, "clocks": clk}
+    if rank == 0 and not args.no_cpu_baseline:
+        dt, nbytes = oracle_quant_sample(4096)
+        line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+                                "seconds": dt, "sample": "the whole M=4096 sweep tensor [4096 x 7168]: oracle row "
+                                                        "and column quantisation, 4.0625 B per element"}
     if rank == 0:
         print(json.dumps(line))
+
+
+def oracle_quant_sample(M: int):
+    """Time the oracle's row and column quantisation of the [M x 7168] sweep
+    tensor; returns (seconds, algorithmic bytes)."""
+    import numpy as np
+    import oracle
+    import workloads
+    x = workloads.quant_sweep(M)
+    f = oracle.bf16_bits_to_float64(x.contiguous().view(torch.int16).numpy().view(np.uint16))
+    t0 = time.perf_counter()
+    oracle.mx_quantize_rowwise(f)
+    oracle.mx_quantize_colwise(f)
+    dt = time.perf_counter() - t0
+    return dt, 4.0625 * x.numel()
 
 
 def _linear_set(projs, mx):
