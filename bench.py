@@ -584,10 +584,13 @@ def run_quant_sweep(args, rank, world, peaks, peak_src):
                          "peak_source": f"{peak_src} hbm_gbs", "launch": f"M={big}"},
             "gpu_launches": len(xs) * args.steps, "clocks": clk}
     if rank == 0 and not args.no_cpu_baseline:
-        dt, nbytes = oracle_quant_sample(4096)
+        dt, nbytes = 0.0, 0.0
+        for m in (4096, 8192):
+            d_, b_ = oracle_quant_sample(m)
+            dt, nbytes = dt + d_, nbytes + b_
         line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
-                                "seconds": dt, "sample": "the whole M=4096 sweep tensor [4096 x 7168]: oracle row "
-                                                        "and column quantisation, 4.0625 B per element"}
+                                "seconds": dt, "sample": "the whole M=4096 and M=8192 sweep tensors [M x 7168]: "
+                                                        "oracle row and column quantisation, 4.0625 B per element"}
     if rank == 0:
         print(json.dumps(line))
 
@@ -1042,10 +1045,10 @@ def main():
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        fl, dt = oracle_dense_sample(1536, 1536)
+        fl, dt = oracle_dense_sample(2560, 2560)
         line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
                                 "kind": "oracle", "seconds": dt,
-                                "sample": "1536x1536 output block of each of fprop/dgrad/wgrad (dense FFN "
+                                "sample": "2560x2560 output block of each of fprop/dgrad/wgrad (dense FFN "
                                           "up-proj), with the oracle quantisation of the operand rows it reads"}
     if rank == 0:
         print(json.dumps(line))
