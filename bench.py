@@ -631,23 +631,34 @@ def _linear_set(projs, mx):
 
 
 def _linear_step(layers, mx, stream, timers=None):
-    """Per layer: quantise X, W, dY (both copies each), then fprop, dgrad, wgrad."""
+    """Per layer: quantise X and W (one launch) and dY (both copies each); then
+    fprop, and the backward pass's dgrad + wgrad in one launch."""
     sp = stream.cuda_stream
     for ly in layers:
-        for i, (x, (r, c)) in enumerate(zip(ly["src"], ly["q"])):
+        for names in ((0, 1), (2,)):
+            descs = []
+            for i in names:
+                x, (r, c) = ly["src"][i], ly["q"][i]
+                descs.append(mx.MXQuantTensorC(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), r.data.data_ptr(),
+                                               r.scale.data_ptr(), c.data.data_ptr(), c.scale.data_ptr()))
             e = timers.span("quant", stream) if timers else None
-            mx.mx_quantize(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), mx.MX_BOTH, r.data.data_ptr(),
-                           r.scale.data_ptr(), c.data.data_ptr(), c.scale.data_ptr(), None, 0, 0, None, sp)
+            mx.mx_quantize_multi(descs, mx.MX_BOTH, None, sp)
             if e is not None:
                 e.record(stream)
         (xr, xc), (wr, wc), (dr, dc) = ly["q"]
-        for j, (mode, a, b) in enumerate(((mx.MX_FPROP, xr, wr), (mx.MX_DGRAD, dr, wc), (mx.MX_WGRAD, dc, xc))):
-            out = ly["out"][j]
-            e = timers.span((ly["name"], j), stream) if timers else None
-            mx.mx_gemm_with_workspace(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0),
-                                      ly["ws"].data_ptr(), ly["ws_bytes"], None, sp)
-            if e is not None:
-                e.record(stream)
+        y, dx, dw = ly["out"]
+        e = timers.span((ly["name"], 0), stream) if timers else None
+        mx.mx_gemm_with_workspace(mx.MX_FPROP, xr.c_operand(), wr.c_operand(), y.data_ptr(), y.stride(0),
+                                  ly["ws"].data_ptr(), ly["ws_bytes"], None, sp)
+        if e is not None:
+            e.record(stream)
+        e = timers.span((ly["name"], 1), stream) if timers else None
+        mx.mx_gemm_multi([mx.MXGemmProblemC(dr.c_operand(), wc.c_operand(), dx.data_ptr(), dx.stride(0),
+                                            mx.MX_DGRAD, 0),
+                          mx.MXGemmProblemC(dc.c_operand(), xc.c_operand(), dw.data_ptr(), dw.stride(0),
+                                            mx.MX_WGRAD, 0)], None, sp)
+        if e is not None:
+            e.record(stream)
 
 
 def gemm_launches(mx, mode, a, b, workspace=False):
@@ -676,9 +687,10 @@ def _timed(step, args, world):
 
 def run_mla(args, rank, world, peaks, peak_src):
     """MLA projection set at M = 16384 tokens (q_down 2048->1536, kv_down
-    2048->576, kv_up 512->4096, o_proj 2048->2048): per projection the three
-    quantisations and the fprop, dgrad and wgrad GEMMs. Each GEMM's roofline
-    time is max(FLOPs / FP8 peak, algorithmic bytes / HBM bandwidth)."""
+    2048->576, kv_up 512->4096, o_proj 2048->2048): per projection X and W
+    quantised in one launch and dY in another, then fprop, then dgrad + wgrad
+    in one launch. A GEMM's roofline time is max(FLOPs / FP8 peak, algorithmic
+    bytes / HBM bandwidth); the backward launch's is the sum of its two."""
     import workloads
     import mxfp8_block_scaled_gb300 as mx
     projs = []
@@ -700,16 +712,23 @@ def run_mla(args, rank, world, peaks, peak_src):
     ms = max_over_ranks(t0.elapsed_time(t1), world)
     peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     per_gemm, flops_total, gemm_ms_total = [], 0.0, 0.0
+
+    def roof(M, N, K):
+        fl = 2.0 * M * N * K
+        byts = (M * K + N * K) * (1 + 1 / 32) + 2 * M * N
+        return fl, max(fl / (peak_fp8 * 1e12), byts / (peaks["hbm_gbs"] * 1e9)) * 1e3, \
+            "tensor" if fl / (peak_fp8 * 1e12) >= byts / (peaks["hbm_gbs"] * 1e9) else "hbm"
+
     for ly in layers:
-        for j, (label, M, N, K) in enumerate(_gemm_shapes(ly)):
-            fl = 2.0 * M * N * K
-            byts = (M * K + N * K) * (1 + 1 / 32) + 2 * M * N
+        (_, M, N, K), dg, wg = _gemm_shapes(ly)
+        for j, (label, shapes) in enumerate((("fprop", [(M, N, K)]), ("dgrad + wgrad (one launch)", [dg[1:], wg[1:]]))):
+            parts = [roof(*sh) for sh in shapes]
+            fl = sum(pt[0] for pt in parts)
+            roof_ms = sum(pt[1] for pt in parts)
             g_ms = timers.total_ms((ly["name"], j)) / timers.count((ly["name"], j))
-            roof_ms = max(fl / (peak_fp8 * 1e12), byts / (peaks["hbm_gbs"] * 1e9)) * 1e3
-            per_gemm.append({"gemm": f"{ly['name']} {label}", "shape": [M, N, K], "ms": g_ms,
+            per_gemm.append({"gemm": f"{ly['name']} {label}", "shapes": [list(sh) for sh in shapes], "ms": g_ms,
                              "tflops": fl / (g_ms / 1e3) / 1e12, "roofline_ms": roof_ms,
-                             "bound": "tensor" if fl / (peak_fp8 * 1e12) >= byts / (peaks["hbm_gbs"] * 1e9) else "hbm",
-                             "frac": roof_ms / g_ms})
+                             "bound": "+".join(pt[2] for pt in parts), "frac": roof_ms / g_ms})
             flops_total += fl
             gemm_ms_total += g_ms
     value = world * args.steps * flops_total / (ms / 1e3) / 1e12
@@ -726,10 +745,8 @@ def run_mla(args, rank, world, peaks, peak_src):
                          "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8, "traffic": None,
                          "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}",
                          "roofline_time_frac": sum(g["roofline_ms"] for g in per_gemm) / gemm_ms_total},
-            "gpu_launches": sum(3 + sum(gemm_launches(mx, mode, a, b, workspace=True) for mode, a, b in
-                                         ((mx.MX_FPROP, ly["q"][0][0], ly["q"][1][0]),
-                                          (mx.MX_DGRAD, ly["q"][2][0], ly["q"][1][1]),
-                                          (mx.MX_WGRAD, ly["q"][2][1], ly["q"][0][1])))
+            # per layer: two quantiser launches, fprop (+ its split-tail reduction), dgrad + wgrad
+            "gpu_launches": sum(2 + gemm_launches(mx, mx.MX_FPROP, ly["q"][0][0], ly["q"][1][0], workspace=True) + 1
                                 for ly in layers) * args.steps,
             "clocks": clk}
     if rank == 0:

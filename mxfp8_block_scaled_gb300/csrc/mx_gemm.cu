@@ -58,7 +58,11 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "mx_internal.h"
 #include "mx_ptx.cuh"
@@ -129,7 +133,7 @@ struct PairCfg {
   static constexpr int kSfCols = 4 + 8;
   static constexpr uint32_t kSfCol0 = BN;
   static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
-  static constexpr int kBarBytes = (4 * kStages + 4) * 8 + 16;
+  static constexpr int kBarBytes = (4 * kStages + 4) * 8 + 16 + 2 * MX_MAX_GEMM_MULTI * 4;  // + schedule words
   static constexpr int kGroupBytes = 3 * (kMaxGroups + 1) * 4;
   __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
     return 1024 + static_cast<size_t>(kStages) * kStageTx + kEpiBufs * kEpiBytes + kBarBytes +
@@ -832,6 +836,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // GEMMs whose tiles one persistent grid walks in turn (problem i owns launch
 // tiles [tile0[i], tile0[i+1])), or a single GEMM of any kind (n = 1).
 constexpr int kMaxProblems = MX_MAX_GEMM_MULTI;
+// A balanced schedule (sched = 1) gives cluster c cnt[i][c] consecutive tiles
+// of problem i, starting after the tiles of clusters 0 .. c-1; otherwise
+// cluster c takes launch tiles c, c + clusters, ... .
+constexpr int kMaxSchedClusters = 96;
 struct PairProblem {
   CUtensorMap a, b, sfa, sfb, c;
   GParams p;
@@ -840,6 +848,8 @@ struct PairArgs {
   PairProblem prob[kMaxProblems];
   int64_t tile0[kMaxProblems + 1];
   int n;
+  int sched;
+  uint8_t cnt[kMaxProblems][kMaxSchedClusters];
 };
 static_assert(sizeof(PairArgs) <= 4096, "kernel parameter space");
 
@@ -884,6 +894,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(s_tmem + 1);
   int32_t* s_flag = reinterpret_cast<int32_t*>(s_tmem + 2);
   int32_t* s_total = reinterpret_cast<int32_t*>(s_tmem + 3);
+  int32_t* s_seq = reinterpret_cast<int32_t*>(s_tmem + 4);  // scheduled: [first tile of each problem][count]
   GroupInfo g;
   g.off = reinterpret_cast<int32_t*>(smem + C::smem_bytes(false) - 1024);
   g.tile = g.off + (kMaxGroups + 1);
@@ -914,6 +925,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int s = 0; s < S; ++s) mbar_init(&sf_full[s], 1);
     mbar_init(sf_drain, 1);
     *s_abort = 0;
+    if (kMulti && args.sched) {
+      // This cluster's range of each problem's tiles.
+      const int c = static_cast<int>(blockIdx.x >> 1);
+      for (int i = 0; i < args.n; ++i) {
+        int32_t first = 0;
+        for (int q = 0; q < c; ++q) first += args.cnt[i][q];
+        s_seq[i] = first;
+        s_seq[kMaxProblems + i] = args.cnt[i][c];
+      }
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -941,6 +962,20 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (kMulti) ntiles = args.tile0[args.n];
   const int64_t t_first = blockIdx.x >> 1;
   const int64_t t_step = gridDim.x >> 1;
+  // The i-th launch tile of this cluster, or -1 past its last.
+  const bool sched = kMulti && args.sched;
+  auto next_tile = [&](int64_t i) -> int64_t {
+    if (!sched) {
+      const int64_t t = t_first + i * t_step;
+      return t < ntiles ? t : -1;
+    }
+    for (int q = 0; q < args.n; ++q) {
+      const int64_t cnt = s_seq[kMaxProblems + q];
+      if (i < cnt) return args.tile0[q] + s_seq[q] + i;
+      i -= cnt;
+    }
+    return -1;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
@@ -950,7 +985,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     bool ok = true;
     // Lane 0 alone runs the loop (the rows-ragged scale gather has a warp of
     // its own: a per-stage warp shuffle here cost ~5% of GEMM throughput).
-    for (int64_t t = t_first; t < ntiles && ok && lane == 0; t += t_step) {
+    for (int64_t it = 0, t; lane == 0 && ok && (t = next_tile(it)) >= 0; ++it) {
       const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
         const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
@@ -1007,7 +1042,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+      for (int64_t it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
         const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
         const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
@@ -1059,7 +1094,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+      for (int64_t it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
         const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
         const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
@@ -1081,7 +1116,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+      for (int64_t it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
         const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
         const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
@@ -1118,7 +1153,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t t = t_first; t < ntiles && ok; t += t_step) {
+      for (int64_t it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
         const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
         const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
@@ -1160,7 +1195,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint8_t* stg = sEpi + (warp - 2) * C::kEpiBufs * kEpiWarpBytes;
     const uint32_t lacc_empty = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t acc_phase = 0;
-    for (int64_t t = t_first; t < ntiles; t += t_step) {
+    for (int64_t it = 0, t; (t = next_tile(it)) >= 0; ++it) {
       const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
         const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
@@ -1889,10 +1924,63 @@ GParams make_gparams(const GemmLaunch& L) {
   return p;
 }
 
+// Cost of one pair tile of L in 128-K blocks, plus the per-tile drain and
+// epilogue (about two blocks' time).
+int64_t pair_tile_cost(const GemmLaunch& L) { return (L.K + kBK - 1) / kBK + 2; }
+
+// Greedy longest-first schedule of the problems' tiles over `clusters` SM
+// pairs (problems already in decreasing tile cost): every tile goes to the
+// cluster that would finish first. Fills args->cnt; returns the latest
+// finish, or -1 if a count does not fit the table.
+int64_t schedule_greedy(PairArgs* args, const GemmLaunch* Ls, int n, int64_t clusters) {
+  std::vector<int64_t> load(static_cast<size_t>(clusters), 0);
+  using Slot = std::pair<int64_t, int64_t>;  // (load, cluster): ties go to the lower index
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int64_t c = 0; c < clusters; ++c) heap.push({0, c});
+  for (int i = 0; i < n; ++i) {
+    const int64_t cost = pair_tile_cost(Ls[i]);
+    std::vector<int64_t> cnt(static_cast<size_t>(clusters), 0);
+    for (int64_t t = 0; t < pair_tiles_upper(Ls[i]); ++t) {
+      Slot sl = heap.top();
+      heap.pop();
+      ++cnt[static_cast<size_t>(sl.second)];
+      sl.first += cost;
+      heap.push(sl);
+    }
+    for (int64_t c = 0; c < clusters; ++c) {
+      if (cnt[static_cast<size_t>(c)] > 255) return -1;
+      args->cnt[i][c] = static_cast<uint8_t>(cnt[static_cast<size_t>(c)]);
+    }
+  }
+  int64_t worst = 0;
+  while (!heap.empty()) {
+    worst = std::max(worst, heap.top().first);
+    heap.pop();
+  }
+  return worst;
+}
+
+// Latest finish of round-robin: cluster c takes launch tiles c, c + clusters, ...
+int64_t schedule_round_robin(const GemmLaunch* Ls, int n, int64_t clusters) {
+  std::vector<int64_t> load(static_cast<size_t>(clusters), 0);
+  int64_t t = 0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t cost = pair_tile_cost(Ls[i]);
+    for (int64_t j = 0; j < pair_tiles_upper(Ls[i]); ++j, ++t) load[static_cast<size_t>(t % clusters)] += cost;
+  }
+  return *std::max_element(load.begin(), load.end());
+}
+
 // Several dense GEMMs in one launch of the pair kernel.
-mx_status launch_pair_multi(const GemmLaunch* Ls, int n, cudaStream_t s) {
+mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
   PairArgs* args = pair_args_scratch();
   std::memset(args, 0, sizeof(PairArgs));
+  // Longest tiles first: they start early and the short ones fill in behind.
+  GemmLaunch Ls[kMaxProblems];
+  for (int i = 0; i < n; ++i) Ls[i] = Ls_in[i];
+  std::stable_sort(Ls, Ls + n, [](const GemmLaunch& a, const GemmLaunch& b) {
+    return pair_tile_cost(a) > pair_tile_cost(b);
+  });
   int64_t tiles = 0;
   for (int i = 0; i < n; ++i) {
     const GemmLaunch& L = Ls[i];
@@ -1917,6 +2005,14 @@ mx_status launch_pair_multi(const GemmLaunch* Ls, int n, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count() / 2));
+  // The balanced schedule where it finishes clearly earlier than round-robin
+  // (same tiles, same results; only the order of work changes).
+  static const int sched_mode = env_int("MXFP8_GEMM_SCHEDULE", 1);  // 0: round-robin only
+  if (sched_mode != 0 && clusters <= kMaxSchedClusters) {
+    const int64_t greedy = schedule_greedy(args, Ls, n, clusters);
+    const int64_t rr = schedule_round_robin(Ls, n, clusters);
+    args->sched = (greedy > 0 && greedy * 100 < rr * 97) ? 1 : 0;
+  }
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));

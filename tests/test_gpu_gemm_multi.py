@@ -147,3 +147,26 @@ def test_multi_captured_in_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(gX.view(torch.int16), dX.view(torch.int16))
     assert torch.equal(gW.view(torch.int16), dW.view(torch.int16))
+
+
+def test_balanced_schedule_mla_backward_matches_separate_calls():
+    """MLA q_down backward: dgrad 16384 x 2048 (K 1536) and wgrad 1536 x 2048
+    (K 16384 tokens) in one launch. Their tiles differ ~9x in length, so the
+    launch takes the balanced (longest-first) schedule; every tile is computed
+    the same way whichever cluster runs it, so the outputs equal separate
+    mx_gemm calls bit for bit, and sampled entries match the oracle."""
+    M, K, N = 16384, 2048, 1536
+    X, W, dY, probs = linear_backward(M, N, K, 70)
+    dX, dW = run_multi(probs)
+    st = mx.new_status()
+    sX = mx.gemm(probs[0][0], probs[0][1], probs[0][2], status=st)
+    sW = mx.gemm(probs[1][0], probs[1][1], probs[1][2], status=st)
+    ok = torch.cuda.synchronize() or mx.read_status(st) == 0
+    assert ok
+    assert torch.equal(dX.view(torch.int16), sX.view(torch.int16)), "dgrad differs from the separate call"
+    assert torch.equal(dW.view(torch.int16), sW.view(torch.int16)), "wgrad differs from the separate call"
+    Xc, Wc, dYc = X.cuda(), W.cuda(), dY.cuda()
+    ii, jj = sample_entries(M, K, 300, seed=71, tile_m=128, tile_n=256)
+    check_gemm_sampled(dX, dYc, mx.MX_ROWWISE, Wc, mx.MX_COLWISE, ii, jj, "q_down dgrad (scheduled)")
+    ii, jj = sample_entries(N, K, 300, seed=72, tile_m=128, tile_n=256)
+    check_gemm_sampled(dW, dYc, mx.MX_COLWISE, Xc, mx.MX_COLWISE, ii, jj, "q_down wgrad (scheduled)")
