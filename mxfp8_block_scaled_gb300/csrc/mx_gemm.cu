@@ -1340,41 +1340,44 @@ __global__ void __launch_bounds__(256) mx_gemm_sk_reduce_kernel(const GParams p)
 //
 // "浮点格式、数值稳定性与混合精度" §七.3: the block scales change along K, so
 // each 128-K block's partial sum is promoted to FP32 with its two scales. Here
-// the tensor core computes each block's partial sum (the block-scaled MMA with
-// unit E8M0 scales, loaded into TMEM once) into one of two TMEM buffers, and
-// the epilogue warps fold it into FP32 registers while the MMAs fill the other
-// buffer. 128 x 128 tiles: two 128-column partial buffers plus the unit
-// scales fit TMEM.
+// the tensor core computes each block's partial sum (plain E4M3 MMAs, exact
+// products, FP32 accumulation, no block scales) into one of two TMEM buffers,
+// and the epilogue warps fold it into FP32 registers while the MMAs fill the
+// other buffer. 128 x 256 tiles: the two 256-column partial buffers take all
+// of TMEM (no scale columns are needed); 128 x 128 tiles for narrow outputs.
 
+template <int BN_>
 struct BwCfg {
-  static constexpr int BN = 128;
-  static constexpr int kStages = 6;
+  static constexpr int BN = BN_;
+  static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr int kParts = 2;  // partial-sum buffers in TMEM (a third measured no faster)
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
-  static constexpr uint32_t kSfCol0 = kParts * BN;  // unit scales after the partial buffers
-  static_assert(kSfCol0 + 8 <= kTmemCols, "TMEM budget");
+  static_assert(kParts * BN <= kTmemCols, "TMEM budget");
   static constexpr int kBarBytes = (2 * kStages + 2 * kParts + 1) * 8 + 16;
   static constexpr size_t smem_bytes() {
-    return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kEpiBytes + 512 + kBarBytes;
+    return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kEpiBytes + kBarBytes;
   }
 };
+// producer, MMA issuer and 8 epilogue warps (no scale copies)
+constexpr int kBwThreads = 320;
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN_>
+__global__ void __launch_bounds__(kBwThreads, 1)
     mx_gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                              const __grid_constant__ CUtensorMap tmap_c, const GParams p,
                              const float* __restrict__ sa, const float* __restrict__ sb) {
-  using C = BwCfg;
+  using C = BwCfg<BN_>;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
+  constexpr int kCols = BN / 2;  // columns per epilogue thread (its TMEM lane)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * C::kABytes;
   uint8_t* sEpi = sB + S * C::kBBytes;
-  uint8_t* sUnit = sEpi + kEpiBytes;  // a scale atom of 0x7F bytes (E8M0 1.0)
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sUnit + 512);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + kEpiBytes);
   uint64_t* empty_bar = full_bar + S;
   constexpr int P = C::kParts;
   uint64_t* part_full = empty_bar + S;   // [P] a partial sum is in TMEM
@@ -1386,10 +1389,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 128) {
-    reinterpret_cast<uint32_t*>(sUnit)[threadIdx.x] = 0x7F7F7F7Fu;
-    fence_proxy_async_smem();  // read by the tensor-core copy (async proxy)
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -1417,6 +1416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *s_tmem;
   const int64_t ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
   const int64_t kbs = (p.K + kBK - 1) / kBK;
+  const int64_t nbw = (p.N + 127) / 128;  // weight blocks along N
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
@@ -1459,11 +1459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_mxf8_e4m3(kBM, BN);
-      const uint32_t sf_t = tmem_base + C::kSfCol0;
-      // Unit scales for A and B, once; later MMAs of this thread see them in order.
-      tc_cp_32x128b_warpx4(sf_t, sdesc_scale_atom(smem_u32(sUnit)));
-      tc_cp_32x128b_warpx4(sf_t + 4, sdesc_scale_atom(smem_u32(sUnit)));
+      constexpr uint32_t idesc = idesc_f8_e4m3_f32(kBM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int64_t gk = 0;  // k blocks issued so far: buffer gk % P, its use count gk / P
@@ -1482,9 +1478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::kABytes));
           const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::kBBytes));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc_mma_mxf8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_id(idesc, k, k), sf_t, sf_t + 4,
-                        k != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) tc_mma_f8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0 ? 1u : 0u);
           tc_commit(&empty_bar[stage]);
           tc_commit(&part_full[buf]);
           if (++stage == S) {
@@ -1497,55 +1491,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain_bar, 0, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp < 2 + kEpiThreads / 32) {
+  } else {
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int col_off = half * 64;
+    const int col_off = half * kCols;
     uint8_t* stg = sEpi + (warp - 2) * kEpiWarpBytes;
     int64_t gk = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile ti = get_tile<BN, GEMM_DENSE>(p, g, t);
       const int64_t grow = ti.m0 + quarter * 32 + lane;
-      const int64_t nb = ti.n0 / 128;
-      float acc[64];
+      // This warp's columns lie in one 128-wide weight block; past N there is
+      // none (the partial sums there are zeros), so its multiplier is 1.
+      const int64_t nb = (ti.n0 + col_off) >> 7;
+      const bool nb_in = nb < nbw;
+      float acc[kCols];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
       bool ok = true;
       // The blocks' two multipliers, fetched one block ahead so their latency
       // hides behind the previous block's promotion; rows past the end hold
       // zeros, give them 1.
       float a_s = (ti.nkb > 0 && grow < p.M) ? sa[grow] : 1.0f;
-      float b_s = ti.nkb > 0 ? sb[nb * kbs] : 1.0f;
+      float b_s = (ti.nkb > 0 && nb_in) ? sb[nb * kbs] : 1.0f;
       for (int kb = 0; kb < ti.nkb; ++kb, ++gk) {
         const int buf = static_cast<int>(gk % P);
         float a_next = 1.0f, b_next = 1.0f;
         if (kb + 1 < ti.nkb) {
           a_next = grow < p.M ? sa[(kb + 1) * p.M + grow] : 1.0f;
-          b_next = sb[nb * kbs + kb + 1];
+          b_next = nb_in ? sb[nb * kbs + kb + 1] : 1.0f;
         }
         if (!wait_or_abort(&part_full[buf], static_cast<uint32_t>((gk / P) & 1), p, s_abort)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        uint32_t pr[64];
+        const float f = 1.0f / (a_s * b_s);
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN + col_off);
-        tmem_ld_32x32b_x32(taddr, pr);
-        tmem_ld_32x32b_x32(taddr + 32, pr + 32);
-        tmem_ld_wait();
+        // One chunk of columns per TMEM load: the register budget of ten
+        // warps (168 per thread) holds the 128 FP32 sums and a 16-column
+        // chunk; 32-column chunks spilled and ran 15% slower.
+#ifndef MX_BW_CHUNK
+#define MX_BW_CHUNK 16
+#endif
+        constexpr int kChunk = MX_BW_CHUNK;
+#pragma unroll
+        for (int ch = 0; ch < kCols / kChunk; ++ch) {
+          uint32_t pr[kChunk];
+          if constexpr (kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * kChunk, pr);
+          else tmem_ld_32x32b_x16(taddr + ch * kChunk, pr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < kChunk; ++i) acc[ch * kChunk + i] = fmaf(__uint_as_float(pr[i]), f, acc[ch * kChunk + i]);
+        }
         tc_fence_before_sync();
         mbar_arrive(&part_empty[buf]);
-        const float f = 1.0f / (a_s * b_s);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = fmaf(__uint_as_float(pr[i]), f, acc[i]);
         a_s = a_next;
         b_s = b_next;
       }
       if (!ok) break;
-      store_tile<GEMM_DENSE, 64>(p, ti, reinterpret_cast<const uint32_t*>(acc), quarter, lane, 2, col_off, stg,
-                                 &tmap_c);
+      store_tile<GEMM_DENSE, kCols>(p, ti, reinterpret_cast<const uint32_t*>(acc), quarter, lane, kCols / 32,
+                                    col_off, stg, &tmap_c);
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
@@ -1858,22 +1865,28 @@ bool use_pairs(const GemmLaunch& L) {
   return pair_tiles_upper(L) >= sm_count() / 2;
 }
 
-mx_status launch_blockwise(const GemmLaunch& L, GParams p, cudaStream_t s) {
+template <int BN>
+mx_status launch_blockwise_bn(const GemmLaunch& L, GParams p, cudaStream_t s) {
+  using C = BwCfg<BN>;
   CUtensorMap ma, mb, mc;
   mx_status st = make_map(&ma, L.a_data, L.M, L.K, L.a_ld, kBM);
   if (st != MX_OK) return st;
-  st = make_map(&mb, L.b_data, L.N, L.K, L.b_ld, BwCfg::BN);
+  st = make_map(&mb, L.b_data, L.N, L.K, L.b_ld, BN);
   if (st != MX_OK) return st;
   output_map(L, p, &mc, GEMM_DENSE);
-  const size_t smem = BwCfg::smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(mx_gemm_blockwise_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const size_t smem = C::smem_bytes();
+  auto kern = mx_gemm_blockwise_kernel<BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(blockwise smem)");
-  const int64_t tiles = (L.M + kBM - 1) / kBM * ((L.N + BwCfg::BN - 1) / BwCfg::BN);
+  const int64_t tiles = (L.M + kBM - 1) / kBM * ((L.N + BN - 1) / BN);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count()));
-  mx_gemm_blockwise_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(ma, mb, mc, p, L.bw_a_scale,
-                                                                              L.bw_b_scale);
+  kern<<<static_cast<unsigned>(grid), kBwThreads, smem, s>>>(ma, mb, mc, p, L.bw_a_scale, L.bw_b_scale);
   return cuda_status(cudaGetLastError(), "mx_gemm_fp8_blockwise launch");
+}
+
+// 128 x 256 tiles unless N fits one 128-wide tile.
+mx_status launch_blockwise(const GemmLaunch& L, GParams p, cudaStream_t s) {
+  return L.N > 128 ? launch_blockwise_bn<256>(L, p, s) : launch_blockwise_bn<128>(L, p, s);
 }
 
 }  // namespace

@@ -320,6 +320,19 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D (+)= A . B^T for one K=32 step of E4M3 x E4M3 without block scales (the
+// blockwise FP8 recipe applies its FP32 multipliers outside the MMA); A, B in
+// shared memory (descriptors), D in TMEM.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Each thread of the warp reads 32 consecutive 32-bit columns of its own lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -331,6 +344,17 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) 
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
         "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
         "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Each thread of the warp reads 16 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }
@@ -372,6 +396,13 @@ __device__ __forceinline__ uint64_t sdesc_scale_atom(uint32_t saddr) {
 // byte selectors go in bits [29,31) (A) and [4,6) (B).
 __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(uint32_t m, uint32_t n) {
   return ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f8f6f4 (no block scaling): D in F32 (bits
+// [4,6) = 1), A and B E4M3 (format 0 at [7,10) and [10,13)), both K-major
+// (bits 15, 16 = 0), N>>3 at [17,23), M>>4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_f8_e4m3_f32(uint32_t m, uint32_t n) {
+  return (1u << 4) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t sfa_id, uint32_t sfb_id) {
