@@ -1350,34 +1350,38 @@ template <int BN_>
 struct BwCfg {
   static constexpr int BN = BN_;
   static constexpr int kStages = BN == 256 ? 4 : 6;
+  // Epilogue warps: four per TMEM lane quarter at BN = 256 (64 columns each),
+  // two at BN = 128.
+  static constexpr int kEpiWarps = BN == 256 ? 16 : 8;
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kEpiStage = kEpiWarps * kEpiWarpBytes;
   static constexpr int kParts = 2;  // partial-sum buffers in TMEM (a third measured no faster)
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static_assert(kParts * BN <= kTmemCols, "TMEM budget");
   static constexpr int kBarBytes = (2 * kStages + 2 * kParts + 1) * 8 + 16;
   static constexpr size_t smem_bytes() {
-    return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kEpiBytes + kBarBytes;
+    return 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kEpiStage + kBarBytes;
   }
 };
-// producer, MMA issuer and 8 epilogue warps (no scale copies)
-constexpr int kBwThreads = 320;
 
 template <int BN_>
-__global__ void __launch_bounds__(kBwThreads, 1)
+__global__ void __launch_bounds__(BwCfg<BN_>::kThreads, 1)
     mx_gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                              const __grid_constant__ CUtensorMap tmap_c, const GParams p,
                              const float* __restrict__ sa, const float* __restrict__ sb) {
   using C = BwCfg<BN_>;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
-  constexpr int kCols = BN / 2;  // columns per epilogue thread (its TMEM lane)
+  constexpr int kSplit = C::kEpiWarps / 4;  // epilogue warps sharing a TMEM lane quarter
+  constexpr int kCols = BN / kSplit;       // columns per epilogue thread (its TMEM lane)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * C::kABytes;
   uint8_t* sEpi = sB + S * C::kBBytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + kEpiBytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + C::kEpiStage);
   uint64_t* empty_bar = full_bar + S;
   constexpr int P = C::kParts;
   uint64_t* part_full = empty_bar + S;   // [P] a partial sum is in TMEM
@@ -1396,7 +1400,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     }
     for (int b = 0; b < P; ++b) {
       mbar_init(&part_full[b], 1);
-      mbar_init(&part_empty[b], kEpiThreads);
+      mbar_init(&part_empty[b], C::kEpiWarps * 32);
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -1494,8 +1498,8 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int col_off = half * kCols;
+    const int part = (warp - 2) >> 2;  // which kCols-wide slice of the tile
+    const int col_off = part * kCols;
     uint8_t* stg = sEpi + (warp - 2) * kEpiWarpBytes;
     int64_t gk = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -1529,18 +1533,18 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         const float f = 1.0f / (a_s * b_s);
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN + col_off);
-        // One chunk of columns per TMEM load: the register budget of ten
-        // warps (168 per thread) holds the 128 FP32 sums and a 16-column
-        // chunk; 32-column chunks spilled and ran 15% slower.
-#ifndef MX_BW_CHUNK
-#define MX_BW_CHUNK 16
-#endif
-        constexpr int kChunk = MX_BW_CHUNK;
+        // One chunk of columns per TMEM load, within the register budget:
+        // at BN = 256 eighteen warps leave 96 registers a thread for 64 FP32
+        // sums and an 8-column chunk (ten warps holding 128 sums each, or
+        // 16-column chunks here, spilled and ran 4-8% slower); at BN = 128
+        // ten warps hold 64 sums and 32-column chunks.
+        constexpr int kChunk = BN == 256 ? 8 : 32;
 #pragma unroll
         for (int ch = 0; ch < kCols / kChunk; ++ch) {
           uint32_t pr[kChunk];
           if constexpr (kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * kChunk, pr);
-          else tmem_ld_32x32b_x16(taddr + ch * kChunk, pr);
+          else if constexpr (kChunk == 16) tmem_ld_32x32b_x16(taddr + ch * kChunk, pr);
+          else tmem_ld_32x32b_x8(taddr + ch * kChunk, pr);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < kChunk; ++i) acc[ch * kChunk + i] = fmaf(__uint_as_float(pr[i]), f, acc[ch * kChunk + i]);
@@ -1880,7 +1884,7 @@ mx_status launch_blockwise_bn(const GemmLaunch& L, GParams p, cudaStream_t s) {
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(blockwise smem)");
   const int64_t tiles = (L.M + kBM - 1) / kBM * ((L.N + BN - 1) / BN);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count()));
-  kern<<<static_cast<unsigned>(grid), kBwThreads, smem, s>>>(ma, mb, mc, p, L.bw_a_scale, L.bw_b_scale);
+  kern<<<static_cast<unsigned>(grid), C::kThreads, smem, s>>>(ma, mb, mc, p, L.bw_a_scale, L.bw_b_scale);
   return cuda_status(cudaGetLastError(), "mx_gemm_fp8_blockwise launch");
 }
 
