@@ -354,10 +354,10 @@ def cpu_threads():
 # main
 # ---------------------------------------------------------------------------
 
-def profile_traffic(kernel: str):
-    """DRAM traffic of the dense step's launches of `kernel` (bytes per step,
-    as the roofline entries count their time) from a committed ncu summary,
-    if it was taken from the current kernel source (else None)."""
+def profile_traffic(kernel: str, field: str = "bytes_per_step"):
+    """DRAM traffic of a roofline entry's launches (bytes per step, or per
+    launch, as that entry counts its time) from a committed ncu summary, if it
+    was taken from the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -370,7 +370,7 @@ def profile_traffic(kernel: str):
     if not os.path.exists(src):
         return None
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return ent.get("bytes_per_step") if h == ent.get("source_sha256_16") else None
+    return ent.get(field) if h == ent.get("source_sha256_16") else None
 
 
 def run_reference(args, rank, world):
@@ -582,7 +582,8 @@ def run_quant_sweep(args, rank, world, peaks, peak_src):
             "per_M_gbs": per_m,
             "roofline": {"bound": "hbm", "kernel": "mx_quant_kernel", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": profile_traffic("mx_quant_kernel:quant_sweep_M32768"), "bytes_per_launch": per_elem * big * C,
+                         "traffic": profile_traffic("mx_quant_kernel:quant_sweep_M32768", "bytes_per_launch"),
+                         "bytes_per_launch": per_elem * big * C,
                          "peak_source": f"{peak_src} hbm_gbs", "launch": f"M={big}"},
             "gpu_launches": len(xs) * args.steps, "clocks": clk}
     if rank == 0 and not args.no_cpu_baseline:
@@ -881,7 +882,8 @@ def run_wrefresh(args, rank, world, peaks, peak_src):
             "per_projection_gbs": per,
             "roofline": {"bound": "hbm", "kernel": "mx_quant_f32_kernel", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": None, "bytes_per_launch": max(nbytes), "peak_source": f"{peak_src} hbm_gbs"},
+                         "traffic": profile_traffic("mx_quant_f32_kernel:gate_up", "bytes_per_launch"),
+                         "bytes_per_launch": max(nbytes), "peak_source": f"{peak_src} hbm_gbs"},
             "gpu_launches": 2 * args.steps, "clocks": clk}
     if rank == 0:
         print(json.dumps(line))
@@ -936,7 +938,8 @@ def run_blockwise(args, rank, world, peaks, peak_src):
             "config": {"workload": "dense_ffn_up_proj fprop M=8192 K=2048 N=10944, blockwise FP8 variant",
                        "parallelism": f"replicas{world}", "l2": "no flush: a step moves ~0.3 GB (> 129 MB L2)"},
             "roofline": {"bound": "tensor", "kernel": "mx_gemm_blockwise_kernel", "achieved": achieved,
-                         "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8, "traffic": None,
+                         "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
+                         "traffic": profile_traffic("mx_gemm_blockwise_kernel"),
                          "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}",
                          "avg_launch_ms": gemm_ms},
             "quant_ms_per_launch": timers.total_ms("quant") / timers.count("quant"),
