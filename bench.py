@@ -141,6 +141,10 @@ class ClockSampler:
 # workloads
 # ---------------------------------------------------------------------------
 
+TIMING_NOTE = ("value: the timed region, K steps with no event inside them; per-kernel durations (roofline): "
+               "K further steps with a CUDA-event span around each kernel launch or launch group")
+
+
 class Timers:
     """CUDA events around the launches of one kernel family inside the timed region."""
 
@@ -481,24 +485,7 @@ class MoEExperts:
 def run_moe(args, rank, world, peaks, peak_src):
     wl = MoEExperts()
     stream = torch.cuda.Stream()
-    for _ in range(args.warmup):
-        wl.step(stream)
-    torch.cuda.synchronize()
-    timers = Timers()
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        wl.step(stream, timers)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms, timers, clk = _measure(lambda t: wl.step(stream, t), args, world, stream)
     value = world * args.steps * wl.step_flops() / (ms / 1e3) / 1e12
     pairs = timers.pairs["gemm"]
     fl = wl.gemm_flops()
@@ -526,6 +513,7 @@ def run_moe(args, rank, world, peaks, peak_src):
             "weight_quant_ms_per_projection": timers.total_ms("wquant") / timers.count("wquant"),
             "gpu_launches": wl.launches_per_step() * args.steps, "clocks": clk}
     if rank == 0:
+        line["timing"] = TIMING_NOTE
         print(json.dumps(line))
 
 
@@ -549,24 +537,7 @@ def run_quant_sweep(args, rank, world, peaks, peak_src):
             if e is not None:
                 e.record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    timers = Timers()
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(timers)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms, timers, clk = _measure(step, args, world, stream)
     per_elem = 2 + 1 + 1 + 2 / 32
     step_bytes = sum(per_elem * M * C for M in xs)
     value = world * args.steps * step_bytes / (ms / 1e3) / 1e9
@@ -595,6 +566,7 @@ def run_quant_sweep(args, rank, world, peaks, peak_src):
                                 "seconds": dt, "sample": "the whole M=4096 and M=8192 sweep tensors [M x 7168]: "
                                                         "oracle row and column quantisation, 4.0625 B per element"}
     if rank == 0:
+        line["timing"] = TIMING_NOTE
         print(json.dumps(line))
 
 
@@ -676,16 +648,40 @@ def _gemm_shapes(ly):
     return (("fprop", M, N, K), ("dgrad", M, K, N), ("wgrad", N, K, M))
 
 
-def _timed(step, args, world):
+def _measure(step, args, world, stream):
+    """W warm-up steps, the timed region, then the kernel pass.
+
+    The timed region is exactly K steps with no event inside them, bracketed
+    by a barrier and a synchronize on both sides; its CUDA-event time gives
+    `value` and `ms_per_step`. The kernel pass runs K more steps with a
+    CUDA-event span around each kernel launch (or launch group) and gives the
+    per-kernel durations of the roofline entries. Each timing event costs the
+    stream about 2 us (a dense FFN step took 456 us without its six events and
+    469 us with them), which is why the whole-step time comes from the pass
+    without them. Clocks are sampled across both passes.
+    Returns (max-over-ranks ms of the timed region, Timers, clock record)."""
     for _ in range(args.warmup):
         step(None)
     torch.cuda.synchronize()
-    timers = Timers()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    return timers, clocks
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    timers = Timers()
+    for _ in range(args.steps):
+        step(timers)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    return max_over_ranks(t0.elapsed_time(t1), world), timers, clk
 
 
 def run_mla(args, rank, world, peaks, peak_src):
@@ -702,17 +698,7 @@ def run_mla(args, rank, world, peaks, peak_src):
         projs.append((name, d["X"], d["W"], d["dY"]))
     layers = _linear_set(projs, mx)
     stream = torch.cuda.Stream()
-    timers, clocks = _timed(lambda t: _linear_step(layers, mx, stream, t), args, world)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        _linear_step(layers, mx, stream, timers)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms, timers, clk = _measure(lambda t: _linear_step(layers, mx, stream, t), args, world, stream)
     peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     per_gemm, flops_total, gemm_ms_total = [], 0.0, 0.0
 
@@ -753,6 +739,7 @@ def run_mla(args, rank, world, peaks, peak_src):
                                 for ly in layers) * args.steps,
             "clocks": clk}
     if rank == 0:
+        line["timing"] = TIMING_NOTE
         print(json.dumps(line))
 
 
@@ -784,17 +771,13 @@ def run_single(args, rank, world, peaks, peak_src):
         if e is not None:
             e.record(stream)
 
-    # eager: every call through the C ABI, per-kernel spans on the stream
-    timers, clocks = _timed(step, args, world)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(timers)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    eager_us = max_over_ranks(t0.elapsed_time(t1), world) / args.steps * 1e3
+    # eager: every call through the C ABI (K steps without events, then K
+    # with per-kernel spans)
+    eager_ms, timers, _ = _measure(step, args, world, stream)
+    eager_us = eager_ms / args.steps * 1e3
     eager_out = out.clone()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
 
     # the same step recorded once into a CUDA graph and replayed; its output
     # must equal the eager step's bit for bit
@@ -832,6 +815,7 @@ def run_single(args, rank, world, peaks, peak_src):
                               "gemm": timers.total_ms("gemm") / timers.count("gemm") * 1e3},
             "gpu_launches": (1 + gemm_launches(mx, mx.MX_FPROP, xr, wr)) * args.steps, "clocks": clk}
     if rank == 0:
+        line["timing"] = TIMING_NOTE
         print(json.dumps(line))
 
 
@@ -856,17 +840,7 @@ def run_wrefresh(args, rank, world, peaks, peak_src):
             if e is not None:
                 e.record(stream)
 
-    timers, clocks = _timed(step, args, world)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(timers)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms, timers, clk = _measure(step, args, world, stream)
     per_elem = 4 + 1 + 1 + 2 / 32
     nbytes = [per_elem * w.numel() for w in masters]
     value = world * args.steps * sum(nbytes) / (ms / 1e3) / 1e9
@@ -886,6 +860,7 @@ def run_wrefresh(args, rank, world, peaks, peak_src):
                          "bytes_per_launch": max(nbytes), "peak_source": f"{peak_src} hbm_gbs"},
             "gpu_launches": 2 * args.steps, "clocks": clk}
     if rank == 0:
+        line["timing"] = TIMING_NOTE
         print(json.dumps(line))
 
 
@@ -916,17 +891,7 @@ def run_blockwise(args, rank, world, peaks, peak_src):
         if e is not None:
             e.record(stream)
 
-    timers, clocks = _timed(step, args, world)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(timers)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms, timers, clk = _measure(step, args, world, stream)
     fl = 2.0 * M * N * K
     gemm_ms = timers.total_ms("gemm") / timers.count("gemm")
     achieved = fl / (gemm_ms / 1e3) / 1e12
@@ -945,6 +910,7 @@ def run_blockwise(args, rank, world, peaks, peak_src):
             "quant_ms_per_launch": timers.total_ms("quant") / timers.count("quant"),
             "gpu_launches": 3 * args.steps, "clocks": clk}
     if rank == 0:
+        line["timing"] = TIMING_NOTE
         print(json.dumps(line))
 
 
@@ -989,27 +955,8 @@ def main():
     wl = DenseFFN()
     stream = torch.cuda.Stream()
 
-    for _ in range(args.warmup):
-        wl.step(stream)
-    torch.cuda.synchronize()
-
-    # --- timed region: exactly K steps ---
-    timers = Timers()
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for _ in range(args.steps):
-        wl.step(stream, timers)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
-    ms_max = max_over_ranks(ms, world)
+    # --- timed region: exactly K steps (then K more with per-kernel spans) ---
+    ms_max, timers, clk = _measure(lambda t: wl.step(stream, t), args, world, stream)
     value = world * args.steps * wl.step_flops() / (ms_max / 1e3) / 1e12
 
     gemm_ms = timers.total_ms("gemm") / args.steps            # fprop + the fused dgrad/wgrad launch
@@ -1073,6 +1020,7 @@ def main():
                                 "sample": "2560x2560 output block of fprop, 2560x2048 of dgrad and wgrad (dense FFN "
                                           "up-proj), with the oracle quantisation of the operand rows it reads"}
     if rank == 0:
+        line["timing"] = TIMING_NOTE
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
