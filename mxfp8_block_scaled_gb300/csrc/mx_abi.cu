@@ -130,6 +130,14 @@ mx_status cuda_status(cudaError_t e, const char* what) {
   return MX_ERR_CUDA;
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* s = std::getenv("MXFP8_PDL");
+    return !(s && *s && std::atoi(s) == 0);
+  }();
+  return on;
+}
+
 uint64_t wait_timeout_ns() {
   // At least 1 ms: the drain after an abort waits for copies and MMAs already
   // in flight (they finish within microseconds) under the same bound.

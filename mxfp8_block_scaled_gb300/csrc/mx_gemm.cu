@@ -586,7 +586,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // Programmatic dependent launch: the next kernel on the stream may be
+  // scheduled from here on; this grid touches global memory only after the
+  // previous kernel has completed (grouped launches read the group offsets
+  // first, dense launches wait after the on-chip setup).
+  pdl_launch_dependents();
   if (KIND != GEMM_DENSE) {
+    pdl_wait();
     if (!setup_groups<KIND>(p, g, s_flag, s_total)) return;
   }
 
@@ -617,6 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  if (KIND == GEMM_DENSE) pdl_wait();
   const uint32_t tmem_base = *s_tmem;
   const int64_t ntiles = num_tiles<BN, KIND>(p, g);
 
@@ -906,8 +913,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t crank = cluster_ctarank();
   const bool leader = crank == 0;
 
-  // Both CTAs of a pair read the same offsets and reach the same verdict.
+  // Programmatic dependent launch, as in mx_gemm_kernel. Both CTAs of a pair
+  // read the same offsets and reach the same verdict.
+  pdl_launch_dependents();
   if (KIND != GEMM_DENSE) {
+    pdl_wait();
     if (!setup_groups<KIND>(p, g, s_flag, s_total, 2 * kBM)) return;
   }
 
@@ -953,6 +963,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   __syncthreads();
   cluster_sync();  // barriers of both CTAs exist before either signals the other
   tc_fence_after_sync();
+  if (KIND == GEMM_DENSE) pdl_wait();
   const uint32_t tmem_base = *s_tmem;
   const int64_t nt = (p.N + BN - 1) / BN;
   int64_t ntiles = (KIND == GEMM_GROUPED_M)
@@ -1275,6 +1286,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 // are two float4 of every unit, and the loads of up to four units are in
 // flight at once.
 __global__ void __launch_bounds__(256) mx_gemm_sk_reduce_kernel(const GParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the partials come from the GEMM launch before this one
   const int64_t nkb = (p.K + kBK - 1) / kBK;
   const int c = blockIdx.x & 15;
   const int crank = (blockIdx.x >> 4) & 1;
@@ -1393,6 +1406,7 @@ __global__ void __launch_bounds__(BwCfg<BN_>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();  // the next kernel on the stream may be scheduled from here on
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -1417,6 +1431,7 @@ __global__ void __launch_bounds__(BwCfg<BN_>::kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  pdl_wait();  // global memory only once the previous kernel on the stream has completed
   const uint32_t tmem_base = *s_tmem;
   const int64_t ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
   const int64_t kbs = (p.K + kBK - 1) / kBK;
@@ -1669,8 +1684,8 @@ mx_status launch_cfg(const GemmLaunch& L, const GParams& p_in, int64_t tiles_upp
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(smem)");
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_upper, sm_count()));
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(ma, mb, mc, p);
-  return cuda_status(cudaGetLastError(), "mx_gemm launch");
+  return cuda_status(launch_kernel(kern, static_cast<unsigned>(grid), kThreads, smem, s, 1, ma, mb, mc, p),
+                     "mx_gemm launch");
 }
 
 // Upper bound of the 256 x 256 pair tiles (rows-ragged: one partial tile per
@@ -1777,28 +1792,15 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
     }
     clusters = pl.clusters;
   }
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  cfg.blockDim = dim3(kPairThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   PairArgs* args = pair_args_scratch();
   std::memset(args, 0, sizeof(PairArgs));
   args->prob[0] = PairProblem{ma, mb, msa, msb, mc, p};
   args->n = 1;
-  st = cuda_status(cudaLaunchKernelEx(&cfg, kern, *args), "mx_gemm launch (CTA pairs)");
-  if (st == MX_OK && p.sk_w > 0) {
-    mx_gemm_sk_reduce_kernel<<<static_cast<unsigned>(32 * pl.tail_tiles), 256, 0, s>>>(p);
-    st = cuda_status(cudaGetLastError(), "mx_gemm split-tail reduction launch");
-  }
+  st = cuda_status(launch_kernel(kern, static_cast<unsigned>(2 * clusters), kPairThreads, smem, s, 2, *args),
+                   "mx_gemm launch (CTA pairs)");
+  if (st == MX_OK && p.sk_w > 0)
+    st = cuda_status(launch_kernel(mx_gemm_sk_reduce_kernel, static_cast<unsigned>(32 * pl.tail_tiles), 256, 0, s, 1, p),
+                     "mx_gemm split-tail reduction launch");
   return st;
 }
 
@@ -1884,8 +1886,9 @@ mx_status launch_blockwise_bn(const GemmLaunch& L, GParams p, cudaStream_t s) {
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(blockwise smem)");
   const int64_t tiles = (L.M + kBM - 1) / kBM * ((L.N + BN - 1) / BN);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count()));
-  kern<<<static_cast<unsigned>(grid), C::kThreads, smem, s>>>(ma, mb, mc, p, L.bw_a_scale, L.bw_b_scale);
-  return cuda_status(cudaGetLastError(), "mx_gemm_fp8_blockwise launch");
+  return cuda_status(launch_kernel(kern, static_cast<unsigned>(grid), C::kThreads, smem, s, 1, ma, mb, mc, p,
+                                   L.bw_a_scale, L.bw_b_scale),
+                     "mx_gemm_fp8_blockwise launch");
 }
 
 // 128 x 256 tiles unless N fits one 128-wide tile.
@@ -2030,20 +2033,8 @@ mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
     const int64_t rr = schedule_round_robin(Ls, n, clusters);
     args->sched = (greedy > 0 && greedy * 100 < rr * 97) ? 1 : 0;
   }
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  cfg.blockDim = dim3(kPairThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, *args), "mx_gemm_multi launch (CTA pairs)");
+  return cuda_status(launch_kernel(kern, static_cast<unsigned>(2 * clusters), kPairThreads, smem, s, 2, *args),
+                     "mx_gemm_multi launch (CTA pairs)");
 }
 
 }  // namespace

@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <cstring>
+#include <utility>
 
 #include "../../include/mxfp8.h"
 
@@ -21,6 +23,44 @@ uint64_t wait_timeout_ns();
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Programmatic dependent launch on (default); MXFP8_PDL=0 turns it off.
+bool pdl_enabled();
+
+// Launches kern on stream s. With programmatic stream serialization the grid
+// may be scheduled while the kernel before it on the stream is finishing; each
+// kernel of this library runs griddepcontrol.wait before its first global
+// memory access, which returns once that previous grid has completed and its
+// writes are visible, and griddepcontrol.launch_dependents at its start.
+// cluster_x > 1 also sets the cluster shape.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                          unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  std::memset(attr, 0, sizeof(attr));
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // --- quantiser -------------------------------------------------------------
 struct QuantLaunch {

@@ -58,6 +58,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Programmatic dependent launch. pdl_launch_dependents lets the next kernel
+// on the stream be scheduled while this grid runs; pdl_wait returns once the
+// previous kernel on the stream has completed and its memory writes are
+// visible to this grid (at once when it was not launched programmatically).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Wait for phase `parity` of `bar` to complete, for at most `timeout_ns`
 // nanoseconds of wall time. Returns false when the limit is reached.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {

@@ -237,6 +237,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 template <bool kRow, bool kCol, bool kGrouped, bool kMulti>
 __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     mx_quant_kernel(const __grid_constant__ QuantArgs qa) {
+  // Programmatic dependent launch: let the next kernel on the stream be
+  // scheduled, and touch global memory only once the previous one completed.
+  pdl_launch_dependents();
+  pdl_wait();
   const QParams& p = qa.p[0];  // grouped and shared fields (status word, bound)
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the unit of the 128-byte swizzle pattern.
@@ -567,6 +571,10 @@ __device__ __forceinline__ uint32_t quant4_f32(float a, float b, float c, float 
 template <bool kRow, bool kCol>
 __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     mx_quant_f32_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams p) {
+  // Programmatic dependent launch: let the next kernel on the stream be
+  // scheduled, and touch global memory only once the previous one completed.
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;                                        // kStages x 2 boxes x [128 rows][128 bytes]
@@ -770,6 +778,10 @@ __device__ __forceinline__ uint32_t blockwise_quad(uint32_t w0, uint32_t w1, flo
 __global__ void __launch_bounds__(256) fp8_quant_1x128_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
                                                               int64_t cols, int64_t ldx, uint8_t* __restrict__ data,
                                                               float* __restrict__ scale) {
+  // Programmatic dependent launch: let the next kernel on the stream be
+  // scheduled, and touch global memory only once the previous one completed.
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int hl = lane & 15;
   const int64_t kbs = cols / 128;
@@ -799,6 +811,10 @@ __global__ void __launch_bounds__(256) fp8_quant_128x128_kernel(const __nv_bfloa
                                                                 int64_t cols, int64_t ldx,
                                                                 uint8_t* __restrict__ data,
                                                                 float* __restrict__ scale) {
+  // Programmatic dependent launch: let the next kernel on the stream be
+  // scheduled, and touch global memory only once the previous one completed.
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t warp_max[8];
   const int tid = threadIdx.x;
   const int64_t kbs = cols / 128;
@@ -866,8 +882,7 @@ mx_status launch_one(const QuantArgs& qa, int64_t tiles_upper, cudaStream_t s) {
   if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   const int64_t grid =
       std::max<int64_t>(1, std::min<int64_t>(tiles_upper, static_cast<int64_t>(std::max(per_sm, 1)) * sm_count()));
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(qa);
-  return cuda_status(cudaGetLastError(), "mx_quantize launch");
+  return cuda_status(launch_kernel(kern, static_cast<unsigned>(grid), kThreads, smem, s, 1, qa), "mx_quantize launch");
 }
 
 template <bool R, bool C>
@@ -881,8 +896,8 @@ mx_status launch_f32_one(const CUtensorMap& map, const QParams& p, int64_t tiles
   if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   const int64_t grid =
       std::max<int64_t>(1, std::min<int64_t>(tiles, static_cast<int64_t>(std::max(per_sm, 1)) * sm_count()));
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(map, p);
-  return cuda_status(cudaGetLastError(), "mx_quantize_f32 launch");
+  return cuda_status(launch_kernel(kern, static_cast<unsigned>(grid), kThreads, smem, s, 1, map, p),
+                     "mx_quantize_f32 launch");
 }
 
 // FP32 input: [batch, rows, cols] through 32-column boxes in the 128-byte swizzle.
@@ -922,14 +937,17 @@ mx_status launch_quantize_blockwise(const void* x, int64_t rows, int64_t cols, i
   if (blocks == 0) return MX_OK;
   if (block == 1) {
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((blocks + 15) / 16, 16LL * sm_count()));
-    fp8_quant_1x128_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, cols, ldx, static_cast<uint8_t*>(data), scale);
+    return cuda_status(launch_kernel(fp8_quant_1x128_kernel, static_cast<unsigned>(grid), 256, 0, s, 1,
+                                     static_cast<const __nv_bfloat16*>(x), rows, cols, ldx,
+                                     static_cast<uint8_t*>(data), scale),
+                       "mx_quantize_fp8_blockwise launch");
   } else {
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(blocks, 8LL * sm_count()));
-    fp8_quant_128x128_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, cols, ldx, static_cast<uint8_t*>(data), scale);
+    return cuda_status(launch_kernel(fp8_quant_128x128_kernel, static_cast<unsigned>(grid), 256, 0, s, 1,
+                                     static_cast<const __nv_bfloat16*>(x), rows, cols, ldx,
+                                     static_cast<uint8_t*>(data), scale),
+                       "mx_quantize_fp8_blockwise launch");
   }
-  return cuda_status(cudaGetLastError(), "mx_quantize_fp8_blockwise launch");
 }
 
 namespace {
