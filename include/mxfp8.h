@@ -18,7 +18,11 @@
  *   (mx_gemm_workspace_bytes). No state is kept between calls.
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *   void*; NULL is the legacy default stream) on the current device, which must
- *   be an sm_103 GPU. Nothing is synchronised.
+ *   be an sm_103 GPU. Nothing is synchronised. Kernels are launched with
+ *   programmatic stream serialization: one may be scheduled while the kernel
+ *   before it on the stream finishes, but it reads and writes memory only once
+ *   that kernel has completed, so stream order is what the caller sees
+ *   (environment MXFP8_PDL=0 launches without it).
  * - Every call validates its arguments on the host first; on failure it
  *   returns a non-OK status and launches nothing. There is no fallback to any
  *   other kernel or precision ([DSV3] §13.4 and §15: a failure must be raised,
