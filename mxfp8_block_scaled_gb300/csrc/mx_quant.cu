@@ -256,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   __shared__ int32_t s_bad;
   __shared__ int32_t s_total_tiles;
   __shared__ volatile int32_t s_abort;
+  // Each stage's tile geometry (and tensor, several tensors per launch), written
+  // by the producer before its arrival on the stage's full barrier.
+  __shared__ TileGeo s_geo[kStages];
+  __shared__ int32_t s_geo_ti[kStages];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -332,7 +336,9 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
             kGrouped ? tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile)
                      : tile_geo<kGrouped>(pt, t - qa.tile0[ti], (pt.cols + kTileCols - 1) / kTileCols,
                                           (pt.rows + kTileRows - 1) / kTileRows, g_off, g_tile);
-        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        s_geo[s] = g;
+        s_geo_ti[s] = ti;
+        mbar_arrive_expect_tx(&full[s], kTileBytes);  // releases the two words above with the stage
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           tma_load_3d(tiles + s * kTileBytes + h * (kTileBytes / 2), &qa.map[ti], &full[s],
@@ -352,17 +358,21 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   } else {
     // ----------------------------------------------------------- consumers
     int j = 0;
-    int ti = 0;  // tensor of tile t (t only grows)
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
       const int s = j % kStages;
       const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
-      if constexpr (kMulti)
-        while (t >= qa.tile0[ti + 1]) ++ti;
+      // Every consumer runs every iteration (and every consumers_sync) even
+      // after an abort, so the named barrier can never strand a warp.
+      const bool ok = !s_abort && wait_or_abort(&full[s], ph, qa.p[0], &s_abort);
+      // The tile's geometry and tensor as the producer published them with
+      // the stage; read before this thread releases the stage.
+      TileGeo g{};
+      int ti = 0;
+      if (ok) {
+        g = s_geo[s];
+        if constexpr (kMulti) ti = s_geo_ti[s];
+      }
       const QParams& p = qa.p[ti];
-      const TileGeo g =
-          kGrouped ? tile_geo<kGrouped>(p, t, col_tiles, row_tiles, g_off, g_tile)
-                   : tile_geo<kGrouped>(p, t - qa.tile0[ti], (p.cols + kTileCols - 1) / kTileCols,
-                                        (p.rows + kTileRows - 1) / kTileRows, g_off, g_tile);
       uint8_t* const row_data = p.row_data + g.b * p.row_data_bs;
       uint8_t* const row_scale = p.row_scale + g.b * p.row_scale_bs;
       uint8_t* const col_data = p.col_data + g.b * p.col_data_bs;
@@ -370,9 +380,6 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
       const uint32_t* tile = reinterpret_cast<const uint32_t*>(tiles + s * kTileBytes);
       const uint4* tile16 = reinterpret_cast<const uint4*>(tiles + s * kTileBytes);
       uint8_t* csc = col_sc + (j & 1) * 512;
-      // Every consumer runs every iteration (and every consumers_sync) even
-      // after an abort, so the named barrier can never strand a warp.
-      const bool ok = !s_abort && wait_or_abort(&full[s], ph, p, &s_abort);
 
       if (kRow && ok) {
         // ---- row copy: one thread per 1x32 block; lanes 8b..8b+7 take block b
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
 #pragma unroll
           for (int i = 0; i < 32; ++i) w[i] = src[i * 32 + ((cc ^ (i & 7)) << 2)];
           mbar_arrive(&empty[s]);  // this thread is done with the tile
-          if (kGrouped) {
+          if (kGrouped && g.valid_rows < kTileRows) {
             // rows past the group's end hold the next group's data: they count as zero padding
 #pragma unroll
             for (int i = 0; i < 32; ++i)
