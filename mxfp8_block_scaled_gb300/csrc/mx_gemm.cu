@@ -1286,8 +1286,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 // are two float4 of every unit, and the loads of up to four units are in
 // flight at once.
 __global__ void __launch_bounds__(256) mx_gemm_sk_reduce_kernel(const GParams p) {
-  pdl_launch_dependents();
-  pdl_wait();  // the partials come from the GEMM launch before this one
+  // The partials come from the GEMM launch before this one; the next kernel is
+  // let in once this CTA's stores are issued (as in the blockwise GEMM).
+  pdl_wait();
   const int64_t nkb = (p.K + kBK - 1) / kBK;
   const int c = blockIdx.x & 15;
   const int crank = (blockIdx.x >> 4) & 1;
@@ -1344,6 +1345,7 @@ __global__ void __launch_bounds__(256) mx_gemm_sk_reduce_kernel(const GParams p)
         if (col + e < p.n_out) reinterpret_cast<uint16_t*>(dst)[e] = static_cast<uint16_t>(wv[e >> 1] >> ((e & 1) * 16));
     }
   }
+  pdl_launch_dependents();
 }
 
 // ===========================================================================
@@ -1406,7 +1408,6 @@ __global__ void __launch_bounds__(BwCfg<BN_>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  pdl_launch_dependents();  // the next kernel on the stream may be scheduled from here on
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -1431,7 +1432,12 @@ __global__ void __launch_bounds__(BwCfg<BN_>::kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  pdl_wait();  // global memory only once the previous kernel on the stream has completed
+  // Programmatic dependent launch: global memory only once the previous
+  // kernel on the stream has completed. The next kernel is let in only after
+  // this CTA's tiles (below): the registers and shared memory this kernel
+  // leaves free hold a small CTA, and one waiting there would take issue
+  // slots from the promotion.
+  pdl_wait();
   const uint32_t tmem_base = *s_tmem;
   const int64_t ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
   const int64_t kbs = (p.K + kBK - 1) / kBK;
@@ -1577,6 +1583,7 @@ __global__ void __launch_bounds__(BwCfg<BN_>::kThreads, 1)
     __syncwarp();
   }
 
+  pdl_launch_dependents();  // this CTA's tiles are done
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {

@@ -785,9 +785,10 @@ __device__ __forceinline__ uint32_t blockwise_quad(uint32_t w0, uint32_t w1, flo
 __global__ void __launch_bounds__(256) fp8_quant_1x128_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
                                                               int64_t cols, int64_t ldx, uint8_t* __restrict__ data,
                                                               float* __restrict__ scale) {
-  // Programmatic dependent launch: let the next kernel on the stream be
-  // scheduled, and touch global memory only once the previous one completed.
-  pdl_launch_dependents();
+  // Programmatic dependent launch: touch global memory only once the previous
+  // kernel on the stream has completed; let the next one be scheduled once
+  // this CTA's work is done (its small CTAs waiting beside a running grid
+  // would take issue slots from it).
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int hl = lane & 15;
@@ -811,6 +812,7 @@ __global__ void __launch_bounds__(256) fp8_quant_1x128_kernel(const __nv_bfloat1
       if (hl == 0) scale[kb * rows + r] = s;
     }
   }
+  pdl_launch_dependents();
 }
 
 // 128 x 128 blocks: one CTA per block; thread t holds 64 elements of row t/2.
@@ -818,10 +820,7 @@ __global__ void __launch_bounds__(256) fp8_quant_128x128_kernel(const __nv_bfloa
                                                                 int64_t cols, int64_t ldx,
                                                                 uint8_t* __restrict__ data,
                                                                 float* __restrict__ scale) {
-  // Programmatic dependent launch: let the next kernel on the stream be
-  // scheduled, and touch global memory only once the previous one completed.
-  pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait();  // as in fp8_quant_1x128_kernel
   __shared__ uint32_t warp_max[8];
   const int tid = threadIdx.x;
   const int64_t kbs = cols / 128;
@@ -857,6 +856,7 @@ __global__ void __launch_bounds__(256) fp8_quant_128x128_kernel(const __nv_bfloa
     }
     if (tid == 0) scale[rb * kbs + kb] = s;
   }
+  pdl_launch_dependents();
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
