@@ -13,9 +13,12 @@
  * ---------------------------------------
  * - All pointers named *_data, *_scale, x, c, workspace and group_offsets are
  *   DEVICE pointers, allocated and owned by the caller. The library never
- *   allocates, frees or keeps device memory: the one scratch buffer any call
- *   can use (mx_gemm_with_workspace) is the caller's, sized by a query
- *   (mx_gemm_workspace_bytes). No state is kept between calls.
+ *   allocates or frees device memory. Scratch memory is the caller's buffer
+ *   (mx_gemm_with_workspace, sized by mx_gemm_workspace_bytes), except for
+ *   mx_gemm_static_workspace, whose scratch is one fixed array of
+ *   MX_STATIC_WORKSPACE_BYTES that the library declares in device memory
+ *   (held on every device that loads the library's kernels). No other state
+ *   is kept between calls.
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *   void*; NULL is the legacy default stream) on the current device, which must
  *   be an sm_103 GPU. Nothing is synchronised. Kernels are launched with
@@ -269,6 +272,44 @@ mx_status mx_gemm(int mode, const mx_operand* a, const mx_operand* b, void* c, i
 mx_status mx_gemm_workspace_bytes(int mode, const mx_operand* a, const mx_operand* b, size_t* bytes);
 mx_status mx_gemm_with_workspace(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,
                                  void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
+/*
+ * mx_gemm_static_workspace - mx_gemm_with_workspace for callers that must not
+ * allocate device memory at all: not through cudaMalloc, not through a
+ * framework's caching allocator, not by asking the caller for a buffer. Such
+ * callers include code that runs inside a memory allocator's own callbacks
+ * (allocating there would re-enter the allocator), runtimes that reserve all
+ * of their device memory once at start-up and forbid allocation afterwards
+ * (a later allocation can fail or fragment the reservation, and cudaFree
+ * can synchronise the whole device), and plug-ins that receive only their
+ * input and output buffers from a host application. (The pages have no
+ * counterpart of this call: it is a property of this library's interface,
+ * not of the method.)
+ *
+ * The split tail's scratch lives in one array of MX_STATIC_WORKSPACE_BYTES
+ * bytes that the library declares in device memory. Each GPU that loads the
+ * library's kernels holds that array until the process exits, whether or not
+ * this call is used. The first call on a device looks up the array's device
+ * address (a runtime query, no allocation) and caches it; make that first
+ * call before any stream capture on the device.
+ *
+ *   Arguments, results, layouts and errors are exactly mx_gemm's, and the
+ *   output equals mx_gemm_with_workspace's with a large enough caller
+ *   workspace, bit for bit.
+ *   A GEMM whose split tail would need more than MX_STATIC_WORKSPACE_BYTES
+ *   (mx_gemm_workspace_bytes reports the need) is rejected with
+ *   MX_ERR_UNSUPPORTED_SHAPE before anything is launched; on a GB300 (76 SM
+ *   pairs) no GEMM needs more than 38 MiB.
+ *   The array needs no clearing: a split GEMM writes every partial it reads
+ *   back in the same call. But every call shares the one array and it keeps
+ *   the last call's contents: two calls whose work overlaps on the GPU (on
+ *   two streams, or two host threads) race on it and give wrong results.
+ *   Order such calls on one stream, or use mx_gemm_with_workspace with a
+ *   buffer per stream.
+ */
+#define MX_STATIC_WORKSPACE_BYTES (40u * 1024u * 1024u)
+mx_status mx_gemm_static_workspace(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,
+                                   int* dev_status, void* stream);
 
 /* One GEMM of an mx_gemm_multi call: the arguments of mx_gemm. */
 typedef struct mx_gemm_problem {

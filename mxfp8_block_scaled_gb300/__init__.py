@@ -34,7 +34,9 @@ EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quant
             "mx_quantize_multi",
             "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_quantize_fp8_blockwise",
             "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version",
-            "mx_selftest_wait_timeout", "mx_gemm_workspace_bytes", "mx_gemm_with_workspace", "mx_gemm_multi")
+            "mx_selftest_wait_timeout", "mx_gemm_workspace_bytes", "mx_gemm_with_workspace", "mx_gemm_multi",
+            "mx_gemm_static_workspace")
+MX_STATIC_WORKSPACE_BYTES = 40 * 1024 * 1024
 
 
 class MXError(RuntimeError):
@@ -92,6 +94,9 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm_with_workspace.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp,
                                          ctypes.c_size_t, vp, vp]
     L.mx_gemm_with_workspace.restype = i32
+    L.mx_gemm_static_workspace.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64,
+                                           vp, vp]
+    L.mx_gemm_static_workspace.restype = i32
     L.mx_gemm_multi.argtypes = [ctypes.POINTER(MXGemmProblemC), i32, vp, vp]
     L.mx_gemm_multi.restype = i32
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
@@ -203,6 +208,11 @@ def mx_gemm_with_workspace(mode, a: MXOperandC, b: MXOperandC, c, ldc, workspace
                            stream) -> None:
     _check(lib().mx_gemm_with_workspace(mode, _ref(a), _ref(b), c, ldc, workspace, workspace_bytes, dev_status,
                                         stream), "mx_gemm_with_workspace")
+
+
+def mx_gemm_static_workspace(mode, a: MXOperandC, b: MXOperandC, c, ldc, dev_status, stream) -> None:
+    _check(lib().mx_gemm_static_workspace(mode, _ref(a), _ref(b), c, ldc, dev_status, stream),
+           "mx_gemm_static_workspace")
 
 
 def mx_gemm_multi(problems, dev_status, stream) -> None:

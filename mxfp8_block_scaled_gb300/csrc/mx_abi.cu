@@ -564,6 +564,30 @@ mx_status mx_gemm_with_workspace(int mode, const mx_operand* a, const mx_operand
   return dense_gemm_run(L, stream);
 }
 
+mx_status mx_gemm_static_workspace(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc,
+                                   int* dev_status, void* stream) {
+  GemmLaunch L;
+  mx_status st = dense_gemm_setup("mx_gemm_static_workspace", mode, a, b, c, ldc, dev_status, true, &L);
+  if (st != MX_OK) return st;
+  if (L.M == 0 || L.N == 0) return MX_OK;
+  st = check_device();
+  if (st != MX_OK) return st;
+  if (L.K > 0) {
+    const size_t need = gemm_workspace_bytes(L);
+    if (need > MX_STATIC_WORKSPACE_BYTES) {
+      set_error("mx_gemm_static_workspace: this GEMM needs %zu bytes of scratch, more than the %zu bytes of the "
+                "static workspace; use mx_gemm_with_workspace with a caller buffer",
+                need, static_cast<size_t>(MX_STATIC_WORKSPACE_BYTES));
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (need > 0) {
+      st = static_workspace(&L.ws, &L.ws_bytes);
+      if (st != MX_OK) return st;
+    }
+  }
+  return dense_gemm_run(L, stream);
+}
+
 mx_status mx_gemm_multi(const mx_gemm_problem* problems, int n, int* dev_status, void* stream) {
   if (n < 0 || n > MX_MAX_GEMM_MULTI) {
     set_error("mx_gemm_multi: n = %d is outside 0 .. %d", n, MX_MAX_GEMM_MULTI);

@@ -1905,6 +1905,36 @@ mx_status launch_blockwise(const GemmLaunch& L, GParams p, cudaStream_t s) {
 
 }  // namespace
 
+// Scratch memory of mx_gemm_static_workspace: a fixed array in device memory,
+// reserved when the library's kernels are loaded on a device and held until
+// the process exits, for callers that may not allocate. Every call uses the
+// same array.
+static __device__ __align__(256) float g_static_ws[MX_STATIC_WORKSPACE_BYTES / sizeof(float)];
+
+mx_status static_workspace(void** ptr, size_t* bytes) {
+  // Host code cannot use g_static_ws's name as a device address: the address
+  // comes from the runtime, once per device, with that device current.
+  static std::mutex mu;
+  static void* cache[64] = {nullptr};
+  int dev = 0;
+  mx_status st = cuda_status(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != MX_OK) return st;
+  if (dev < 0 || dev >= 64) {
+    set_error("device ordinal %d is outside the static workspace table", dev);
+    return MX_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    st = cuda_status(cudaGetSymbolAddress(&p, g_static_ws), "cudaGetSymbolAddress(static workspace)");
+    if (st != MX_OK) return st;
+    cache[dev] = p;
+  }
+  *ptr = cache[dev];
+  *bytes = MX_STATIC_WORKSPACE_BYTES;
+  return MX_OK;
+}
+
 size_t gemm_workspace_bytes(const GemmLaunch& L) {
   if (L.kind != GEMM_DENSE || L.swiglu || L.bw_a_scale || L.M == 0 || L.N == 0 || L.K == 0) return 0;
   GemmLaunch q = L;

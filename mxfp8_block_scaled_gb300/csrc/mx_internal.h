@@ -120,6 +120,9 @@ struct GemmLaunch {
 mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // Bytes of workspace the dense GEMM L would use for its split tail (0: none).
 size_t gemm_workspace_bytes(const GemmLaunch& L);
+// Device address and size of the library's static scratch array on the
+// current device (looked up on the first call per device).
+mx_status static_workspace(void** ptr, size_t* bytes);
 // Up to MX_MAX_GEMM_MULTI independent dense GEMMs; one launch of the pair
 // kernel when they fill the GPU together, else one launch each.
 mx_status launch_gemm_multi(const GemmLaunch* Ls, int n, cudaStream_t s);
