@@ -30,6 +30,18 @@
  *   returns a non-OK status and launches nothing. There is no fallback to any
  *   other kernel or precision ([DSV3] §13.4 and §15: a failure must be raised,
  *   never replaced by a high-precision GEMM).
+ * - Grouped calls (mx_quantize with group offsets, mx_grouped_gemm,
+ *   mx_grouped_gemm_swiglu) take at most MX_MAX_GROUPS groups; more is
+ *   MX_ERR_UNSUPPORTED_SHAPE on the host, before anything is launched. (The
+ *   kernels keep every group's offsets in shared memory beside the operand
+ *   pipeline.)
+ * - Environment: MXFP8_PDL=0 launches without programmatic dependent launch;
+ *   MXFP8_WAIT_TIMEOUT_NS bounds every device-side wait (default 2 s, at
+ *   least 1 ms). Nothing else in the environment changes what the library
+ *   does. (A library built with MXFP8_DISPATCH_OVERRIDES defined, for
+ *   measurements only, also reads MXFP8_GEMM_PAIR, MXFP8_GEMM_BN,
+ *   MXFP8_GEMM_SPLIT and MXFP8_GEMM_SCHEDULE to force a GEMM configuration;
+ *   the default build ignores them.)
  * - `dev_status` (device int*, may be NULL): checks that only the device can
  *   make (group offsets) and bounded waits that expire write a non-zero
  *   mx_status value there; the kernels never trap. The caller zeroes it
@@ -73,6 +85,9 @@ extern "C" {
 #endif
 
 #define MXFP8_ABI_VERSION 1
+
+/* Largest n_groups of the grouped calls (see the conventions above). */
+#define MX_MAX_GROUPS 512
 
 typedef enum mx_status {
   MX_OK = 0,
@@ -141,7 +156,7 @@ int64_t mx_grouped_padded_rows(const int64_t* host_offsets, int n_groups);
  *            (pitch col_capacity bytes). col_scale holds
  *            mx_scale_bytes(cols, col_capacity) bytes. col_capacity must be a
  *            multiple of 128 and >= the padded total; columns beyond the padded
- *            total are not written. Bad offsets or too small a capacity are
+ *            total are not written. 1 <= n_groups <= MX_MAX_GROUPS. Bad offsets or too small a capacity are
  *            reported as MX_ERR_DEVICE_CHECK through dev_status and nothing is
  *            written. The row copy is unaffected by groups.
  *   All outputs 16-byte aligned. Unused outputs may be NULL.
@@ -345,7 +360,8 @@ mx_status mx_gemm_multi(const mx_gemm_problem* problems, int n, int* dev_status,
  * mx_grouped_gemm - per-expert block-scaled GEMMs over contiguous token ranges
  * ([DSV3] §5.2 routed experts and §13.4 low_precision_grouped_matmul with
  * group_list; [TT] npu_grouped_matmul). group_offsets is the int64 device array
- * described for mx_quantize. Empty and uneven groups are allowed ([DSV3] §16.3).
+ * described for mx_quantize. Empty and uneven groups are allowed ([DSV3] §16.3);
+ * 1 <= n_groups <= MX_MAX_GROUPS.
  *
  *   MX_FPROP / MX_DGRAD (rows ragged): a = [M_total, K] row copy whose rows are
  *     grouped by expert; b = stacked per-expert copies: expert e's rows start at
@@ -405,7 +421,8 @@ mx_status mx_gemm_fp8_blockwise(const void* a_data, const float* a_scale, int64_
  *   c       BF16 [M_total, F], row pitch ldc: c[i, f] = silu(g) * u with
  *           g = (A . B_e^T)[i, f], u = (A . B_e^T)[i, F + f], e the expert of row
  *           i, silu(x) = x / (1 + exp(-x)).
- *   Groups, validation, empty experts and errors as mx_grouped_gemm.
+ *   Groups (at most MX_MAX_GROUPS), validation, empty experts and errors as
+ *   mx_grouped_gemm.
  */
 mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
                                  int n_groups, void* c, int64_t ldc, int* dev_status, void* stream);

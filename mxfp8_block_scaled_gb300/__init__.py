@@ -26,6 +26,7 @@ MX_ROWWISE, MX_COLWISE, MX_BOTH = 1, 2, 3
 MX_FPROP, MX_DGRAD, MX_WGRAD = 0, 1, 2
 MX_MAX_MULTI = 8
 MX_MAX_GEMM_MULTI = 4
+MX_MAX_GROUPS = 512
 STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_SHAPE", 3: "MX_ERR_ALIGNMENT",
                 4: "MX_ERR_CUDA", 5: "MX_ERR_DEVICE_CHECK", 6: "MX_ERR_TIMEOUT", 7: "MX_ERR_NO_DEVICE"}
 

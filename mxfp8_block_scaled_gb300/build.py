@@ -23,6 +23,10 @@ LIB_NAME = "libmxfp8_gb300.so"
 SOURCES = ("mx_abi.cu", "mx_quant.cu", "mx_gemm.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v"] + ARCH
+# MXFP8_DISPATCH_OVERRIDES=1 at build time: a measurement build whose GEMM
+# dispatch reads MXFP8_GEMM_PAIR / _BN / _SPLIT / _SCHEDULE from the environment.
+if os.environ.get("MXFP8_DISPATCH_OVERRIDES", "") == "1":
+    NVCC_FLAGS.append("-DMXFP8_DISPATCH_OVERRIDES")
 
 
 def nvcc() -> str:

@@ -345,6 +345,10 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, in
       set_error("mx_quantize: n_groups must be >= 1");
       return MX_ERR_INVALID_ARG;
     }
+    if (n_groups > MX_MAX_GROUPS) {
+      set_error("mx_quantize: n_groups = %d is above MX_MAX_GROUPS (%d)", n_groups, MX_MAX_GROUPS);
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
     if (col_capacity < 0 || col_capacity % 128 != 0) {
       set_error("mx_quantize: col_capacity must be a non-negative multiple of 128");
       return MX_ERR_UNSUPPORTED_SHAPE;
@@ -728,6 +732,10 @@ mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const
     set_error("mx_grouped_gemm_swiglu: group_offsets must be non-null and n_groups >= 1");
     return MX_ERR_INVALID_ARG;
   }
+  if (n_groups > MX_MAX_GROUPS) {
+    set_error("mx_grouped_gemm_swiglu: n_groups = %d is above MX_MAX_GROUPS (%d)", n_groups, MX_MAX_GROUPS);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
   if (a->k != b->k) {
     set_error("mx_grouped_gemm_swiglu: a.k != b.k");
     return MX_ERR_INVALID_ARG;
@@ -780,6 +788,10 @@ mx_status mx_grouped_gemm(int mode, const mx_operand* a, const mx_operand* b, co
   if (!group_offsets || n_groups < 1) {
     set_error("mx_grouped_gemm: group_offsets must be non-null and n_groups >= 1");
     return MX_ERR_INVALID_ARG;
+  }
+  if (n_groups > MX_MAX_GROUPS) {
+    set_error("mx_grouped_gemm: n_groups = %d is above MX_MAX_GROUPS (%d)", n_groups, MX_MAX_GROUPS);
+    return MX_ERR_UNSUPPORTED_SHAPE;
   }
   if (a->k != b->k) {
     set_error("mx_grouped_gemm: a.k != b.k");

@@ -77,7 +77,7 @@ constexpr int kCopierWarp = 10;
 constexpr int kPairThreads = 384;  // the pair kernel adds a scale-gather warp
 constexpr int kGatherWarp = 11;
 constexpr int kEpiThreads = 256;
-constexpr int kMaxGroups = 512;
+constexpr int kMaxGroups = MX_MAX_GROUPS;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiWarpBytes = 32 * 64;  // one 32-row x 32-column BF16 box per epilogue warp
 constexpr int kEpiBytes = 8 * kEpiWarpBytes;
@@ -1811,9 +1811,18 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   return st;
 }
 
+// Dispatch overrides (MXFP8_GEMM_PAIR, _BN, _SPLIT, _SCHEDULE) for measuring
+// one configuration against another. They exist only in a library built with
+// MXFP8_DISPATCH_OVERRIDES defined; the default build ignores the environment
+// here, so a stray variable cannot change which kernel runs.
 int env_int(const char* name, int dflt) {
+#ifdef MXFP8_DISPATCH_OVERRIDES
   const char* v = std::getenv(name);
   return (v && *v) ? std::atoi(v) : dflt;
+#else
+  (void)name;
+  return dflt;
+#endif
 }
 
 // Dense tile configurations and their estimated time: rounds of tiles over

@@ -51,7 +51,7 @@ constexpr int kThreads = kConsumers + 32;     // plus one producer warp
 #define MX_QUANT_STAGES 2
 #endif
 constexpr int kStages = MX_QUANT_STAGES;
-constexpr int kMaxGroups = 1024;
+constexpr int kMaxGroups = MX_MAX_GROUPS;
 constexpr int kTileBytes = kTileRows * kTileCols * 2;
 constexpr int kHalfCols = 64;  // columns of one swizzled TMA box (128 bytes per row)
 // 1: the column copy of a tile goes through a shared-memory staging buffer

@@ -160,6 +160,22 @@ def test_grouped_gemm_rejects_bad_arguments_on_host(L):
                       None, None) == SHAPE
 
 
+def test_group_limit_rejected_on_host(L):
+    """n_groups above MX_MAX_GROUPS (512) is MX_ERR_UNSUPPORTED_SHAPE from every
+    grouped call, decided on the host: the pointers here are not device memory
+    and no GPU exists, so a launch or a device read could not have happened."""
+    g, c, x = 0x8000, 0x4000, 0x10000
+    assert mx.MX_MAX_GROUPS == 512
+    for n in (513, 1024):
+        assert _status_of(mx.mx_grouped_gemm, mx.MX_FPROP, _op(), _op(), g, n, c, 128, None, None) == SHAPE
+        assert _status_of(mx.mx_grouped_gemm, mx.MX_WGRAD, _op(orient=mx.MX_COLWISE, k=256),
+                          _op(orient=mx.MX_COLWISE, k=256), g, n, c, 128, None, None) == SHAPE
+        assert _status_of(mx.mx_grouped_gemm_swiglu, _op(), _op(rows=256), g, n, c, 128, None, None) == SHAPE
+        assert _status_of(mx.mx_quantize, x, 64, 64, 64, 2, None, None, 0x1000, 0x2000, g, n, 128, None,
+                          None) == SHAPE
+        assert "MX_MAX_GROUPS" in mx.mx_last_error()
+
+
 def test_quantize_rejects_bad_arguments_on_host(L):
     x = 0x10000
     assert _status_of(mx.mx_quantize, x, 64, 64, 64, 0, 0x1000, 0x2000, None, None, None, 0, 0, None, None) == INVALID
