@@ -11,6 +11,16 @@ import mxfp8_block_scaled_gb300 as mx
 
 needs_gpu = pytest.mark.gpu
 
+# Error reports of every GEMM parity check of the session (what, report); the
+# conftest prints them at the end of the run, including the count of entries
+# that would fail the bound measured against BF16(ref) (reported, not gated).
+REPORTS: list = []
+
+
+def _record(what: str, rep: dict) -> dict:
+    REPORTS.append((what, rep))
+    return rep
+
 
 def bits(t: torch.Tensor) -> np.ndarray:
     """BF16 tensor -> uint16 bit patterns (numpy)."""
@@ -62,7 +72,7 @@ def check_gemm_full(out_gpu: torch.Tensor, a_codes, a_scale, b_codes, b_scale, w
         rep = oracle.error_report(out, ref, S)
         raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} outside tolerance; first "
                              f"{[(tuple(i), out[tuple(i)], ref[tuple(i)]) for i in bad]}; {rep}")
-    return oracle.error_report(out, ref, S)
+    return _record(what, oracle.error_report(out, ref, S))
 
 
 def logical_scales(t: "mx.MXTensor") -> np.ndarray:
@@ -109,4 +119,56 @@ def check_gemm_sampled(out_gpu: torch.Tensor, a_src, a_orient: int, b_src, b_ori
         bad = np.flatnonzero(~ok)[:8]
         raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} sampled entries outside tolerance; "
                              f"first {[(int(ii[b]), int(jj[b]), out[b], ref[b]) for b in bad]}")
-    return oracle.error_report(out, ref, S)
+    return _record(what, oracle.error_report(out, ref, S))
+
+
+def check_values(out, ref, S, what: str) -> dict:
+    """Element-wise acceptance of already computed oracle values; records the report."""
+    out = np.asarray(out, dtype=np.float64)
+    ok = oracle.within_tolerance(out, ref, S)
+    if not ok.all():
+        bad = np.flatnonzero(~ok.reshape(-1))[:8]
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} outside tolerance; first "
+                             f"{[(int(b), out.reshape(-1)[b], ref.reshape(-1)[b]) for b in bad]}")
+    return _record(what, oracle.error_report(out, ref, S))
+
+
+# ---------------------------------------------------------------------------
+# Full-tensor quantisation parity at workload sizes (oracle run over the host
+# cores by tests.oracle_pool; every data byte and every scale byte, padding
+# included)
+# ---------------------------------------------------------------------------
+
+def check_row_copy_full(x_cpu: torch.Tensor, row: "mx.MXTensor", what: str = "row"):
+    from tests import oracle_pool
+    d, s = oracle_pool.rowwise(bits(x_cpu))
+    assert_bytes_equal(u8(row.data), d, what + " data")
+    assert_bytes_equal(u8(row.scale), oracle.mx_scale_swizzle(s), what + " scales")
+
+
+def check_col_copy_full(x_cpu: torch.Tensor, col: "mx.MXTensor", what: str = "col"):
+    from tests import oracle_pool
+    d, s = oracle_pool.colwise(bits(x_cpu))
+    assert_bytes_equal(u8(col.data), d, what + " data")
+    assert_bytes_equal(u8(col.scale), oracle.mx_scale_swizzle(s), what + " scales")
+
+
+def check_grouped_col_copy_full(x_cpu: torch.Tensor, offsets, col: "mx.MXTensor", what: str = "grouped col"):
+    """The per-group padded column copy [D, capacity] (capacity = padded total)."""
+    from tests import oracle_pool
+    d, s = oracle_pool.colwise_grouped(bits(x_cpu), offsets)
+    assert col.k == d.shape[1], (what, col.k, d.shape)
+    assert_bytes_equal(u8(col.data), d, what + " data")
+    assert_bytes_equal(u8(col.scale), oracle.mx_scale_swizzle(s), what + " scales")
+
+
+def check_stacked_full(w_cpu: torch.Tensor, row: "mx.MXStacked", col: "mx.MXStacked", what: str = "stacked"):
+    """Row and column copies of every matrix of stacked weights [E, N, K]."""
+    from tests import oracle_pool
+    rd, rs, cd, cs = oracle_pool.stacked(bits(w_cpu))
+    assert_bytes_equal(u8(row.data), rd, what + " row data")
+    assert_bytes_equal(u8(col.data), cd, what + " col data")
+    gr, gc = u8(row.scale), u8(col.scale)
+    for e in range(rd.shape[0]):
+        assert_bytes_equal(gr[e], oracle.mx_scale_swizzle(rs[e]), f"{what} row scales, expert {e}")
+        assert_bytes_equal(gc[e], oracle.mx_scale_swizzle(cs[e]), f"{what} col scales, expert {e}")

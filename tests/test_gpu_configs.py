@@ -1,8 +1,12 @@
 """Parity at the full workload sizes, in the launch configuration bench.py
-times: quantisation bit-exact (full tensors where the oracle is quick, else
-sampled rows and columns including every tile boundary) and GEMM outputs on
-sampled entries (seeded random entries plus both sides of every tile
-boundary), each computed by the oracle straight from the BF16 inputs."""
+times.
+
+Quantisation is checked bit for bit on every element and every scale byte
+(padding included) of every tensor each workload quantises: the oracle runs
+over the host cores in row or column slabs (tests.oracle_pool), straight from
+the BF16 inputs. GEMM outputs are checked on sampled entries (seeded random
+entries plus both sides of every tile boundary), each computed by the oracle
+from the BF16 inputs, within |out - ref| <= 2^-8 |ref| + 1e-6 S."""
 import numpy as np
 import pytest
 import torch
@@ -10,41 +14,33 @@ import torch
 import oracle
 import workloads
 import mxfp8_block_scaled_gb300 as mx
-from tests.gpu_util import (assert_bytes_equal, check_col_copy, check_gemm_sampled, check_row_copy, f64,
-                            sample_entries, u8)
+from tests.gpu_util import (check_col_copy_full, check_gemm_sampled, check_grouped_col_copy_full,
+                            check_row_copy_full, check_stacked_full, check_values, f64, sample_entries)
 
 pytestmark = pytest.mark.gpu
 
 
-def quant_both(xb_cpu):
+def quant_multi(xs_cpu):
+    """Both copies of each tensor, the tensors in one launch (as the bench step does)."""
     st = mx.new_status()
-    x = xb_cpu.cuda()
-    row, col = mx.quantize(x, mx.MX_BOTH, status=st)
+    outs = mx.quantize_multi([x.cuda() for x in xs_cpu], mx.MX_BOTH, status=st)
     torch.cuda.synchronize()
     assert mx.read_status(st) == 0
-    return row, col
+    return outs
 
 
-def boundary_rows(n, seed, k=256, tile=128):
-    g = np.random.Generator(np.random.Philox(seed))
-    b = {min(n - 1, t + d) for t in range(0, n, tile) for d in (0, tile - 1)} | {n - 1}
-    return np.unique(np.concatenate([g.integers(0, n, k), np.array(sorted(b))]))
+def check_both_full(x_cpu, q, what):
+    check_row_copy_full(x_cpu, q[0], what + " row")
+    check_col_copy_full(x_cpu, q[1], what + " col")
 
 
-def check_rows_sampled(x_cpu, row, rows, what):
-    """Selected rows of a row copy (data and logical scales) against the oracle."""
-    d, s = oracle.mx_quantize_rowwise(f64(x_cpu[torch.from_numpy(rows)]))
-    assert_bytes_equal(u8(row.data)[rows], d, what + " data")
-    gs = oracle.mx_scale_unswizzle(u8(row.scale), row.rows, row.k // 32)[rows]
-    assert_bytes_equal(gs, s, what + " scales")
-
-
-def check_cols_sampled(x_cpu, col, cols, what):
-    """Selected columns of the source through its column copy."""
-    d, s = oracle.mx_quantize_colwise(f64(x_cpu[:, torch.from_numpy(cols)]))
-    assert_bytes_equal(u8(col.data)[cols], d, what + " data")
-    gs = oracle.mx_scale_unswizzle(u8(col.scale), col.rows, col.k // 32)[cols]
-    assert_bytes_equal(gs, s, what + " scales")
+def backward_in_one_launch(dr, wc, dc, xc):
+    """dgrad and wgrad of one layer in one mx_gemm_multi launch (the bench's backward)."""
+    st = mx.new_status()
+    dx, dw = mx.gemm_multi([(mx.MX_DGRAD, dr, wc), (mx.MX_WGRAD, dc, xc)], status=st)
+    torch.cuda.synchronize()
+    assert mx.read_status(st) == 0
+    return dx, dw
 
 
 # ---------------------------------------------------------------------------
@@ -54,18 +50,15 @@ def check_cols_sampled(x_cpu, col, cols, what):
 @pytest.fixture(scope="module")
 def ffn():
     d = workloads.dense_ffn()
-    q = {k: quant_both(d[k]) for k in ("X", "W", "dY")}
-    return d, q
+    qx, qw = quant_multi([d["X"], d["W"]])
+    (qdy,) = quant_multi([d["dY"]])
+    return d, {"X": qx, "W": qw, "dY": qdy}
 
 
 def test_ffn_quantisation(ffn):
     d, q = ffn
-    for k in ("X", "W"):
-        check_row_copy(d[k], q[k][0], k + " row")
-        check_col_copy(d[k], q[k][1], k + " col")
-    dy = d["dY"]
-    check_rows_sampled(dy, q["dY"][0], boundary_rows(dy.shape[0], 1), "dY row")
-    check_cols_sampled(dy, q["dY"][1], boundary_rows(dy.shape[1], 2), "dY col")
+    for k in ("X", "W", "dY"):
+        check_both_full(d[k], q[k], k)
 
 
 @pytest.mark.parametrize("mode", [mx.MX_FPROP, mx.MX_DGRAD, mx.MX_WGRAD])
@@ -77,16 +70,16 @@ def test_ffn_gemm(ffn, mode):
         out = mx.gemm(mode, xr, wr, status=st)
         srcs = (d["X"], mx.MX_ROWWISE, d["W"], mx.MX_ROWWISE)
     elif mode == mx.MX_DGRAD:
-        out = mx.gemm(mode, dr, wc, status=st)
+        out = backward_in_one_launch(dr, wc, dc, xc)[0]
         srcs = (d["dY"], mx.MX_ROWWISE, d["W"], mx.MX_COLWISE)
     else:
-        out = mx.gemm(mode, dc, xc, status=st)
+        out = backward_in_one_launch(dr, wc, dc, xc)[1]
         srcs = (d["dY"], mx.MX_COLWISE, d["X"], mx.MX_COLWISE)
     torch.cuda.synchronize()
     assert mx.read_status(st) == 0
     assert bool(torch.isfinite(out.float()).all())
     ii, jj = sample_entries(out.shape[0], out.shape[1], 4096, 10 + mode, tile_n=256)
-    rep = check_gemm_sampled(out, *srcs, ii, jj, what=f"ffn mode {mode}")
+    rep = check_gemm_sampled(out, *srcs, ii, jj, what=f"dense FFN mode {mode}")
     assert rep["fail"] == 0
 
 
@@ -97,21 +90,21 @@ def test_ffn_gemm(ffn, mode):
 @pytest.mark.parametrize("name", [p[0] for p in workloads.MLA_PROJECTIONS])
 def test_mla_projection(name):
     d = workloads.mla_projection(name)
-    (xr, xc), (wr, wc), (dr, dc) = quant_both(d["X"]), quant_both(d["W"]), quant_both(d["dY"])
-    check_row_copy(d["W"], wr, name + " W row")
-    check_col_copy(d["W"], wc, name + " W col")
-    check_rows_sampled(d["X"], xr, boundary_rows(d["X"].shape[0], 3, 128), name + " X row")
-    check_cols_sampled(d["X"], xc, boundary_rows(d["X"].shape[1], 4, 128), name + " X col")
+    (xr, xc), (wr, wc) = quant_multi([d["X"], d["W"]])
+    ((dr, dc),) = quant_multi([d["dY"]])
+    for k, q in (("X", (xr, xc)), ("W", (wr, wc)), ("dY", (dr, dc))):
+        check_both_full(d[k], q, f"{name} {k}")
+    # fprop with the caller workspace (it may split its last round), then
+    # dgrad + wgrad in one launch, as the bench step runs them
     st = mx.new_status()
-    y = mx.gemm(mx.MX_FPROP, xr, wr, status=st)
-    dx = mx.gemm(mx.MX_DGRAD, dr, wc, status=st)
-    dw = mx.gemm(mx.MX_WGRAD, dc, xc, status=st)
+    y = mx.gemm(mx.MX_FPROP, xr, wr, status=st, workspace=mx.gemm_workspace(mx.MX_FPROP, xr, wr))
     torch.cuda.synchronize()
     assert mx.read_status(st) == 0
+    dx, dw = backward_in_one_launch(dr, wc, dc, xc)
     for out, srcs, tag in ((y, (d["X"], 1, d["W"], 1), "fprop"), (dx, (d["dY"], 1, d["W"], 2), "dgrad"),
                            (dw, (d["dY"], 2, d["X"], 2), "wgrad")):
         ii, jj = sample_entries(out.shape[0], out.shape[1], 1024, 20, tile_n=256)
-        check_gemm_sampled(out, *srcs, ii, jj, what=f"{name} {tag}")
+        check_gemm_sampled(out, *srcs, ii, jj, what=f"MLA {name} {tag}")
 
 
 # ---------------------------------------------------------------------------
@@ -164,28 +157,33 @@ def test_moe_grouped(moe, proj):
     dY = moe["dY_gate_up"] if proj == "gate_up" else moe["dY_down"]  # [M, N]
     E, N, K = W.shape
     st = mx.new_status()
-    ar, _ = mx.quantize(A.cuda(), mx.MX_ROWWISE, status=st)
-    wr, wc = mx.quantize_stacked(W.cuda(), mx.MX_BOTH, status=st)
-    dr, _ = mx.quantize(dY.cuda(), mx.MX_ROWWISE, status=st)
     cap = mx.mx_grouped_padded_rows(offs)
-    _, dcg = mx.quantize(dY.cuda(), mx.MX_COLWISE, group_offsets=o, col_capacity=cap, status=st)
-    _, acg = mx.quantize(A.cuda(), mx.MX_COLWISE, group_offsets=o, col_capacity=cap, status=st)
+    # as the bench step: row copy + per-group padded column copy in one pass
+    # for the activation and the output gradient, stacked weights both ways
+    ar, acg = mx.quantize(A.cuda(), mx.MX_BOTH, group_offsets=o, col_capacity=cap, status=st)
+    dr, dcg = mx.quantize(dY.cuda(), mx.MX_BOTH, group_offsets=o, col_capacity=cap, status=st)
+    wr, wc = mx.quantize_stacked(W.cuda(), mx.MX_BOTH, status=st)
     y = mx.grouped_gemm(mx.MX_FPROP, ar, wr, o, status=st)
     dx = mx.grouped_gemm(mx.MX_DGRAD, dr, wc, o, status=st)
     dw = mx.grouped_gemm(mx.MX_WGRAD, dcg, acg, o, status=st)
     torch.cuda.synchronize()
     assert mx.read_status(st) == 0
 
+    # every byte of every copy
+    check_row_copy_full(A, ar, f"{proj} A row")
+    check_grouped_col_copy_full(A, offs, acg, f"{proj} A grouped col")
+    check_row_copy_full(dY, dr, f"{proj} dY row")
+    check_grouped_col_copy_full(dY, offs, dcg, f"{proj} dY grouped col")
+    check_stacked_full(W, wr, wc, f"{proj} W")
+
     # fprop: Y[t, n] = sum_k A[t, k] W_e[n, k]
     ii, jj = moe_samples(offs, N, 31)
     ref, S = grouped_entry_refs(A, mx.MX_ROWWISE, W, mx.MX_ROWWISE, offs, ii, jj)
-    out = f64(y[torch.from_numpy(ii), torch.from_numpy(jj)])
-    assert oracle.within_tolerance(out, ref, S).all(), f"{proj} fprop"
+    check_values(f64(y[torch.from_numpy(ii), torch.from_numpy(jj)]), ref, S, f"MoE {proj} fprop")
     # dgrad: dX[t, k] = sum_n dY[t, n] W_e[n, k]
     ii, jj = moe_samples(offs, K, 32)
     ref, S = grouped_entry_refs(dY, mx.MX_ROWWISE, W, mx.MX_COLWISE, offs, ii, jj)
-    out = f64(dx[torch.from_numpy(ii), torch.from_numpy(jj)])
-    assert oracle.within_tolerance(out, ref, S).all(), f"{proj} dgrad"
+    check_values(f64(dx[torch.from_numpy(ii), torch.from_numpy(jj)]), ref, S, f"MoE {proj} dgrad")
     # wgrad: dW_e[n, k] = sum_{t in e} dY[t, n] A[t, k]; sampled (e, n, k)
     g = np.random.Generator(np.random.Philox(33))
     for e in range(E):
@@ -201,8 +199,8 @@ def test_moe_grouped(moe, proj):
         b, bs, _ = oracle.mx_quantize_colwise_grouped(f64(A[offs[e]:offs[e + 1]][:, torch.from_numpy(k_idx)]),
                                                       seg_off)
         ref, S = oracle.mx_gemm_ref(a, as_, b, bs)
-        out = f64(dw[e][torch.from_numpy(n_idx)][:, torch.from_numpy(k_idx)])
-        assert oracle.within_tolerance(out, ref, S).all(), f"{proj} wgrad expert {e}"
+        check_values(f64(dw[e][torch.from_numpy(n_idx)][:, torch.from_numpy(k_idx)]), ref, S,
+                     f"MoE {proj} wgrad expert {e}")
 
 
 # ---------------------------------------------------------------------------
@@ -212,10 +210,8 @@ def test_moe_grouped(moe, proj):
 @pytest.mark.parametrize("M", list(workloads.QUANT_SWEEP_M))
 def test_quant_sweep(M):
     x = workloads.quant_sweep(M)
-    row, col = quant_both(x)
-    if M == 4096:
-        check_row_copy(x, row, f"sweep {M} row")
-        check_col_copy(x, col, f"sweep {M} col")
-    else:
-        check_rows_sampled(x, row, boundary_rows(M, 40 + M % 97), f"sweep {M} row")
-        check_cols_sampled(x, col, boundary_rows(7168, 41 + M % 89), f"sweep {M} col")
+    st = mx.new_status()
+    row, col = mx.quantize(x.cuda(), mx.MX_BOTH, status=st)
+    torch.cuda.synchronize()
+    assert mx.read_status(st) == 0
+    check_both_full(x, (row, col), f"sweep M={M}")
