@@ -3,8 +3,10 @@
 One step = one pass of the path over one batch of synthetic inputs:
 MX-quantise X, W and dY (row and column copies, one fused pass each), then the
 fprop, dgrad and wgrad block-scaled GEMMs. Default workload: the dense FFN
-up-projection (tokens M=8192, K=2048, N=10944), DeepSeek-V3 16B shaped.
-Other workloads (--workload mla|moe|quant) print their own line.
+up-projection (tokens M=8192, K=2048, N=10944), DeepSeek-V3 16B shaped. The
+default line also carries every other workload's own measurement under
+"configs" (single Linear, MLA projections, routed experts, quantiser sweep,
+blockwise FP8 variant, FP32 weight refresh); --workload NAME prints one alone.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dense_ffn]
     python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -37,6 +39,30 @@ import torch  # noqa: E402
 
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+# The headline metric: the same string on both arms, so the two lines compare.
+METRIC_DENSE = "MXFP8 GEMM TFLOPS (fprop+dgrad+wgrad step incl. MX quantisation, dense FFN up-proj)"
+WORKLOAD_DENSE = ("dense_ffn_up_proj M=8192 K=2048 N=10944: quantise X,W,dY (row+col) + fprop + dgrad + wgrad")
+
+
+def fp8_peaks(peaks, src):
+    """FP8 tensor peak (TFLOP/s) as the measured BF16 cuBLAS rate x the nominal
+    FP8/BF16 ratio: the burst figure for the bench's timed regions (milliseconds
+    to tens of milliseconds, far shorter than the sustained probe's seconds
+    under the power cap), and the sustained one, reported beside it."""
+    burst = peaks["bf16_tflops"] * FP8_OVER_BF16
+    sustained = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    label = (f"{src} bf16 burst {peaks['bf16_tflops']} x nominal fp8/bf16 ratio {FP8_OVER_BF16} (timed region "
+             f"< 1 s); frac_sustained uses bf16 sustained {peaks['bf16_tflops_sustained']}")
+    return burst, sustained, label
+
+
+def tensor_roofline(kernel, achieved, peaks, src, **extra):
+    burst, sustained, label = fp8_peaks(peaks, src)
+    d = {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+         "frac": achieved / burst, "frac_sustained": achieved / sustained, "peak_source": label}
+    d.update(extra)
+    return d
 
 
 def load_peaks():
@@ -310,30 +336,30 @@ def dense_host_inputs():
     return _DENSE_HOST
 
 
-def oracle_dense_sample(rows: int, cols: int, seed: int = 7):
-    """Time the oracle on a bounded sample of the dense FFN step: for each of
-    fprop/dgrad/wgrad, a [rows x cols] block of outputs, including the oracle
+def _f64(t):
+    import oracle
+    return oracle.bf16_bits_to_float64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def oracle_linear_sample(X, W, dY, rows: int, cols: int, seed: int = 7):
+    """Time the oracle on a bounded sample of one Linear layer's step (X [M, K],
+    W [N, K], dY [M, N]): for each of fprop/dgrad/wgrad, a [rows x cols] block
+    of outputs (fewer where the GEMM is narrower), including the oracle
     quantisation of exactly the operand rows/columns that block reads.
     Returns (flops_of_sample, seconds)."""
     import oracle
-    M, K, N = 8192, 2048, 10944
-    d = dense_host_inputs()
+    M, K = X.shape
+    N = W.shape[0]
     g = np.random.Generator(np.random.Philox(seed))
-
-    def f64(t):
-        return oracle.bf16_bits_to_float64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
-
-    X, W, dY = d["X"], d["W"], d["dY"]
     picks = []
     for (Mg, Ng, Kg) in ((M, N, K), (M, K, N), (N, K, M)):
-        # a block of at most rows x cols outputs (dgrad and wgrad have 2048 columns)
         picks.append((np.sort(g.choice(Mg, min(rows, Mg), replace=False)),
                       np.sort(g.choice(Ng, min(cols, Ng), replace=False)), Kg))
     # slices of the BF16 sources (host copies, not timed)
     (i0, j0, _), (i1, j1, _), (i2, j2, _) = picks
-    srcs = [(f64(X[torch.from_numpy(i0)]), f64(W[torch.from_numpy(j0)])),
-            (f64(dY[torch.from_numpy(i1)]), f64(W[:, torch.from_numpy(j1)])),
-            (f64(dY[:, torch.from_numpy(i2)]), f64(X[:, torch.from_numpy(j2)]))]
+    srcs = [(_f64(X[torch.from_numpy(i0)]), _f64(W[torch.from_numpy(j0)])),
+            (_f64(dY[torch.from_numpy(i1)]), _f64(W[:, torch.from_numpy(j1)])),
+            (_f64(dY[:, torch.from_numpy(i2)]), _f64(X[:, torch.from_numpy(j2)]))]
     t0 = time.perf_counter()
     a, b = srcs[0]
     oracle.mx_gemm_ref(*oracle.mx_quantize_rowwise(a), *oracle.mx_quantize_rowwise(b))
@@ -344,6 +370,12 @@ def oracle_dense_sample(rows: int, cols: int, seed: int = 7):
     dt = time.perf_counter() - t0
     flops = sum(2.0 * len(i) * len(j) * Kg for (i, j, Kg) in picks)
     return flops, dt
+
+
+def oracle_dense_sample(rows: int, cols: int, seed: int = 7):
+    """The dense FFN up-projection's sample (see oracle_linear_sample)."""
+    d = dense_host_inputs()
+    return oracle_linear_sample(d["X"], d["W"], d["dY"], rows, cols, seed)
 
 
 def cpu_threads():
@@ -390,11 +422,11 @@ def run_reference(args, rank, world):
         t_total += dt
         flops_total += fl
     v = flops_total / t_total / 1e12
-    line = {"impl": "reference", "metric": "MXFP8 GEMM TFLOPS (fprop+dgrad+wgrad step, dense FFN up-proj)",
+    line = {"impl": "reference", "metric": METRIC_DENSE,
             "value": v, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * t_total / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "dense_ffn_up_proj M=8192 K=2048 N=10944 (fprop+dgrad+wgrad)",
+            "config": {"workload": WORKLOAD_DENSE,
                        "sample": f"{rows}x{cols} output block per GEMM per step"},
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
                              "sample": f"{rows}x{cols} output block of each GEMM per step, with the oracle "
@@ -406,16 +438,15 @@ def run_reference(args, rank, world):
 class MoEExperts:
     """Routed-expert step (64 experts, 49152 rows, gate_up N=2816/K=2048 and
     down N=2048/K=1408): quantise the activation and the output gradient of each
-    projection (row copy + per-group padded column copy in one pass) and the
-    stacked weights (row + column copies per expert), then the grouped fprop,
-    dgrad and wgrad GEMMs of both projections."""
+    projection (row copy + per-group padded column copy in one pass), then the
+    grouped fprop, dgrad and wgrad GEMMs of both projections. The stacked
+    weights' row and column copies are refreshed apart (refresh_weights)."""
     name = "moe_routed_experts"
 
     def __init__(self):
-        import workloads
         import mxfp8_block_scaled_gb300 as mx
         self.mx = mx
-        d = workloads.moe_experts()
+        d = moe_host_inputs()
         self.offsets = torch.from_numpy(d["offsets"]).cuda()
         self.counts = d["counts"]
         self.M = int(d["offsets"][-1])
@@ -441,10 +472,28 @@ class MoEExperts:
     def step_flops(self):
         return sum(self.gemm_flops())
 
+    def refresh_weights(self, stream, timers=None):
+        """The weight refresh after an optimizer step: row and column copies of
+        both projections' stacked weights ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8
+        训练设计" §8.1: weights are quantised once after each optimizer step and
+        reused by the micro-batches and recomputation that follow)."""
+        mx = self.mx
+        sp = stream.cuda_stream
+        for pr in self.proj:
+            W, wr, wc = pr["W"], pr["wr"], pr["wc"]
+            e = timers.span("wquant", stream) if timers else None
+            mx.mx_quantize_batched(W.data_ptr(), pr["E"], pr["N"], pr["K"], pr["K"], pr["N"] * pr["K"], mx.MX_BOTH,
+                                   wr.data.data_ptr(), wr.scale.data_ptr(), wc.data.data_ptr(), wc.scale.data_ptr(),
+                                   None, sp)
+            if e is not None:
+                e.record(stream)
+
     def step(self, stream, timers=None):
-        """Forward chain gate_up -> SwiGLU (fused into gate_up's epilogue) -> down,
-        then each projection's dgrad and wgrad; the output gradients are the
-        synthetic dY tensors, the stacked weights are re-quantised every step."""
+        """One micro-batch: the forward chain gate_up -> SwiGLU (fused into
+        gate_up's epilogue) -> down, then each projection's dgrad and wgrad, with
+        the activations and output gradients quantised (row copy + per-expert
+        column copy in one pass each). The output gradients are the synthetic dY
+        tensors; the weights' copies come from the last refresh_weights."""
         mx = self.mx
         sp = stream.cuda_stream
         o = self.offsets.data_ptr()
@@ -457,13 +506,7 @@ class MoEExperts:
                                self.cap, None, sp)
                 if e is not None:
                     e.record(stream)
-            W, wr, wc = pr["W"], pr["wr"], pr["wc"]
-            e = timers.span("wquant", stream) if timers else None
-            mx.mx_quantize_batched(W.data_ptr(), pr["E"], pr["N"], pr["K"], pr["K"], pr["N"] * pr["K"], mx.MX_BOTH,
-                                   wr.data.data_ptr(), wr.scale.data_ptr(), wc.data.data_ptr(), wc.scale.data_ptr(),
-                                   None, sp)
-            if e is not None:
-                e.record(stream)
+            wr, wc = pr["wr"], pr["wc"]
             for mode, a, b, out in ((mx.MX_FPROP, pr["ar"], wr, pr["out"]["Y"]),
                                     (mx.MX_DGRAD, pr["dr"], wc, pr["out"]["dX"]),
                                     (mx.MX_WGRAD, pr["dc"], pr["ac"], pr["out"]["dW"])):
@@ -479,12 +522,68 @@ class MoEExperts:
                     e.record(stream)
 
     def launches_per_step(self):
-        return sum(2 + 1 + 3 for pr in self.proj)
+        return sum(2 + 3 for pr in self.proj)
+
+
+_MOE_HOST = {}
+
+
+def moe_host_inputs():
+    if not _MOE_HOST:
+        import workloads
+        _MOE_HOST.update(workloads.moe_experts())
+    return _MOE_HOST
+
+
+def oracle_moe_sample(rows: int, cols: int, seed: int = 11):
+    """Time the oracle on a bounded sample of the routed-expert step: for the
+    largest expert of each projection, a [rows x cols] block of its fprop,
+    dgrad and wgrad outputs, with the oracle quantisation (per-expert column
+    blocks for wgrad) of exactly the operand rows/columns that block reads.
+    Returns (flops_of_sample, seconds)."""
+    import oracle
+    d = moe_host_inputs()
+    offs = d["offsets"]
+    e = int(np.argmax(np.diff(offs)))
+    lo, hi = int(offs[e]), int(offs[e + 1])
+    g = np.random.Generator(np.random.Philox(seed))
+    flops, dt = 0.0, 0.0
+    for a_key, w_key, dy_key in (("X", "W_gate_up", "dY_gate_up"), ("A_down", "W_down", "dY_down")):
+        A, W, dY = d[a_key][lo:hi], d[w_key][e], d[dy_key][lo:hi]
+        m, K = A.shape
+        N = W.shape[0]
+        i = np.sort(g.choice(m, min(rows, m), replace=False))
+        jn = np.sort(g.choice(N, min(cols, N), replace=False))
+        jk = np.sort(g.choice(K, min(cols, K), replace=False))
+        src = [_f64(A[torch.from_numpy(i)]), _f64(W[torch.from_numpy(jn)]), _f64(dY[torch.from_numpy(i)]),
+               _f64(W[:, torch.from_numpy(jk)]), _f64(dY[:, torch.from_numpy(jn[:rows])]),
+               _f64(A[:, torch.from_numpy(jk)])]
+        seg = np.array([0, m], dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.mx_gemm_ref(*oracle.mx_quantize_rowwise(src[0]), *oracle.mx_quantize_rowwise(src[1]))
+        oracle.mx_gemm_ref(*oracle.mx_quantize_rowwise(src[2]), *oracle.mx_quantize_colwise(src[3]))
+        a, as_, _ = oracle.mx_quantize_colwise_grouped(src[4], seg)
+        b, bs, _ = oracle.mx_quantize_colwise_grouped(src[5], seg)
+        oracle.mx_gemm_ref(a, as_, b, bs)
+        dt += time.perf_counter() - t0
+        flops += 2.0 * len(i) * len(jn) * K + 2.0 * len(i) * len(jk) * N + 2.0 * min(rows, len(jn)) * len(jk) * m
+    return flops, dt
+
+
+def timed_cpu_baseline(fn, budget_s: float, unit_scale: float = 1e12):
+    """Repeat an oracle sample (seeds 0, 1, ...) until budget_s of oracle time;
+    returns (work per second / unit_scale, seconds, repetitions)."""
+    work, dt, n = 0.0, 0.0, 0
+    while dt < budget_s:
+        w, t = fn(n)
+        work, dt, n = work + w, dt + t, n + 1
+    return work / dt / unit_scale, dt, n
 
 
 def run_moe(args, rank, world, peaks, peak_src):
     wl = MoEExperts()
     stream = torch.cuda.Stream()
+    wl.refresh_weights(stream)
     ms, timers, clk = _measure(lambda t: wl.step(stream, t), args, world, stream)
     value = world * args.steps * wl.step_flops() / (ms / 1e3) / 1e12
     pairs = timers.pairs["gemm"]
@@ -494,32 +593,48 @@ def run_moe(args, rank, world, peaks, peak_src):
                               "down dgrad", "down wgrad"]):
         t = sum(pairs[j][0].elapsed_time(pairs[j][1]) for j in range(i, len(pairs), 6)) / args.steps
         per_gemm.append({"gemm": name, "ms": t, "tflops": fl[i] / (t / 1e3) / 1e12})
-    gemm_ms = timers.total_ms("gemm") / timers.count("gemm")
-    achieved = (sum(fl) / 6) / (gemm_ms / 1e3) / 1e12
-    peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
-    line = {"metric": "MXFP8 grouped-GEMM TFLOPS (fprop+dgrad+wgrad of gate_up and down, incl. MX quantisation)",
+    gemm_ms = timers.total_ms("gemm") / args.steps
+    achieved = sum(fl) / (gemm_ms / 1e3) / 1e12
+    # the refresh after an optimizer step, timed on its own (K refreshes back to back)
+    rms, rtimers, _ = _measure(lambda t: wl.refresh_weights(stream, t), args, world, stream, clocks=False)
+    w_elems = sum(pr["E"] * pr["N"] * pr["K"] for pr in wl.proj)
+    refresh_ms = rms / args.steps
+    line = {"metric": "MXFP8 grouped-GEMM TFLOPS (routed experts, fprop+dgrad+wgrad of gate_up and down incl. "
+                      "MX quantisation of activations and gradients)",
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3", "data": "synthetic",
             "config": {"workload": "moe_routed_experts: 64 experts, 49152 rows (Zipf 1.1, 4 empty), gate_up "
                                    "2048->2816 with SwiGLU fused into its epilogue (writes down's input), "
                                    "down 1408->2048", "parallelism": f"replicas{world}",
+                       "weights": "quantised once per optimizer step (refresh_weights, timed apart); a step is "
+                                  "one micro-batch",
                        "l2": "no flush: a step moves several GB (> 129 MB L2)"},
             "per_gemm": per_gemm,
-            "roofline": {"bound": "tensor", "kernel": "mx_gemm_pair_kernel (grouped)", "achieved": achieved,
-                         "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8, "traffic": None,
-                         "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}"},
-            "quant_ms_per_launch": timers.total_ms("quant") / timers.count("quant"),
-            "weight_quant_ms_per_projection": timers.total_ms("wquant") / timers.count("wquant"),
+            "roofline": tensor_roofline("mx_gemm_pair_kernel (grouped)", achieved, peaks, peak_src, traffic=None,
+                                        ms_per_step=gemm_ms,
+                                        basis="the six grouped GEMMs' FLOPs (true expert rows, no padding) over "
+                                              "their summed launch durations"),
+            "quant_ms_per_step": timers.total_ms("quant") / args.steps,
+            "weight_refresh": {"ms": refresh_ms, "launches": 2,
+                               "gbs": (2 + 1 + 1 + 2 / 32) * w_elems / (refresh_ms / 1e3) / 1e9,
+                               "tflops_with_one_refresh_per_step": wl.step_flops() /
+                               ((ms / args.steps + refresh_ms) / 1e3) / 1e12},
             "gpu_launches": wl.launches_per_step() * args.steps, "clocks": clk}
-    if rank == 0:
-        line["timing"] = TIMING_NOTE
-        print(json.dumps(line))
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, n = timed_cpu_baseline(lambda i: oracle_moe_sample(256, 256, seed=11 + i), args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                                "seconds": dt, "sample": f"{n} x (largest expert of each projection: 256x256 "
+                                                         "blocks of fprop, dgrad and wgrad with the oracle "
+                                                         "quantisation of the rows they read)"}
+    return line
 
 
 def run_quant_sweep(args, rank, world, peaks, peak_src):
     """Quantiser bandwidth sweep: BF16 [M x 7168], M in {4096 .. 32768}, both
-    copies in one fused pass per launch. One step = one launch per M."""
+    copies in one fused pass per launch. One step = one launch per M. Each M's
+    own figure comes from K launches of that M back to back (no event between
+    them), after the timed region of whole steps."""
     import workloads
     import mxfp8_block_scaled_gb300 as mx
     C = 7168
@@ -528,61 +643,72 @@ def run_quant_sweep(args, rank, world, peaks, peak_src):
     stream = torch.cuda.Stream()
     sp = stream.cuda_stream
 
-    def step(timers=None):
-        for M, x in xs.items():
-            r, c = outs[M]
-            e = timers.span(M, stream) if timers else None
-            mx.mx_quantize(x.data_ptr(), M, C, C, mx.MX_BOTH, r.data.data_ptr(), r.scale.data_ptr(), c.data.data_ptr(),
-                           c.scale.data_ptr(), None, 0, 0, None, sp)
-            if e is not None:
-                e.record(stream)
+    def launch(M):
+        x = xs[M]
+        r, c = outs[M]
+        mx.mx_quantize(x.data_ptr(), M, C, C, mx.MX_BOTH, r.data.data_ptr(), r.scale.data_ptr(), c.data.data_ptr(),
+                       c.scale.data_ptr(), None, 0, 0, None, sp)
 
-    ms, timers, clk = _measure(step, args, world, stream)
+    def step(timers=None):
+        for M in xs:
+            launch(M)
+
+    ms, _, clk = _measure(step, args, world, stream, kernel_pass=False)
     per_elem = 2 + 1 + 1 + 2 / 32
     step_bytes = sum(per_elem * M * C for M in xs)
     value = world * args.steps * step_bytes / (ms / 1e3) / 1e9
-    per_m = {str(M): per_elem * M * C / (timers.total_ms(M) / timers.count(M) / 1e3) / 1e9 for M in xs}
+    per_m = {}
+    for M in xs:
+        m_ms, _, _ = _measure(lambda t, M=M: launch(M), args, world, stream, kernel_pass=False, clocks=False)
+        gbs = per_elem * M * C / (m_ms / args.steps / 1e3) / 1e9
+        per_m[str(M)] = {"gbs": gbs, "us_per_launch": m_ms / args.steps * 1e3, "frac": gbs / peaks["hbm_gbs"],
+                         "bytes_per_launch": per_elem * M * C}
     big = max(xs)
-    achieved = per_m[str(big)]
+    achieved = per_m[str(big)]["gbs"]
     line = {"metric": "MX quantiser GB/s (row + column copies, one fused pass)", "value": value, "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
             "data": "synthetic",
             "config": {"workload": "quant_sweep BF16 [M x 7168], M in 4096/8192/16384/32768, axis both",
                        "parallelism": f"replicas{world}", "l2": "no flush: each step moves ~1.8 GB (> 129 MB L2)"},
-            "per_M_gbs": per_m,
+            "per_M": per_m,
             "roofline": {"bound": "hbm", "kernel": "mx_quant_kernel", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": profile_traffic("mx_quant_kernel:quant_sweep_M32768", "bytes_per_launch"),
                          "bytes_per_launch": per_elem * big * C,
                          "peak_source": f"{peak_src} hbm_gbs", "launch": f"M={big}"},
+            "frac_min_over_M": min(v["frac"] for v in per_m.values()),
             "gpu_launches": len(xs) * args.steps, "clocks": clk}
     if rank == 0 and not args.no_cpu_baseline:
-        dt, nbytes = 0.0, 0.0
-        for m in (4096, 8192):
-            d_, b_ = oracle_quant_sample(m)
-            dt, nbytes = dt + d_, nbytes + b_
-        line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
-                                "seconds": dt, "sample": "the whole M=4096 and M=8192 sweep tensors [M x 7168]: "
-                                                        "oracle row and column quantisation, 4.0625 B per element"}
-    if rank == 0:
-        line["timing"] = TIMING_NOTE
-        print(json.dumps(line))
+        v, dt, n = timed_cpu_baseline(lambda i: oracle_quant_sample(4096, 1024, seed=i), args.cpu_budget,
+                                      unit_scale=1e9)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+                                "seconds": dt, "sample": f"{n} x a [1024 x 7168] row slab of the M=4096 sweep "
+                                                         "tensor: oracle row and column quantisation, 4.0625 B per "
+                                                         "element"}
+    return line
 
 
-def oracle_quant_sample(M: int):
-    """Time the oracle's row and column quantisation of the [M x 7168] sweep
-    tensor; returns (seconds, algorithmic bytes)."""
-    import numpy as np
+_SWEEP_HOST = {}
+
+
+def oracle_quant_sample(M: int, rows: int = 1024, seed: int = 0):
+    """Time the oracle's row and column quantisation of a slab of `rows`
+    consecutive rows (a multiple of 32, so the column blocks stay whole) of the
+    [M x 7168] sweep tensor; returns (algorithmic bytes, seconds)."""
     import oracle
     import workloads
-    x = workloads.quant_sweep(M)
-    f = oracle.bf16_bits_to_float64(x.contiguous().view(torch.int16).numpy().view(np.uint16))
+    if M not in _SWEEP_HOST:
+        _SWEEP_HOST.clear()
+        _SWEEP_HOST[M] = workloads.quant_sweep(M)
+    x = _SWEEP_HOST[M]
+    r0 = (seed * rows) % M
+    f = _f64(x[r0:r0 + rows])
     t0 = time.perf_counter()
     oracle.mx_quantize_rowwise(f)
     oracle.mx_quantize_colwise(f)
     dt = time.perf_counter() - t0
-    return dt, 4.0625 * x.numel()
+    return 4.0625 * f.size, dt
 
 
 def _linear_set(projs, mx):
@@ -648,7 +774,7 @@ def _gemm_shapes(ly):
     return (("fprop", M, N, K), ("dgrad", M, K, N), ("wgrad", N, K, M))
 
 
-def _measure(step, args, world, stream):
+def _measure(step, args, world, stream, kernel_pass=True, clocks=True):
     """W warm-up steps, the timed region, then the kernel pass.
 
     The timed region is exactly K steps with no event inside them, bracketed
@@ -659,12 +785,14 @@ def _measure(step, args, world, stream):
     stream about 2 us (a dense FFN step took 456 us without its six events and
     469 us with them), which is why the whole-step time comes from the pass
     without them. Clocks are sampled across both passes.
+    kernel_pass=False skips the second pass; clocks=False samples no clocks.
     Returns (max-over-ranks ms of the timed region, Timers, clock record)."""
     for _ in range(args.warmup):
         step(None)
     torch.cuda.synchronize()
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
+    sampler = ClockSampler(torch.cuda.current_device()) if clocks else None
+    if sampler:
+        sampler.start()
     barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -676,11 +804,12 @@ def _measure(step, args, world, stream):
     torch.cuda.synchronize()
     barrier(world)
     timers = Timers()
-    for _ in range(args.steps):
-        step(timers)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
+    if kernel_pass:
+        for _ in range(args.steps):
+            step(timers)
+        torch.cuda.synchronize()
+        barrier(world)
+    clk = sampler.stop() if sampler else None
     return max_over_ranks(t0.elapsed_time(t1), world), timers, clk
 
 
@@ -699,7 +828,7 @@ def run_mla(args, rank, world, peaks, peak_src):
     layers = _linear_set(projs, mx)
     stream = torch.cuda.Stream()
     ms, timers, clk = _measure(lambda t: _linear_step(layers, mx, stream, t), args, world, stream)
-    peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    peak_fp8, _, _ = fp8_peaks(peaks, peak_src)
     per_gemm, flops_total, gemm_ms_total = [], 0.0, 0.0
 
     def roof(M, N, K):
@@ -730,17 +859,28 @@ def run_mla(args, rank, world, peaks, peak_src):
                                    "kv_up 512->4096, o_proj 2048->2048", "parallelism": f"replicas{world}",
                        "l2": "no flush: a step moves ~1.5 GB (> 129 MB L2)"},
             "per_gemm": per_gemm,
-            "roofline": {"bound": "tensor", "kernel": "mx_gemm_pair_kernel / mx_gemm_kernel", "achieved": achieved,
-                         "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8, "traffic": None,
-                         "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}",
-                         "roofline_time_frac": sum(g["roofline_ms"] for g in per_gemm) / gemm_ms_total},
+            "roofline": tensor_roofline("mx_gemm_pair_kernel / mx_gemm_kernel", achieved, peaks, peak_src,
+                                        traffic=None, ms_per_step=gemm_ms_total,
+                                        roofline_time_frac=sum(g["roofline_ms"] for g in per_gemm) / gemm_ms_total,
+                                        basis="per GEMM launch max(FLOPs / FP8 peak, algorithmic bytes / HBM); "
+                                              "frac = the GEMMs' FLOPs over their summed launch durations"),
             # per layer: two quantiser launches, fprop (+ its split-tail reduction), dgrad + wgrad
             "gpu_launches": sum(2 + gemm_launches(mx, mx.MX_FPROP, ly["q"][0][0], ly["q"][1][0], workspace=True) + 1
                                 for ly in layers) * args.steps,
             "clocks": clk}
-    if rank == 0:
-        line["timing"] = TIMING_NOTE
-        print(json.dumps(line))
+    if rank == 0 and not args.no_cpu_baseline:
+        def sample(i):
+            fl, dt = 0.0, 0.0
+            for _, X, W, dY in projs:
+                f_, d_ = oracle_linear_sample(X, W, dY, 128, 128, seed=21 + i)
+                fl, dt = fl + f_, dt + d_
+            return fl, dt
+        v, dt, n = timed_cpu_baseline(sample, args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                                "seconds": dt, "sample": f"{n} x (each projection: a 128x128 output block of its "
+                                                         "fprop, dgrad and wgrad with the oracle quantisation of "
+                                                         "the rows they read)"}
+    return line
 
 
 def run_single(args, rank, world, peaks, peak_src):
@@ -814,9 +954,25 @@ def run_single(args, rank, world, peaks, peak_src):
             "per_kernel_us": {"quant_x_and_w": timers.total_ms("quant") / timers.count("quant") * 1e3,
                               "gemm": timers.total_ms("gemm") / timers.count("gemm") * 1e3},
             "gpu_launches": (1 + gemm_launches(mx, mx.MX_FPROP, xr, wr)) * args.steps, "clocks": clk}
-    if rank == 0:
-        line["timing"] = TIMING_NOTE
-        print(json.dumps(line))
+    gemm_us = line["per_kernel_us"]["gemm"]
+    fl = 2.0 * X.shape[0] * W.shape[0] * X.shape[1]
+    line["roofline"] = tensor_roofline("mx_gemm_kernel", fl / (gemm_us / 1e6) / 1e12, peaks, peak_src,
+                                       traffic=None, note="launch-latency bound: 6.7e7 FLOP take ~0.02 us at the "
+                                                          "tensor peak, so the fraction says nothing about the "
+                                                          "kernel; the time per step is the figure")
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        fx, fw = _f64(d["X"]), _f64(d["W"])
+
+        def sample(i):
+            t0 = time.perf_counter()
+            oracle.mx_gemm_ref(*oracle.mx_quantize_rowwise(fx), *oracle.mx_quantize_rowwise(fw))
+            return 1.0, time.perf_counter() - t0
+        n_per_s, dt, n = timed_cpu_baseline(sample, min(args.cpu_budget, 3.0), unit_scale=1.0)
+        line["cpu_baseline"] = {"value": 1e6 / n_per_s, "unit": "us", "cores": cpu_threads(), "kind": "oracle",
+                                "seconds": dt, "sample": f"{n} x the whole step: oracle 1x32 quantisation of X "
+                                                         "and W and the full 256x256x512 GEMM"}
+    return line
 
 
 def run_wrefresh(args, rank, world, peaks, peak_src):
@@ -859,9 +1015,20 @@ def run_wrefresh(args, rank, world, peaks, peak_src):
                          "traffic": profile_traffic("mx_quant_f32_kernel:gate_up", "bytes_per_launch"),
                          "bytes_per_launch": max(nbytes), "peak_source": f"{peak_src} hbm_gbs"},
             "gpu_launches": 2 * args.steps, "clocks": clk}
-    if rank == 0:
-        line["timing"] = TIMING_NOTE
-        print(json.dumps(line))
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        w0 = masters[1][0].cpu().numpy().astype(np.float64)   # one down expert [2048, 1408], exact FP32 values
+
+        def sample(i):
+            t0 = time.perf_counter()
+            oracle.mx_quantize_rowwise(w0)
+            oracle.mx_quantize_colwise(w0)
+            return per_elem * w0.size, time.perf_counter() - t0
+        v, dt, n = timed_cpu_baseline(sample, args.cpu_budget, unit_scale=1e9)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+                                "seconds": dt, "sample": f"{n} x one expert's FP32 master [2048 x 1408]: oracle row "
+                                                         "and column quantisation, 6.0625 B per element"}
+    return line
 
 
 def run_blockwise(args, rank, world, peaks, peak_src):
@@ -895,63 +1062,37 @@ def run_blockwise(args, rank, world, peaks, peak_src):
     fl = 2.0 * M * N * K
     gemm_ms = timers.total_ms("gemm") / timers.count("gemm")
     achieved = fl / (gemm_ms / 1e3) / 1e12
-    peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     line = {"metric": "FP8 blockwise GEMM TFLOPS (DeepSeek-V3 1x128 / 128x128 recipe, fprop incl. quantisation)",
             "value": world * args.steps * fl / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": {"workload": "dense_ffn_up_proj fprop M=8192 K=2048 N=10944, blockwise FP8 variant",
                        "parallelism": f"replicas{world}", "l2": "no flush: a step moves ~0.3 GB (> 129 MB L2)"},
-            "roofline": {"bound": "tensor", "kernel": "mx_gemm_blockwise_kernel", "achieved": achieved,
-                         "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
-                         "traffic": profile_traffic("mx_gemm_blockwise_kernel"),
-                         "peak_source": f"{peak_src} bf16 sustained x nominal fp8/bf16 ratio {FP8_OVER_BF16}",
-                         "avg_launch_ms": gemm_ms},
+            "roofline": tensor_roofline("mx_gemm_blockwise_kernel", achieved, peaks, peak_src,
+                                        traffic=profile_traffic("mx_gemm_blockwise_kernel"), avg_launch_ms=gemm_ms),
             "quant_ms_per_launch": timers.total_ms("quant") / timers.count("quant"),
             "gpu_launches": 3 * args.steps, "clocks": clk}
-    if rank == 0:
-        line["timing"] = TIMING_NOTE
-        print(json.dumps(line))
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        xs, ws = _f64(d["X"][:256]), _f64(d["W"][:256])
+
+        def sample(i):
+            t0 = time.perf_counter()
+            qa_, sa_ = oracle.quantize_1x128(xs)
+            qb_, sb_ = oracle.quantize_128x128(ws)
+            oracle.gemm_blockwise_ref(qa_, sa_, qb_, sb_)
+            return 2.0 * 256 * 256 * K, time.perf_counter() - t0
+        v, dt, n = timed_cpu_baseline(sample, args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                                "seconds": dt, "sample": f"{n} x (256 rows of X quantised 1x128, the first 256 rows "
+                                                         "of W in 128x128 blocks, their 256x256x2048 blockwise GEMM)"}
+    return line
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dense_ffn", choices=["dense_ffn", "quant", "moe", "mla", "single", "wrefresh", "blockwise"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=20)
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
-
-    rank, world, local = dist_setup(args.gpus)
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-        return
-
-    import mxfp8_block_scaled_gb300 as mx
-    mx.lib()
-    peaks, peak_src = load_peaks()
-    if args.workload == "quant":
-        run_quant_sweep(args, rank, world, peaks, peak_src)
-        return
-    if args.workload == "moe":
-        run_moe(args, rank, world, peaks, peak_src)
-        return
-    if args.workload == "mla":
-        run_mla(args, rank, world, peaks, peak_src)
-        return
-    if args.workload == "single":
-        run_single(args, rank, world, peaks, peak_src)
-        return
-    if args.workload == "wrefresh":
-        run_wrefresh(args, rank, world, peaks, peak_src)
-        return
-    if args.workload == "blockwise":
-        run_blockwise(args, rank, world, peaks, peak_src)
-        return
+def run_dense(args, rank, world, peaks, peak_src):
+    """The headline: the dense FFN up-projection step (quantise X + W, dY;
+    fprop; dgrad + wgrad in one launch), plus its end-to-end run from pinned
+    host buffers."""
     wl = DenseFFN()
     stream = torch.cuda.Stream()
 
@@ -962,7 +1103,6 @@ def main():
     gemm_ms = timers.total_ms("gemm") / args.steps            # fprop + the fused dgrad/wgrad launch
     quant_ms = timers.total_ms("quant") / args.steps          # both quantiser launches of a step
     achieved = wl.step_flops() / (gemm_ms / 1e3) / 1e12
-    peak_fp8 = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     qbytes = sum(wl.quant_bytes().values())                    # X, W and dY per step
     q_gbs = qbytes / (quant_ms / 1e3) / 1e9
 
@@ -983,22 +1123,18 @@ def main():
         e2e_value = world * args.e2e_steps * wl.step_flops() / (e2e_ms / 1e3) / 1e12
 
     line = {
-        "metric": "MXFP8 GEMM TFLOPS (fprop+dgrad+wgrad step incl. MX quantisation, dense FFN up-proj)",
+        "metric": METRIC_DENSE,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": "dense_ffn_up_proj M=8192 K=2048 N=10944: quantise X,W,dY (row+col) + "
-                               "fprop + dgrad + wgrad", "M": wl.M, "K": wl.K, "N": wl.N,
+        "config": {"workload": WORKLOAD_DENSE, "M": wl.M, "K": wl.K, "N": wl.N,
                    "parallelism": f"replicas{world}",
                    "l2": "no flush: a step reads/writes ~0.7 GB (> 129 MB L2)"},
-        "roofline": {"bound": "tensor", "kernel": "mx_gemm_pair_kernel", "achieved": achieved,
-                     "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
-                     "traffic": profile_traffic("mx_gemm_pair_kernel"),
-                     "peak_source": f"{peak_src} bf16 sustained {peaks['bf16_tflops_sustained']} x nominal fp8/bf16 "
-                                    f"ratio {FP8_OVER_BF16}",
-                     "flops_per_step": wl.step_flops(), "ms_per_step": gemm_ms, "launches_per_step": 2,
-                     "basis": "fprop, dgrad and wgrad FLOPs (2MNK each) over the summed duration of the step's "
-                              "two GEMM launches (fprop; dgrad + wgrad in one launch)"},
+        "roofline": tensor_roofline("mx_gemm_pair_kernel", achieved, peaks, peak_src,
+                                    traffic=profile_traffic("mx_gemm_pair_kernel"),
+                                    flops_per_step=wl.step_flops(), ms_per_step=gemm_ms, launches_per_step=2,
+                                    basis="fprop, dgrad and wgrad FLOPs (2MNK each) over the summed duration of "
+                                          "the step's two GEMM launches (fprop; dgrad + wgrad in one launch)"),
         "quant_roofline": {"bound": "hbm", "kernel": "mx_quant_kernel", "achieved": q_gbs,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": q_gbs / peaks["hbm_gbs"],
                            "traffic": profile_traffic("mx_quant_kernel"), "bytes_per_step": qbytes,
@@ -1014,11 +1150,58 @@ def main():
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        fl, dt = oracle_dense_sample(2560, 2560)
-        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+        v, dt, n = timed_cpu_baseline(lambda i: oracle_dense_sample(1024, 1024, seed=7 + i), args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(),
                                 "kind": "oracle", "seconds": dt,
-                                "sample": "2560x2560 output block of fprop, 2560x2048 of dgrad and wgrad (dense FFN "
-                                          "up-proj), with the oracle quantisation of the operand rows it reads"}
+                                "sample": f"{n} x (1024x1024 output block of fprop, dgrad and wgrad of the dense FFN "
+                                          "up-proj, with the oracle quantisation of the operand rows it reads)"}
+    del wl
+    return line
+
+
+RUNS = {"dense_ffn": run_dense, "single": run_single, "mla": run_mla, "moe": run_moe, "quant": run_quant_sweep,
+        "wrefresh": run_wrefresh, "blockwise": run_blockwise}
+# Sub-results of the default line, keyed by the workload they measure.
+SUB_CONFIGS = (("config1_single_linear", "single"), ("config3_mla_projections", "mla"),
+               ("config4_moe_routed_experts", "moe"), ("config5_quant_sweep", "quant"),
+               ("variant_blockwise_fp8", "blockwise"), ("weight_refresh_fp32_master", "wrefresh"))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="all", choices=["all"] + list(RUNS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=5.0,
+                    help="seconds of oracle work behind each cpu_baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import mxfp8_block_scaled_gb300 as mx
+    mx.lib()
+    peaks, peak_src = load_peaks()
+    if args.workload != "all":
+        line = RUNS[args.workload](args, rank, world, peaks, peak_src)
+    else:
+        # the headline (dense FFN step, BASELINE's metric and config) carrying
+        # every other configuration's own measurement as a sub-result
+        line = run_dense(args, rank, world, peaks, peak_src)
+        line["configs"] = {}
+        for key, wl_name in SUB_CONFIGS:
+            torch.cuda.empty_cache()
+            sub = RUNS[wl_name](args, rank, world, peaks, peak_src)
+            for k in ("n_gpus", "steps", "warmup", "scaling", "vs_baseline", "data"):
+                sub.pop(k, None)
+            line["configs"][key] = sub
     if rank == 0:
         line["timing"] = TIMING_NOTE
         print(json.dumps(line))

@@ -55,4 +55,9 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, p.stdout
     line = lines[0]
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    # the same metric and workload as the product arm's headline, so the driver can divide them
+    sys.path.insert(0, ROOT)
+    import bench
+    assert line["metric"] == bench.METRIC_DENSE and line["config"]["workload"] == bench.WORKLOAD_DENSE
+    assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
