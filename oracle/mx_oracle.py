@@ -44,6 +44,10 @@ Readings taken where the pages are silent (each is also pinned by a test):
 * Blockwise variant recipe (1x128 / 128x128 with FP32 multipliers): the
   multiplier s = fl32(448 / amax) and the product fl32(s * x) are FP32
   steps, then RNE to E4M3; an all-zero block takes s = 1.
+* Current-scaling variant (one FP32 scale per tensor or per leading group):
+  scale = fl32(amax / 448) for a finite amax above zero, else 1.0; element =
+  E4M3(fl32(x / scale)). 448 stands in for the HiF8 format maxima the page
+  gives, since the data format here is E4M3.
 * SwiGLU after the grouped gate_up GEMM: gate = the first F output columns,
   up = the last F ([DSV3] §5 lays gate_up_proj out as [E, 2F, H]), computed in
   float64 on the unrounded dots; see ``swiglu_within_tolerance``.
@@ -495,6 +499,87 @@ def gemm_blockwise_ref(a_codes, a_s, b_codes, b_s) -> tuple[np.ndarray, np.ndarr
         ref += Ad @ Bd.T
         S += np.abs(Ad) @ np.abs(Bd).T
     return ref, S
+
+
+# ----------------------------------------------------------------------------
+# Variant recipe: current scaling with one FP32 scale per tensor or per group
+# ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §3: the FP32 scale of HiF8
+# current scaling is a scalar for a dense tensor and one per leading group for
+# a grouped tensor, taken from the current tensor's amax; §3.2: scale =
+# valid(amax) ? amax / format_max : 1.0 in FP32, dense tensors per tensor, 3-D
+# grouped weights per leading group; §8.2: activations and gradients take
+# amax and scale at every quantisation, weights after the optimizer step.)
+# Here the data format is E4M3, so format_max is E4M3's largest value 448;
+# the page's 15 and 224 belong to the HiF8 format, which is not built.
+# ----------------------------------------------------------------------------
+
+CURRENT_FORMAT_MAX = E4M3_MAX
+
+
+def current_amax(x) -> float:
+    """amax = max |x| over the whole tensor (NaN propagates)."""
+    with np.errstate(invalid="ignore"):
+        return float(np.max(np.abs(np.asarray(x, dtype=np.float64))))
+
+
+def current_scale(amax, format_max: float = CURRENT_FORMAT_MAX) -> np.float32:
+    """scale = amax / format_max as an FP32 division when amax is valid
+    (finite and above zero), else 1.0."""
+    a = np.float32(amax)
+    if not (np.isfinite(a) and a > 0):
+        return np.float32(1.0)
+    return np.float32(a) / np.float32(format_max)
+
+
+def current_encode(x, scale) -> np.ndarray:
+    """E4M3 codes of fl32(x / scale): the quotient rounded once to FP32, then
+    to E4M3 (nearest, ties to even, saturating; NaN keeps its sign bit)."""
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        q = (np.asarray(x, dtype=np.float32) / np.float32(scale)).astype(np.float32)
+    return e4m3_encode(q.astype(np.float64))
+
+
+def current_quantize(x, format_max: float = CURRENT_FORMAT_MAX):
+    """One tensor (any shape) with its own scale: (codes, scale, amax)."""
+    amax = current_amax(x)
+    s = current_scale(amax, format_max)
+    return current_encode(x, s), s, amax
+
+
+def current_quantize_groups(w, format_max: float = CURRENT_FORMAT_MAX):
+    """Stacked w[E, ...]: each leading group with its own amax and scale.
+    Returns (codes [E, ...], scales FP32 [E], amax [E])."""
+    w = np.asarray(w, dtype=np.float64)
+    out = [current_quantize(w[e], format_max) for e in range(w.shape[0])]
+    return (np.stack([o[0] for o in out]), np.array([o[1] for o in out], dtype=np.float32),
+            np.array([o[2] for o in out]))
+
+
+def current_dequantize(codes, scale) -> np.ndarray:
+    """Value of each element: its E4M3 value times the FP32 scale."""
+    return e4m3_decode(codes) * np.float64(np.float32(scale))
+
+
+def current_transpose_grouped(codes, offsets) -> np.ndarray:
+    """The layout of a grouped column operand: codes [M, D] of rows grouped by
+    offsets, transposed to [D, padded] with each group's segment starting at
+    the same 128-multiple column as the MX grouped column copy and zero codes
+    in the padding (the scale is one per tensor, so only the layout changes)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    o = np.asarray(offsets, dtype=np.int64)
+    poff = mx_padded_offsets(o)
+    out = np.zeros((c.shape[1], int(poff[-1])), dtype=np.uint8)
+    for e in range(len(o) - 1):
+        m = int(o[e + 1] - o[e])
+        out[:, poff[e]:poff[e] + m] = c[o[e]:o[e + 1]].T
+    return out
+
+
+def current_gemm_ref(a_codes, a_scale, b_codes, b_scale) -> tuple[np.ndarray, np.ndarray]:
+    """C = A . B^T on the dequantised operands in float64, with S = sum |a*b|."""
+    A = current_dequantize(a_codes, a_scale)
+    B = current_dequantize(b_codes, b_scale)
+    return A @ B.T, np.abs(A) @ np.abs(B).T
 
 
 # ----------------------------------------------------------------------------

@@ -533,6 +533,107 @@ def pin_blockwise_fp8(O):
     assert abs(Fraction(r2[0, 0]) - exact) <= abs(exact) * Fraction(1, 2 ** 50)
 
 
+def _fp32_rn(q: Fraction) -> Fraction:
+    """The FP32 number nearest to the rational q (ties to even), by exact
+    arithmetic: 24 significant bits, subnormal spacing 2**-149."""
+    if q == 0:
+        return Fraction(0)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)                      # binade [2**e, 2**(e+1)), or the subnormal range
+    ulp = Fraction(2) ** (e - 23)
+    m = a / ulp
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * n * ulp
+
+
+def pin_current_scaling(O):
+    """Current scaling with one FP32 scale per tensor or per leading group
+    ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §3.2: scale = valid(amax) ?
+    amax / format_max : 1.0 in FP32; dense per tensor, 3-D grouped weights per
+    leading group), on E4M3 data: closed forms, the FP32 rounding of the scale
+    and of the quotient, validity, per-group independence, exact GEMM values."""
+    # the page's own format maxima: amax 30 with 15 -> 2, amax 448 with 224 -> 2
+    assert O.current_scale(30.0, 15.0) == 2.0 and O.current_scale(448.0, 224.0) == 2.0
+    assert O.current_scale(7.5, 15.0) == 0.5
+    # E4M3: 448 -> 1, 224 -> 0.5, 896 -> 2 (exact), and amax 1 -> the FP32 nearest 1/448
+    assert O.current_scale(448.0) == 1.0 and O.current_scale(224.0) == 0.5 and O.current_scale(896.0) == 2.0
+    assert Fraction(float(O.current_scale(1.0))) == _fp32_rn(Fraction(1, 448))
+    # invalid amax (zero, infinite, NaN) -> 1.0
+    for a in (0.0, float("inf"), float("nan")):
+        assert O.current_scale(a) == 1.0
+    # the scale is the FP32 rounding of amax / 448 over BF16 amax values,
+    # subnormal FP32 scales included (BF16 subnormal amax)
+    g = np.random.Generator(np.random.Philox(31))
+    pats = np.concatenate([g.integers(0x0001, 0x7F80, 400), [0x0001, 0x007F, 0x0080, 0x7F7F]]).astype(np.uint32)
+    for b in pats:
+        a = float((b << 16).astype(np.uint32).view(np.float32))
+        assert Fraction(float(O.current_scale(a))) == _fp32_rn(Fraction(a) / 448), hex(int(b))
+    # one element: amax 3 -> s = fl32(3/448); x = 1 -> fl32(1/s) = 149.33... lies in
+    # [144, 160) below the midpoint 152 -> 144 = 1.125 * 2**7 -> 0x71; x = -3 -> -448 -> 0xFE
+    s3 = O.current_scale(3.0)
+    assert Fraction(float(s3)) == _fp32_rn(Fraction(3, 448))
+    assert O.current_encode(np.array([1.0, -3.0, 0.0, -0.0]), s3).tolist() == [0x71, 0xFE, 0x00, 0x80]
+    # the quotient is rounded to FP32 before E4M3: amax 0.6875 -> s = fl32(11/7168);
+    # x = 33/512 gives x/s = 42.0000009..., whose FP32 rounding is exactly 42, the
+    # midpoint of 40 (0x62, even mantissa) and 44 (0x63): ties to even -> 0x62 (the
+    # exact quotient would round up to 0x63)
+    s = O.current_scale(0.6875)
+    assert Fraction(float(s)) == _fp32_rn(Fraction(11, 7168))
+    q = Fraction(33, 512) / Fraction(float(s))
+    assert q > 42 and _fp32_rn(q) == 42
+    assert O.current_encode(np.array([0.064453125]), s)[0] == 0x62
+    # every element against exact arithmetic on a random tensor with an outlier;
+    # the amax element lands on +-448 (the quotient is within an FP32 rounding of 448)
+    x = g.standard_normal((8, 40)).astype(np.float32).astype(np.float64)
+    x[3, 7] = -57.25
+    codes, sc, amax = O.current_quantize(x)
+    assert amax == 57.25 and Fraction(float(sc)) == _fp32_rn(Fraction(57.25) / 448)
+    assert codes[3, 7] == 0xFE
+    for i in range(0, 8, 3):
+        for j in range(0, 40, 7):
+            qv = _fp32_rn(Fraction(x[i, j]) / Fraction(float(sc)))
+            assert codes[i, j] == O.e4m3_encode(np.array([float(qv)]))[0]
+    # scale 1 (amax exactly 448): the codes are the plain E4M3 codes
+    y = np.array([[448.0, 2.0, -0.25, 3.3]])
+    cy, sy, _ = O.current_quantize(y)
+    assert sy == 1.0 and np.array_equal(cy, O.e4m3_encode(y))
+    # per leading group: each group's scale from its own amax only
+    w = g.standard_normal((3, 16, 32)) * np.array([1.0, 100.0, 0.001])[:, None, None]
+    cw, sw, aw = O.current_quantize_groups(w)
+    for e in range(3):
+        assert sw[e] == O.current_scale(np.abs(w[e]).max()) and aw[e] == np.abs(w[e]).max()
+    cw2, sw2, _ = O.current_quantize_groups(w[::-1])
+    assert np.array_equal(sw2, sw[::-1]) and np.array_equal(cw2, cw[::-1])
+    # GEMM: exact rational sum of (qa * s_a) * (qb * s_b)
+    a = g.integers(0, 0x7E, size=(3, 64)).astype(np.uint8) | (g.integers(0, 2, size=(3, 64)) << 7).astype(np.uint8)
+    b = g.integers(0, 0x7E, size=(2, 64)).astype(np.uint8)
+    sa, sb = np.float32(0.3), np.float32(1.7)
+    ref, S = O.current_gemm_ref(a, sa, b, sb)
+    av, bv = O.e4m3_decode(a), O.e4m3_decode(b)
+    for i in range(3):
+        for j in range(2):
+            exact = sum(Fraction(av[i, k]) * Fraction(bv[j, k]) for k in range(64)) * Fraction(float(sa)) * \
+                Fraction(float(sb))
+            assert abs(Fraction(ref[i, j]) - exact) <= abs(exact) * Fraction(1, 2 ** 48) + Fraction(1, 2 ** 80)
+            assert S[i, j] >= abs(ref[i, j])
+    # grouped operand layout: rows of group e transposed into its padded segment
+    c = g.integers(1, 255, size=(200, 5)).astype(np.uint8)
+    offs = np.array([0, 0, 130, 131, 200])
+    t = O.current_transpose_grouped(c, offs)
+    assert t.shape == (5, 0 + 256 + 128 + 128)
+    for col in range(5):
+        assert np.array_equal(t[col, 0:130], c[0:130, col]) and np.all(t[col, 130:256] == 0)
+        assert t[col, 256] == c[130, col] and np.all(t[col, 257:384] == 0)
+        assert np.array_equal(t[col, 384:453], c[131:200, col]) and np.all(t[col, 453:] == 0)
+
+
 def pin_swiglu(O):
     """SiLU by its closed forms, SwiGLU's gate/up halves by explicit loops, and
     the grouped SwiGLU reference on one-hot operands whose dots are single
@@ -602,5 +703,5 @@ ALL_PINS = [
     pin_e4m3_vs_torch, pin_e4m3_saturation, pin_bf16_vs_torch, pin_scale_hand_blocks,
     pin_fp32_master_blocks, pin_quant_error_bound, pin_row_col_blocking, pin_scale_layout, pin_grouped_quant,
     pin_gemm_bruteforce, pin_gemm_single_block, pin_gemm_modes, pin_grouped_gemm, pin_blockwise_fp8, pin_swiglu,
-    pin_tolerance,
+    pin_current_scaling, pin_tolerance,
 ]

@@ -209,6 +209,42 @@ def m_blockwise_weight_rows(O):
     O.quantize_128x128 = q
 
 
+def m_current_scale_inverted(O):
+    orig = O.current_scale
+    O.current_scale = lambda amax, fmt=448.0: np.float32(1.0) / orig(amax, fmt)
+
+
+def m_current_multiplies(O):
+    O.current_encode = lambda x, s: O.e4m3_encode((np.asarray(x, dtype=np.float32) * np.float32(s)).astype(np.float64))
+
+
+def m_current_exact_quotient(O):
+    O.current_encode = lambda x, s: O.e4m3_encode(np.asarray(x, dtype=np.float64) / np.float64(np.float32(s)))
+
+
+def m_current_no_validity(O):
+    def sc(amax, fmt=448.0):
+        with np.errstate(all="ignore"):
+            return np.float32(np.float32(amax) / np.float32(fmt))
+    O.current_scale = sc
+
+
+def m_current_groups_share_amax(O):
+    def q(w, fmt=448.0):
+        w = np.asarray(w, dtype=np.float64)
+        amax = O.current_amax(w)
+        s = O.current_scale(amax, fmt)
+        E = w.shape[0]
+        return O.current_encode(w, s), np.full(E, s, dtype=np.float32), np.full(E, amax)
+    O.current_quantize_groups = q
+
+
+def m_current_transpose_unpadded(O):
+    def t(codes, offsets):
+        return np.ascontiguousarray(np.asarray(codes, dtype=np.uint8).T)
+    O.current_transpose_grouped = t
+
+
 def m_tolerance_loose(O):
     O.within_tolerance = lambda out, ref, S: np.abs(np.asarray(out) - ref) <= 2.0 ** -5 * np.abs(ref) + 1e-6 * S
 
@@ -218,7 +254,9 @@ MUTANTS = [m_scale_off_by_one, m_scale_ceil, m_zero_block_scale_one, m_ties_away
            m_colwise_not_transposed, m_gemm_transposed, m_gemm_drop_b_scale, m_dequant_scale_sign,
            m_swizzle_swapped, m_group_blocks_not_restarting, m_group_pad_64, m_bf16_truncate,
            m_tolerance_loose, m_input_bf16_prerounding, m_swiglu_halves_swapped, m_silu_sign,
-           m_blockwise_scale_inverted, m_blockwise_promote_multiplies, m_blockwise_weight_rows]
+           m_blockwise_scale_inverted, m_blockwise_promote_multiplies, m_blockwise_weight_rows,
+           m_current_scale_inverted, m_current_multiplies, m_current_exact_quotient, m_current_no_validity,
+           m_current_groups_share_amax, m_current_transpose_unpadded]
 
 
 def _caught(O):
