@@ -6,7 +6,8 @@ fprop, dgrad and wgrad block-scaled GEMMs. Default workload: the dense FFN
 up-projection (tokens M=8192, K=2048, N=10944), DeepSeek-V3 16B shaped. The
 default line also carries every other workload's own measurement under
 "configs" (single Linear, MLA projections, routed experts, quantiser sweep,
-blockwise FP8 variant, FP32 weight refresh); --workload NAME prints one alone.
+blockwise FP8 and current-scaling variants, FP32 weight refresh); --workload
+NAME prints one alone.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dense_ffn]
     python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -1089,6 +1090,81 @@ def run_blockwise(args, rank, world, peaks, peak_src):
     return line
 
 
+def run_current(args, rank, world, peaks, peak_src):
+    """Variant recipe: the dense FFN up-projection step with current scaling
+    (one FP32 scale per tensor from its amax, E4M3 data): per tensor an amax
+    launch and a quantisation launch (row + transposed copy), then fprop, dgrad
+    and wgrad on the 256 x 256 pair kernel with two accumulators and the two
+    scales applied in the epilogue."""
+    import mxfp8_block_scaled_gb300 as mx
+    d = dense_host_inputs()
+    src = {k: d[k].cuda() for k in ("X", "W", "dY")}
+    M, K = src["X"].shape
+    N = src["W"].shape[0]
+    amax = {k: torch.empty(1, dtype=torch.float32, device="cuda") for k in src}
+    q = {k: mx.quantize_current(v, mx.MX_BOTH, amax=mx.current_amax(v)) for k, v in src.items()}
+    outs = [torch.empty(sh, dtype=torch.bfloat16, device="cuda") for sh in ((M, N), (M, K), (N, K))]
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+
+    def step(timers):
+        for k, x in src.items():
+            r, c = q[k]
+            e = timers.span("quant", stream) if timers else None
+            mx.mx_current_amax(x.data_ptr(), 1, x.shape[0], x.shape[1], x.stride(0), 0, amax[k].data_ptr(), None, sp)
+            mx.mx_quantize_current(x.data_ptr(), 1, x.shape[0], x.shape[1], x.stride(0), 0, mx.MX_BOTH,
+                                   amax[k].data_ptr(), mx.CURRENT_FORMAT_MAX, r.data.data_ptr(), c.data.data_ptr(),
+                                   r.scale.data_ptr(), None, 0, 0, None, sp)
+            if e is not None:
+                e.record(stream)
+        (xr, xc), (wr, wc), (dr, dc) = q["X"], q["W"], q["dY"]
+        for mode, a, b, o in ((mx.MX_FPROP, xr, wr, outs[0]), (mx.MX_DGRAD, dr, wc, outs[1]),
+                              (mx.MX_WGRAD, dc, xc, outs[2])):
+            e = timers.span("gemm", stream) if timers else None
+            mx.mx_gemm_current(mode, a.c_operand(), b.c_operand(), o.data_ptr(), o.stride(0), None, sp)
+            if e is not None:
+                e.record(stream)
+
+    ms, timers, clk = _measure(step, args, world, stream)
+    fl = 3 * 2.0 * M * N * K
+    gemm_ms = timers.total_ms("gemm") / args.steps
+    quant_ms = timers.total_ms("quant") / args.steps
+    # amax pass: 2 B read per element; quantisation: 2 B read + 2 x 1 B written
+    qbytes = sum((2 + 2 + 1 + 1) * x.numel() for x in src.values())
+    line = {"metric": "MXFP8-path GEMM TFLOPS with current scaling (one FP32 scale per tensor; fprop+dgrad+wgrad "
+                      "step incl. amax and quantisation, dense FFN up-proj)",
+            "value": world * args.steps * fl / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": "dense_ffn_up_proj M=8192 K=2048 N=10944, current-scaling variant",
+                       "parallelism": f"replicas{world}", "l2": "no flush: a step moves ~1 GB (> 129 MB L2)"},
+            "roofline": tensor_roofline("mx_gemm_pair_kernel (tensor-scaled)", fl / (gemm_ms / 1e3) / 1e12, peaks,
+                                        peak_src, traffic=None, ms_per_step=gemm_ms),
+            "quant_roofline": {"bound": "hbm", "kernel": "cur_amax_kernel + mx_quant_kernel (current)",
+                               "achieved": qbytes / (quant_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": qbytes / (quant_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                               "bytes_per_step": qbytes, "ms_per_step": quant_ms,
+                               "basis": "amax pass 2 B/element + quantisation 4 B/element over the six launches"},
+            "gpu_launches": 9 * args.steps, "clocks": clk}
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        g = np.random.Generator(np.random.Philox(5))
+        rows = {k: np.sort(g.choice(v.shape[0], 256, replace=False)) for k, v in d.items() if k in ("X", "W")}
+
+        def sample(i):
+            fx, fw = _f64(d["X"][torch.from_numpy(rows["X"])]), _f64(d["W"][torch.from_numpy(rows["W"])])
+            t0 = time.perf_counter()
+            cx, sx, _ = oracle.current_quantize(fx)
+            cw, sw, _ = oracle.current_quantize(fw)
+            oracle.current_gemm_ref(cx, sx, cw, sw)
+            return 2.0 * 256 * 256 * K, time.perf_counter() - t0
+        v, dt, n = timed_cpu_baseline(sample, args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                                "seconds": dt, "sample": f"{n} x (256 rows of X and of W quantised with their own "
+                                                         "current scale, their 256x256x2048 GEMM)"}
+    return line
+
+
 def run_dense(args, rank, world, peaks, peak_src):
     """The headline: the dense FFN up-projection step (quantise X + W, dY;
     fprop; dgrad + wgrad in one launch), plus its end-to-end run from pinned
@@ -1160,11 +1236,12 @@ def run_dense(args, rank, world, peaks, peak_src):
 
 
 RUNS = {"dense_ffn": run_dense, "single": run_single, "mla": run_mla, "moe": run_moe, "quant": run_quant_sweep,
-        "wrefresh": run_wrefresh, "blockwise": run_blockwise}
+        "wrefresh": run_wrefresh, "blockwise": run_blockwise, "current": run_current}
 # Sub-results of the default line, keyed by the workload they measure.
 SUB_CONFIGS = (("config1_single_linear", "single"), ("config3_mla_projections", "mla"),
                ("config4_moe_routed_experts", "moe"), ("config5_quant_sweep", "quant"),
-               ("variant_blockwise_fp8", "blockwise"), ("weight_refresh_fp32_master", "wrefresh"))
+               ("variant_blockwise_fp8", "blockwise"), ("variant_current_scaling", "current"),
+               ("weight_refresh_fp32_master", "wrefresh"))
 
 
 def main():

@@ -407,6 +407,61 @@ mx_status mx_gemm_fp8_blockwise(const void* a_data, const float* a_scale, int64_
                                 void* stream);
 
 /*
+ * Variant recipe: current scaling with one FP32 scale per tensor or per
+ * leading group ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §3: HiF8 current
+ * scaling takes an FP32 scale from the current tensor's amax, a scalar for a
+ * dense tensor and one per leading group for a grouped one; §3.2: scale =
+ * valid(amax) ? amax / format_max : 1.0 in FP32, dense tensors per tensor,
+ * 3-D grouped weights per leading group; §8.2: activations and gradients take
+ * amax and scale at every quantisation, weights after the optimizer step).
+ * Here the data are E4M3 codes, so format_max is normally 448 (E4M3's largest
+ * value); the HiF8 dtype itself is not built. An element's code is
+ * E4M3(fl32(x / scale)): the quotient rounded to FP32, then to nearest E4M3,
+ * ties to even, saturating at 448 (NaN keeps its sign, +-Inf gives +-448).
+ * A valid amax is finite and above zero; otherwise the scale is 1.
+ *
+ * mx_current_amax - amax[b] = max |x| over matrix b of a BF16 stack
+ *   ([batch][rows, cols], row pitch ldx, matrix stride x_batch_stride
+ *   elements; cols % 32 == 0; x 16-byte aligned, ldx and the stride multiples
+ *   of 8). amax: FP32 device array of batch entries, written (NaN if a matrix
+ *   holds NaN, +Inf if it holds an infinity, 0 for an empty matrix). The
+ *   values can be combined (e.g. a maximum across ranks) before
+ *   mx_quantize_current reads them.
+ *
+ * mx_quantize_current - quantise with scale[b] = amax[b] / format_max (FP32;
+ *   1 for an invalid amax), written to scale (FP32 device array of batch).
+ *   The scale does not depend on the direction, so the two copies hold the
+ *   same codes in two layouts, each K-major for the GEMMs below:
+ *   row copy (MX_ROWWISE/BOTH): row_data [batch][rows][cols];
+ *   column copy (MX_COLWISE/BOTH): col_data [batch][cols][rows] (rows % 32 ==
+ *     0), or, with group offsets (batch 1, the int64 device offsets of
+ *     mx_quantize, 1 <= n_groups <= MX_MAX_GROUPS), [cols][col_capacity] with
+ *     group e's rows at columns poff[e] .. and zero codes in each segment's
+ *     padding to a multiple of 128 (the layout of mx_quantize's grouped column
+ *     copy). Outputs 16-byte aligned; errors as mx_quantize.
+ *
+ * mx_gemm_current / mx_grouped_gemm_current - mx_gemm / mx_grouped_gemm on
+ *   such operands: each mx_operand's `scale` is the FP32 scale array written
+ *   by mx_quantize_current (4-byte aligned): one value for an activation, a
+ *   gradient or a dense weight; one per expert for stacked expert weights
+ *   (b of the rows-ragged fprop and dgrad). C = (A_codes . B_codes^T) * s_a *
+ *   s_b with FP32 accumulation, the product of the two scales applied to the
+ *   FP32 accumulator once, then BF16 round-to-nearest-even. Modes, layouts,
+ *   groups and errors as mx_gemm / mx_grouped_gemm (wgrad: a and b are the
+ *   grouped column copies of dY and X, each with its one scale).
+ */
+mx_status mx_current_amax(const void* x, int64_t batch, int64_t rows, int64_t cols, int64_t ldx,
+                          int64_t x_batch_stride, float* amax, int* dev_status, void* stream);
+mx_status mx_quantize_current(const void* x, int64_t batch, int64_t rows, int64_t cols, int64_t ldx,
+                              int64_t x_batch_stride, int axis, const float* amax, float format_max, void* row_data,
+                              void* col_data, float* scale, const int64_t* group_offsets, int n_groups,
+                              int64_t col_capacity, int* dev_status, void* stream);
+mx_status mx_gemm_current(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,
+                          void* stream);
+mx_status mx_grouped_gemm_current(int mode, const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                                  int n_groups, void* c, int64_t ldc, int* dev_status, void* stream);
+
+/*
  * mx_grouped_gemm_swiglu - the routed experts' gate_up fprop with the grouped
  * SwiGLU fused into its epilogue ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计"
  * §5: gate_up_proj [E, 2F, H] and the grouped SwiGLU between gate_up and

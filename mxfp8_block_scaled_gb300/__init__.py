@@ -36,7 +36,8 @@ EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quant
             "mx_gemm", "mx_grouped_gemm", "mx_grouped_gemm_swiglu", "mx_quantize_fp8_blockwise",
             "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version",
             "mx_selftest_wait_timeout", "mx_gemm_workspace_bytes", "mx_gemm_with_workspace", "mx_gemm_multi",
-            "mx_gemm_static_workspace")
+            "mx_gemm_static_workspace", "mx_current_amax", "mx_quantize_current", "mx_gemm_current",
+            "mx_grouped_gemm_current")
 MX_STATIC_WORKSPACE_BYTES = 40 * 1024 * 1024
 
 
@@ -98,6 +99,16 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm_static_workspace.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64,
                                            vp, vp]
     L.mx_gemm_static_workspace.restype = i32
+    L.mx_current_amax.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp, vp]
+    L.mx_current_amax.restype = i32
+    L.mx_quantize_current.argtypes = [vp, i64, i64, i64, i64, i64, i32, vp, ctypes.c_float, vp, vp, vp, vp, i32, i64,
+                                      vp, vp]
+    L.mx_quantize_current.restype = i32
+    L.mx_gemm_current.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i64, vp, vp]
+    L.mx_gemm_current.restype = i32
+    L.mx_grouped_gemm_current.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp,
+                                          i64, vp, vp]
+    L.mx_grouped_gemm_current.restype = i32
     L.mx_gemm_multi.argtypes = [ctypes.POINTER(MXGemmProblemC), i32, vp, vp]
     L.mx_gemm_multi.restype = i32
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
@@ -214,6 +225,28 @@ def mx_gemm_with_workspace(mode, a: MXOperandC, b: MXOperandC, c, ldc, workspace
 def mx_gemm_static_workspace(mode, a: MXOperandC, b: MXOperandC, c, ldc, dev_status, stream) -> None:
     _check(lib().mx_gemm_static_workspace(mode, _ref(a), _ref(b), c, ldc, dev_status, stream),
            "mx_gemm_static_workspace")
+
+
+def mx_current_amax(x, batch, rows, cols, ldx, x_batch_stride, amax, dev_status, stream) -> None:
+    _check(lib().mx_current_amax(x, batch, rows, cols, ldx, x_batch_stride, amax, dev_status, stream),
+           "mx_current_amax")
+
+
+def mx_quantize_current(x, batch, rows, cols, ldx, x_batch_stride, axis, amax, format_max, row_data, col_data, scale,
+                        group_offsets, n_groups, col_capacity, dev_status, stream) -> None:
+    _check(lib().mx_quantize_current(x, batch, rows, cols, ldx, x_batch_stride, axis, amax, format_max, row_data,
+                                     col_data, scale, group_offsets, n_groups, col_capacity, dev_status, stream),
+           "mx_quantize_current")
+
+
+def mx_gemm_current(mode, a: MXOperandC, b: MXOperandC, c, ldc, dev_status, stream) -> None:
+    _check(lib().mx_gemm_current(mode, _ref(a), _ref(b), c, ldc, dev_status, stream), "mx_gemm_current")
+
+
+def mx_grouped_gemm_current(mode, a: MXOperandC, b: MXOperandC, group_offsets, n_groups, c, ldc, dev_status,
+                            stream) -> None:
+    _check(lib().mx_grouped_gemm_current(mode, _ref(a), _ref(b), group_offsets, n_groups, c, ldc, dev_status, stream),
+           "mx_grouped_gemm_current")
 
 
 def mx_gemm_multi(problems, dev_status, stream) -> None:
@@ -481,4 +514,79 @@ def gemm_fp8_blockwise(a: FP8Blockwise, b: FP8Blockwise, out=None, status=None, 
         out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
     mx_gemm_fp8_blockwise(a.data.data_ptr(), a.scale.data_ptr(), a.rows, b.data.data_ptr(), b.scale.data_ptr(),
                           b.rows, a.k, out.data_ptr(), out.stride(0), _ptr(status), _stream(stream))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Current-scaling variant (one FP32 scale per tensor or per expert)
+# ---------------------------------------------------------------------------
+
+CURRENT_FORMAT_MAX = 448.0
+
+
+def current_amax(x, status=None, stream=None):
+    """amax of a 2-D BF16 tensor ([1] FP32) or of each matrix of a 3-D stack ([E])."""
+    torch = _torch()
+    xs = x if x.dim() == 3 else x.unsqueeze(0)
+    assert xs.dtype == torch.bfloat16 and xs.is_cuda and xs.stride(2) == 1
+    E, R, C = xs.shape
+    amax = torch.empty(E, dtype=torch.float32, device=x.device)
+    mx_current_amax(xs.data_ptr(), E, R, C, xs.stride(1), xs.stride(0), amax.data_ptr(), _ptr(status), _stream(stream))
+    return amax
+
+
+def quantize_current(x, axis: int = MX_BOTH, amax=None, format_max: float = CURRENT_FORMAT_MAX, group_offsets=None,
+                     col_capacity: Optional[int] = None, status=None, stream=None):
+    """Current-scaling quantisation of a 2-D BF16 tensor (or a 3-D stack, one
+    scale per matrix). amax: FP32 [batch] (computed here when None). Returns
+    (row_copy, col_copy); each copy's `scale` is the FP32 scale tensor [batch]
+    (the same tensor for both copies)."""
+    torch = _torch()
+    stacked = x.dim() == 3
+    xs = x if stacked else x.unsqueeze(0)
+    E, R, C = xs.shape
+    dev = x.device
+    if amax is None:
+        amax = current_amax(x, status=status, stream=stream)
+    scale = torch.empty(E, dtype=torch.float32, device=dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    row = col = None
+    n_groups, cap = 0, 0
+    if axis & MX_ROWWISE:
+        d = torch.empty((E, R, C), **u8)
+        row = (MXStacked(d, scale, R, C, MX_ROWWISE) if stacked else MXTensor(d[0], scale, R, C, MX_ROWWISE))
+    if axis & MX_COLWISE:
+        if group_offsets is not None:
+            assert not stacked
+            n_groups = group_offsets.numel() - 1
+            cap = int(col_capacity) if col_capacity is not None else ((R + 127 * n_groups + 127) // 128) * 128
+            col = MXTensor(torch.empty((C, cap), **u8), scale, C, cap, MX_COLWISE)
+        else:
+            d = torch.empty((E, C, R), **u8)
+            col = (MXStacked(d, scale, C, R, MX_COLWISE) if stacked else MXTensor(d[0], scale, C, R, MX_COLWISE))
+    mx_quantize_current(xs.data_ptr(), E, R, C, xs.stride(1), xs.stride(0), axis, amax.data_ptr(), float(format_max),
+                        _ptr(row.data) if row else None, _ptr(col.data) if col else None, scale.data_ptr(),
+                        _ptr(group_offsets), n_groups, cap, _ptr(status), _stream(stream))
+    return row, col
+
+
+def gemm_current(mode: int, a, b, out=None, status=None, stream=None):
+    """C[M, N] = (A . B^T) * s_a * s_b in BF16 for current-scaled operands."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
+    mx_gemm_current(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), _ptr(status), _stream(stream))
+    return out
+
+
+def grouped_gemm_current(mode: int, a, b, group_offsets, out=None, status=None, stream=None):
+    """Grouped GEMM on current-scaled operands (layouts as grouped_gemm; the
+    stacked weights carry one scale per expert)."""
+    torch = _torch()
+    E = group_offsets.numel() - 1
+    if out is None:
+        shape = (E, a.rows, b.rows) if mode == MX_WGRAD else (a.rows, b.rows)
+        out = torch.empty(shape, dtype=torch.bfloat16, device=a.data.device)
+    mx_grouped_gemm_current(mode, a.c_operand(), b.c_operand(), group_offsets.data_ptr(), E, out.data_ptr(),
+                            out.stride(-2), _ptr(status), _stream(stream))
     return out

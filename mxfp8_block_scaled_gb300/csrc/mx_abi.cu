@@ -638,6 +638,271 @@ mx_status mx_gemm_multi(const mx_gemm_problem* problems, int n, int* dev_status,
   return m ? launch_gemm_multi(live, m, s) : MX_OK;
 }
 
+static mx_status current_input_check(const char* fn, const void* x, int64_t batch, int64_t rows, int64_t cols,
+                                     int64_t ldx, int64_t x_batch_stride) {
+  if (batch < 0 || rows < 0 || cols < 0 || ldx < cols || x_batch_stride < 0) {
+    set_error("%s: bad sizes", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (batch > 0x7FFFFFFFLL || rows > 0x7FFFFFFFLL) {
+    set_error("%s: batch and rows must be < 2^31", fn);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (batch > 1 && x_batch_stride < rows * ldx) {
+    set_error("%s: x_batch_stride < rows * ldx", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (cols % 32 != 0) {
+    set_error("%s: cols = %lld is not a multiple of 32", fn, static_cast<long long>(cols));
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (batch > 0 && rows > 0 && cols > 0) {
+    if (!x) {
+      set_error("%s: x is null", fn);
+      return MX_ERR_INVALID_ARG;
+    }
+    if (!aligned16(x) || ldx % 8 != 0 || (batch > 1 && x_batch_stride % 8 != 0)) {
+      set_error("%s: x must be 16-byte aligned with ldx and x_batch_stride multiples of 8", fn);
+      return MX_ERR_ALIGNMENT;
+    }
+  }
+  return MX_OK;
+}
+
+mx_status mx_current_amax(const void* x, int64_t batch, int64_t rows, int64_t cols, int64_t ldx,
+                          int64_t x_batch_stride, float* amax, int* dev_status, void* stream) {
+  (void)dev_status;
+  mx_status st = current_input_check("mx_current_amax", x, batch, rows, cols, ldx, x_batch_stride);
+  if (st != MX_OK) return st;
+  if (batch == 0) return MX_OK;
+  if (!amax || (reinterpret_cast<uintptr_t>(amax) & 3u) != 0) {
+    set_error("mx_current_amax: amax must be a non-null, 4-byte aligned device array of batch floats");
+    return amax ? MX_ERR_ALIGNMENT : MX_ERR_INVALID_ARG;
+  }
+  st = check_device();
+  if (st != MX_OK) return st;
+  QuantLaunch q{};
+  q.x = x;
+  q.rows = rows;
+  q.cols = cols;
+  q.ldx = ldx;
+  q.batch = batch;
+  q.x_batch_stride = x_batch_stride;
+  return launch_current_amax(q, amax, static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_quantize_current(const void* x, int64_t batch, int64_t rows, int64_t cols, int64_t ldx,
+                              int64_t x_batch_stride, int axis, const float* amax, float format_max, void* row_data,
+                              void* col_data, float* scale, const int64_t* group_offsets, int n_groups,
+                              int64_t col_capacity, int* dev_status, void* stream) {
+  const char* fn = "mx_quantize_current";
+  mx_status st = current_input_check(fn, x, batch, rows, cols, ldx, x_batch_stride);
+  if (st != MX_OK) return st;
+  if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) {
+    set_error("%s: axis must be MX_ROWWISE, MX_COLWISE or MX_BOTH", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (!(format_max > 0.0f) || !(format_max <= 3.402823466e38f)) {
+    set_error("%s: format_max must be finite and above zero", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  const bool do_row = (axis & MX_ROWWISE) != 0;
+  const bool do_col = (axis & MX_COLWISE) != 0;
+  const bool grouped = group_offsets != nullptr;
+  if (grouped) {
+    if (!do_col || batch != 1 || n_groups < 1) {
+      set_error("%s: group offsets apply to the column copy of one matrix, with n_groups >= 1", fn);
+      return MX_ERR_INVALID_ARG;
+    }
+    if (n_groups > MX_MAX_GROUPS) {
+      set_error("%s: n_groups = %d is above MX_MAX_GROUPS (%d)", fn, n_groups, MX_MAX_GROUPS);
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (col_capacity < 0 || col_capacity % 128 != 0) {
+      set_error("%s: col_capacity must be a non-negative multiple of 128", fn);
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+  } else if (do_col && rows % 32 != 0) {
+    set_error("%s: the column copy needs rows %% 32 == 0", fn);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (batch == 0) return MX_OK;
+  if (!amax || !scale || (reinterpret_cast<uintptr_t>(amax) & 3u) || (reinterpret_cast<uintptr_t>(scale) & 3u)) {
+    set_error("%s: amax and scale must be non-null, 4-byte aligned device arrays of batch floats", fn);
+    return (amax && scale) ? MX_ERR_ALIGNMENT : MX_ERR_INVALID_ARG;
+  }
+  if (rows > 0 && cols > 0) {
+    if ((do_row && !row_data) || (do_col && !col_data)) {
+      set_error("%s: a requested output is null", fn);
+      return MX_ERR_INVALID_ARG;
+    }
+    if ((do_row && !aligned16(row_data)) || (do_col && !aligned16(col_data))) {
+      set_error("%s: outputs must be 16-byte aligned", fn);
+      return MX_ERR_ALIGNMENT;
+    }
+    if (grouped && col_capacity == 0) {
+      set_error("%s: col_capacity is 0 but rows > 0", fn);
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+  }
+  st = check_device();
+  if (st != MX_OK) return st;
+  QuantLaunch q{};
+  q.x = x;
+  q.rows = rows;
+  q.cols = cols;
+  q.ldx = ldx;
+  q.row_data = row_data;
+  q.col_data = col_data;
+  q.offsets = group_offsets;
+  q.n_groups = grouped ? n_groups : 0;
+  q.col_pitch = grouped ? col_capacity : rows;
+  q.batch = batch;
+  q.x_batch_stride = x_batch_stride;
+  q.dev_status = dev_status;
+  return launch_quantize_current(q, amax, format_max, scale, do_row, do_col, static_cast<cudaStream_t>(stream));
+}
+
+// Operands of the current-scaling GEMMs: E4M3 codes as for mx_gemm, `scale`
+// an FP32 device array (one scale, or one per expert for stacked weights).
+static mx_status check_current_operand(const mx_operand* o, const char* name) {
+  if (!o) {
+    set_error("%s: null operand", name);
+    return MX_ERR_INVALID_ARG;
+  }
+  mx_operand m = *o;
+  const void* sc = m.scale;
+  m.scale = m.data;  // the E8M0 checks do not apply to an FP32 scale
+  mx_status st = check_operand(&m, name);
+  if (st != MX_OK) return st;
+  if (o->rows > 0 && o->k > 0) {
+    if (!sc) {
+      set_error("%s: null scale", name);
+      return MX_ERR_INVALID_ARG;
+    }
+    if ((reinterpret_cast<uintptr_t>(sc) & 3u) != 0) {
+      set_error("%s: the FP32 scale must be 4-byte aligned", name);
+      return MX_ERR_ALIGNMENT;
+    }
+  }
+  return MX_OK;
+}
+
+mx_status mx_gemm_current(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,
+                          void* stream) {
+  const char* fn = "mx_gemm_current";
+  mx_status st = check_current_operand(a, "a");
+  if (st != MX_OK) return st;
+  st = check_current_operand(b, "b");
+  if (st != MX_OK) return st;
+  st = check_mode(mode, a, b);
+  if (st != MX_OK) return st;
+  if (a->k != b->k) {
+    set_error("%s: a.k != b.k", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (a->rows > 0x7FFFFFFFLL || b->rows > 0x7FFFFFFFLL || a->k > 0x7FFFFFFFLL) {
+    set_error("%s: sizes must be < 2^31", fn);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  st = check_output(c, ldc, b->rows, a->rows);
+  if (st != MX_OK) return st;
+  if (a->rows == 0 || b->rows == 0) return MX_OK;
+  st = check_device();
+  if (st != MX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->k == 0) return zero_output(c, ldc, b->rows, a->rows, s);
+  GemmLaunch L;
+  L.kind = GEMM_DENSE;
+  L.a_data = a->data;
+  L.a_scale = a->scale;
+  L.a_ld = a->ld ? a->ld : a->k;
+  L.b_data = b->data;
+  L.b_scale = b->scale;
+  L.b_ld = b->ld ? b->ld : b->k;
+  L.M = a->rows;
+  L.N = b->rows;
+  L.K = a->k;
+  L.b_rows_total = b->rows;
+  L.c = c;
+  L.ldc = ldc;
+  L.offsets = nullptr;
+  L.n_groups = 0;
+  L.dev_status = dev_status;
+  L.tensor_scaled = true;
+  return launch_gemm(L, s);
+}
+
+mx_status mx_grouped_gemm_current(int mode, const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                                  int n_groups, void* c, int64_t ldc, int* dev_status, void* stream) {
+  const char* fn = "mx_grouped_gemm_current";
+  mx_status st = check_current_operand(a, "a");
+  if (st != MX_OK) return st;
+  st = check_current_operand(b, "b");
+  if (st != MX_OK) return st;
+  st = check_mode(mode, a, b);
+  if (st != MX_OK) return st;
+  if (!group_offsets || n_groups < 1) {
+    set_error("%s: group_offsets must be non-null and n_groups >= 1", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (n_groups > MX_MAX_GROUPS) {
+    set_error("%s: n_groups = %d is above MX_MAX_GROUPS (%d)", fn, n_groups, MX_MAX_GROUPS);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (a->k != b->k) {
+    set_error("%s: a.k != b.k", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (a->rows > 0x7FFFFFFFLL || b->rows > 0x7FFFFFFFLL || a->k > 0x7FFFFFFFLL) {
+    set_error("%s: sizes must be < 2^31", fn);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemmLaunch L;
+  L.a_data = a->data;
+  L.a_scale = a->scale;
+  L.a_ld = a->ld ? a->ld : a->k;
+  L.b_data = b->data;
+  L.b_scale = b->scale;
+  L.b_ld = b->ld ? b->ld : b->k;
+  L.K = a->k;
+  L.c = c;
+  L.ldc = ldc;
+  L.offsets = group_offsets;
+  L.n_groups = n_groups;
+  L.dev_status = dev_status;
+  L.tensor_scaled = true;
+  if (mode == MX_WGRAD) {
+    if (a->k % 128 != 0) {
+      set_error("%s: wgrad capacity (a.k) must be a multiple of 128", fn);
+      return MX_ERR_UNSUPPORTED_SHAPE;
+    }
+    st = check_output(c, ldc, b->rows, a->rows * static_cast<int64_t>(n_groups));
+    if (st != MX_OK) return st;
+    if (a->rows == 0 || b->rows == 0) return MX_OK;
+    st = check_device();
+    if (st != MX_OK) return st;
+    if (a->k == 0) return zero_output(c, ldc, b->rows, a->rows * static_cast<int64_t>(n_groups), s);
+    L.kind = GEMM_GROUPED_K;
+    L.M = a->rows;
+    L.N = b->rows;
+    L.b_rows_total = b->rows;
+  } else {
+    st = check_output(c, ldc, b->rows, a->rows);
+    if (st != MX_OK) return st;
+    if (a->rows == 0 || b->rows == 0) return MX_OK;
+    st = check_device();
+    if (st != MX_OK) return st;
+    if (a->k == 0) return zero_output(c, ldc, b->rows, a->rows, s);
+    L.kind = GEMM_GROUPED_M;
+    L.M = a->rows;
+    L.N = b->rows;
+    L.b_rows_total = b->rows * static_cast<int64_t>(n_groups);
+  }
+  return launch_gemm(L, s);
+}
+
 mx_status mx_quantize_fp8_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,
                                     float* scale, int* dev_status, void* stream) {
   (void)dev_status;

@@ -114,32 +114,49 @@ struct Cfg {
   }
 };
 
-// CTA-pair configuration: 256 x 256 tiles, each CTA holds 128 rows of A and
-// 128 rows of B per stage plus its A scale atom and both B scale atoms.
+// CTA-pair configurations: 256 x 256 tiles. Each CTA loads its 128 rows of A
+// and 128 rows of B per stage (plus, with block scales, its A scale atom and
+// both B scale atoms), and its tensor memory holds its 128 rows of the
+// accumulator.
+//   Block scales: one 256-column accumulator; the six stages' scale slots
+//     take 72 of the remaining columns, so the next tile's MMAs wait for the
+//     epilogue to drain the accumulator.
+//   kTS (one FP32 scale per tensor or per group, no block scales): two
+//     256-column accumulators take all 512 columns, so the epilogue drains
+//     one while the MMAs fill the other; no scale slots, no scale copies.
 #ifndef MX_PAIR_STAGES
 #define MX_PAIR_STAGES 6
 #endif
 #ifndef MX_PAIR_EPI_BUFS
 #define MX_PAIR_EPI_BUFS 1
 #endif
-struct PairCfg {
-  static constexpr int BN = 256;
+template <int BN_, bool kTS_, bool kGrouped_>
+struct PairCfgT {
+  static constexpr int BN = BN_;
+  static constexpr bool kTS = kTS_;
+  static_assert(BN == 256, "pair tiles are 256 wide");
   static constexpr int kStages = MX_PAIR_STAGES;
   static constexpr int kEpiBufs = MX_PAIR_EPI_BUFS;  // staging boxes per epilogue warp
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = (BN / 2) * kBK;
-  static constexpr int kSfbBytes = 2 * 512;
-  static constexpr int kStageTx = kABytes + kBBytes + 512 + kSfbBytes;  // bytes one CTA loads per stage
-  static constexpr int kSfCols = 4 + 8;
-  static constexpr uint32_t kSfCol0 = BN;
+  static constexpr int kSfaBytes = kTS ? 0 : 512;
+  static constexpr int kSfbBytes = kTS ? 0 : 2 * 512;
+  static constexpr int kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // bytes of one CTA's stage
+  static constexpr int kSfCols = kTS ? 0 : 4 + 8;
+  static constexpr int kAcc = (2 * BN + kStages * kSfCols <= static_cast<int>(kTmemCols)) ? 2 : 1;
+  static constexpr uint32_t kSfCol0 = kAcc * BN;
   static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM budget");
-  static constexpr int kBarBytes = (4 * kStages + 4) * 8 + 16 + 2 * MX_MAX_GEMM_MULTI * 4;  // + schedule words
+  static constexpr int kBarBytes = (4 * kStages + 6) * 8 + 16 + 2 * MX_MAX_GEMM_MULTI * 4;  // + schedule words
   static constexpr int kGroupBytes = 3 * (kMaxGroups + 1) * 4;
-  __host__ __device__ static constexpr size_t smem_bytes(bool grouped) {
+  __host__ __device__ static constexpr size_t smem_bytes() {
     return 1024 + static_cast<size_t>(kStages) * kStageTx + kEpiBufs * kEpiBytes + kBarBytes +
-           (grouped ? kGroupBytes : 0);
+           (kGrouped_ ? kGroupBytes : 0);
   }
 };
+// The configuration bookkeeping that does not depend on the tile width.
+using PairCfg = PairCfgT<256, false, false>;
+static_assert(PairCfgT<256, false, true>::smem_bytes() <= 232448, "shared memory");
+static_assert(PairCfgT<256, true, true>::smem_bytes() <= 232448, "shared memory");
 
 struct GParams {
   const uint8_t* a_scale;
@@ -171,6 +188,10 @@ struct GParams {
   int32_t sk_w;
   int32_t sk_slots;
   float* ws;
+  // One FP32 scale per tensor (kTS kernels): C = (A . B^T) * ts_a[0] * ts_b[g]
+  // with g the tile's expert for rows-ragged grouped GEMMs, else 0.
+  const float* ts_a;
+  const float* ts_b;
 };
 
 // One segment's partial tile in the workspace: [unit][cta of the pair][epilogue
@@ -269,11 +290,10 @@ __device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, i
 }
 
 // Pair tiles: t enumerates (pair of M tiles, N tile); the CTA's rank in its
-// cluster picks the M tile, both CTAs share the 256-wide N tile. K-ragged
+// cluster picks the M tile, both CTAs share the BN-wide N tile. K-ragged
 // grouped: experts in decreasing-K order, each expert's pair tiles M-fastest.
-template <int KIND, bool kSwiGLU = false>
+template <int KIND, bool kSwiGLU, int BN>
 __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo& g, int64_t t, uint32_t crank) {
-  constexpr int BN = PairCfg::BN;
   const int64_t nt = (p.N + BN - 1) / BN;
   const int64_t mu = ((p.M + kBM - 1) / kBM + 1) / 2;
   Tile ti;
@@ -868,32 +888,37 @@ __device__ __forceinline__ int problem_of(const PairArgs& args, int64_t t) {
   return i;
 }
 
-template <int KIND, bool kSwiGLU = false, bool kMulti = false>
+template <int KIND, bool kSwiGLU, bool kMulti, int BN_, bool kTS>
 __global__ void __launch_bounds__(kPairThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ PairArgs args) {
-  using C = PairCfg;
+  using C = PairCfgT<BN_, kTS, KIND != GEMM_DENSE>;
   static_assert(!kMulti || (KIND == GEMM_DENSE && !kSwiGLU), "several problems per launch: dense GEMMs only");
   // Problem 0 holds the fields every problem shares (status word, wait bound)
   // and, unless kMulti, the whole GEMM.
   const GParams& p = args.prob[0].p;
-  static_assert(!kSwiGLU || KIND == GEMM_GROUPED_M, "the SwiGLU epilogue follows the grouped gate_up fprop");
+  static_assert(!kSwiGLU || (KIND == GEMM_GROUPED_M && BN_ == 256 && !kTS),
+                "the SwiGLU epilogue follows the grouped gate_up fprop");
   // Rows-ragged tiles start at any row: each CTA gathers its A scale atom.
-  constexpr bool kGatherSfa = (KIND == GEMM_GROUPED_M);
+  constexpr bool kGatherSfa = (KIND == GEMM_GROUPED_M) && !kTS;
+  constexpr bool kGather = kGatherSfa;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
+  constexpr int ACC = C::kAcc;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Operand tiles (1024-byte aligned for the 128-byte swizzle), the epilogue's
+  // staging boxes (1024-byte aligned), then the scale atoms (16-byte aligned).
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * C::kABytes;
-  uint8_t* sSfa = sB + S * C::kBBytes;
-  uint8_t* sSfb = sSfa + S * 512;
-  uint8_t* sEpi = sSfb + S * C::kSfbBytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + C::kEpiBufs * kEpiBytes);  // used in the even CTA
+  uint8_t* sEpi = sB + S * C::kBBytes;
+  uint8_t* sSfa = sEpi + C::kEpiBufs * kEpiBytes;
+  uint8_t* sSfb = sSfa + S * C::kSfaBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sSfb + S * C::kSfbBytes);  // used in the even CTA
   uint64_t* empty_bar = full_bar + S;
-  uint64_t* acc_full = empty_bar + S;
-  uint64_t* acc_empty = acc_full + 1;  // used in the even CTA
-  uint64_t* drain_bar = acc_empty + 1;
+  uint64_t* acc_full = empty_bar + S;  // [ACC]
+  uint64_t* acc_empty = acc_full + 2;  // [ACC], used in the even CTA
+  uint64_t* drain_bar = acc_empty + 2;
   uint64_t* sf_full = drain_bar + 1;  // used in the even CTA
   uint64_t* sf_drain = sf_full + S;
   uint64_t* gfull = sf_drain + 1;  // odd CTA: its own gathered scale atom landed
@@ -903,7 +928,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   int32_t* s_total = reinterpret_cast<int32_t*>(s_tmem + 3);
   int32_t* s_seq = reinterpret_cast<int32_t*>(s_tmem + 4);  // scheduled: [first tile of each problem][count]
   GroupInfo g;
-  g.off = reinterpret_cast<int32_t*>(smem + C::smem_bytes(false) - 1024);
+  g.off = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(s_tmem) + 16 + 2 * MX_MAX_GEMM_MULTI * 4);
   g.tile = g.off + (kMaxGroups + 1);
   g.order = g.tile + (kMaxGroups + 1);
   g.total = 0;
@@ -925,12 +950,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int s = 0; s < S; ++s) {
       // The leader's expect_tx (both CTAs' loads complete the bytes); with a
       // scale gather also the leader's 32 cp.async lanes and the odd CTA's relay.
-      mbar_init(&full_bar[s], kGatherSfa ? 34 : 1);
+      mbar_init(&full_bar[s], kGather ? 34 : 1);
       mbar_init(&empty_bar[s], 1);  // the leader's MMA commit, multicast to both CTAs
       mbar_init(&gfull[s], 32);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 16);       // one arrival per epilogue warp of both CTAs
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 16);  // one arrival per epilogue warp of both CTAs
+    }
     mbar_init(drain_bar, 1);
     for (int s = 0; s < S; ++s) mbar_init(&sf_full[s], 1);
     mbar_init(sf_drain, 1);
@@ -951,8 +978,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int i = 0; i < (kMulti ? args.n : 1); ++i) {
       tma_prefetch_desc(&args.prob[i].a);
       tma_prefetch_desc(&args.prob[i].b);
-      tma_prefetch_desc(&args.prob[i].sfa);
-      tma_prefetch_desc(&args.prob[i].sfb);
+      if (!kTS && !kGatherSfa) tma_prefetch_desc(&args.prob[i].sfa);
+      if (!kTS) tma_prefetch_desc(&args.prob[i].sfb);
     }
   }
   if (warp == 1) {
@@ -999,7 +1026,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int64_t it = 0, t; lane == 0 && ok && (t = next_tile(it)) >= 0; ++it) {
       const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
+        const Tile ti = get_pair_tile<KIND, kSwiGLU, BN>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
       // Rows-ragged: B's scale atoms are those of the tile's expert. SwiGLU:
       // the second atom holds the up rows, N/256 atoms after the gate rows.
       const int64_t sfb_atom_row = (KIND == GEMM_GROUPED_M ? ti.group * pp.b_ra : 0) + (ti.n0 >> 7);
@@ -1012,18 +1039,23 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int64_t katom = ti.k_atom0 + kb;
         {
           const uint32_t lfull = mapa_shared(smem_u32(&full_bar[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * (C::kStageTx - (kGatherSfa ? 512 : 0)));
+          // Both CTAs' TMA bytes complete on the leader's barrier; gathered
+          // scale words arrive through the gather warps instead.
+          if (leader)
+            mbar_arrive_expect_tx(&full_bar[stage], 2 * (C::kStageTx - (kGatherSfa ? C::kSfaBytes : 0)));
           const int32_t kx = static_cast<int32_t>(katom * kBK);
           tma_load_2d_pair(sA + stage * C::kABytes, &args.prob[pi].a, lfull, kx, static_cast<int32_t>(ti.a_row));
           tma_load_2d_pair(sB + stage * C::kBBytes, &args.prob[pi].b, lfull, kx, static_cast<int32_t>(ti.b_row));
           // Scale atoms through [atoms][128 words] views (rows past the end read as zero).
-          if constexpr (!kGatherSfa)
-            tma_load_2d_pair(sSfa + stage * 512, &args.prob[pi].sfa, lfull, 0,
+          if constexpr (!kTS && !kGatherSfa)
+            tma_load_2d_pair(sSfa + stage * C::kSfaBytes, &args.prob[pi].sfa, lfull, 0,
                              static_cast<int32_t>((ti.m0 >> 7) * pp.ka + katom));
+          if constexpr (!kTS) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_load_2d_pair(sSfb + stage * C::kSfbBytes + j * 512, &args.prob[pi].sfb, lfull, 0,
-                             static_cast<int32_t>((sfb_atom_row + j * sfb_atom_step) * pp.ka + katom));
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(sSfb + stage * C::kSfbBytes + j * 512, &args.prob[pi].sfb, lfull, 0,
+                               static_cast<int32_t>((sfb_atom_row + j * sfb_atom_step) * pp.ka + katom));
+          }
         }
         ++issued;
         if (++stage == S) {
@@ -1048,33 +1080,40 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_mxf8_e4m3(2 * kBM, BN);
+      constexpr uint32_t idesc = kTS ? idesc_f8_e4m3_f32(2 * kBM, BN) : idesc_mxf8_e4m3(2 * kBM, BN);
       int stage = 0;
       uint32_t phase = 0;
+      int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
         const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
+        const Tile ti = get_pair_tile<KIND, kSwiGLU, BN>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
         if (ti.part == -2) continue;  // an empty split-tail segment
-        if (!wait_or_abort<true>(acc_empty, acc_phase ^ 1, p, s_abort)) break;
+        if (!wait_or_abort<true>(&acc_empty[acc], acc_phase ^ 1, p, s_abort)) break;
         tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort) ||
-              !wait_or_abort<true>(&sf_full[stage], phase, p, s_abort)) {
+              (!kTS && !wait_or_abort<true>(&sf_full[stage], phase, p, s_abort))) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t sfa_t = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
-          const uint32_t sfb_t = sfa_t + 4;
           const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::kABytes));
           const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::kBBytes));
+          if constexpr (kTS) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc_mma_mxf8_pair(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
-                             (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) tc_mma_f8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          } else {
+            const uint32_t sfa_t = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
+            const uint32_t sfb_t = sfa_t + 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc_mma_mxf8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
+                               (kb | k) != 0 ? 1u : 0u);
+          }
           tc_commit_pair_multicast(&empty_bar[stage], static_cast<uint16_t>(0x3));
           if (++stage == S) {
             stage = 0;
@@ -1082,8 +1121,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit_pair_multicast(acc_full, static_cast<uint16_t>(0x3));
-        acc_phase ^= 1;
+        tc_commit_pair_multicast(&acc_full[acc], static_cast<uint16_t>(0x3));
+        if (++acc == ACC) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
       // All copies into and MMAs on tensor memory must finish before it is freed.
       tc_commit_pair_multicast(drain_bar, static_cast<uint16_t>(0x1));
@@ -1095,7 +1137,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // A stage's slot in tensor memory is free again once its full barrier
     // completes: the producer refilled the stage only after the MMAs that
     // read the previous contents had committed.
-    if (lane == 0 && !leader && kGatherSfa) {
+    if (lane == 0 && !leader && kGather) {
       // Odd CTA: forward each stage's landed scale gather to the leader's full
       // barrier, after making it visible to the tensor-core copies. The words
       // sit in this CTA's own shared memory and are read by this SM's share of
@@ -1108,7 +1150,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (int64_t it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
         const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
+        const Tile ti = get_pair_tile<KIND, kSwiGLU, BN>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort(&gfull[stage], phase, p, s_abort)) {
             ok = false;
@@ -1123,24 +1165,24 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
       }
     }
-    if (lane == 0 && leader) {
+    if (lane == 0 && leader && !kTS) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
         const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
+        const Tile ti = get_pair_tile<KIND, kSwiGLU, BN>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort)) {
             ok = false;
             break;
           }
-          // The leader's gathered atom was written through the generic proxy.
-          if constexpr (kGatherSfa) fence_proxy_async_smem();
+          // The leader's gathered words were written through the generic proxy.
+          if constexpr (kGather) fence_proxy_async_smem();
           tc_fence_after_sync();
           const uint32_t sfa = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
-          tc_cp_32x128b_warpx4_pair(sfa, sdesc_scale_atom(smem_u32(sSfa + stage * 512)));
+          tc_cp_32x128b_warpx4_pair(sfa, sdesc_scale_atom(smem_u32(sSfa + stage * C::kSfaBytes)));
           tc_cp_32x128b_warpx4_pair(sfa + 4, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes)));
           tc_cp_32x128b_warpx4_pair(sfa + 8, sdesc_scale_atom(smem_u32(sSfb + stage * C::kSfbBytes + 512)));
           tc_commit_pair_multicast(&sf_full[stage], static_cast<uint16_t>(0x1));
@@ -1156,18 +1198,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     __syncwarp();
   } else if (warp == kGatherWarp) {
     // ----------------------------------------- A scale gather (rows-ragged)
-    // Scale words of A rows m0 .. m0+127 gathered into the stage's atom with
-    // 4-byte asynchronous copies; each lane's arrival fires when its copies
-    // have landed (the leader's full barrier, or the odd CTA's local barrier
-    // that its relay warp forwards to the leader).
-    if constexpr (kGatherSfa) {
+    // Scale words of A rows m0 .. m0+127 (any start row) gathered into the
+    // stage's atom with 4-byte asynchronous copies; each lane's arrival fires
+    // when its copies have landed (the leader's full barrier, or the odd
+    // CTA's local barrier that its relay warp forwards to the leader).
+    if constexpr (kGather) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
         const int pi = problem_of<kMulti>(args, t);
         const GParams& pp = args.prob[pi].p;
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
+        const Tile ti = get_pair_tile<KIND, kSwiGLU, BN>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           uint32_t good = 1;
           if (lane == 0) good = wait_or_abort<true>(&empty_bar[stage], phase ^ 1, p, s_abort) ? 1u : 0u;
@@ -1177,15 +1219,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             break;
           }
           const int64_t katom = ti.k_atom0 + kb;
-          uint8_t* dst = sSfa + stage * 512 + lane * 16;
+          if constexpr (kGatherSfa) {
+            uint8_t* dst = sSfa + stage * C::kSfaBytes + lane * 16;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int64_t r = ti.a_row + lane + 32 * q;
-            const bool in = r < pp.a_ra * 128;  // rows past the scale buffer read as zero
-            cp_async_4(dst + 4 * q,
-                       in ? pp.a_scale + (((r >> 7) * pp.ka + katom) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2)
-                          : pp.a_scale,
-                       in ? 4u : 0u);
+            for (int q = 0; q < 4; ++q) {
+              const int64_t r = ti.a_row + lane + 32 * q;
+              const bool in = r < pp.a_ra * 128;  // rows past the scale buffer read as zero
+              cp_async_4(dst + 4 * q,
+                         in ? pp.a_scale + (((r >> 7) * pp.ka + katom) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2)
+                            : pp.a_scale,
+                         in ? 4u : 0u);
+            }
           }
           cp_async_arrive_noinc(leader ? &full_bar[stage] : &gfull[stage]);
           if (++stage == S) {
@@ -1204,14 +1248,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     constexpr int kCols = BN / 2;
     const int col_off = half * kCols;
     uint8_t* stg = sEpi + (warp - 2) * C::kEpiBufs * kEpiWarpBytes;
-    const uint32_t lacc_empty = mapa_shared(smem_u32(acc_empty), 0);
+    int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t it = 0, t; (t = next_tile(it)) >= 0; ++it) {
       const int pi = problem_of<kMulti>(args, t);
-        const GParams& pp = args.prob[pi].p;
-        const Tile ti = get_pair_tile<KIND, kSwiGLU>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
+      const GParams& pp = args.prob[pi].p;
+      const Tile ti = get_pair_tile<KIND, kSwiGLU, BN>(pp, g, kMulti ? t - args.tile0[pi] : t, crank);
       if (ti.part == -2) continue;
-      if (!wait_or_abort<true>(acc_full, acc_phase, p, s_abort)) break;
+      float ts = 1.0f;  // the tile's product of tensor scales (kTS), read while the MMAs run
+      if constexpr (kTS) ts = __ldg(pp.ts_a) * __ldg(pp.ts_b + (KIND == GEMM_GROUPED_M ? ti.group : 0));
+      if (!wait_or_abort<true>(&acc_full[acc], acc_phase, p, s_abort)) break;
       tc_fence_after_sync();
       uint32_t r[kCols];
       if (ti.nkb > 0) {
@@ -1224,7 +1270,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           tmem_ld_32x32b_x32(taddr + 128, r + 64);
           tmem_ld_32x32b_x32(taddr + 160, r + 96);
         } else {
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(col_off);
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(acc * BN + col_off);
 #pragma unroll
           for (int ch = 0; ch < kCols / 32; ++ch) tmem_ld_32x32b_x32(taddr + ch * 32, r + ch * 32);
         }
@@ -1235,17 +1282,27 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(lacc_empty);  // the even CTA's MMAs may overwrite the accumulator
-      acc_phase ^= 1;
-      if (KIND == GEMM_DENSE && ti.part >= 0) {
-        // Split-tail segment: the FP32 partial goes to the workspace.
-        float4* dst = reinterpret_cast<float4*>(pp.ws) +
-                      ((static_cast<int64_t>(ti.part) * 2 + crank) * 8 + (warp - 2)) * (32 * 32) + lane;
+      // the even CTA's MMAs may overwrite this accumulator
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+      if (++acc == ACC) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+      if constexpr (kTS) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          dst[j * 32] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        continue;
+        for (int i = 0; i < kCols; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * ts);
+      }
+      if constexpr (KIND == GEMM_DENSE && BN == 256 && !kTS) {
+        if (ti.part >= 0) {
+          // Split-tail segment: the FP32 partial goes to the workspace.
+          float4* dst = reinterpret_cast<float4*>(pp.ws) +
+                        ((static_cast<int64_t>(ti.part) * 2 + crank) * 8 + (warp - 2)) * (32 * 32) + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            dst[j * 32] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          continue;
+        }
       }
       if constexpr (kSwiGLU) {
         // SwiGLU in FP32 on the FP32 accumulators, one rounding to BF16 at the store
@@ -1695,10 +1752,10 @@ mx_status launch_cfg(const GemmLaunch& L, const GParams& p_in, int64_t tiles_upp
                      "mx_gemm launch");
 }
 
-// Upper bound of the 256 x 256 pair tiles (rows-ragged: one partial tile per
+// Upper bound of the 256 x bn pair tiles (rows-ragged: one partial tile per
 // expert at most).
-int64_t pair_tiles_upper(const GemmLaunch& L) {
-  const int64_t nt = (L.N + PairCfg::BN - 1) / PairCfg::BN;
+int64_t pair_tiles_upper(const GemmLaunch& L, int bn = 256) {
+  const int64_t nt = (L.N + bn - 1) / bn;
   const int64_t mu = ((L.M + kBM - 1) / kBM + 1) / 2;
   if (L.kind == GEMM_GROUPED_M) return (mu + L.n_groups) * nt;
   if (L.kind == GEMM_GROUPED_K) return mu * nt * L.n_groups;
@@ -1766,28 +1823,36 @@ PairArgs* pair_args_scratch() {
   return &args;
 }
 
-template <int KIND, bool kSwiGLU = false>
+template <int KIND, bool kSwiGLU = false, int BN = 256, bool kTS = false>
 mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) {
   GParams p = p_in;
   CUtensorMap ma, mb, msa, msb, mc;
+  std::memset(&msa, 0, sizeof(msa));
+  std::memset(&msb, 0, sizeof(msb));
   mx_status st = make_map(&ma, L.a_data, L.M, L.K, L.a_ld, kBM);
   if (st != MX_OK) return st;
-  st = make_map(&mb, L.b_data, L.b_rows_total, L.K, L.b_ld, PairCfg::BN / 2);
+  st = make_map(&mb, L.b_data, L.b_rows_total, L.K, L.b_ld, BN / 2);
   if (st != MX_OK) return st;
-  st = make_scale_map(&msa, L.a_scale, L.M, L.K);
-  if (st != MX_OK) return st;
-  // Stacked experts: one [E x row atoms x K atoms] view of all experts' scales.
-  const int64_t sfb_rows = (KIND == GEMM_GROUPED_M) ? L.n_groups * ((L.N + 127) / 128 * 128) : L.N;
-  st = make_scale_map(&msb, L.b_scale, sfb_rows, L.K);
-  if (st != MX_OK) return st;
+  if constexpr (kTS) {
+    // one FP32 scale per tensor (per expert for the stacked weights)
+    p.ts_a = static_cast<const float*>(L.a_scale);
+    p.ts_b = static_cast<const float*>(L.b_scale);
+  } else {
+    st = make_scale_map(&msa, L.a_scale, L.M, L.K);
+    if (st != MX_OK) return st;
+    // Stacked experts: one [E x row atoms x K atoms] view of all experts' scales.
+    const int64_t sfb_rows = (KIND == GEMM_GROUPED_M) ? L.n_groups * ((L.N + 127) / 128 * 128) : L.N;
+    st = make_scale_map(&msb, L.b_scale, sfb_rows, L.K);
+    if (st != MX_OK) return st;
+  }
   output_map(L, p, &mc, KIND);
-  const size_t smem = PairCfg::smem_bytes(KIND != GEMM_DENSE);
-  auto kern = mx_gemm_pair_kernel<KIND, kSwiGLU, false>;
+  const size_t smem = PairCfgT<BN, kTS, KIND != GEMM_DENSE>::smem_bytes();
+  auto kern = mx_gemm_pair_kernel<KIND, kSwiGLU, false, BN, kTS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
-  int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pair_tiles_upper(L), sm_count() / 2));
+  int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(pair_tiles_upper(L, BN), sm_count() / 2));
   PairPlan pl;
-  if constexpr (KIND == GEMM_DENSE) {
+  if constexpr (KIND == GEMM_DENSE && BN == 256 && !kTS) {
     pl = plan_pair_dense(L, true);
     if (pl.sk_w > 0 && !split_allowed(L, pl.ws_bytes)) pl = plan_pair_dense(L, false);
     if (pl.sk_w > 0) {
@@ -1853,6 +1918,7 @@ double dense_cfg_time_us(const GemmLaunch& L, int cfg) {
 }
 
 int choose_dense_cfg(const GemmLaunch& L) {
+  // MXFP8_GEMM_PAIR (measurement builds): 0 no pairs, 2 force pairs.
   static const int pair_mode = env_int("MXFP8_GEMM_PAIR", 1);
   static const int forced_bn = env_int("MXFP8_GEMM_BN", 0);
   if (pair_mode == 2 && L.N > 128) return CFG_PAIR;
@@ -1883,7 +1949,7 @@ int choose_bn(const GemmLaunch& L) {
 bool use_pairs(const GemmLaunch& L) {
   static const int mode = env_int("MXFP8_GEMM_PAIR", 1);
   if (mode == 0 || L.N <= 128) return false;
-  if (mode == 2) return true;
+  if (mode >= 2) return true;
   return pair_tiles_upper(L) >= sm_count() / 2;
 }
 
@@ -1945,7 +2011,8 @@ mx_status static_workspace(void** ptr, size_t* bytes) {
 }
 
 size_t gemm_workspace_bytes(const GemmLaunch& L) {
-  if (L.kind != GEMM_DENSE || L.swiglu || L.bw_a_scale || L.M == 0 || L.N == 0 || L.K == 0) return 0;
+  if (L.kind != GEMM_DENSE || L.swiglu || L.bw_a_scale || L.tensor_scaled || L.M == 0 || L.N == 0 || L.K == 0)
+    return 0;
   GemmLaunch q = L;
   q.ws = reinterpret_cast<void*>(uintptr_t{16});  // any workspace: the size a split would need
   q.ws_bytes = SIZE_MAX;
@@ -1987,6 +2054,8 @@ GParams make_gparams(const GemmLaunch& L) {
   p.sk_w = 0;
   p.sk_slots = 0;
   p.ws = nullptr;
+  p.ts_a = nullptr;
+  p.ts_b = nullptr;
   return p;
 }
 
@@ -2039,6 +2108,7 @@ int64_t schedule_round_robin(const GemmLaunch* Ls, int n, int64_t clusters) {
 
 // Several dense GEMMs in one launch of the pair kernel.
 mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
+  constexpr int BN = 256;
   PairArgs* args = pair_args_scratch();
   std::memset(args, 0, sizeof(PairArgs));
   // Longest tiles first: they start early and the short ones fill in behind.
@@ -2054,7 +2124,7 @@ mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
     pr.p = make_gparams(L);
     mx_status st = make_map(&pr.a, L.a_data, L.M, L.K, L.a_ld, kBM);
     if (st != MX_OK) return st;
-    st = make_map(&pr.b, L.b_data, L.b_rows_total, L.K, L.b_ld, PairCfg::BN / 2);
+    st = make_map(&pr.b, L.b_data, L.b_rows_total, L.K, L.b_ld, BN / 2);
     if (st != MX_OK) return st;
     st = make_scale_map(&pr.sfa, L.a_scale, L.M, L.K);
     if (st != MX_OK) return st;
@@ -2066,8 +2136,8 @@ mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
   }
   args->tile0[n] = tiles;
   args->n = n;
-  const size_t smem = PairCfg::smem_bytes(false);
-  auto kern = mx_gemm_pair_kernel<GEMM_DENSE, false, true>;
+  const size_t smem = PairCfgT<BN, false, false>::smem_bytes();
+  auto kern = mx_gemm_pair_kernel<GEMM_DENSE, false, true, BN, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count() / 2));
@@ -2083,6 +2153,7 @@ mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
                      "mx_gemm_multi launch (CTA pairs)");
 }
 
+
 }  // namespace
 
 mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
@@ -2095,6 +2166,12 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   GParams p = make_gparams(L);
 
   if (L.bw_a_scale) return launch_blockwise(L, p, s);
+  if (L.tensor_scaled) {
+    // one FP32 scale per tensor / per expert: 256 x 256 pair tiles, two accumulators
+    if (L.kind == GEMM_DENSE) return launch_pair<GEMM_DENSE, false, 256, true>(L, p, s);
+    if (L.kind == GEMM_GROUPED_M) return launch_pair<GEMM_GROUPED_M, false, 256, true>(L, p, s);
+    return launch_pair<GEMM_GROUPED_K, false, 256, true>(L, p, s);
+  }
   if (L.swiglu) return launch_pair<GEMM_GROUPED_M, true>(L, p, s);
   int bn;
   if (L.kind == GEMM_DENSE) {

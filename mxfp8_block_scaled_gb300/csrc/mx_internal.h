@@ -81,6 +81,12 @@ struct QuantLaunch {
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s);
 // Several dense BF16 matrices (batch 1 each, no groups) in one launch.
 mx_status launch_quantize_multi(const QuantLaunch* qs, int n, bool do_row, bool do_col, cudaStream_t s);
+// Current scaling: amax of each matrix of the stack q (zeroed first, then
+// reduced), and the quantisation with scale[b] = amax[b] / format_max (1 for an
+// invalid amax), written to `scale`.
+mx_status launch_current_amax(const QuantLaunch& q, float* amax, cudaStream_t s);
+mx_status launch_quantize_current(const QuantLaunch& q, const float* amax, float format_max, float* scale,
+                                  bool do_row, bool do_col, cudaStream_t s);
 // Blockwise FP8 variant: block = 1 (1 x 128 activation blocks, scale[kb][rows])
 // or 128 (128 x 128 weight blocks, scale[row block][kb]).
 mx_status launch_quantize_blockwise(const void* x, int64_t rows, int64_t cols, int64_t ldx, int block, void* data,
@@ -116,6 +122,9 @@ struct GemmLaunch {
   // too small a one) the GEMM runs whole tiles only.
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  // Current-scaling recipe: a_scale / b_scale are FP32 tensor scales (b: one
+  // per expert for rows-ragged grouped GEMMs) applied in the epilogue.
+  bool tensor_scaled = false;
 };
 mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // Bytes of workspace the dense GEMM L would use for its split tail (0: none).

@@ -177,6 +177,18 @@ __device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc
       : "memory");
 }
 
+// D (+)= A . B^T over the pair for one K=32 step of E4M3 x E4M3 without block
+// scales (operands and D placed as in tc_mma_mxf8_pair).
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on the mbarrier at this offset in every CTA of `cta_mask` once the
 // pair's prior tcgen05 operations issued by this thread have completed.
 __device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {

@@ -77,6 +77,12 @@ struct QParams {
   int64_t row_data_bs, row_scale_bs, col_data_bs, col_scale_bs;  // per-matrix output strides, bytes
   int* dev_status;
   uint64_t timeout_ns;
+  // Current scaling (kCur kernels): matrix b's scale is cur_amax[b] /
+  // cur_fmt in FP32 (1 for an amax that is zero, infinite or NaN), written to
+  // cur_scale[b]; elements are E4M3(fl32(x / scale)); no scale bytes.
+  const float* cur_amax;
+  float cur_fmt;
+  float* cur_scale;
 };
 
 // Up to kMaxTensors independent matrices per launch (dense quantisation of
@@ -128,6 +134,31 @@ __device__ __forceinline__ uint32_t quant_quad(uint32_t a, uint32_t b, float inv
 }
 
 __device__ __forceinline__ uint32_t half_max(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
+
+// --- current scaling (one FP32 scale per matrix) ---------------------------
+
+// The matrix's scale: amax / format_max as an IEEE FP32 division, or 1 when
+// amax is zero, infinite or NaN.
+__device__ __forceinline__ float current_scale_of(float amax, float fmt) {
+  return (amax > 0.0f && amax <= 3.402823466e38f) ? __fdiv_rn(amax, fmt) : 1.0f;
+}
+
+// E4M3 codes of the two BF16 values of w divided by s (quotients rounded to
+// FP32 first, then to E4M3 nearest-even with saturation); low half -> low byte.
+__device__ __forceinline__ uint32_t cur_word(uint32_t w, float s) {
+  return cvt_pair(__fdiv_rn(lo_f(w), s), __fdiv_rn(hi_f(w), s));
+}
+
+// Replace the code of each NaN half of w by the E4M3 NaN with that half's sign.
+__device__ __forceinline__ uint32_t cur_fix_nan(uint32_t c2, uint32_t w) {
+  if ((w & 0x7FFFu) > 0x7F80u) c2 = (c2 & 0xFF00u) | 0x7Fu | ((w >> 8) & 0x80u);
+  if (((w >> 16) & 0x7FFFu) > 0x7F80u) c2 = (c2 & 0x00FFu) | ((0x7Fu | ((w >> 24) & 0x80u)) << 8);
+  return c2;
+}
+
+__device__ __forceinline__ bool word_has_nan(uint32_t w) {
+  return (w & 0x7FFFu) > 0x7F80u || ((w >> 16) & 0x7FFFu) > 0x7F80u;
+}
 
 // Barrier among the eight consumer warps only (the producer warp never joins).
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
@@ -234,9 +265,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 // kMulti: the launch holds several matrices and each tile looks up its own;
 // otherwise every tile belongs to matrix 0 and its fields stay fixed
 // parameter operands.
-template <bool kRow, bool kCol, bool kGrouped, bool kMulti>
+template <bool kRow, bool kCol, bool kGrouped, bool kMulti, bool kCur = false>
 __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     mx_quant_kernel(const __grid_constant__ QuantArgs qa) {
+  static_assert(!kCur || !kMulti, "current scaling: one matrix (or one stack) per launch");
   // Programmatic dependent launch: let the next kernel on the stream be
   // scheduled, and touch global memory only once the previous one completed.
   pdl_launch_dependents();
@@ -296,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     }
     row_tiles = s_total_tiles;
     // Row-scale padding rows [rows, ceil(rows/128)*128) belong to no group tile.
-    if (kRow) {
+    if (kRow && !kCur) {
       const int64_t padded = (p.rows + kTileRows - 1) / kTileRows * kTileRows;
       for (int64_t ct = blockIdx.x; ct < col_tiles; ct += gridDim.x)
         for (int64_t r = p.rows + tid; r < padded; r += kThreads)
@@ -313,6 +345,11 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     }
     s_abort = 0;
     fence_mbar_init();
+  }
+  if constexpr (kCur) {
+    // the scale each matrix was quantised with, for the GEMM that reads it
+    if (blockIdx.x == 0)
+      for (int64_t b = tid; b < p.batch; b += kThreads) p.cur_scale[b] = current_scale_of(p.cur_amax[b], p.cur_fmt);
   }
   __syncthreads();
 
@@ -380,6 +417,8 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
       const uint32_t* tile = reinterpret_cast<const uint32_t*>(tiles + s * kTileBytes);
       const uint4* tile16 = reinterpret_cast<const uint4*>(tiles + s * kTileBytes);
       uint8_t* csc = col_sc + (j & 1) * 512;
+      float cs = 1.0f;  // current scaling: this tile's matrix scale
+      if constexpr (kCur) cs = current_scale_of(__ldg(p.cur_amax + g.b), p.cur_fmt);
 
       if (kRow && ok) {
         // ---- row copy: one thread per 1x32 block; lanes 8b..8b+7 take block b
@@ -396,6 +435,33 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
           uint4 v[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) v[j] = src[r0 * 8 + ((cbase + j) ^ rsub)];
+          const int64_t grow = g.row0 + r;
+          if constexpr (kCur) {
+            uint32_t q[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              q[2 * j] = cur_word(v[j].x, cs) | (cur_word(v[j].y, cs) << 16);
+              q[2 * j + 1] = cur_word(v[j].z, cs) | (cur_word(v[j].w, cs) << 16);
+            }
+            bool has_nan = false;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              has_nan |= word_has_nan(v[j].x) | word_has_nan(v[j].y) | word_has_nan(v[j].z) | word_has_nan(v[j].w);
+            if (__any_sync(0xFFFFFFFFu, has_nan) && has_nan) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                q[2 * j] = cur_fix_nan(q[2 * j] & 0xFFFFu, v[j].x) | (cur_fix_nan(q[2 * j] >> 16, v[j].y) << 16);
+                q[2 * j + 1] =
+                    cur_fix_nan(q[2 * j + 1] & 0xFFFFu, v[j].z) | (cur_fix_nan(q[2 * j + 1] >> 16, v[j].w) << 16);
+              }
+            }
+            if (r < g.valid_rows && blk * 32 < g.valid_cols) {
+              uint4* dst = reinterpret_cast<uint4*>(row_data + grow * p.cols + g.c0 + blk * 32);
+              dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+              dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            }
+            continue;
+          }
           uint32_t m = 0;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -417,7 +483,6 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
               q[2 * j + 1] = nan_pair(v[j].z) | (nan_pair(v[j].w) << 16);
             }
           }
-          const int64_t grow = g.row0 + r;
           if (r < g.valid_rows && blk * 32 < g.valid_cols) {
             uint4* dst = reinterpret_cast<uint4*>(row_data + grow * p.cols + g.c0 + blk * 32);
             dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
@@ -449,35 +514,60 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
             for (int i = 0; i < 32; ++i)
               if (rb * 32 + i >= g.valid_rows) w[i] = 0u;
           }
-          uint32_t m = 0;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
-          const uint32_t code_lo = scale_code(m & 0xFFFFu);
-          const uint32_t code_hi = scale_code(m >> 16);
-          const bool nan_lo = code_lo == 0xFFu, nan_hi = code_hi == 0xFFu;
-          const float inv_lo = inv_scale(nan_lo ? 0u : code_lo);
-          const float inv_hi = inv_scale(nan_hi ? 0u : code_hi);
           uint32_t out_lo[8], out_hi[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
-            out_lo[q] = cvt_pair(lo_f(a) * inv_lo, lo_f(bb) * inv_lo) |
-                        (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
-            out_hi[q] = cvt_pair(hi_f(a) * inv_hi, hi_f(bb) * inv_hi) |
-                        (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
-          }
-          if (__any_sync(0xFFFFFFFFu, nan_lo || nan_hi)) {
+          if constexpr (kCur) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
-              if (nan_lo)
-                out_lo[q] = nan_pair((a & 0xFFFFu) | (bb << 16)) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
-              if (nan_hi)
-                out_hi[q] = nan_pair((a >> 16) | (bb & 0xFFFF0000u)) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
+              out_lo[q] = cvt_pair(__fdiv_rn(lo_f(a), cs), __fdiv_rn(lo_f(bb), cs)) |
+                          (cvt_pair(__fdiv_rn(lo_f(c), cs), __fdiv_rn(lo_f(d), cs)) << 16);
+              out_hi[q] = cvt_pair(__fdiv_rn(hi_f(a), cs), __fdiv_rn(hi_f(bb), cs)) |
+                          (cvt_pair(__fdiv_rn(hi_f(c), cs), __fdiv_rn(hi_f(d), cs)) << 16);
             }
+            bool has_nan = false;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) has_nan |= word_has_nan(w[i]);
+            if (__any_sync(0xFFFFFFFFu, has_nan) && has_nan) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
+                // low halves are column 2cp, high halves column 2cp + 1
+                out_lo[q] = cur_fix_nan(out_lo[q] & 0xFFFFu, (a & 0xFFFFu) | (bb << 16)) |
+                            (cur_fix_nan(out_lo[q] >> 16, (c & 0xFFFFu) | (d << 16)) << 16);
+                out_hi[q] = cur_fix_nan(out_hi[q] & 0xFFFFu, (a >> 16) | (bb & 0xFFFF0000u)) |
+                            (cur_fix_nan(out_hi[q] >> 16, (c >> 16) | (d & 0xFFFF0000u)) << 16);
+              }
+            }
+          } else {
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+            const uint32_t code_lo = scale_code(m & 0xFFFFu);
+            const uint32_t code_hi = scale_code(m >> 16);
+            const bool nan_lo = code_lo == 0xFFu, nan_hi = code_hi == 0xFFu;
+            const float inv_lo = inv_scale(nan_lo ? 0u : code_lo);
+            const float inv_hi = inv_scale(nan_hi ? 0u : code_hi);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
+              out_lo[q] = cvt_pair(lo_f(a) * inv_lo, lo_f(bb) * inv_lo) |
+                          (cvt_pair(lo_f(c) * inv_lo, lo_f(d) * inv_lo) << 16);
+              out_hi[q] = cvt_pair(hi_f(a) * inv_hi, hi_f(bb) * inv_hi) |
+                          (cvt_pair(hi_f(c) * inv_hi, hi_f(d) * inv_hi) << 16);
+            }
+            if (__any_sync(0xFFFFFFFFu, nan_lo || nan_hi)) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
+                if (nan_lo)
+                  out_lo[q] = nan_pair((a & 0xFFFFu) | (bb << 16)) | (nan_pair((c & 0xFFFFu) | (d << 16)) << 16);
+                if (nan_hi)
+                  out_hi[q] = nan_pair((a >> 16) | (bb & 0xFFFF0000u)) | (nan_pair((c >> 16) | (d & 0xFFFF0000u)) << 16);
+              }
+            }
+            csc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
+            csc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
           }
-          csc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
-          csc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
 #if MX_QUANT_COL_STAGE
           // Output rows 2cp and 2cp+1, 16-byte chunks 2rb and 2rb+1 of the
           // tile's 128 bytes along K; chunk q of row o sits at q ^ (o % 8).
@@ -531,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
           }
         }
 #endif
-        if (ok && tid < kTileCols) {
+        if (!kCur && ok && tid < kTileCols) {
           const uint32_t word = *reinterpret_cast<const uint32_t*>(csc + tid * 4);
           *reinterpret_cast<uint32_t*>(col_scale + scale_offset(g.c0 + tid, g.kpos >> 5, p.col_ka)) = word;
         }
@@ -540,6 +630,53 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
       }
     }
   }
+}
+
+// ===========================================================================
+// Current scaling: amax of each matrix of a BF16 stack
+// ===========================================================================
+//
+// "DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §3 / §8.2: the FP32 scale of a
+// tensor comes from the amax of the current tensor (of each leading group for
+// a stacked one). One warp per input row at a time, 16-byte loads (four in
+// flight per lane), an unsigned max over the BF16 magnitude bits (NaN > Inf >
+// finite, as for the blocks), a warp reduction, and one atomic max per warp
+// and matrix on the FP32 bit pattern (non-negative floats order like their
+// bits). The caller zeroes amax first.
+__global__ void __launch_bounds__(256) cur_amax_kernel(const uint16_t* __restrict__ x, int64_t batch, int64_t rows,
+                                                       int64_t cols, int64_t ldx, int64_t bstride,
+                                                       uint32_t* __restrict__ amax_bits) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t vpr = cols >> 3;  // 16-byte vectors per row (cols % 32 == 0)
+  uint32_t m = 0;
+  int64_t cur_b = -1;
+  auto flush = [&]() {
+    const uint32_t r = __reduce_max_sync(0xFFFFFFFFu, half_max(m));
+    if (lane == 0 && cur_b >= 0 && r > 0) atomicMax(amax_bits + cur_b, r << 16);
+    m = 0;
+  };
+  for (int64_t gr = warp_id; gr < batch * rows; gr += warps) {
+    const int64_t b = gr / rows;
+    if (b != cur_b) {  // warp-uniform
+      flush();
+      cur_b = b;
+    }
+    const uint4* row = reinterpret_cast<const uint4*>(x + b * bstride + (gr - b * rows) * ldx);
+    for (int64_t v = lane; v < vpr; v += 128) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = (v + 32 * u < vpr) ? __ldcs(row + v + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        m = __vmaxu2(__vmaxu2(m, __vmaxu2(q[u].x & 0x7FFF7FFFu, q[u].y & 0x7FFF7FFFu)),
+                     __vmaxu2(q[u].z & 0x7FFF7FFFu, q[u].w & 0x7FFF7FFFu));
+    }
+  }
+  flush();
 }
 
 // ===========================================================================
@@ -877,11 +1014,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <bool R, bool C, bool G, bool M = false>
+template <bool R, bool C, bool G, bool M = false, bool kCur = false>
 mx_status launch_one(const QuantArgs& qa, int64_t tiles_upper, cudaStream_t s) {
   const size_t smem = 1024 + static_cast<size_t>(kStages) * kTileBytes + 2 * kColStageBytes + 1024 + 2 * kStages * 8 +
                       (G ? 2 * (kMaxGroups + 1) * sizeof(int32_t) : 0);
-  auto kern = mx_quant_kernel<R, C, G, M>;
+  auto kern = mx_quant_kernel<R, C, G, M, kCur>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(quant smem)");
   int per_sm = 0;
@@ -1021,6 +1158,47 @@ mx_status launch_by_axis(const QuantArgs& qa, int64_t tiles, bool do_row, bool d
 }
 
 }  // namespace
+
+mx_status launch_current_amax(const QuantLaunch& q, float* amax, cudaStream_t s) {
+  mx_status st = cuda_status(cudaMemsetAsync(amax, 0, static_cast<size_t>(q.batch) * sizeof(float), s),
+                             "cudaMemsetAsync(amax)");
+  if (st != MX_OK || q.rows == 0 || q.cols == 0) return st;
+  const int64_t bstride = q.batch > 1 ? q.x_batch_stride : q.rows * q.ldx;
+  const int64_t warps_needed = q.batch * q.rows;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((warps_needed + 7) / 8, 8LL * sm_count()));
+  return cuda_status(launch_kernel(cur_amax_kernel, static_cast<unsigned>(grid), 256, 0, s, 1,
+                                   static_cast<const uint16_t*>(q.x), q.batch, q.rows, q.cols, q.ldx, bstride,
+                                   reinterpret_cast<uint32_t*>(amax)),
+                     "current amax launch");
+}
+
+mx_status launch_quantize_current(const QuantLaunch& q, const float* amax, float format_max, float* scale,
+                                  bool do_row, bool do_col, cudaStream_t s) {
+  QParams p = make_qparams(q);
+  p.cur_amax = amax;
+  p.cur_fmt = format_max;
+  p.cur_scale = scale;
+  const bool grouped = q.offsets != nullptr && do_col;
+  const int64_t col_tiles = (q.cols + kTileCols - 1) / kTileCols;
+  int64_t row_tiles = (q.rows + kTileRows - 1) / kTileRows;
+  if (grouped) row_tiles += q.n_groups;  // upper bound of sum ceil(m_e / 128)
+  QuantArgs qa;
+  std::memset(&qa, 0, sizeof(qa));
+  mx_status st = make_bf16_input_map(q, &qa.map[0]);
+  if (st != MX_OK) return st;
+  qa.p[0] = p;
+  qa.n = 1;
+  // an empty matrix still gets its scale (1): one tile's worth of launch
+  const int64_t tiles = std::max<int64_t>(1, row_tiles * col_tiles * q.batch);
+  qa.tile0[0] = 0;
+  qa.tile0[1] = row_tiles * col_tiles * q.batch;
+  if (grouped)
+    return do_row ? launch_one<true, true, true, false, true>(qa, tiles, s)
+                  : launch_one<false, true, true, false, true>(qa, tiles, s);
+  if (do_row && do_col) return launch_one<true, true, false, false, true>(qa, tiles, s);
+  if (do_row) return launch_one<true, false, false, false, true>(qa, tiles, s);
+  return launch_one<false, true, false, false, true>(qa, tiles, s);
+}
 
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s) {
   const QParams p = make_qparams(q);

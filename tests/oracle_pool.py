@@ -85,3 +85,17 @@ def stacked(bits: np.ndarray):
     cols = list(pool().map(_cols_task, [bits[e] for e in range(E)]))
     return (np.stack([r[0] for r in rows]), np.stack([r[1] for r in rows]),
             np.stack([c[0] for c in cols]), np.stack([c[1] for c in cols]))
+
+
+def _current_task(bits, scale):
+    import oracle
+    return oracle.current_encode(oracle.bf16_bits_to_float64(bits), scale)
+
+
+def current_codes(bits: np.ndarray, scale, target_elems: int = 1 << 22):
+    """oracle.current_encode of BF16 bits [R, C] with one scale (element-wise,
+    so any row slab works): codes [R, C]."""
+    R, C = bits.shape
+    step = max(1, target_elems // max(C, 1))
+    sl = _slabs(R, step)
+    return np.concatenate(list(pool().map(_current_task, [bits[a:b] for a, b in sl], [scale] * len(sl))))
