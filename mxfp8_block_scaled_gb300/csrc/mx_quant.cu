@@ -77,12 +77,15 @@ struct QParams {
   int64_t row_data_bs, row_scale_bs, col_data_bs, col_scale_bs;  // per-matrix output strides, bytes
   int* dev_status;
   uint64_t timeout_ns;
-  // Current scaling (kCur kernels): matrix b's scale is cur_amax[b] /
-  // cur_fmt in FP32 (1 for an amax that is zero, infinite or NaN), written to
-  // cur_scale[b]; elements are E4M3(fl32(x / scale)); no scale bytes.
-  const float* cur_amax;
-  float cur_fmt;
-  float* cur_scale;
+};
+
+// Current scaling (kCur kernels, one matrix or one stack per launch): matrix
+// b's scale is amax[b] / fmt in FP32 (1 for an amax that is zero, infinite or
+// NaN), written to scale[b]; elements are E4M3(fl32(x / scale)); no scale bytes.
+struct CurParams {
+  const float* amax;
+  float fmt;
+  float* scale;
 };
 
 // Up to kMaxTensors independent matrices per launch (dense quantisation of
@@ -143,10 +146,43 @@ __device__ __forceinline__ float current_scale_of(float amax, float fmt) {
   return (amax > 0.0f && amax <= 3.402823466e38f) ? __fdiv_rn(amax, fmt) : 1.0f;
 }
 
-// E4M3 codes of the two BF16 values of w divided by s (quotients rounded to
-// FP32 first, then to E4M3 nearest-even with saturation); low half -> low byte.
-__device__ __forceinline__ uint32_t cur_word(uint32_t w, float s) {
-  return cvt_pair(__fdiv_rn(lo_f(w), s), __fdiv_rn(hi_f(w), s));
+// Division by a matrix's scale s, correctly rounded to FP32. With r = RN(1/s),
+// q0 = RN(x * r) lies within one ulp of x / s, the remainder x - q0 * s is
+// exact as one FMA, and RN(q0 + (x - q0 * s) * r) is the correctly rounded
+// quotient (Markstein's theorem: P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990) while nothing underflows or overflows. q0 = +-0 (x = +-0, or a
+// quotient below FP32's normal range) and an infinite q0 are already the
+// rounded quotient's value for every E4M3 decision and keep their sign, so
+// they are taken as they are. For s >= 2^-100 a subnormal x gives a quotient
+// below 2^-26, far below E4M3's smallest subnormal; smaller scales take the
+// IEEE division itself (a matrix-uniform branch). Checked against IEEE
+// division on every finite BF16 x for every positive finite BF16 amax.
+struct CurDiv {
+  float s, r;
+  bool fast;
+};
+
+__device__ __forceinline__ CurDiv cur_div_of(float s) {
+  CurDiv d;
+  d.s = s;
+  d.fast = s >= 7.8886090522101181e-31f;  // 2^-100
+  d.r = d.fast ? __frcp_rn(s) : 1.0f;
+  return d;
+}
+
+__device__ __forceinline__ float cur_div(float x, const CurDiv& d) {
+  if (!d.fast) return __fdiv_rn(x, d.s);
+  const float q0 = __fmul_rn(x, d.r);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, d.s, x), d.r, q0);
+  return (q0 == 0.0f || fabsf(q0) > 3.402823466e38f) ? q0 : q1;
+}
+
+// E4M3 codes of the two BF16 values of w divided by the scale (quotients
+// rounded to FP32 first, then to E4M3 nearest-even with saturation); low half
+// -> low byte.
+__device__ __forceinline__ uint32_t cur_word(uint32_t w, const CurDiv& d) {
+  return cvt_pair(cur_div(lo_f(w), d), cur_div(hi_f(w), d));
 }
 
 // Replace the code of each NaN half of w by the E4M3 NaN with that half's sign.
@@ -265,9 +301,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 // kMulti: the launch holds several matrices and each tile looks up its own;
 // otherwise every tile belongs to matrix 0 and its fields stay fixed
 // parameter operands.
-template <bool kRow, bool kCol, bool kGrouped, bool kMulti, bool kCur = false>
-__global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
-    mx_quant_kernel(const __grid_constant__ QuantArgs qa) {
+// The body of both quantiser kernels below: block scales (MX) or one
+// current scale per matrix (kCur).
+template <bool kRow, bool kCol, bool kGrouped, bool kMulti, bool kCur>
+__device__ __forceinline__ void quant_body(const QuantArgs& qa, const CurParams& cur) {
   static_assert(!kCur || !kMulti, "current scaling: one matrix (or one stack) per launch");
   // Programmatic dependent launch: let the next kernel on the stream be
   // scheduled, and touch global memory only once the previous one completed.
@@ -349,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   if constexpr (kCur) {
     // the scale each matrix was quantised with, for the GEMM that reads it
     if (blockIdx.x == 0)
-      for (int64_t b = tid; b < p.batch; b += kThreads) p.cur_scale[b] = current_scale_of(p.cur_amax[b], p.cur_fmt);
+      for (int64_t b = tid; b < p.batch; b += kThreads) cur.scale[b] = current_scale_of(cur.amax[b], cur.fmt);
   }
   __syncthreads();
 
@@ -417,8 +454,8 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
       const uint32_t* tile = reinterpret_cast<const uint32_t*>(tiles + s * kTileBytes);
       const uint4* tile16 = reinterpret_cast<const uint4*>(tiles + s * kTileBytes);
       uint8_t* csc = col_sc + (j & 1) * 512;
-      float cs = 1.0f;  // current scaling: this tile's matrix scale
-      if constexpr (kCur) cs = current_scale_of(__ldg(p.cur_amax + g.b), p.cur_fmt);
+      CurDiv cs{1.0f, 1.0f, true};  // current scaling: this tile's matrix scale
+      if constexpr (kCur) cs = cur_div_of(current_scale_of(__ldg(cur.amax + g.b), cur.fmt));
 
       if (kRow && ok) {
         // ---- row copy: one thread per 1x32 block; lanes 8b..8b+7 take block b
@@ -435,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
           uint4 v[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) v[j] = src[r0 * 8 + ((cbase + j) ^ rsub)];
-          const int64_t grow = g.row0 + r;
           if constexpr (kCur) {
+            const int64_t grow = g.row0 + r;
             uint32_t q[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -483,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
               q[2 * j + 1] = nan_pair(v[j].z) | (nan_pair(v[j].w) << 16);
             }
           }
+          const int64_t grow = g.row0 + r;
           if (r < g.valid_rows && blk * 32 < g.valid_cols) {
             uint4* dst = reinterpret_cast<uint4*>(row_data + grow * p.cols + g.c0 + blk * 32);
             dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
@@ -514,29 +552,37 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
             for (int i = 0; i < 32; ++i)
               if (rb * 32 + i >= g.valid_rows) w[i] = 0u;
           }
-          uint32_t out_lo[8], out_hi[8];
           if constexpr (kCur) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
-              out_lo[q] = cvt_pair(__fdiv_rn(lo_f(a), cs), __fdiv_rn(lo_f(bb), cs)) |
-                          (cvt_pair(__fdiv_rn(lo_f(c), cs), __fdiv_rn(lo_f(d), cs)) << 16);
-              out_hi[q] = cvt_pair(__fdiv_rn(hi_f(a), cs), __fdiv_rn(hi_f(bb), cs)) |
-                          (cvt_pair(__fdiv_rn(hi_f(c), cs), __fdiv_rn(hi_f(d), cs)) << 16);
-            }
+            // One column at a time, straight into the staging tile (fewer live
+            // registers beside the division's).
+            static_assert(MX_QUANT_COL_STAGE, "current scaling stages its column copy");
             bool has_nan = false;
 #pragma unroll
             for (int i = 0; i < 32; ++i) has_nan |= word_has_nan(w[i]);
-            if (__any_sync(0xFFFFFFFFu, has_nan) && has_nan) {
+            const bool fix = __any_sync(0xFFFFFFFFu, has_nan) && has_nan;
+            uint8_t* stg = col_stage + (j & 1) * kColStageBytes;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t o[8];
 #pragma unroll
               for (int q = 0; q < 8; ++q) {
                 const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
-                // low halves are column 2cp, high halves column 2cp + 1
-                out_lo[q] = cur_fix_nan(out_lo[q] & 0xFFFFu, (a & 0xFFFFu) | (bb << 16)) |
-                            (cur_fix_nan(out_lo[q] >> 16, (c & 0xFFFFu) | (d << 16)) << 16);
-                out_hi[q] = cur_fix_nan(out_hi[q] & 0xFFFFu, (a >> 16) | (bb & 0xFFFF0000u)) |
-                            (cur_fix_nan(out_hi[q] >> 16, (c >> 16) | (d & 0xFFFF0000u)) << 16);
+                const float fa = h ? hi_f(a) : lo_f(a), fb = h ? hi_f(bb) : lo_f(bb);
+                const float fc = h ? hi_f(c) : lo_f(c), fd = h ? hi_f(d) : lo_f(d);
+                o[q] = cvt_pair(cur_div(fa, cs), cur_div(fb, cs)) | (cvt_pair(cur_div(fc, cs), cur_div(fd, cs)) << 16);
+                if (fix) {
+                  // the halves of column 2cp + h, rows 4q .. 4q + 3
+                  const uint32_t ab = h ? ((a >> 16) | (bb & 0xFFFF0000u)) : ((a & 0xFFFFu) | (bb << 16));
+                  const uint32_t cd = h ? ((c >> 16) | (d & 0xFFFF0000u)) : ((c & 0xFFFFu) | (d << 16));
+                  o[q] = cur_fix_nan(o[q] & 0xFFFFu, ab) | (cur_fix_nan(o[q] >> 16, cd) << 16);
+                }
               }
+              // output row 2cp + h, 16-byte chunks 2rb and 2rb + 1; chunk q of row o at q ^ (o % 8)
+              const int orow = 2 * cp + h;
+              *reinterpret_cast<uint4*>(stg + orow * 128 + (((2 * rb) ^ (orow & 7)) << 4)) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(stg + orow * 128 + (((2 * rb + 1) ^ (orow & 7)) << 4)) =
+                  make_uint4(o[4], o[5], o[6], o[7]);
             }
           } else {
             uint32_t m = 0;
@@ -547,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
             const bool nan_lo = code_lo == 0xFFu, nan_hi = code_hi == 0xFFu;
             const float inv_lo = inv_scale(nan_lo ? 0u : code_lo);
             const float inv_hi = inv_scale(nan_hi ? 0u : code_hi);
+            uint32_t out_lo[8], out_hi[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const uint32_t a = w[4 * q], bb = w[4 * q + 1], c = w[4 * q + 2], d = w[4 * q + 3];
@@ -567,7 +614,6 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
             }
             csc[(2 * cp) * 4 + rb] = static_cast<uint8_t>(code_lo);
             csc[(2 * cp + 1) * 4 + rb] = static_cast<uint8_t>(code_hi);
-          }
 #if MX_QUANT_COL_STAGE
           // Output rows 2cp and 2cp+1, 16-byte chunks 2rb and 2rb+1 of the
           // tile's 128 bytes along K; chunk q of row o sits at q ^ (o % 8).
@@ -598,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
             }
           }
 #endif
+          }  // block scales
         }
         // The four 32-row blocks of a column sit in four warps: gather their
         // scale bytes (double-buffered by iteration, so one barrier suffices).
@@ -630,6 +677,20 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
       }
     }
   }
+}
+
+template <bool kRow, bool kCol, bool kGrouped, bool kMulti>
+__global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
+    mx_quant_kernel(const __grid_constant__ QuantArgs qa) {
+  quant_body<kRow, kCol, kGrouped, kMulti, false>(qa, CurParams{nullptr, 0.0f, nullptr});
+}
+
+// Current scaling (a separate kernel, so that the MX kernels' parameter block
+// stays as it is).
+template <bool kRow, bool kCol, bool kGrouped>
+__global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
+    mx_quant_current_kernel(const __grid_constant__ QuantArgs qa, const CurParams cur) {
+  quant_body<kRow, kCol, kGrouped, false, true>(qa, cur);
 }
 
 // ===========================================================================
@@ -1015,10 +1076,22 @@ EncodeTiledFn encode_fn() {
 }
 
 template <bool R, bool C, bool G, bool M = false, bool kCur = false>
-mx_status launch_one(const QuantArgs& qa, int64_t tiles_upper, cudaStream_t s) {
+mx_status launch_one(const QuantArgs& qa, int64_t tiles_upper, cudaStream_t s, CurParams cur = CurParams{}) {
   const size_t smem = 1024 + static_cast<size_t>(kStages) * kTileBytes + 2 * kColStageBytes + 1024 + 2 * kStages * 8 +
                       (G ? 2 * (kMaxGroups + 1) * sizeof(int32_t) : 0);
-  auto kern = mx_quant_kernel<R, C, G, M, kCur>;
+  if constexpr (kCur) {
+    auto kern = mx_quant_current_kernel<R, C, G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(quant smem)");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    const int64_t grid =
+        std::max<int64_t>(1, std::min<int64_t>(tiles_upper, static_cast<int64_t>(std::max(per_sm, 1)) * sm_count()));
+    return cuda_status(launch_kernel(kern, static_cast<unsigned>(grid), kThreads, smem, s, 1, qa, cur),
+                       "mx_quantize_current launch");
+  }
+  auto kern = mx_quant_kernel<R, C, G, M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(quant smem)");
   int per_sm = 0;
@@ -1174,10 +1247,7 @@ mx_status launch_current_amax(const QuantLaunch& q, float* amax, cudaStream_t s)
 
 mx_status launch_quantize_current(const QuantLaunch& q, const float* amax, float format_max, float* scale,
                                   bool do_row, bool do_col, cudaStream_t s) {
-  QParams p = make_qparams(q);
-  p.cur_amax = amax;
-  p.cur_fmt = format_max;
-  p.cur_scale = scale;
+  const QParams p = make_qparams(q);
   const bool grouped = q.offsets != nullptr && do_col;
   const int64_t col_tiles = (q.cols + kTileCols - 1) / kTileCols;
   int64_t row_tiles = (q.rows + kTileRows - 1) / kTileRows;
@@ -1188,16 +1258,17 @@ mx_status launch_quantize_current(const QuantLaunch& q, const float* amax, float
   if (st != MX_OK) return st;
   qa.p[0] = p;
   qa.n = 1;
+  const CurParams cur{amax, format_max, scale};
   // an empty matrix still gets its scale (1): one tile's worth of launch
   const int64_t tiles = std::max<int64_t>(1, row_tiles * col_tiles * q.batch);
   qa.tile0[0] = 0;
   qa.tile0[1] = row_tiles * col_tiles * q.batch;
   if (grouped)
-    return do_row ? launch_one<true, true, true, false, true>(qa, tiles, s)
-                  : launch_one<false, true, true, false, true>(qa, tiles, s);
-  if (do_row && do_col) return launch_one<true, true, false, false, true>(qa, tiles, s);
-  if (do_row) return launch_one<true, false, false, false, true>(qa, tiles, s);
-  return launch_one<false, true, false, false, true>(qa, tiles, s);
+    return do_row ? launch_one<true, true, true, false, true>(qa, tiles, s, cur)
+                  : launch_one<false, true, true, false, true>(qa, tiles, s, cur);
+  if (do_row && do_col) return launch_one<true, true, false, false, true>(qa, tiles, s, cur);
+  if (do_row) return launch_one<true, false, false, false, true>(qa, tiles, s, cur);
+  return launch_one<false, true, false, false, true>(qa, tiles, s, cur);
 }
 
 mx_status launch_quantize(const QuantLaunch& q, bool do_row, bool do_col, cudaStream_t s) {

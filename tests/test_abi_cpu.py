@@ -286,3 +286,63 @@ def test_selftest_rejects_bad_arguments_on_host(L):
     assert _status_of(mx.mx_selftest_wait_timeout, 0, 0x1000, None) == INVALID
     assert _status_of(mx.mx_selftest_wait_timeout, 1000000, None, None) == INVALID
     assert _status_of(mx.mx_selftest_wait_timeout, 20 * 10 ** 9, 0x1000, None) == INVALID
+
+
+def test_static_workspace_gemm_validates_on_host(L):
+    c = 0x4000
+    q = mx.mx_gemm_static_workspace
+    assert _status_of(q, mx.MX_DGRAD, _op(), _op(), c, 128, None, None) == INVALID
+    assert _status_of(q, mx.MX_FPROP, _op(k=48), _op(k=48), c, 128, None, None) == SHAPE
+    assert _status_of(q, mx.MX_FPROP, _op(), _op(), c, 100, None, None) == INVALID
+    assert _status_of(q, mx.MX_FPROP, _op(rows=0), _op(), c, 128, None, None) == 0   # empty: no device needed
+    assert mx.MX_STATIC_WORKSPACE_BYTES == 40 * 1024 * 1024
+
+
+def test_current_scaling_entry_points_validate_on_host(L):
+    x, amax, scale, c = 0x10000, 0x20000, 0x30000, 0x4000
+    qc = mx.mx_quantize_current
+    # (x, batch, rows, cols, ldx, stride, axis, amax, fmt, row, col, scale, offs, n_groups, cap, status, stream)
+    ok = (x, 1, 64, 64, 64, 0, mx.MX_BOTH, amax, 448.0, 0x1000, 0x2000, scale, None, 0, 0, None, None)
+
+    def with_(**kw):
+        names = ["x", "batch", "rows", "cols", "ldx", "stride", "axis", "amax", "fmt", "row", "col", "scale", "offs",
+                 "n", "cap", "st", "s"]
+        a = list(ok)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return a
+    assert _status_of(qc, *with_(cols=48, ldx=48)) == SHAPE                 # cols % 32
+    assert _status_of(qc, *with_(rows=48)) == SHAPE                         # column copy needs rows % 32
+    assert _status_of(qc, *with_(axis=0)) == INVALID
+    assert _status_of(qc, *with_(fmt=0.0)) == INVALID
+    assert _status_of(qc, *with_(fmt=float("inf"))) == INVALID
+    assert _status_of(qc, *with_(amax=None)) == INVALID
+    assert _status_of(qc, *with_(scale=scale + 2)) == ALIGN
+    assert _status_of(qc, *with_(x=x + 2)) == ALIGN
+    assert _status_of(qc, *with_(row=None)) == INVALID
+    assert _status_of(qc, *with_(col=0x2008)) == ALIGN
+    assert _status_of(qc, *with_(ldx=60)) == INVALID                        # ldx < cols
+    assert _status_of(qc, *with_(batch=2, stride=100)) == INVALID           # stride < rows * ldx
+    # grouped: column copy of one matrix, 1 .. MX_MAX_GROUPS groups, capacity a multiple of 128
+    assert _status_of(qc, *with_(offs=0x9000, n=2, cap=100)) == SHAPE
+    assert _status_of(qc, *with_(offs=0x9000, n=513, cap=128)) == SHAPE
+    assert _status_of(qc, *with_(offs=0x9000, n=2, cap=128, batch=2, stride=64 * 64)) == INVALID
+    assert _status_of(qc, *with_(offs=0x9000, n=2, cap=128, axis=mx.MX_ROWWISE)) == INVALID
+    assert _status_of(qc, *with_(batch=0)) == 0                             # nothing to do
+    am = mx.mx_current_amax
+    assert _status_of(am, x, 1, 64, 48, 48, 0, amax, None, None) == SHAPE
+    assert _status_of(am, x, 1, 64, 64, 64, 0, None, None, None) == INVALID
+    assert _status_of(am, x, 1, 64, 64, 64, 0, amax + 1, None, None) == ALIGN
+    assert _status_of(am, x, 0, 64, 64, 64, 0, amax, None, None) == 0
+    # GEMMs: an FP32 scale needs only 4-byte alignment; the rest is mx_gemm's checking
+    g = mx.mx_gemm_current
+    assert _status_of(g, mx.MX_FPROP, _op(scale=0x2004), _op(), c, 128, None, None) != ALIGN
+    assert _status_of(g, mx.MX_FPROP, _op(scale=0x2002), _op(), c, 128, None, None) == ALIGN
+    assert _status_of(g, mx.MX_FPROP, _op(scale=0), _op(), c, 128, None, None) == INVALID
+    assert _status_of(g, mx.MX_DGRAD, _op(), _op(), c, 128, None, None) == INVALID
+    assert _status_of(g, mx.MX_FPROP, _op(k=48), _op(k=48), c, 128, None, None) == SHAPE
+    gg = mx.mx_grouped_gemm_current
+    assert _status_of(gg, mx.MX_FPROP, _op(), _op(), None, 4, c, 128, None, None) == INVALID
+    assert _status_of(gg, mx.MX_FPROP, _op(), _op(), 0x8000, 513, c, 128, None, None) == SHAPE
+    assert _status_of(gg, mx.MX_WGRAD, _op(orient=mx.MX_COLWISE, k=160), _op(orient=mx.MX_COLWISE, k=160), 0x8000,
+                      2, c, 128, None, None) == SHAPE

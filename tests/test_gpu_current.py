@@ -221,3 +221,35 @@ def test_dense_ffn_full_size():
         Bd = oracle.current_dequantize(np.ascontiguousarray(B[jj]), sb)
         ref, S = np.sum(Ad * Bd, axis=1), np.sum(np.abs(Ad * Bd), axis=1)
         check_values(f64(out[torch.from_numpy(ii), torch.from_numpy(jj)]), ref, S, f"current dense FFN mode {mode}")
+
+
+def test_quotient_exhaustive_against_ieee_division():
+    """Every finite BF16 x divided by the scale of every positive finite BF16
+    amax: the quantiser's codes equal E4M3 of the IEEE FP32 quotient (torch's
+    division on the GPU, then torch's E4M3 conversion, which the oracle pins
+    check against the E4M3 rounding rule), saturated at +-448. This covers the
+    reciprocal-and-correction division the kernel uses for the quotient."""
+    pats = torch.arange(0, 1 << 16, dtype=torch.int32)
+    finite = (pats & 0x7F80) != 0x7F80
+    xbits = pats[finite].to(torch.int16)                      # 65280 finite patterns (both signs)
+    assert xbits.numel() == 510 * 128
+    x = xbits.view(torch.bfloat16).reshape(510, 128).cuda()
+    amax_bits = torch.arange(1, 0x7F80, dtype=torch.int32)     # every positive finite BF16 amax
+    amaxes = (amax_bits << 16).view(torch.float32).cuda()
+    E = 480
+    xs = x.unsqueeze(0).expand(E, 510, 128).contiguous()
+    xf = x.float()
+    for start in range(0, amaxes.numel(), E):
+        am = amaxes[start:start + E]
+        n = am.numel()
+        row, _ = mx.quantize_current(xs[:n], mx.MX_ROWWISE, amax=am)
+        # IEEE FP32 division, as the scale rule (a tensor divisor: torch turns a
+        # scalar divisor into a multiplication by its reciprocal)
+        s = am / torch.full_like(am, 448.0)
+        assert torch.equal(row.scale.view(torch.int32), s.view(torch.int32))
+        q = (xf.unsqueeze(0) / s.view(n, 1, 1)).clamp(-448.0, 448.0)
+        ref = q.to(torch.float8_e4m3fn).view(torch.uint8)
+        got = row.data.view(n, 510, 128)
+        if not torch.equal(got, ref):
+            bad = (got != ref).nonzero()[:5].tolist()
+            raise AssertionError(f"amax block {start}: first mismatches {bad}")
