@@ -207,6 +207,7 @@ struct Tile {
   int32_t valid_m;     // rows of the tile that exist (may be <= 0 for a pair's spare tile)
   int32_t group;       // expert (grouped kinds)
   int32_t part;        // -1: whole tile; >= 0: split-tail segment (workspace unit); -2: empty segment
+  int32_t n_mma;       // pair tiles: the MMA's N (the tile width, or less for the last columns of C)
   const uint8_t* sfb;  // base of B's scales for this tile's expert
   __nv_bfloat16* cbase;  // C element (m0, n0)
 };
@@ -292,12 +293,24 @@ __device__ __forceinline__ Tile get_tile(const GParams& p, const GroupInfo& g, i
 // Pair tiles: t enumerates (pair of M tiles, N tile); the CTA's rank in its
 // cluster picks the M tile, both CTAs share the BN-wide N tile. K-ragged
 // grouped: experts in decreasing-K order, each expert's pair tiles M-fastest.
+// The MMA width of a pair tile starting at column n0: the tile width, or, for
+// the last tile of a C whose width is not a multiple of it, the columns left
+// rounded up to 32 (each CTA then holds a multiple of 16 rows of B). The MMAs
+// take time in proportion to their N, so a narrow last tile costs only its
+// own columns.
+template <int BN>
+__device__ __forceinline__ int32_t pair_n_mma(int64_t N, int64_t n0) {
+  const int64_t left = N - n0;
+  return left >= BN ? BN : static_cast<int32_t>((left + 31) & ~int64_t{31});
+}
+
 template <int KIND, bool kSwiGLU, int BN>
 __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo& g, int64_t t, uint32_t crank) {
   const int64_t nt = (p.N + BN - 1) / BN;
   const int64_t mu = ((p.M + kBM - 1) / kBM + 1) / 2;
   Tile ti;
   ti.part = -1;
+  ti.n_mma = BN;
   int64_t mp, nb;
   if (KIND == GEMM_GROUPED_M) {
     // Pair row tiles of 256 inside one expert, N-fastest; the odd CTA's half
@@ -314,7 +327,8 @@ __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo&
       ti.b_row = static_cast<int64_t>(e) * p.b_rows_group + crank * (p.N >> 1) + ti.n0;
     } else {
       ti.n0 = nb * BN;
-      ti.b_row = static_cast<int64_t>(e) * p.b_rows_group + ti.n0 + crank * (BN / 2);
+      ti.n_mma = pair_n_mma<BN>(p.N, ti.n0);
+      ti.b_row = static_cast<int64_t>(e) * p.b_rows_group + ti.n0 + crank * (ti.n_mma / 2);
     }
     ti.k_atom0 = 0;
     ti.nkb = static_cast<int32_t>((p.K + kBK - 1) / kBK);
@@ -367,7 +381,8 @@ __device__ __forceinline__ Tile get_pair_tile(const GParams& p, const GroupInfo&
   ti.m0 = (2 * mp + crank) * kBM;
   ti.n0 = nb * BN;
   ti.a_row = ti.m0;
-  ti.b_row = ti.n0 + crank * (BN / 2);
+  ti.n_mma = pair_n_mma<BN>(p.N, ti.n0);
+  ti.b_row = ti.n0 + crank * (ti.n_mma / 2);
   ti.valid_m = static_cast<int32_t>(min64(kBM, p.M - ti.m0));
   ti.sfb = p.b_scale;
   ti.cbase = p.c + static_cast<int64_t>(ti.group) * p.c_group_stride + ti.m0 * p.ldc + ti.n0;
@@ -1094,6 +1109,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (!wait_or_abort<true>(&acc_empty[acc], acc_phase ^ 1, p, s_abort)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t idesc_t = ti.n_mma == BN ? idesc
+                                 : (kTS ? idesc_f8_e4m3_f32(2 * kBM, static_cast<uint32_t>(ti.n_mma))
+                                        : idesc_mxf8_e4m3(2 * kBM, static_cast<uint32_t>(ti.n_mma)));
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!wait_or_abort<true>(&full_bar[stage], phase, p, s_abort) ||
               (!kTS && !wait_or_abort<true>(&sf_full[stage], phase, p, s_abort))) {
@@ -1105,13 +1123,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::kBBytes));
           if constexpr (kTS) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) tc_mma_f8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              tc_mma_f8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_t, (kb | k) != 0 ? 1u : 0u);
           } else {
             const uint32_t sfa_t = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * C::kSfCols);
             const uint32_t sfb_t = sfa_t + 4;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              tc_mma_mxf8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
+              tc_mma_mxf8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_id(idesc_t, k, k), sfa_t, sfb_t,
                                (kb | k) != 0 ? 1u : 0u);
           }
           tc_commit_pair_multicast(&empty_bar[stage], static_cast<uint16_t>(0x3));
