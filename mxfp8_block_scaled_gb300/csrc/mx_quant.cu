@@ -497,6 +497,14 @@ __device__ __forceinline__ void quant_body(const QuantArgs& qa, const CurParams&
               dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
               dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
             }
+            if constexpr (kCol) {
+              // One scale for the whole matrix: the column copy holds the same
+              // codes, transposed. They replace the first two of the four
+              // 16-byte chunks this thread read (its own), for the column pass.
+              uint4* own = const_cast<uint4*>(src) + r0 * 8;
+              own[cbase ^ rsub] = make_uint4(q[0], q[1], q[2], q[3]);
+              own[(cbase + 1) ^ rsub] = make_uint4(q[4], q[5], q[6], q[7]);
+            }
             continue;
           }
           uint32_t m = 0;
@@ -535,7 +543,53 @@ __device__ __forceinline__ void quant_body(const QuantArgs& qa, const CurParams&
       }
 
       if constexpr (kCol) {
-        if (ok) {
+        if constexpr (kCur && kRow) {
+          // Current scaling with both copies: the row pass left every code in
+          // the tile (the 32 codes of row r, columns 32b .. 32b + 31, in
+          // 16-byte chunks 4(b % 2) and 4(b % 2) + 1 of row r of half b / 2,
+          // swizzled like the input). Once all of them are there, the column
+          // copy only transposes bytes.
+          consumers_sync();
+          if (ok) {
+            const int cp = tid & 63;
+            const int rb = tid >> 6;
+            const uint8_t* half = tiles + s * kTileBytes + (cp >> 5) * (kTileBytes / 2);
+            const int chunk = ((cp >> 4) & 1) * 4 + ((cp >> 3) & 1);
+            const int byte = 2 * (cp & 7);
+            uint8_t* stg = col_stage + (j & 1) * kColStageBytes;
+            // rows 16u .. 16u + 15 of the block: one 16-byte output chunk per column
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              uint32_t c[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int r = rb * 32 + 16 * u + i;
+                c[i] = *reinterpret_cast<const uint16_t*>(half + r * 128 + ((chunk ^ (r & 7)) << 4) + byte);
+              }
+              if (u == 1) mbar_arrive(&empty[s]);  // this thread is done with the tile
+              if (kGrouped && g.valid_rows < kTileRows) {
+                // rows past the group's end hold the next group's data: zero padding
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (rb * 32 + 16 * u + i >= g.valid_rows) c[i] = 0u;
+              }
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  // byte h of rows 4q .. 4q + 3
+                  const uint32_t t01 = __byte_perm(c[4 * q], c[4 * q + 1], 0x5140);
+                  const uint32_t t23 = __byte_perm(c[4 * q + 2], c[4 * q + 3], 0x5140);
+                  o[q] = __byte_perm(t01, t23, h ? 0x7632 : 0x5410);
+                }
+                const int orow = 2 * cp + h;
+                *reinterpret_cast<uint4*>(stg + orow * 128 + (((2 * rb + u) ^ (orow & 7)) << 4)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+              }
+            }
+          }
+        } else if (ok) {
           // ---- column copy: thread = (column pair cp, 32-row block rb) ----
           const int cp = tid & 63;
           const int rb = tid >> 6;
