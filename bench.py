@@ -814,17 +814,20 @@ def _measure(step, args, world, stream, kernel_pass=True, clocks=True):
     return max_over_ranks(t0.elapsed_time(t1), world), timers, clk
 
 
-def run_mla(args, rank, world, peaks, peak_src):
+def run_mla(args, rank, world, peaks, peak_src, pages: bool = False):
     """MLA projection set at M = 16384 tokens (q_down 2048->1536, kv_down
-    2048->576, kv_up 512->4096, o_proj 2048->2048): per projection X and W
-    quantised in one launch and dY in another, then fprop, then dgrad + wgrad
+    2048->576, kv_up 512->4096, o_proj 2048->2048; with `pages`, the frozen 16B
+    configuration's own projections q_proj 2048->2048, kv_a_proj_with_mqa
+    2048->3136, kv_b_proj 3072->3072, o_proj 2048->2048): per projection X and
+    W quantised in one launch and dY in another, then fprop, then dgrad + wgrad
     in one launch. A GEMM's roofline time is max(FLOPs / FP8 peak, algorithmic
     bytes / HBM bandwidth); the backward launch's is the sum of its two."""
     import workloads
     import mxfp8_block_scaled_gb300 as mx
     projs = []
-    for name, _, _ in workloads.MLA_PROJECTIONS:
-        d = workloads.mla_projection(name)
+    table = workloads.MLA_PROJECTIONS_PAGES if pages else workloads.MLA_PROJECTIONS
+    for name, _, _ in table:
+        d = workloads.mla_projection(name, pages=pages)
         projs.append((name, d["X"], d["W"], d["dY"]))
     layers = _linear_set(projs, mx)
     stream = torch.cuda.Stream()
@@ -856,8 +859,10 @@ def run_mla(args, rank, world, peaks, peak_src):
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": "mla_projections M=16384: q_down 2048->1536, kv_down 2048->576, "
-                                   "kv_up 512->4096, o_proj 2048->2048", "parallelism": f"replicas{world}",
+            "config": {"workload": ("mla_projections_pages_shapes M=16384: q_proj 2048->2048, kv_a_proj_with_mqa "
+                                    "2048->3136, kv_b_proj 3072->3072, o_proj 2048->2048" if pages else
+                                    "mla_projections M=16384: q_down 2048->1536, kv_down 2048->576, "
+                                    "kv_up 512->4096, o_proj 2048->2048"), "parallelism": f"replicas{world}",
                        "l2": "no flush: a step moves ~1.5 GB (> 129 MB L2)"},
             "per_gemm": per_gemm,
             "roofline": tensor_roofline("mx_gemm_pair_kernel / mx_gemm_kernel", achieved, peaks, peak_src,
@@ -1235,10 +1240,15 @@ def run_dense(args, rank, world, peaks, peak_src):
     return line
 
 
-RUNS = {"dense_ffn": run_dense, "single": run_single, "mla": run_mla, "moe": run_moe, "quant": run_quant_sweep,
-        "wrefresh": run_wrefresh, "blockwise": run_blockwise, "current": run_current}
+def run_mla_pages(args, rank, world, peaks, peak_src):
+    return run_mla(args, rank, world, peaks, peak_src, pages=True)
+
+
+RUNS = {"dense_ffn": run_dense, "single": run_single, "mla": run_mla, "mla_pages": run_mla_pages, "moe": run_moe,
+        "quant": run_quant_sweep, "wrefresh": run_wrefresh, "blockwise": run_blockwise, "current": run_current}
 # Sub-results of the default line, keyed by the workload they measure.
 SUB_CONFIGS = (("config1_single_linear", "single"), ("config3_mla_projections", "mla"),
+               ("config3b_mla_projections_pages_shapes", "mla_pages"),
                ("config4_moe_routed_experts", "moe"), ("config5_quant_sweep", "quant"),
                ("variant_blockwise_fp8", "blockwise"), ("variant_current_scaling", "current"),
                ("weight_refresh_fp32_master", "wrefresh"))

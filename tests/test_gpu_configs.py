@@ -87,9 +87,10 @@ def test_ffn_gemm(ffn, mode):
 # MLA projections at M = 16384
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", [p[0] for p in workloads.MLA_PROJECTIONS])
-def test_mla_projection(name):
-    d = workloads.mla_projection(name)
+@pytest.mark.parametrize("name,pages", [(p[0], False) for p in workloads.MLA_PROJECTIONS] +
+                         [(p[0], True) for p in workloads.MLA_PROJECTIONS_PAGES])
+def test_mla_projection(name, pages):
+    d = workloads.mla_projection(name, pages=pages)
     (xr, xc), (wr, wc) = quant_multi([d["X"], d["W"]])
     ((dr, dc),) = quant_multi([d["dY"]])
     for k, q in (("X", (xr, xc)), ("W", (wr, wc)), ("dY", (dr, dc))):
@@ -104,7 +105,7 @@ def test_mla_projection(name):
     for out, srcs, tag in ((y, (d["X"], 1, d["W"], 1), "fprop"), (dx, (d["dY"], 1, d["W"], 2), "dgrad"),
                            (dw, (d["dY"], 2, d["X"], 2), "wgrad")):
         ii, jj = sample_entries(out.shape[0], out.shape[1], 1024, 20, tile_n=256)
-        check_gemm_sampled(out, *srcs, ii, jj, what=f"MLA {name} {tag}")
+        check_gemm_sampled(out, *srcs, ii, jj, what=f"MLA {'pages ' if pages else ''}{name} {tag}")
 
 
 # ---------------------------------------------------------------------------

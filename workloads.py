@@ -137,12 +137,23 @@ def dense_ffn(seed: int = SEED_BASE + 2, M: int = 8192, K: int = 2048, N: int = 
 MLA_PROJECTIONS = (("q_down", 2048, 1536), ("kv_down", 2048, 576),
                    ("kv_up", 512, 4096), ("o_proj", 2048, 2048))
 
+# The attention projections of the frozen 16B model configuration itself
+# ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计", frozen 16B spec: hidden 2048,
+# 16 heads, q_lora_rank null, kv_lora_rank 3072, qk_nope / qk_rope head dims
+# 64 / 64, v_head_dim 128), with the DeepSeek-V3 attention's projection widths:
+# q_proj 2048 -> 16 * (64 + 64), kv_a_proj_with_mqa 2048 -> 3072 + 64,
+# kv_b_proj 3072 -> 16 * (64 + 128), o_proj 16 * 128 -> 2048.
+MLA_PROJECTIONS_PAGES = (("q_proj", 2048, 2048), ("kv_a_proj_with_mqa", 2048, 3136),
+                         ("kv_b_proj", 3072, 3072), ("o_proj", 2048, 2048))
 
-def mla_projection(name: str, seed: int = SEED_BASE + 3, M: int = 16384):
-    """X[M, K_in] ~ N(0,1), W[N_out, K_in] ~ N(0, 0.02), dY[M, N_out] ~ N(0,1)."""
-    idx = [p[0] for p in MLA_PROJECTIONS].index(name)
-    _, k_in, n_out = MLA_PROJECTIONS[idx]
-    s = seed * 16 + idx
+
+def mla_projection(name: str, seed: int = SEED_BASE + 3, M: int = 16384, pages: bool = False):
+    """X[M, K_in] ~ N(0,1), W[N_out, K_in] ~ N(0, 0.02), dY[M, N_out] ~ N(0,1).
+    pages: a projection of MLA_PROJECTIONS_PAGES (seeds of their own)."""
+    table = MLA_PROJECTIONS_PAGES if pages else MLA_PROJECTIONS
+    idx = [p[0] for p in table].index(name)
+    _, k_in, n_out = table[idx]
+    s = seed * 16 + idx + (8 if pages else 0)
     return {"X": normal_bf16((M, k_in), s), "W": normal_bf16((n_out, k_in), s + 1, 0.02),
             "dY": normal_bf16((M, n_out), s + 2)}
 
