@@ -306,10 +306,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 template <bool kRow, bool kCol, bool kGrouped, bool kMulti, bool kCur>
 __device__ __forceinline__ void quant_body(const QuantArgs& qa, const CurParams& cur) {
   static_assert(!kCur || !kMulti, "current scaling: one matrix (or one stack) per launch");
-  // Programmatic dependent launch: let the next kernel on the stream be
-  // scheduled, and touch global memory only once the previous one completed.
-  pdl_launch_dependents();
-  pdl_wait();
   const QParams& p = qa.p[0];  // grouped and shared fields (status word, bound)
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the unit of the 128-byte swizzle pattern.
@@ -333,6 +329,25 @@ __device__ __forceinline__ void quant_body(const QuantArgs& qa, const CurParams&
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+
+  // What touches no global memory runs before the wait for the previous
+  // kernel: the stage barriers and the tensor-map prefetch (the maps are
+  // kernel parameters).
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kConsumers / 32 && lane == 0)
+    for (int i = 0; i < qa.n; ++i) tma_prefetch_desc(&qa.map[i]);
+  // Programmatic dependent launch: let the next kernel on the stream be
+  // scheduled, and touch global memory only once the previous one completed.
+  pdl_launch_dependents();
+  pdl_wait();
+
   const int64_t col_tiles = (p.cols + kTileCols - 1) / kTileCols;
   int64_t row_tiles = (p.rows + kTileRows - 1) / kTileRows;
 
@@ -375,14 +390,6 @@ __device__ __forceinline__ void quant_body(const QuantArgs& qa, const CurParams&
 
   // Grouped launches hold one matrix and take their tile grid from the groups.
   const int64_t ntiles = kGrouped ? row_tiles * col_tiles : qa.tile0[qa.n];
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers);
-    }
-    s_abort = 0;
-    fence_mbar_init();
-  }
   if constexpr (kCur) {
     // the scale each matrix was quantised with, for the GEMM that reads it
     if (blockIdx.x == 0)
@@ -393,7 +400,6 @@ __device__ __forceinline__ void quant_body(const QuantArgs& qa, const CurParams&
   if (warp == kConsumers / 32) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int i = 0; i < qa.n; ++i) tma_prefetch_desc(&qa.map[i]);
       int j = 0;
       int ti = 0;  // tensor of tile t (t only grows)
       int last_phase_issued[kStages];
@@ -830,10 +836,6 @@ __device__ __forceinline__ uint32_t quant4_f32(float a, float b, float c, float 
 template <bool kRow, bool kCol>
 __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     mx_quant_f32_kernel(const __grid_constant__ CUtensorMap tmap_x, QParams p) {
-  // Programmatic dependent launch: let the next kernel on the stream be
-  // scheduled, and touch global memory only once the previous one completed.
-  pdl_launch_dependents();
-  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;                                        // kStages x 2 boxes x [128 rows][128 bytes]
@@ -849,6 +851,8 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
   const int64_t col_tiles = (p.cols + kF32Cols - 1) / kF32Cols;
   const int64_t row_tiles = (p.rows + kTileRows - 1) / kTileRows;
   const int64_t ntiles = row_tiles * col_tiles * p.batch;
+  // Barriers and the tensor-map prefetch touch no global memory: they run
+  // before the wait for the previous kernel (as in the BF16 quantiser).
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -857,12 +861,16 @@ __global__ void __launch_bounds__(kThreads, MX_QUANT_MIN_BLOCKS)
     s_abort = 0;
     fence_mbar_init();
   }
+  if (warp == kConsumers / 32 && lane == 0) tma_prefetch_desc(&tmap_x);
+  // Programmatic dependent launch: let the next kernel on the stream be
+  // scheduled, and touch global memory only once the previous one completed.
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
 
   if (warp == kConsumers / 32) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_x);
       int j = 0;
       int last_phase_issued[kStages];
 #pragma unroll
