@@ -462,6 +462,17 @@ mx_status mx_grouped_gemm_current(int mode, const mx_operand* a, const mx_operan
                                   int n_groups, void* c, int64_t ldc, int* dev_status, void* stream);
 
 /*
+ * mx_gemm_current_multi - up to MX_MAX_GEMM_MULTI independent tensor-scaled
+ * dense GEMMs (each as mx_gemm_current, operands from mx_quantize_current) in
+ * one launch, e.g. a layer's dgrad and wgrad (the step data flow of
+ * "DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §10 with the current-scaling
+ * recipe of §3.2 / §8.2). Problem descriptors, requirements and errors as
+ * mx_gemm_multi; every output equals mx_gemm_current's for that problem bit
+ * for bit (the same whole tiles in the same order).
+ */
+mx_status mx_gemm_current_multi(const mx_gemm_problem* problems, int n, int* dev_status, void* stream);
+
+/*
  * mx_grouped_gemm_swiglu - the routed experts' gate_up fprop with the grouped
  * SwiGLU fused into its epilogue ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计"
  * §5: gate_up_proj [E, 2F, H] and the grouped SwiGLU between gate_up and

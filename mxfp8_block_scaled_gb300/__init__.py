@@ -37,7 +37,7 @@ EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quant
             "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version",
             "mx_selftest_wait_timeout", "mx_gemm_workspace_bytes", "mx_gemm_with_workspace", "mx_gemm_multi",
             "mx_gemm_static_workspace", "mx_current_amax", "mx_quantize_current", "mx_gemm_current",
-            "mx_grouped_gemm_current")
+            "mx_grouped_gemm_current", "mx_gemm_current_multi")
 MX_STATIC_WORKSPACE_BYTES = 40 * 1024 * 1024
 
 
@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
     L.mx_grouped_gemm_current.restype = i32
     L.mx_gemm_multi.argtypes = [ctypes.POINTER(MXGemmProblemC), i32, vp, vp]
     L.mx_gemm_multi.restype = i32
+    L.mx_gemm_current_multi.argtypes = [ctypes.POINTER(MXGemmProblemC), i32, vp, vp]
+    L.mx_gemm_current_multi.restype = i32
     L.mx_grouped_gemm.argtypes = [i32, ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
                                   vp, vp]
     L.mx_grouped_gemm.restype = i32
@@ -253,6 +255,12 @@ def mx_gemm_multi(problems, dev_status, stream) -> None:
     """``problems``: a sequence of MXGemmProblemC."""
     arr = (MXGemmProblemC * max(len(problems), 1))(*problems)
     _check(lib().mx_gemm_multi(arr, len(problems), dev_status, stream), "mx_gemm_multi")
+
+
+def mx_gemm_current_multi(problems, dev_status, stream) -> None:
+    """``problems``: a sequence of MXGemmProblemC over current-scaled operands."""
+    arr = (MXGemmProblemC * max(len(problems), 1))(*problems)
+    _check(lib().mx_gemm_current_multi(arr, len(problems), dev_status, stream), "mx_gemm_current_multi")
 
 
 def mx_grouped_gemm(mode, a: MXOperandC, b: MXOperandC, group_offsets, n_groups, c, ldc, dev_status,
@@ -577,6 +585,22 @@ def gemm_current(mode: int, a, b, out=None, status=None, stream=None):
         out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
     mx_gemm_current(mode, a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), _ptr(status), _stream(stream))
     return out
+
+
+def gemm_current_multi(problems, status=None, stream=None):
+    """Several independent current-scaled GEMMs (mode, a, b[, out]) in one
+    launch; returns the outputs (BF16 [a.rows, b.rows], allocated where not
+    given)."""
+    torch = _torch()
+    outs, descs = [], []
+    for pr in problems:
+        mode, a, b = pr[0], pr[1], pr[2]
+        out = pr[3] if len(pr) > 3 and pr[3] is not None else \
+            torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
+        outs.append(out)
+        descs.append(MXGemmProblemC(a.c_operand(), b.c_operand(), out.data_ptr(), out.stride(0), mode, 0))
+    mx_gemm_current_multi(descs, _ptr(status), _stream(stream))
+    return outs
 
 
 def grouped_gemm_current(mode: int, a, b, group_offsets, out=None, status=None, stream=None):

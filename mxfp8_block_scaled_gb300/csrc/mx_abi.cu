@@ -788,9 +788,11 @@ static mx_status check_current_operand(const mx_operand* o, const char* name) {
   return MX_OK;
 }
 
-mx_status mx_gemm_current(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,
-                          void* stream) {
-  const char* fn = "mx_gemm_current";
+// Host checks and launch description of one tensor-scaled dense GEMM (shared
+// by mx_gemm_current and mx_gemm_current_multi). L->M == 0 or L->N == 0:
+// nothing to do; L->K == 0: the output is zeroed by the caller.
+static mx_status current_gemm_setup(const char* fn, int mode, const mx_operand* a, const mx_operand* b, void* c,
+                             int64_t ldc, int* dev_status, GemmLaunch* L) {
   mx_status st = check_current_operand(a, "a");
   if (st != MX_OK) return st;
   st = check_current_operand(b, "b");
@@ -807,30 +809,82 @@ mx_status mx_gemm_current(int mode, const mx_operand* a, const mx_operand* b, vo
   }
   st = check_output(c, ldc, b->rows, a->rows);
   if (st != MX_OK) return st;
-  if (a->rows == 0 || b->rows == 0) return MX_OK;
+  L->kind = GEMM_DENSE;
+  L->a_data = a->data;
+  L->a_scale = a->scale;
+  L->a_ld = a->ld ? a->ld : a->k;
+  L->b_data = b->data;
+  L->b_scale = b->scale;
+  L->b_ld = b->ld ? b->ld : b->k;
+  L->M = a->rows;
+  L->N = b->rows;
+  L->K = a->k;
+  L->b_rows_total = b->rows;
+  L->c = c;
+  L->ldc = ldc;
+  L->offsets = nullptr;
+  L->n_groups = 0;
+  L->dev_status = dev_status;
+  L->tensor_scaled = true;
+  return MX_OK;
+}
+
+mx_status mx_gemm_current(int mode, const mx_operand* a, const mx_operand* b, void* c, int64_t ldc, int* dev_status,
+                          void* stream) {
+  GemmLaunch L;
+  mx_status st = current_gemm_setup("mx_gemm_current", mode, a, b, c, ldc, dev_status, &L);
+  if (st != MX_OK) return st;
+  if (L.M == 0 || L.N == 0) return MX_OK;
   st = check_device();
   if (st != MX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a->k == 0) return zero_output(c, ldc, b->rows, a->rows, s);
-  GemmLaunch L;
-  L.kind = GEMM_DENSE;
-  L.a_data = a->data;
-  L.a_scale = a->scale;
-  L.a_ld = a->ld ? a->ld : a->k;
-  L.b_data = b->data;
-  L.b_scale = b->scale;
-  L.b_ld = b->ld ? b->ld : b->k;
-  L.M = a->rows;
-  L.N = b->rows;
-  L.K = a->k;
-  L.b_rows_total = b->rows;
-  L.c = c;
-  L.ldc = ldc;
-  L.offsets = nullptr;
-  L.n_groups = 0;
-  L.dev_status = dev_status;
-  L.tensor_scaled = true;
+  if (L.K == 0) return zero_output(c, ldc, L.N, L.M, s);
   return launch_gemm(L, s);
+}
+
+mx_status mx_gemm_current_multi(const mx_gemm_problem* problems, int n, int* dev_status, void* stream) {
+  if (n < 0 || n > MX_MAX_GEMM_MULTI) {
+    set_error("mx_gemm_current_multi: n = %d is outside 0 .. %d", n, MX_MAX_GEMM_MULTI);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (n == 0) return MX_OK;
+  if (!problems) {
+    set_error("mx_gemm_current_multi: problems is null");
+    return MX_ERR_INVALID_ARG;
+  }
+  GemmLaunch Ls[MX_MAX_GEMM_MULTI];
+  bool any = false;
+  for (int i = 0; i < n; ++i) {
+    const mx_gemm_problem& pr = problems[i];
+    if (pr.reserved != 0) {
+      set_error("mx_gemm_current_multi: problem %d: reserved must be 0", i);
+      return MX_ERR_INVALID_ARG;
+    }
+    mx_status st = current_gemm_setup("mx_gemm_current_multi", pr.mode, &pr.a, &pr.b, pr.c, pr.ldc, dev_status, &Ls[i]);
+    if (st != MX_OK) {
+      char msg[512];
+      std::snprintf(msg, sizeof(msg), "%s", mx_last_error());
+      set_error("problem %d: %s", i, msg);
+      return st;
+    }
+    if (Ls[i].M > 0 && Ls[i].N > 0) any = true;
+  }
+  if (!any) return MX_OK;
+  mx_status st = check_device();
+  if (st != MX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemmLaunch live[MX_MAX_GEMM_MULTI];
+  int m = 0;
+  for (int i = 0; i < n; ++i) {
+    if (Ls[i].M == 0 || Ls[i].N == 0) continue;
+    if (Ls[i].K == 0) {
+      st = zero_output(Ls[i].c, Ls[i].ldc, Ls[i].N, Ls[i].M, s);
+      if (st != MX_OK) return st;
+      continue;
+    }
+    live[m++] = Ls[i];
+  }
+  return m ? launch_gemm_multi(live, m, s) : MX_OK;
 }
 
 mx_status mx_grouped_gemm_current(int mode, const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,

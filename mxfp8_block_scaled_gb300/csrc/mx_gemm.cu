@@ -2135,6 +2135,13 @@ int64_t schedule_round_robin(const GemmLaunch* Ls, int n, int64_t clusters) {
 // Several dense GEMMs in one launch of the pair kernel.
 mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
   constexpr int BN = 256;
+  // Block-scaled problems, or (all of them) one FP32 scale per tensor.
+  const bool ts = Ls_in[0].tensor_scaled;
+  for (int i = 1; i < n; ++i)
+    if (Ls_in[i].tensor_scaled != ts) {
+      set_error("several GEMMs per launch: block-scaled and tensor-scaled problems do not mix");
+      return MX_ERR_INVALID_ARG;
+    }
   PairArgs* args = pair_args_scratch();
   std::memset(args, 0, sizeof(PairArgs));
   // Longest tiles first: they start early and the short ones fill in behind.
@@ -2152,18 +2159,24 @@ mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
     if (st != MX_OK) return st;
     st = make_map(&pr.b, L.b_data, L.b_rows_total, L.K, L.b_ld, BN / 2);
     if (st != MX_OK) return st;
-    st = make_scale_map(&pr.sfa, L.a_scale, L.M, L.K);
-    if (st != MX_OK) return st;
-    st = make_scale_map(&pr.sfb, L.b_scale, L.N, L.K);
-    if (st != MX_OK) return st;
+    if (ts) {
+      pr.p.ts_a = static_cast<const float*>(L.a_scale);
+      pr.p.ts_b = static_cast<const float*>(L.b_scale);
+    } else {
+      st = make_scale_map(&pr.sfa, L.a_scale, L.M, L.K);
+      if (st != MX_OK) return st;
+      st = make_scale_map(&pr.sfb, L.b_scale, L.N, L.K);
+      if (st != MX_OK) return st;
+    }
     output_map(L, pr.p, &pr.c, GEMM_DENSE);
     args->tile0[i] = tiles;
     tiles += pair_tiles_upper(L);
   }
   args->tile0[n] = tiles;
   args->n = n;
-  const size_t smem = PairCfgT<BN, false, false>::smem_bytes();
-  auto kern = mx_gemm_pair_kernel<GEMM_DENSE, false, true, BN, false>;
+  const size_t smem = ts ? PairCfgT<BN, true, false>::smem_bytes() : PairCfgT<BN, false, false>::smem_bytes();
+  auto kern = ts ? mx_gemm_pair_kernel<GEMM_DENSE, false, true, BN, true>
+                 : mx_gemm_pair_kernel<GEMM_DENSE, false, true, BN, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count() / 2));

@@ -346,3 +346,21 @@ def test_current_scaling_entry_points_validate_on_host(L):
     assert _status_of(gg, mx.MX_FPROP, _op(), _op(), 0x8000, 513, c, 128, None, None) == SHAPE
     assert _status_of(gg, mx.MX_WGRAD, _op(orient=mx.MX_COLWISE, k=160), _op(orient=mx.MX_COLWISE, k=160), 0x8000,
                       2, c, 128, None, None) == SHAPE
+
+
+def test_current_gemm_multi_rejects_bad_arguments_on_host(L):
+    """mx_gemm_current_multi: each problem checked as mx_gemm_current (FP32
+    scales need only 4-byte alignment), the list as mx_gemm_multi."""
+    q = mx.mx_gemm_current_multi
+    good = _gp(a=_op(scale=0x2004))
+    assert _status_of(q, [good, _gp(mode=mx.MX_DGRAD)], None, None) == INVALID      # orientation vs mode
+    assert _status_of(q, [good, _gp(a=_op(scale=0x2002))], None, None) == ALIGN
+    assert _status_of(q, [good, _gp(a=_op(scale=0))], None, None) == INVALID
+    assert _status_of(q, [good, _gp(a=_op(k=48), b=_op(k=48))], None, None) == SHAPE
+    bad = _gp()
+    bad.reserved = 1
+    assert _status_of(q, [good, bad], None, None) == INVALID
+    assert _status_of(q, [good] * (mx.MX_MAX_GEMM_MULTI + 1), None, None) == INVALID
+    assert _status_of(q, [], None, None) == 0
+    assert _status_of(q, [_gp(a=_op(rows=0)), _gp(b=_op(rows=0))], None, None) == 0   # empty problems
+    assert "problem 1" in (lambda: (_status_of(q, [good, _gp(ldc=100)], None, None), mx.mx_last_error())[1])()

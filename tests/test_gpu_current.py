@@ -208,7 +208,13 @@ def test_dense_ffn_full_size():
     (xr, xc), (wr, wc), (dr, dc) = q["X"], q["W"], q["dY"]
     outs = {mx.MX_FPROP: mx.gemm_current(mx.MX_FPROP, xr, wr), mx.MX_DGRAD: mx.gemm_current(mx.MX_DGRAD, dr, wc),
             mx.MX_WGRAD: mx.gemm_current(mx.MX_WGRAD, dc, xc)}
+    # dgrad and wgrad in one launch, as the bench step runs them: the same bits
+    st = mx.new_status()
+    dx, dw = mx.gemm_current_multi([(mx.MX_DGRAD, dr, wc), (mx.MX_WGRAD, dc, xc)], status=st)
     torch.cuda.synchronize()
+    assert mx.read_status(st) == 0
+    assert torch.equal(dx.view(torch.int16), outs[mx.MX_DGRAD].view(torch.int16))
+    assert torch.equal(dw.view(torch.int16), outs[mx.MX_WGRAD].view(torch.int16))
     g = np.random.Generator(np.random.Philox(80))
     cX, cW, cD = ref_codes["X"], ref_codes["W"], ref_codes["dY"]
     for mode, (A, sa, B, sb) in {mx.MX_FPROP: (cX, ref_s["X"], cW, ref_s["W"]),
@@ -221,6 +227,39 @@ def test_dense_ffn_full_size():
         Bd = oracle.current_dequantize(np.ascontiguousarray(B[jj]), sb)
         ref, S = np.sum(Ad * Bd, axis=1), np.sum(np.abs(Ad * Bd), axis=1)
         check_values(f64(out[torch.from_numpy(ii), torch.from_numpy(jj)]), ref, S, f"current dense FFN mode {mode}")
+
+
+def test_gemm_current_multi_matches_single_calls():
+    """Several tensor-scaled GEMMs in one launch (mixed modes and shapes, one
+    of them small enough that its tiles alone would not fill the GPU): every
+    output equals the mx_gemm_current result bit for bit, and the oracle's
+    within the bound."""
+    cases = [(mx.MX_FPROP, 992, 1088, 2048), (mx.MX_DGRAD, 2048, 2560, 1024), (mx.MX_WGRAD, 320, 224, 96)]
+    probs, refs = [], []
+    for i, (mode, M, N, K) in enumerate(cases):
+        A = workloads.normal_bf16((M, K) if mode != mx.MX_WGRAD else (K, M), 70 + i)
+        B = workloads.normal_bf16((N, K) if mode == mx.MX_FPROP else (K, N), 80 + i, 0.02)
+        ra, ca_ = mx.quantize_current(A.cuda(), mx.MX_BOTH)
+        rb, cb_ = mx.quantize_current(B.cuda(), mx.MX_BOTH)
+        oa, sa, _ = oracle_copy(A)
+        ob, sb, _ = oracle_copy(B)
+        if mode == mx.MX_FPROP:
+            a, b, ra_c, rb_c = ra, rb, oa, ob
+        elif mode == mx.MX_DGRAD:
+            a, b, ra_c, rb_c = ra, cb_, oa, np.ascontiguousarray(ob.T)
+        else:
+            a, b, ra_c, rb_c = ca_, cb_, np.ascontiguousarray(oa.T), np.ascontiguousarray(ob.T)
+        probs.append((mode, a, b))
+        refs.append((ra_c, sa, rb_c, sb))
+    st = mx.new_status()
+    outs = mx.gemm_current_multi(probs, status=st)
+    singles = [mx.gemm_current(mode, a, b) for mode, a, b in probs]
+    torch.cuda.synchronize()
+    assert mx.read_status(st) == 0
+    for (mode, _, _), out, one, (ca, sa, cb, sb) in zip(probs, outs, singles, refs):
+        assert torch.equal(out.view(torch.int16), one.view(torch.int16))
+        ref, S = gemm_ref(ca, sa, cb, sb)
+        check_values(f64(out), ref, S, f"current multi mode {mode}")
 
 
 def test_quotient_exhaustive_against_ieee_division():
