@@ -493,6 +493,34 @@ mx_status mx_gemm_current_multi(const mx_gemm_problem* problems, int n, int* dev
 mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
                                  int n_groups, void* c, int64_t ldc, int* dev_status, void* stream);
 
+/*
+ * mx_grouped_gemm_swiglu_quantize - mx_grouped_gemm_swiglu with its output
+ * quantised in the same epilogue: instead of the BF16 [M_total, F] output it
+ * writes that output's MX copies, byte for byte what mx_quantize(output,
+ * MX_BOTH, group_offsets, col_capacity) would write from it (the output
+ * values rounded to BF16 exactly as mx_grouped_gemm_swiglu stores them, then
+ * the block rule of mx_quantize). These are the down projection's operands:
+ * the row copy for its fprop, the per-expert column copy for its wgrad
+ * ("DeepSeek-V3 16B FSDP2 MXFP8/HiF8 训练设计" §5 and §12.2: quantise by role
+ * before the GEMMs that read the tensor).
+ *
+ *   a, b, group_offsets, n_groups   as mx_grouped_gemm_swiglu.
+ *   row_data   E4M3 [M_total, F]; row_scale  mx_scale_bytes(M_total, F) bytes.
+ *   col_data   E4M3 [F, col_capacity]: group e's rows at columns poff[e] ..,
+ *              each segment zero-padded to a multiple of 128 rows (the layout
+ *              of mx_quantize's grouped column copy); col_scale
+ *              mx_scale_bytes(F, col_capacity) bytes. Columns past the last
+ *              segment are not written.
+ *   col_capacity  a positive multiple of 128, at least the sum over groups of
+ *              their rows rounded up to 128 (mx_grouped_padded_rows); a
+ *              smaller sum on the device is MX_ERR_DEVICE_CHECK in dev_status.
+ *   All four outputs 16-byte aligned and owned by the caller. K = 0 zeroes all
+ *   four buffers (silu(0) * 0 = 0). Errors otherwise as mx_grouped_gemm_swiglu.
+ */
+mx_status mx_grouped_gemm_swiglu_quantize(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                                          int n_groups, void* row_data, void* row_scale, void* col_data,
+                                          void* col_scale, int64_t col_capacity, int* dev_status, void* stream);
+
 /* Static description of a status code. */
 const char* mx_status_string(mx_status s);
 

@@ -37,7 +37,7 @@ EXPORTED = ("mx_scale_bytes", "mx_grouped_padded_rows", "mx_quantize", "mx_quant
             "mx_gemm_fp8_blockwise", "mx_status_string", "mx_last_error", "mx_abi_version",
             "mx_selftest_wait_timeout", "mx_gemm_workspace_bytes", "mx_gemm_with_workspace", "mx_gemm_multi",
             "mx_gemm_static_workspace", "mx_current_amax", "mx_quantize_current", "mx_gemm_current",
-            "mx_grouped_gemm_current", "mx_gemm_current_multi")
+            "mx_grouped_gemm_current", "mx_gemm_current_multi", "mx_grouped_gemm_swiglu_quantize")
 MX_STATIC_WORKSPACE_BYTES = 40 * 1024 * 1024
 
 
@@ -119,6 +119,9 @@ def lib() -> ctypes.CDLL:
     L.mx_grouped_gemm_swiglu.argtypes = [ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp, i64,
                                          vp, vp]
     L.mx_grouped_gemm_swiglu.restype = i32
+    L.mx_grouped_gemm_swiglu_quantize.argtypes = [ctypes.POINTER(MXOperandC), ctypes.POINTER(MXOperandC), vp, i32, vp,
+                                                  vp, vp, vp, i64, vp, vp]
+    L.mx_grouped_gemm_swiglu_quantize.restype = i32
     L.mx_quantize_fp8_blockwise.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp]
     L.mx_quantize_fp8_blockwise.restype = i32
     L.mx_gemm_fp8_blockwise.argtypes = [vp, vp, i64, vp, vp, i64, i64, vp, i64, vp, vp]
@@ -273,6 +276,13 @@ def mx_grouped_gemm_swiglu(a: MXOperandC, b: MXOperandC, group_offsets, n_groups
                            stream) -> None:
     _check(lib().mx_grouped_gemm_swiglu(_ref(a), _ref(b), group_offsets, n_groups, c, ldc, dev_status, stream),
            "mx_grouped_gemm_swiglu")
+
+
+def mx_grouped_gemm_swiglu_quantize(a: MXOperandC, b: MXOperandC, group_offsets, n_groups, row_data, row_scale,
+                                    col_data, col_scale, col_capacity, dev_status, stream) -> None:
+    _check(lib().mx_grouped_gemm_swiglu_quantize(_ref(a), _ref(b), group_offsets, n_groups, row_data, row_scale,
+                                                 col_data, col_scale, col_capacity, dev_status, stream),
+           "mx_grouped_gemm_swiglu_quantize")
 
 
 # ---------------------------------------------------------------------------
@@ -488,6 +498,29 @@ def grouped_gemm_swiglu(a, b, group_offsets, out=None, status=None, stream=None)
     mx_grouped_gemm_swiglu(a.c_operand(), b.c_operand(), group_offsets.data_ptr(), E, out.data_ptr(), out.stride(0),
                            _ptr(status), _stream(stream))
     return out
+
+
+def grouped_gemm_swiglu_quantize(a, b, group_offsets, col_capacity: int, out=None, status=None, stream=None):
+    """grouped_gemm_swiglu with the output's MX copies written instead of the
+    output: returns (row_copy, col_copy) as quantize(output, MX_BOTH,
+    group_offsets, col_capacity) would ([M_total, F] and the per-expert padded
+    [F, col_capacity]). ``out``: an existing (row_copy, col_copy) pair to fill."""
+    torch = _torch()
+    E = group_offsets.numel() - 1
+    R, F = a.rows, b.rows // 2
+    dev = a.data.device
+    if out is None:
+        row = MXTensor(torch.empty((R, F), dtype=torch.uint8, device=dev),
+                       torch.empty(mx_scale_bytes(R, F), dtype=torch.uint8, device=dev), R, F, MX_ROWWISE)
+        col = MXTensor(torch.empty((F, col_capacity), dtype=torch.uint8, device=dev),
+                       torch.empty(mx_scale_bytes(F, col_capacity), dtype=torch.uint8, device=dev), F, col_capacity,
+                       MX_COLWISE)
+    else:
+        row, col = out
+    mx_grouped_gemm_swiglu_quantize(a.c_operand(), b.c_operand(), group_offsets.data_ptr(), E, _ptr(row.data),
+                                    _ptr(row.scale), _ptr(col.data), _ptr(col.scale), col_capacity, _ptr(status),
+                                    _stream(stream))
+    return row, col
 
 
 @dataclass

@@ -1039,8 +1039,11 @@ mx_status mx_gemm_fp8_blockwise(const void* a_data, const float* a_scale, int64_
   return launch_gemm(L, s);
 }
 
-mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
-                                 int n_groups, void* c, int64_t ldc, int* dev_status, void* stream) {
+// Host checks and launch description of the rows-ragged gate_up fprop with
+// the SwiGLU epilogue (shared by both SwiGLU entry points). *F is the number
+// of output features (half of b's rows).
+static mx_status swiglu_setup(const char* fn, const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                              int n_groups, int* dev_status, GemmLaunch* L, int64_t* F) {
   mx_status st = check_operand(a, "a");
   if (st != MX_OK) return st;
   st = check_operand(b, "b");
@@ -1048,26 +1051,50 @@ mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const
   st = check_mode(MX_FPROP, a, b);
   if (st != MX_OK) return st;
   if (!group_offsets || n_groups < 1) {
-    set_error("mx_grouped_gemm_swiglu: group_offsets must be non-null and n_groups >= 1");
+    set_error("%s: group_offsets must be non-null and n_groups >= 1", fn);
     return MX_ERR_INVALID_ARG;
   }
   if (n_groups > MX_MAX_GROUPS) {
-    set_error("mx_grouped_gemm_swiglu: n_groups = %d is above MX_MAX_GROUPS (%d)", n_groups, MX_MAX_GROUPS);
+    set_error("%s: n_groups = %d is above MX_MAX_GROUPS (%d)", fn, n_groups, MX_MAX_GROUPS);
     return MX_ERR_UNSUPPORTED_SHAPE;
   }
   if (a->k != b->k) {
-    set_error("mx_grouped_gemm_swiglu: a.k != b.k");
+    set_error("%s: a.k != b.k", fn);
     return MX_ERR_INVALID_ARG;
   }
   if (a->rows > 0x7FFFFFFFLL || b->rows > 0x7FFFFFFFLL || a->k > 0x7FFFFFFFLL) {
-    set_error("mx_grouped_gemm_swiglu: sizes must be < 2^31");
+    set_error("%s: sizes must be < 2^31", fn);
     return MX_ERR_UNSUPPORTED_SHAPE;
   }
   if (b->rows % 256 != 0) {
-    set_error("mx_grouped_gemm_swiglu: gate_up rows (2F) must be a multiple of 256");
+    set_error("%s: gate_up rows (2F) must be a multiple of 256", fn);
     return MX_ERR_UNSUPPORTED_SHAPE;
   }
-  const int64_t F = b->rows / 2;
+  *F = b->rows / 2;
+  L->kind = GEMM_GROUPED_M;
+  L->a_data = a->data;
+  L->a_scale = a->scale;
+  L->a_ld = a->ld ? a->ld : a->k;
+  L->b_data = b->data;
+  L->b_scale = b->scale;
+  L->b_ld = b->ld ? b->ld : b->k;
+  L->M = a->rows;
+  L->N = b->rows;
+  L->K = a->k;
+  L->b_rows_total = b->rows * static_cast<int64_t>(n_groups);
+  L->offsets = group_offsets;
+  L->n_groups = n_groups;
+  L->dev_status = dev_status;
+  L->swiglu = true;
+  return MX_OK;
+}
+
+mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                                 int n_groups, void* c, int64_t ldc, int* dev_status, void* stream) {
+  GemmLaunch L;
+  int64_t F = 0;
+  mx_status st = swiglu_setup("mx_grouped_gemm_swiglu", a, b, group_offsets, n_groups, dev_status, &L, &F);
+  if (st != MX_OK) return st;
   st = check_output(c, ldc, F, a->rows);
   if (st != MX_OK) return st;
   if (a->rows == 0 || F == 0) return MX_OK;
@@ -1075,24 +1102,52 @@ mx_status mx_grouped_gemm_swiglu(const mx_operand* a, const mx_operand* b, const
   if (st != MX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a->k == 0) return zero_output(c, ldc, F, a->rows, s);  // silu(0) * 0
-  GemmLaunch L;
-  L.kind = GEMM_GROUPED_M;
-  L.a_data = a->data;
-  L.a_scale = a->scale;
-  L.a_ld = a->ld ? a->ld : a->k;
-  L.b_data = b->data;
-  L.b_scale = b->scale;
-  L.b_ld = b->ld ? b->ld : b->k;
-  L.M = a->rows;
-  L.N = b->rows;
-  L.K = a->k;
-  L.b_rows_total = b->rows * static_cast<int64_t>(n_groups);
   L.c = c;
   L.ldc = ldc;
-  L.offsets = group_offsets;
-  L.n_groups = n_groups;
-  L.dev_status = dev_status;
-  L.swiglu = true;
+  return launch_gemm(L, s);
+}
+
+mx_status mx_grouped_gemm_swiglu_quantize(const mx_operand* a, const mx_operand* b, const int64_t* group_offsets,
+                                          int n_groups, void* row_data, void* row_scale, void* col_data,
+                                          void* col_scale, int64_t col_capacity, int* dev_status, void* stream) {
+  const char* fn = "mx_grouped_gemm_swiglu_quantize";
+  GemmLaunch L;
+  int64_t F = 0;
+  mx_status st = swiglu_setup(fn, a, b, group_offsets, n_groups, dev_status, &L, &F);
+  if (st != MX_OK) return st;
+  if (!row_data || !row_scale || !col_data || !col_scale) {
+    set_error("%s: the four outputs must be non-null", fn);
+    return MX_ERR_INVALID_ARG;
+  }
+  if (!aligned16(row_data) || !aligned16(row_scale) || !aligned16(col_data) || !aligned16(col_scale)) {
+    set_error("%s: outputs must be 16-byte aligned", fn);
+    return MX_ERR_ALIGNMENT;
+  }
+  if (a->rows == 0 || F == 0) return MX_OK;
+  if (col_capacity < 128 || col_capacity % 128 != 0) {
+    set_error("%s: col_capacity must be a positive multiple of 128 (at least the sum of the 128-padded groups)", fn);
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  }
+  st = check_device();
+  if (st != MX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->k == 0) {
+    // silu(0) * 0 = 0 everywhere: zero codes and zero scales in both copies
+    const size_t sizes[4] = {static_cast<size_t>(a->rows) * F, mx_scale_bytes(a->rows, F),
+                             static_cast<size_t>(F) * col_capacity, mx_scale_bytes(F, col_capacity)};
+    void* bufs[4] = {row_data, row_scale, col_data, col_scale};
+    for (int i = 0; i < 4; ++i) {
+      if (sizes[i] == 0) continue;
+      st = cuda_status(cudaMemsetAsync(bufs[i], 0, sizes[i], s), "cudaMemsetAsync");
+      if (st != MX_OK) return st;
+    }
+    return MX_OK;
+  }
+  L.q_row_data = row_data;
+  L.q_row_scale = row_scale;
+  L.q_col_data = col_data;
+  L.q_col_scale = col_scale;
+  L.q_cap = col_capacity;
   return launch_gemm(L, s);
 }
 

@@ -64,6 +64,7 @@
 #include <utility>
 #include <vector>
 
+#include "mx_codec.cuh"
 #include "mx_internal.h"
 #include "mx_ptx.cuh"
 
@@ -192,6 +193,20 @@ struct GParams {
   // with g the tile's expert for rows-ragged grouped GEMMs, else 0.
   const float* ts_a;
   const float* ts_b;
+  // Rows-ragged SwiGLU with its output quantised in the epilogue: the column
+  // capacity of the per-expert column copy (0 otherwise; the output pointers
+  // are in the launch's QOut).
+  int64_t q_cap;
+};
+
+// Outputs of the quantised SwiGLU epilogue, exactly as mx_quantize writes them
+// from the BF16 output: the MX row copy [M, n_out] with its scales and the
+// per-expert column copy [n_out, q_cap] with its scales.
+struct QOut {
+  uint8_t* row_data;
+  uint8_t* row_scale;
+  uint8_t* col_data;
+  uint8_t* col_scale;
 };
 
 // One segment's partial tile in the workspace: [unit][cta of the pair][epilogue
@@ -215,7 +230,7 @@ struct Tile {
 struct GroupInfo {
   int32_t* off;    // [E+1] row offsets
   int32_t* tile;   // [E+1] rows-ragged: m-tile prefix; K-ragged: padded 128-block prefix
-  int32_t* order;  // [E] K-ragged: experts by decreasing K
+  int32_t* order;  // K-ragged: [E] experts by decreasing K; rows-ragged: [E+1] 128-padded row prefix
   int32_t total;   // rows-ragged: sum of m-tiles; K-ragged: sum of padded blocks
 };
 
@@ -413,12 +428,23 @@ __device__ bool setup_groups(const GParams& p, GroupInfo& g, int32_t* s_flag, in
     if (tid == 0) {
       // Serial prefix: E <= 512 small integers, once per CTA.
       int32_t run = 0;
+      int32_t prun = 0;
       for (int e = 0; e < E; ++e) {
         const int32_t m = g.off[e + 1] - g.off[e];
         g.tile[e] = run;
         run += (KIND == GEMM_GROUPED_M) ? (m + tile_rows - 1) / tile_rows : (m + 127) / 128;
+        if (KIND == GEMM_GROUPED_M) {
+          // rows-ragged: each expert's first column in a per-expert column copy
+          // whose segments are padded to 128 rows (the SwiGLU epilogue's copy)
+          g.order[e] = prun;
+          prun += (m + 127) / 128 * 128;
+        }
       }
       g.tile[E] = run;
+      if (KIND == GEMM_GROUPED_M) {
+        g.order[E] = prun;
+        if (p.q_cap > 0 && prun > p.q_cap) *s_flag = 1;
+      }
       *s_total = run;
       if (KIND == GEMM_GROUPED_K && static_cast<int64_t>(run) * 128 > p.K) *s_flag = 1;
     }
@@ -473,6 +499,114 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Epilogue of the rows-ragged SwiGLU with its output quantised (the output's
+// MX copies instead of the output): the values are rounded to BF16 exactly as
+// the BF16 output would hold them, and coded as mx_quantize codes that output
+// (both copies, per-expert column segments padded to 128 rows with zero codes).
+// This thread holds row quarter * 32 + lane of the CTA's 128 rows and output
+// features [n0 + 64 half, + 64) as FP32 in v[0 .. 63]; a warp's 32 rows are one
+// 32-row block of the expert (tiles start at the expert's first row).
+__device__ __forceinline__ void swiglu_quant_epilogue(const GParams& p, const QOut& q, const GroupInfo& g,
+                                                      const Tile& ti, const uint32_t* v, int quarter, int half,
+                                                      int lane, uint8_t* stg) {
+  const int r = quarter * 32 + lane;
+  const int64_t grow = ti.m0 + r;
+  const bool rv = r < ti.valid_m;  // the row belongs to the tile's expert
+  const int64_t f0 = ti.n0 + 64 * half;
+  const int64_t F = p.n_out;
+  const int64_t row_ka = (F + 127) / 128;
+  const int64_t col_ka = (p.q_cap + 127) / 128;
+  uint32_t w[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) w[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+
+  // Row copy: the 1x32 blocks of features [f0, f0 + 32) and [f0 + 32, f0 + 64).
+  // The warp's 32 rows x 64 codes are staged in its box (16-byte chunks
+  // swizzled by row) and written back 8 rows x 64 contiguous bytes per store.
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    const uint32_t* wb = w + 16 * blk;
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = __vmaxu2(m, wb[j] & 0x7FFF7FFFu);
+    const uint32_t code = scale_code(half_max(m));
+    const bool nan_block = code == 0xFFu;
+    const float inv = inv_scale(nan_block ? 0u : code);
+    uint32_t c4[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      c4[j] = nan_block ? (nan_pair(wb[2 * j]) | (nan_pair(wb[2 * j + 1]) << 16)) : quant_quad(wb[2 * j], wb[2 * j + 1], inv);
+    st_shared_v4(stg + lane * 64 + (((2 * blk) ^ (lane & 3)) << 4), make_uint4(c4[0], c4[1], c4[2], c4[3]));
+    st_shared_v4(stg + lane * 64 + (((2 * blk + 1) ^ (lane & 3)) << 4), make_uint4(c4[4], c4[5], c4[6], c4[7]));
+    if (rv) q.row_scale[scale_offset(grow, (f0 >> 5) + blk, row_ka)] = static_cast<uint8_t>(code);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int rr = k * 8 + (lane >> 2);  // row of the warp's 32
+    const int cc = lane & 3;             // 16-byte chunk of the row's 64 codes
+    const uint4 c16 = ld_shared_v4(stg + rr * 64 + ((cc ^ (rr & 3)) << 4));
+    if (quarter * 32 + rr < ti.valid_m)
+      *reinterpret_cast<uint4*>(q.row_data + (ti.m0 + quarter * 32 + rr) * F + f0 + 16 * cc) = c16;
+  }
+  __syncwarp();  // the box is reused below
+
+  // Column copy: per feature, the 32x1 block over this warp's rows; rows past
+  // the expert's end are zero padding. A block wholly past the expert's
+  // 128-padded segment belongs to no segment and is not written. The warp
+  // transposes through its staging box, 32 features at a time: each lane
+  // writes its row, then takes one feature's 32 values and codes them (its
+  // block's amax, scale and 32 codes), one 32-byte store per feature.
+  const int e = ti.group;
+  const int64_t rel = ti.m0 - g.off[e] + quarter * 32;
+  const int64_t seg = (static_cast<int64_t>(g.off[e + 1] - g.off[e]) + 127) / 128 * 128;
+  if (rel < seg) {
+    const int64_t cpos = g.order[e] + rel;  // column of the block's first row in the copy
+    uint4* row_box = reinterpret_cast<uint4*>(stg + lane * 64);
+    const uint16_t* col_box = reinterpret_cast<const uint16_t*>(stg);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint32_t* wh = w + 16 * hh;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        row_box[c] = rv ? make_uint4(wh[4 * c], wh[4 * c + 1], wh[4 * c + 2], wh[4 * c + 3]) : make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+      uint32_t x[16];  // the feature's 32 values, two per word (row 2k low, 2k + 1 high)
+      uint32_t m = 0;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        x[k] = static_cast<uint32_t>(col_box[(2 * k) * 32 + lane]) |
+               (static_cast<uint32_t>(col_box[(2 * k + 1) * 32 + lane]) << 16);
+        m = __vmaxu2(m, x[k] & 0x7FFF7FFFu);
+      }
+      __syncwarp();  // the box is rewritten by the next 32 features
+      const uint32_t code = scale_code(half_max(m));
+      const bool nan_block = code == 0xFFu;
+      const float inv = inv_scale(nan_block ? 0u : code);
+      uint32_t c4[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        c4[k] = nan_block ? (nan_pair(x[2 * k]) | (nan_pair(x[2 * k + 1]) << 16)) : quant_quad(x[2 * k], x[2 * k + 1], inv);
+      const int64_t f = f0 + 32 * hh + lane;
+      uint4* dst = reinterpret_cast<uint4*>(q.col_data + f * p.q_cap + cpos);
+      dst[0] = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+      dst[1] = make_uint4(c4[4], c4[5], c4[6], c4[7]);
+      q.col_scale[scale_offset(f, cpos >> 5, col_ka)] = static_cast<uint8_t>(code);
+    }
+  }
+}
+
+// Row-scale padding of the quantised SwiGLU output: rows [M, ceil(M/128)*128)
+// belong to no expert; the first pair tile of each column tile (u == 0, even
+// CTA) zeroes their four scale bytes of its 128 features, one row per
+// epilogue thread.
+__device__ __forceinline__ void swiglu_quant_row_padding(const GParams& p, const QOut& q, const Tile& ti,
+                                                         int epi_thread) {
+  const int64_t pad = (p.M + 127) / 128 * 128 - p.M;
+  if (epi_thread < pad)
+    *reinterpret_cast<uint32_t*>(q.row_scale + scale_offset(p.M + epi_thread, ti.n0 >> 5, (p.n_out + 127) / 128)) = 0u;
 }
 
 // Epilogue of one warp: its 32 rows (TMEM lane quarter) x my_chunks 32-column
@@ -892,6 +1026,7 @@ struct PairProblem {
 struct PairArgs {
   PairProblem prob[kMaxProblems];
   int64_t tile0[kMaxProblems + 1];
+  QOut q;  // the quantised SwiGLU epilogue's outputs (single problem)
   int n;
   int sched;
   uint8_t cnt[kMaxProblems][kMaxSchedClusters];
@@ -906,9 +1041,13 @@ __device__ __forceinline__ int problem_of(const PairArgs& args, int64_t t) {
   return i;
 }
 
-template <int KIND, bool kSwiGLU, bool kMulti, int BN_, bool kTS>
+// kSwiGLU_: 0 none; 1 the SwiGLU epilogue writes its BF16 output; 2 it writes
+// the output's MX copies instead.
+template <int KIND, int kSwiGLU_, bool kMulti, int BN_, bool kTS>
 __global__ void __launch_bounds__(kPairThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ PairArgs args) {
+  constexpr bool kSwiGLU = kSwiGLU_ != 0;
+  constexpr bool kSwiQ = kSwiGLU_ == 2;
   using C = PairCfgT<BN_, kTS, KIND != GEMM_DENSE>;
   static_assert(!kMulti || (KIND == GEMM_DENSE && !kSwiGLU), "several problems per launch: dense GEMMs only");
   // Problem 0 holds the fields every problem shares (status word, wait bound)
@@ -1339,7 +1478,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const float uv = __uint_as_float(r[64 + i]);
           r[i] = __float_as_uint(gv / (1.0f + __expf(-gv)) * uv);
         }
-        store_tile<KIND, 64, C::kEpiBufs>(pp, ti, r, quarter, lane, 2, 64 * half, stg, &args.prob[pi].c);
+        if constexpr (kSwiQ) {
+          swiglu_quant_epilogue(pp, args.q, g, ti, r, quarter, half, lane, stg);
+          if (crank == 0 && t < nt) swiglu_quant_row_padding(pp, args.q, ti, (warp - 2) * 32 + lane);
+        } else {
+          store_tile<KIND, 64, C::kEpiBufs>(pp, ti, r, quarter, lane, 2, 64 * half, stg, &args.prob[pi].c);
+        }
       } else {
         store_tile<KIND, kCols, C::kEpiBufs>(pp, ti, r, quarter, lane, kCols / 32, col_off, stg, &args.prob[pi].c);
       }
@@ -1849,7 +1993,7 @@ PairArgs* pair_args_scratch() {
   return &args;
 }
 
-template <int KIND, bool kSwiGLU = false, int BN = 256, bool kTS = false>
+template <int KIND, int kSwiGLU = 0, int BN = 256, bool kTS = false>
 mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) {
   GParams p = p_in;
   CUtensorMap ma, mb, msa, msb, mc;
@@ -1893,6 +2037,8 @@ mx_status launch_pair(const GemmLaunch& L, const GParams& p_in, cudaStream_t s) 
   PairArgs* args = pair_args_scratch();
   std::memset(args, 0, sizeof(PairArgs));
   args->prob[0] = PairProblem{ma, mb, msa, msb, mc, p};
+  args->q = QOut{static_cast<uint8_t*>(L.q_row_data), static_cast<uint8_t*>(L.q_row_scale),
+                 static_cast<uint8_t*>(L.q_col_data), static_cast<uint8_t*>(L.q_col_scale)};
   args->n = 1;
   st = cuda_status(launch_kernel(kern, static_cast<unsigned>(2 * clusters), kPairThreads, smem, s, 2, *args),
                    "mx_gemm launch (CTA pairs)");
@@ -2082,6 +2228,7 @@ GParams make_gparams(const GemmLaunch& L) {
   p.ws = nullptr;
   p.ts_a = nullptr;
   p.ts_b = nullptr;
+  p.q_cap = L.q_row_data ? L.q_cap : 0;
   return p;
 }
 
@@ -2175,8 +2322,8 @@ mx_status launch_pair_multi(const GemmLaunch* Ls_in, int n, cudaStream_t s) {
   args->tile0[n] = tiles;
   args->n = n;
   const size_t smem = ts ? PairCfgT<BN, true, false>::smem_bytes() : PairCfgT<BN, false, false>::smem_bytes();
-  auto kern = ts ? mx_gemm_pair_kernel<GEMM_DENSE, false, true, BN, true>
-                 : mx_gemm_pair_kernel<GEMM_DENSE, false, true, BN, false>;
+  auto kern = ts ? mx_gemm_pair_kernel<GEMM_DENSE, 0, true, BN, true>
+                 : mx_gemm_pair_kernel<GEMM_DENSE, 0, true, BN, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(pair smem)");
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count() / 2));
@@ -2207,11 +2354,11 @@ mx_status launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   if (L.bw_a_scale) return launch_blockwise(L, p, s);
   if (L.tensor_scaled) {
     // one FP32 scale per tensor / per expert: 256 x 256 pair tiles, two accumulators
-    if (L.kind == GEMM_DENSE) return launch_pair<GEMM_DENSE, false, 256, true>(L, p, s);
-    if (L.kind == GEMM_GROUPED_M) return launch_pair<GEMM_GROUPED_M, false, 256, true>(L, p, s);
-    return launch_pair<GEMM_GROUPED_K, false, 256, true>(L, p, s);
+    if (L.kind == GEMM_DENSE) return launch_pair<GEMM_DENSE, 0, 256, true>(L, p, s);
+    if (L.kind == GEMM_GROUPED_M) return launch_pair<GEMM_GROUPED_M, 0, 256, true>(L, p, s);
+    return launch_pair<GEMM_GROUPED_K, 0, 256, true>(L, p, s);
   }
-  if (L.swiglu) return launch_pair<GEMM_GROUPED_M, true>(L, p, s);
+  if (L.swiglu) return L.q_row_data ? launch_pair<GEMM_GROUPED_M, 2>(L, p, s) : launch_pair<GEMM_GROUPED_M, 1>(L, p, s);
   int bn;
   if (L.kind == GEMM_DENSE) {
     const int cfg = choose_dense_cfg(L);

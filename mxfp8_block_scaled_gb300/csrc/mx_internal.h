@@ -125,6 +125,14 @@ struct GemmLaunch {
   // Current-scaling recipe: a_scale / b_scale are FP32 tensor scales (b: one
   // per expert for rows-ragged grouped GEMMs) applied in the epilogue.
   bool tensor_scaled = false;
+  // Rows-ragged SwiGLU only: instead of the BF16 output, its MX copies as
+  // mx_quantize (both copies, per-expert column segments) would write them from
+  // that output: row copy [M, N/2] + scales, column copy [N/2, q_cap] + scales.
+  void* q_row_data = nullptr;
+  void* q_row_scale = nullptr;
+  void* q_col_data = nullptr;
+  void* q_col_scale = nullptr;
+  int64_t q_cap = 0;
 };
 mx_status launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // Bytes of workspace the dense GEMM L would use for its split tail (0: none).

@@ -364,3 +364,25 @@ def test_current_gemm_multi_rejects_bad_arguments_on_host(L):
     assert _status_of(q, [], None, None) == 0
     assert _status_of(q, [_gp(a=_op(rows=0)), _gp(b=_op(rows=0))], None, None) == 0   # empty problems
     assert "problem 1" in (lambda: (_status_of(q, [good, _gp(ldc=100)], None, None), mx.mx_last_error())[1])()
+
+
+def test_grouped_gemm_swiglu_quantize_rejects_bad_arguments_on_host(L):
+    """The fused SwiGLU + quantisation entry: the SwiGLU checks, four non-null
+    16-byte aligned outputs and a positive column capacity that is a multiple
+    of 128; all decided before launch (the pointers are not device memory)."""
+    q = mx.mx_grouped_gemm_swiglu_quantize
+    g, rd, rs, cd, cs = 0x8000, 0x10000, 0x20000, 0x30000, 0x40000
+    ok = (_op(), _op(rows=256), g, 2, rd, rs, cd, cs, 256, None, None)
+
+    def with_(i, v):
+        a = list(ok)
+        a[i] = v
+        return a
+    assert _status_of(q, *with_(1, _op(rows=128))) == SHAPE        # 2F not a multiple of 256
+    assert _status_of(q, *with_(2, None)) == INVALID                # no group offsets
+    assert _status_of(q, *with_(3, 513)) == SHAPE                   # above MX_MAX_GROUPS
+    assert _status_of(q, *with_(4, None)) == INVALID
+    assert _status_of(q, *with_(7, cs + 8)) == ALIGN
+    assert _status_of(q, *with_(8, 100)) == SHAPE                   # capacity not a multiple of 128
+    assert _status_of(q, *with_(8, 0)) == SHAPE                     # rows to place, no capacity
+    assert _status_of(q, *with_(0, _op(rows=0))) == 0               # nothing to do

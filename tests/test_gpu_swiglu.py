@@ -8,7 +8,7 @@ import torch
 import oracle
 import workloads
 import mxfp8_block_scaled_gb300 as mx
-from tests.gpu_util import f64
+from tests.gpu_util import f64, logical_scales
 
 pytestmark = pytest.mark.gpu
 
@@ -94,3 +94,63 @@ def test_swiglu_equals_gemm_then_swiglu_of_its_bf16_is_close():
     g, u = y[:, :F], y[:, F:]
     bound = 2.0 ** -8 * (1.1 * np.abs(g) * np.abs(u) + np.abs(oracle.silu(g)) * np.abs(u)) + 2.0 ** -7 * np.abs(unfused)
     assert np.all(np.abs(fused - unfused) <= bound + 1e-30)
+
+
+def _fused_vs_two_step(counts, K, F, seed):
+    """The fused SwiGLU + quantisation epilogue against the two-step path (the
+    BF16 output of mx_grouped_gemm_swiglu, then mx_quantize of it with both
+    copies and per-expert column segments): every byte of the four buffers,
+    unwritten bytes included (both start as the same fill)."""
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    E = len(counts)
+    M = int(offs[-1])
+    X = workloads.normal_bf16((M, K), seed)
+    W = workloads.normal_bf16((E, 2 * F, K), seed + 1, 0.05)
+    o = torch.from_numpy(offs).cuda()
+    xr, _ = mx.quantize(X.cuda(), mx.MX_ROWWISE)
+    wr, _ = mx.quantize_stacked(W.cuda(), mx.MX_ROWWISE)
+    cap = int(mx.mx_grouped_padded_rows(offs)) + 128   # room past the last segment, left unwritten
+    st = mx.new_status()
+    y = mx.grouped_gemm_swiglu(xr, wr, o, status=st)
+    fills = []
+    for _ in range(2):
+        r0, c0 = mx.quantize(y, mx.MX_BOTH, group_offsets=o, col_capacity=cap)
+        for t in (r0.data, r0.scale, c0.data, c0.scale):
+            t.fill_(0xAB)
+        fills.append((r0, c0))
+    (r2, c2), (rf, cf) = fills
+    mx.quantize(y, mx.MX_BOTH, group_offsets=o, col_capacity=cap, status=st)  # warm the path
+    mx.mx_quantize(y.data_ptr(), M, F, y.stride(0), mx.MX_BOTH, r2.data.data_ptr(), r2.scale.data_ptr(),
+                   c2.data.data_ptr(), c2.scale.data_ptr(), o.data_ptr(), E, cap, st.data_ptr(),
+                   torch.cuda.current_stream().cuda_stream)
+    mx.grouped_gemm_swiglu_quantize(xr, wr, o, cap, out=(rf, cf), status=st)
+    torch.cuda.synchronize()
+    assert mx.read_status(st) == 0
+    for name, a, b in (("row data", rf.data, r2.data), ("row scales", rf.scale, r2.scale),
+                       ("col data", cf.data, c2.data), ("col scales", cf.scale, c2.scale)):
+        if not torch.equal(a, b):
+            bad = torch.nonzero(a != b)[:6].tolist()
+            raise AssertionError(f"fused SwiGLU quantisation {counts} F={F}: {name} differs at {bad}")
+    return y, offs, cap, rf, cf
+
+
+@pytest.mark.parametrize("counts,F", [([100, 0, 156], 128), ([37, 0, 300, 1, 128], 256), ([0, 0, 129], 384),
+                                      ([256], 128), ([5, 127, 128, 0, 0, 1000, 33, 2], 256), ([1], 128),
+                                      ([31, 33, 0, 200], 128)])
+def test_fused_swiglu_quantisation_equals_two_steps(counts, F):
+    y, offs, cap, rf, cf = _fused_vs_two_step(counts, 256, F, 110 + F + len(counts))
+    # and the codes are the oracle's quantisation of the SwiGLU output's BF16 values
+    yb = f64(y)
+    codes, scales = oracle.mx_quantize_rowwise(yb)
+    assert np.array_equal(rf.data.cpu().numpy(), codes)
+    assert np.array_equal(logical_scales(rf), scales)
+    ccodes, cscales, _ = oracle.mx_quantize_colwise_grouped(yb, offs)
+    kp = ccodes.shape[1]
+    assert np.array_equal(cf.data.cpu().numpy()[:, :kp], ccodes)
+    assert np.array_equal(logical_scales(cf)[:, :kp // 32], cscales)
+
+
+def test_fused_swiglu_quantisation_full_size():
+    """The routed experts' gate_up (49152 Zipf-routed rows, 64 experts, K =
+    2048, 2F = 2816): the fused epilogue against the two-step path, all bytes."""
+    _fused_vs_two_step(list(workloads.moe_counts()), 2048, 1408, 120)
