@@ -31,24 +31,30 @@
 //               in its instruction stream between the MMAs and cost ~10% of
 //               the tensor-pipe time; from a warp of their own they overlap.
 //
-// mx_gemm_pair_kernel (dense, CTA pairs = clusters of two, cta_group::2):
+// mx_gemm_pair_kernel (CTA pairs = clusters of two, cta_group::2; the kernel
+// for every shape that fills the GPU with 256 x 256 tiles):
 //   a 256 x 256 tile per pair. Each CTA loads its 128 rows of A and its half
 //   of B (so a stage is 32 KB instead of 48 KB and six stages fit), the even
 //   CTA issues the pair-wide MMAs (M = 256) and scale copies, and every
-//   completion is multicast to both CTAs. The operand pipeline of the single-CTA kernel is latency
-//   bound (a stage's round trip through L2 is ~1.6 us at 4 stages in flight);
-//   halving the per-CTA bytes of B raises the stages in flight.
+//   completion is multicast to both CTAs. The MMA issuer waits once per stage,
+//   on the copier's barrier (which follows the stage's full barrier); in cycle
+//   traces its own instruction stream, not the operand feed, sets the stage
+//   time. Variants: dense (optionally several independent GEMMs per launch,
+//   and a split tail for few-tile long-K shapes), rows-ragged grouped (A scale
+//   atoms gathered by warp 11 for tiles that start at any row; the SwiGLU
+//   epilogue writing BF16 or the MX copies of its output), K-ragged grouped,
+//   and tensor-scaled (plain E4M3 MMAs, two accumulators, no scale copies).
 //
 // Every mbarrier wait is bounded in wall time; on expiry the CTA records
 // MX_ERR_TIMEOUT in dev_status, drains its own copies and MMAs, frees its
 // tensor memory and returns.
 //
-// Grouped variants (single-CTA kernel): rows-ragged (fprop/dgrad over
-// contiguous token ranges per expert; A tiles start at arbitrary rows, so the
-// producer warp gathers their scale atoms with cp.async) and
-// contraction-ragged (wgrad; per-expert K segments padded to 128, one output
-// matrix per expert, experts with most K scheduled first; an empty expert
-// writes zeros).
+// Grouped variants of the single-CTA kernel (small grids): rows-ragged
+// (fprop/dgrad over contiguous token ranges per expert; A tiles start at
+// arbitrary rows, so the producer warp gathers their scale atoms with
+// cp.async) and contraction-ragged (wgrad; per-expert K segments padded to
+// 128, one output matrix per expert, experts with most K scheduled first; an
+// empty expert writes zeros).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
