@@ -1800,8 +1800,14 @@ __global__ void __launch_bounds__(BwCfg<BN_>::kThreads, 1)
           else if constexpr (kChunk == 16) tmem_ld_32x32b_x16(taddr + ch * kChunk, pr);
           else tmem_ld_32x32b_x8(taddr + ch * kChunk, pr);
           tmem_ld_wait();
+          // Packed FP32 FMAs (two round-to-nearest FMAs per instruction).
 #pragma unroll
-          for (int i = 0; i < kChunk; ++i) acc[ch * kChunk + i] = fmaf(__uint_as_float(pr[i]), f, acc[ch * kChunk + i]);
+          for (int i = 0; i < kChunk; i += 2) {
+            const float2 s2 = __ffma2_rn(make_float2(__uint_as_float(pr[i]), __uint_as_float(pr[i + 1])),
+                                         make_float2(f, f), make_float2(acc[ch * kChunk + i], acc[ch * kChunk + i + 1]));
+            acc[ch * kChunk + i] = s2.x;
+            acc[ch * kChunk + i + 1] = s2.y;
+          }
         }
         tc_fence_before_sync();
         mbar_arrive(&part_empty[buf]);
