@@ -260,7 +260,7 @@ class DenseFFN:
                 r, c = self.q[k]
                 descs.append(mx.MXQuantTensorC(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), r.data.data_ptr(),
                                                r.scale.data_ptr(), c.data.data_ptr(), c.scale.data_ptr()))
-            e = timers.span("quant", stream) if timers else None
+            e = timers.span(("quant", "+".join(names)), stream) if timers else None
             mx.mx_quantize_multi(descs, mx.MX_BOTH, None, sp)
             if e is not None:
                 e.record(stream)
@@ -1188,9 +1188,17 @@ def run_dense(args, rank, world, peaks, peak_src):
     value = world * args.steps * wl.step_flops() / (ms_max / 1e3) / 1e12
 
     gemm_ms = timers.total_ms("gemm") / args.steps            # fprop + the fused dgrad/wgrad launch
-    quant_ms = timers.total_ms("quant") / args.steps          # both quantiser launches of a step
     achieved = wl.step_flops() / (gemm_ms / 1e3) / 1e12
-    qbytes = sum(wl.quant_bytes().values())                    # X, W and dY per step
+    qb = wl.quant_bytes()
+    q_launch = {}                                              # each quantiser launch of a step on its own
+    for names in (("X", "W"), ("dY",)):
+        key = "+".join(names)
+        l_ms = timers.total_ms(("quant", key)) / args.steps
+        l_bytes = sum(qb[k] for k in names)
+        q_launch[key] = {"ms": l_ms, "bytes": l_bytes, "gbs": l_bytes / (l_ms / 1e3) / 1e9,
+                         "frac": l_bytes / (l_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    quant_ms = sum(v["ms"] for v in q_launch.values())        # both quantiser launches of a step
+    qbytes = sum(qb.values())                                  # X, W and dY per step
     q_gbs = qbytes / (quant_ms / 1e3) / 1e9
 
     # --- end to end: pinned host inputs -> device -> step -> host outputs ---
@@ -1225,9 +1233,9 @@ def run_dense(args, rank, world, peaks, peak_src):
         "quant_roofline": {"bound": "hbm", "kernel": "mx_quant_kernel", "achieved": q_gbs,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": q_gbs / peaks["hbm_gbs"],
                            "traffic": profile_traffic("mx_quant_kernel"), "bytes_per_step": qbytes,
-                           "ms_per_step": quant_ms, "launches_per_step": 2,
+                           "ms_per_step": quant_ms, "launches_per_step": 2, "per_launch": q_launch,
                            "basis": "algorithmic bytes of X, W and dY over the summed duration of the step's two "
-                                    "quantiser launches (X+W in one, dY in the other)",
+                                    "quantiser launches (X+W in one, dY in the other; each apart in per_launch)",
                            "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": wl.h2d_bytes(),
                 "d2h_bytes_per_step": wl.d2h_bytes(), "steps": args.e2e_steps,
